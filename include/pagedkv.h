@@ -1,0 +1,286 @@
+/*
+ * pagedkv.h — C ABI of libpagedkv.so: single-token decode attention over a
+ * paged (block_size 16) KV cache with GQA/MQA head groups, for sm_103a.
+ *
+ * What the library computes, per decode step:
+ *
+ *   out[b, hq, :] = softmax_t( scale * q[b, hq, :] . K_b,h[t, :] ) . V_b,h[t, :]
+ *   for t < context_lens[b], h = hq / (Hq / Hkv)
+ *
+ * This is scaled dot-product attention for one new query row
+ * ("苦猿的大模型日记 Day45", PART 02: Attention(Q,K,V) = softmax(QK^T/sqrt(d))V;
+ * "LLM推理优化实战：从KV-Cache到Continuous Batching", §1.1 attention_step),
+ * evaluated against a KV cache that lives in fixed-size physical blocks reached
+ * through a per-sequence block table ("LLM推理优化实战", §2.2 PageAttention,
+ * BLOCK_SIZE = 16; "大模型推理加速核心KV Cache 复用机制与内存布局优化", §三
+ * BlockTable), with groups of query heads sharing one KV head ("大模型推理加速
+ * ——KV Cache篇", §6.2 MHA/GQA/MQA).
+ *
+ * Conventions shared by every entry point
+ *  - Block size is fixed at PKV_BLOCK_SIZE = 16 tokens.
+ *  - Cache layout: k_cache and v_cache are separate dense arrays
+ *    [num_blocks][Hkv][16][D] (D fastest).  A (block, kv-head) tile of 16 tokens
+ *    is therefore one contiguous 16*D-element run.
+ *  - q, out: [B][Hq][D]; k_new, v_new: [B][Hkv][D]; all dense row-major.
+ *  - Query head hq reads kv head hq / (Hq/Hkv) (consecutive groups).
+ *  - FP8 caches (PKV_FP8_E4M3, OCP "e4m3fn": max 448, no infinities) carry one
+ *    fp32 scale per (block, kv-head), separately for K and V:
+ *    k_scale, v_scale: [num_blocks][Hkv]; element value = decode(byte) * scale.
+ *  - context_lens[b] is the attended length INCLUDING the token appended this
+ *    step; the appended token sits at position context_lens[b]-1.
+ *  - Every pointer argument that names a tensor is a DEVICE pointer unless the
+ *    entry point says otherwise.  The caller owns all memory; the library never
+ *    allocates device memory and keeps no per-call state outside `workspace`.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *    never synchronise the host, except where a function says so.
+ *  - Every function returns a pkv_status_t (0 = success, negative = error).
+ *    Arguments are validated before anything is launched: a call that returns
+ *    PKV_EINVAL / PKV_EUNSUPPORTED / PKV_EWORKSPACE has touched no memory.
+ *    PKV_ECUDA means a CUDA runtime call failed; pkv_last_cuda_error() returns
+ *    its cudaError_t.  Nothing is thrown across this boundary.
+ *  - Tensor pointers handed to the TMA engine (k_cache, v_cache, q, out and
+ *    workspace) must be 16-byte aligned.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+#define PKV_BLOCK_SIZE 16
+
+typedef enum {
+  PKV_F32 = 0,
+  PKV_F16 = 1,
+  PKV_BF16 = 2,
+  PKV_FP8_E4M3 = 3
+} pkv_dtype_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,        /* a null pointer, a negative size, Hq % Hkv != 0, ... */
+  PKV_EUNSUPPORTED = -2,  /* a valid but unimplemented shape or dtype combination */
+  PKV_EWORKSPACE = -3,    /* workspace missing, misaligned or too small */
+  PKV_ECUDA = -4,         /* a CUDA runtime call failed (see pkv_last_cuda_error) */
+  PKV_ETIMEOUT = -5,      /* a bounded in-kernel wait gave up (see paged_decode_status) */
+  PKV_EOOM = -6,          /* block manager: no free physical block */
+  PKV_ERANGE = -7,        /* a block id, slot or length outside its table */
+  PKV_ENOTFOUND = -8      /* block manager: unknown sequence id */
+} pkv_status_t;
+
+/* Status bits that kernels record in the workspace header (paged_decode_status). */
+#define PKV_FLAG_TIMEOUT 1   /* a pipeline wait exceeded its time limit */
+#define PKV_FLAG_BAD_LEN 2   /* context_lens[b] < 0 or > 16 * max_blocks_per_seq (clamped) */
+#define PKV_FLAG_BAD_BLOCK 4 /* a block-table entry outside [0, num_blocks) (read as zeros) */
+
+/* ------------------------------------------------------------------------ */
+/* Step a3 — KV append through a slot mapping.                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * Writes the new token's K/V rows into the paged cache:
+ *   k_cache[slot / 16][h][slot % 16][:] = k_new[b][h][:]   (same for V)
+ * with slot = slot_mapping[b] (int64, device).  slot < 0 means "padding, skip";
+ * a slot whose block is >= num_blocks is skipped as well.
+ * The write is the KV-cache update of incremental decoding ("大模型推理加速——KV
+ * Cache篇", §3.1 Attention.forward step 2; "苦猿的大模型日记 Day45", PART 02,
+ * new_k/new_v appended to the cache), addressed through the block table
+ * ("LLM推理优化实战", §2.2, logical block = num_tokens // BLOCK_SIZE).
+ *
+ * Types: for PKV_F32/F16/BF16 caches new_dtype must equal cache_dtype and the
+ * copy is bit-exact.  For a PKV_FP8_E4M3 cache, new_dtype is F32, F16 or BF16
+ * and each element is stored as e4m3(round-to-nearest-even, saturating to
+ * +-448)(x / scale) with the division done in fp32.  The scale is the block's
+ * existing k_scale/v_scale entry, except when slot % 16 == 0 (the token opens a
+ * fresh block): then scale = max_d |x_d| / 448 (1.0 if that is 0) is computed
+ * from the token and written to k_scale/v_scale first.  k_scale and v_scale are
+ * required (non-NULL) exactly when cache_dtype is PKV_FP8_E4M3.
+ * Slots must be distinct within one call.
+ */
+int paged_kv_append(const void *k_new, const void *v_new, int new_dtype,
+                    void *k_cache, void *v_cache, int cache_dtype,
+                    float *k_scale, float *v_scale,
+                    const int64_t *slot_mapping,
+                    int B, int Hkv, int D, int64_t num_blocks,
+                    pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Steps a4–a8 — paged gather, scores, online softmax, PV, split-KV merge.  */
+/* ------------------------------------------------------------------------ */
+/*
+ * Size in bytes of the workspace paged_decode_attention needs for these shapes
+ * on the CURRENT device; written to *bytes_out.  num_splits has the meaning it
+ * has for paged_decode_attention.
+ */
+int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                 int cache_dtype, int q_dtype, int num_splits,
+                                 size_t *bytes_out);
+
+/*
+ * Decode attention for one query token per sequence.
+ *
+ *   out        [B][Hq][D], dtype = q_dtype (fp32 results rounded to nearest even)
+ *   q          [B][Hq][D]; q_dtype: F32 with an F32 cache, else F16/BF16;
+ *              must equal cache_dtype for F16/BF16 caches.
+ *   k_cache, v_cache  [num_blocks][Hkv][16][D] of cache_dtype
+ *   k_scale, v_scale  [num_blocks][Hkv] fp32, FP8 caches only (else NULL)
+ *   block_table       [B][max_blocks_per_seq] int32 physical block ids
+ *   context_lens      [B] int32 attended lengths (0 gives out = 0)
+ *   scale             the softmax temperature, normally 1/sqrt(D)
+ *   D                 64 or 128
+ *
+ * Work decomposition (GB300 design, not taken from the pages): the
+ * concatenation of every (sequence, kv-head) block list is cut into
+ * `num_splits` contiguous, equally long partitions, one per warp; a warp
+ * streams its blocks through a TMA pipeline and keeps an fp32 online softmax
+ * (running max m, running sum l, rescaled accumulator — "LLM推理优化实战", §3.2
+ * flash_attention online softmax).  Partitions that cover only part of a
+ * sequence leave (o, lse) partials that a merge kernel combines with the
+ * log-sum-exp rule (flash-decoding split-KV, named in "苦猿的大模型日记 Day45"
+ * PART 03; the inter-block merge of "大模型推理加速核心KV Cache 复用机制与内存
+ * 布局优化" §四).  num_splits = 0 picks one partition per resident warp of the
+ * current GPU; any positive value is allowed and gives the same result up to
+ * fp32 rounding.
+ *
+ * workspace: device memory of at least paged_decode_workspace_bytes(...) bytes,
+ * 256-byte aligned, owned by the caller, reused across calls; concurrent calls
+ * must use distinct workspaces.  It needs no initialisation.
+ */
+int paged_decode_attention(void *out, const void *q, int q_dtype,
+                           const void *k_cache, const void *v_cache, int cache_dtype,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *context_lens,
+                           int B, int Hq, int Hkv, int D, int64_t num_blocks,
+                           float scale, int num_splits,
+                           void *workspace, size_t workspace_bytes,
+                           pkv_stream_t stream);
+
+/*
+ * Synchronises `stream` and reads the status bits (PKV_FLAG_*) that the last
+ * paged_decode_attention on `workspace` recorded.  Returns PKV_ETIMEOUT if
+ * PKV_FLAG_TIMEOUT is set, PKV_ERANGE if a range flag is set, else PKV_OK;
+ * *flags_out (may be NULL) receives the raw bits.  This is the one call that
+ * blocks the host.
+ */
+int paged_decode_status(const void *workspace, size_t workspace_bytes,
+                        pkv_stream_t stream, int *flags_out);
+
+/*
+ * Log-sum-exp merge of S partial attention results per (b, hq) row:
+ *   M = max_s lse[b][hq][s];  w_s = exp(lse[b][hq][s] - M)
+ *   out[b][hq][:] = sum_s w_s * o_partial[b][hq][s][:] / sum_s w_s
+ * o_partial [B][Hq][S][D] fp32 (each partial already normalised by its own
+ * softmax sum), lse [B][Hq][S] fp32 natural-log log-sum-exp of the partial's
+ * scaled scores; lse = -inf marks an empty partial, and a row whose partials
+ * are all empty gives out = 0.  out dtype is out_dtype (F32, F16 or BF16).
+ * The rule follows from the online-softmax rescaling identity ("LLM推理优化实
+ * 战", §3.2: O·exp(m_old - m_new) + ..., l·exp(m_old - m_new) + ...).
+ */
+int paged_decode_merge(void *out, int out_dtype,
+                       const float *o_partial, const float *lse,
+                       int B, int Hq, int D, int S,
+                       pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step a2 — copy-on-write block copy.                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * For each pair i: cache[dst_i] = cache[src_i] for all kv heads of both K and
+ * V (and the fp8 scales when cache_dtype is PKV_FP8_E4M3), where
+ * src_dst_pairs = {src_0, dst_0, src_1, dst_1, ...} (int32, device).  This is
+ * the copy that copy-on-write performs before a shared block is written
+ * ("LLM推理优化实战", §2.2 Copy-on-Write; "大模型推理加速——KV Cache篇", §6.1).
+ * Pairs with an id outside [0, num_blocks) are skipped.  Destinations must be
+ * distinct and must not appear as sources in the same call.
+ */
+int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype,
+                         float *k_scale, float *v_scale,
+                         const int32_t *src_dst_pairs, int n_pairs,
+                         int Hkv, int D, int64_t num_blocks,
+                         pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step a1 — host block manager: allocate / fork / free / slot mapping.     */
+/* ------------------------------------------------------------------------ */
+/*
+ * A host-side (CPU) physical-block allocator with per-sequence block tables and
+ * reference counts, after the BlockTable of "大模型推理加速核心KV Cache 复用机制
+ * 与内存布局优化" §三: the free list starts as [0, 1, ..., num_blocks-1] and
+ * hands out blocks from its END (LIFO); allocate() takes ceil(n/16) blocks or
+ * fails without change; fork() shares the parent's blocks (refcount + 1);
+ * free() decrements and returns blocks whose count reaches 0 to the end of the
+ * free list, in table order.  All pointers in this section are HOST pointers.
+ * A manager is not thread-safe; use one per thread or lock around it.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* Creates a manager over num_blocks physical blocks; NULL on failure. */
+pkv_block_manager *pkv_bm_create(int64_t num_blocks);
+void pkv_bm_destroy(pkv_block_manager *bm);
+
+/* allocate(seq, num_tokens): fresh table of ceil(num_tokens/16) blocks
+ * (refcount 1).  PKV_EOOM (no change) if the free list is too short,
+ * PKV_EINVAL if seq already exists or num_tokens < 0. */
+int pkv_bm_allocate(pkv_block_manager *bm, int64_t seq, int64_t num_tokens);
+
+/* Adopts an explicit block list for a new sequence holding num_tokens tokens
+ * (refcount + 1 per block; blocks leave the free list, which keeps the order
+ * of the remaining entries).  Used to mirror tables built elsewhere, and to
+ * share one prefix among many sequences.  nblocks must equal
+ * ceil(num_tokens/16); PKV_ERANGE for an id outside [0, num_blocks). */
+int pkv_bm_adopt(pkv_block_manager *bm, int64_t seq, const int32_t *blocks,
+                 int nblocks, int64_t num_tokens);
+
+/* fork(parent, child): the child gets a copy of the parent's table and token
+ * count; every block's refcount + 1.  PKV_ENOTFOUND / PKV_EINVAL on bad ids. */
+int pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child);
+
+/* free(seq): refcount - 1 per block, blocks at 0 go back to the free list. */
+int pkv_bm_free(pkv_block_manager *bm, int64_t seq);
+
+/*
+ * Reserves the slot of one new token for each of the n sequences seqs[i]:
+ *   pos = tokens(seq); if pos % 16 == 0 a fresh block is appended to the table;
+ *   else if the block holding pos is shared (refcount > 1) it is replaced by a
+ *   fresh block and the pair (old, new) is reported for a copy (copy-on-write);
+ *   slot_out[i] = table[pos / 16] * 16 + pos % 16;  tokens(seq) = pos + 1.
+ * cow_pairs_out (capacity 2*n int32) receives {src, dst, ...}; *n_cow_out the
+ * number of pairs.  On PKV_EOOM / PKV_ENOTFOUND every sequence is left as it
+ * was before the call.
+ */
+int pkv_bm_append_slots(pkv_block_manager *bm, const int64_t *seqs, int n,
+                        int64_t *slot_out, int32_t *cow_pairs_out, int *n_cow_out);
+
+/* Exports the block tables of n sequences as a dense [n][max_blocks] int32
+ * array (unused entries = -1) and their token counts as int32 context
+ * lengths.  PKV_ERANGE if a table is longer than max_blocks. */
+int pkv_bm_export(const pkv_block_manager *bm, const int64_t *seqs, int n,
+                  int32_t *table_out, int max_blocks, int32_t *context_lens_out);
+
+int64_t pkv_bm_num_free(const pkv_block_manager *bm);
+/* Refcount of a physical block (-1 for an id out of range). */
+int pkv_bm_refcount(const pkv_block_manager *bm, int64_t block);
+/* Token count of a sequence (-1 if unknown). */
+int64_t pkv_bm_num_tokens(const pkv_block_manager *bm, int64_t seq);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics.                                                             */
+/* ------------------------------------------------------------------------ */
+const char *pkv_status_string(int status);
+/* cudaError_t of the last PKV_ECUDA returned on the calling thread (0 if none). */
+int pkv_last_cuda_error(void);
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

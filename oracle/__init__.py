@@ -1,0 +1,180 @@
+"""CPU double-precision oracle for paged GQA decode attention.
+
+TEST INFRASTRUCTURE ONLY.  This package is the reference the CUDA library is
+checked against.  Only the tests, the smoke check and the benchmark's CPU
+baseline may import it; the library never does, and the two share no code.
+
+The arithmetic lives in ``oracle.c`` (see its header for the passages each
+function follows); this module only marshals numpy arrays through ctypes.
+``block_table.py`` holds the pure-Python block allocator of the page
+"大模型推理加速核心KV Cache 复用机制与内存布局优化" §三.
+
+Arrays are numpy; 16-bit and 8-bit floating caches are passed as their raw
+bits (uint16 / uint8 arrays) together with an explicit dtype name, so the
+oracle decodes every element itself.
+"""
+import ctypes
+import math
+
+import numpy as np
+
+from . import build as _build
+
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "fp8_e4m3": 3}
+_ITEM = {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_double.restype = f64
+        L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_double.restype = f64
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_double.restype = f64
+        L.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        L.oracle_kv_bytes_per_token.argtypes = [i32, i32, i32, f64]
+        L.oracle_kv_bytes_per_token.restype = f64
+        L.oracle_append.argtypes = [P, P, i32, P, P, P, P, i32, P, i32, i32, i32, i64, i32]
+        L.oracle_append.restype = i32
+        L.oracle_decode.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
+                                    i32, i32, i32, i32, i64, i32, f64, i32]
+        L.oracle_decode.restype = i32
+        L.oracle_merge.argtypes = [P, P, P, i32, i32, i32]
+        L.oracle_merge.restype = None
+        L.oracle_num_threads.argtypes = []
+        L.oracle_num_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _raw(a, dtype):
+    """Contiguous numpy view of a tensor's raw element bits for `dtype`."""
+    try:  # torch tensors (CPU) are accepted for convenience
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype in (torch.bfloat16, torch.float16):
+                a = a.view(torch.int16).numpy().view(np.uint16)
+            elif a.dtype == torch.float8_e4m3fn:
+                a = a.view(torch.uint8).numpy()
+            else:
+                a = a.numpy()
+    except ImportError:
+        pass
+    a = np.ascontiguousarray(a)
+    want = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16,
+            "fp8_e4m3": np.uint8}[dtype]
+    if dtype == "f16" and a.dtype == np.float16:
+        a = a.view(np.uint16)
+    if a.dtype != want:
+        raise TypeError(f"expected raw {want} array for {dtype}, got {a.dtype}")
+    return a
+
+
+def num_threads():
+    return lib().oracle_num_threads()
+
+
+def f16_to_double(bits):
+    L = lib()
+    return np.array([L.oracle_f16_to_double(int(b)) for b in np.ravel(bits)])
+
+
+def bf16_to_double(bits):
+    L = lib()
+    return np.array([L.oracle_bf16_to_double(int(b)) for b in np.ravel(bits)])
+
+
+def e4m3_to_double(codes):
+    L = lib()
+    return np.array([L.oracle_e4m3_to_double(int(c)) for c in np.ravel(codes)])
+
+
+def e4m3_from_float(x):
+    L = lib()
+    return np.array([L.oracle_e4m3_from_float(float(v)) for v in
+                     np.ravel(np.asarray(x, dtype=np.float32))], dtype=np.uint8)
+
+
+def kv_bytes_per_token(num_layers, num_kv_heads, head_dim, dtype_bytes):
+    return lib().oracle_kv_bytes_per_token(num_layers, num_kv_heads, head_dim,
+                                           float(dtype_bytes))
+
+
+def append(k_cache, v_cache, cache_dtype, k_new, v_new, new_dtype, slot_mapping,
+           k_scale=None, v_scale=None, block_size=16):
+    """Writes the new tokens into COPIES of the caches; returns
+    (k_cache, v_cache, k_scale, v_scale) after the append."""
+    kc = _raw(k_cache, cache_dtype).copy()
+    vc = _raw(v_cache, cache_dtype).copy()
+    kn = _raw(k_new, new_dtype)
+    vn = _raw(v_new, new_dtype)
+    B, Hkv, D = kn.shape
+    num_blocks = kc.shape[0]
+    ks = None if k_scale is None else np.array(k_scale, dtype=np.float32, copy=True)
+    vs = None if v_scale is None else np.array(v_scale, dtype=np.float32, copy=True)
+    sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64))
+    rc = lib().oracle_append(_ptr(kc), _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs),
+                             _ptr(kn), _ptr(vn), DTYPES[new_dtype], _ptr(sm),
+                             B, Hkv, D, num_blocks, block_size)
+    if rc != 0:
+        raise ValueError("oracle_append: unsupported dtype combination")
+    return kc, vc, ks, vs
+
+
+def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
+           scale=None, k_scale=None, v_scale=None, block_size=16, t_begin=None,
+           nthreads=0, with_lse=False):
+    """Exact attention of each query row over its sequence's gathered cache.
+
+    Returns out as float64 [B, Hq, D] (and lse [B, Hq] when with_lse)."""
+    qr = _raw(q, q_dtype)
+    kc = _raw(k_cache, cache_dtype)
+    vc = _raw(v_cache, cache_dtype)
+    B, Hq, D = qr.shape
+    num_blocks, Hkv = kc.shape[0], kc.shape[1]
+    if kc.shape[2] != block_size or kc.shape[3] != D:
+        raise ValueError("cache shape must be [num_blocks, Hkv, block_size, D]")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    tb = None if t_begin is None else np.ascontiguousarray(np.asarray(t_begin, dtype=np.int32))
+    ks = None if k_scale is None else np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32))
+    vs = None if v_scale is None else np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32))
+    if cache_dtype == "fp8_e4m3" and (ks is None or vs is None):
+        raise ValueError("fp8 cache needs k_scale and v_scale")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    lse = np.empty((B, Hq), dtype=np.float64)
+    rc = lib().oracle_decode(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
+                             _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),
+                             bt.shape[1], _ptr(cl), _ptr(tb), B, Hq, Hkv, D, num_blocks,
+                             block_size, float(scale), int(nthreads))
+    if rc == -1:
+        raise ValueError("oracle_decode: Hq must be a multiple of Hkv")
+    if rc == -2:
+        raise ValueError("oracle_decode: block table entry out of range")
+    return (out, lse) if with_lse else out
+
+
+def merge(o_parts, lse_parts):
+    """o_parts [R, S, D], lse_parts [R, S] (float64) -> out [R, D]."""
+    o = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    l = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64))
+    R, S, D = o.shape
+    out = np.empty((R, D), dtype=np.float64)
+    lib().oracle_merge(_ptr(out), _ptr(o), _ptr(l), R, S, D)
+    return out

@@ -1,0 +1,334 @@
+/*
+ * oracle.c — plain, slow, double-precision CPU reference for paged GQA decode
+ * attention.  TEST INFRASTRUCTURE ONLY: it exists to check the CUDA library,
+ * is called by the tests, by the smoke check and by the benchmark's CPU
+ * baseline, and is never linked into or called by the library itself.  It
+ * shares no code, header or table with the CUDA path.
+ *
+ * Every function states the passage it follows.  Page titles used below:
+ *   [P2] 大模型推理加速核心KV Cache 复用机制与内存布局优化 (mlqm.cn)
+ *   [P3] LLM推理优化实战：从KV-Cache到Continuous Batching的技术演进与代码实现 (tbr8.org)
+ *   [P4] 大模型推理加速——KV Cache篇 (AiGC面试宝典)
+ *   [P5] 苦猿的大模型日记 · Day45 · 大模型推理加速 (devpress.csdn.net)
+ *
+ * Number formats are decoded from their public definitions (IEEE 754
+ * binary16, bfloat16 = the top half of binary32, OCP 8-bit floating point
+ * E4M3 "fn" variant), not through any CUDA or compiler intrinsic.
+ *
+ * Build: cc -O2 -fopenmp -ffp-contract=off -shared -fPIC oracle.c -lm
+ * (no -ffast-math: the fp32 division in the fp8 quantiser must be IEEE).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Element type codes of the oracle's own interface. */
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
+
+/* ---------------------------------------------------------------------- */
+/* Number formats                                                          */
+/* ---------------------------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_f16_to_double(uint16_t h) {
+  int s = h >> 15, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m / 1024.0, -14);
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return s ? -v : v;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits. */
+double oracle_bf16_to_double(uint16_t h) {
+  int s = h >> 15, e = (h >> 7) & 0xff, m = h & 0x7f;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m / 128.0, -126);
+  else if (e == 255)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -v : v;
+}
+
+/* OCP FP8 E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 fraction bits; no
+ * infinities; S.1111.111 is NaN; exponent field 0 is subnormal 2^-6 * 0.m.
+ * Largest finite magnitude 1.75 * 2^8 = 448.  The FP8 KV cache is named in
+ * [P2] §四 (FP8/E4M3 KV Cache) and [P5] PART 02 (FP8 KV Cache). */
+double oracle_e4m3_to_double(uint8_t byte) {
+  int s = byte >> 7, e = (byte >> 3) & 0xf, m = byte & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Nearest E4M3 code to x, ties to the even code (fraction LSB 0), magnitudes
+ * beyond 448 saturating to 448, NaN -> 0x7f.  Brute force over the 127
+ * non-negative finite codes, which are increasing in value. */
+uint8_t oracle_e4m3_from_float(float x) {
+  if (isnan(x)) return 0x7f;
+  int neg = signbit(x) ? 1 : 0;
+  double a = fabs((double)x);
+  int best = 0;
+  double bestd = INFINITY;
+  for (int code = 0; code <= 126; ++code) {
+    double d = fabs(oracle_e4m3_to_double((uint8_t)code) - a);
+    if (d < bestd || (d == bestd && (code & 1) == 0)) {
+      bestd = d;
+      best = code;
+    }
+  }
+  return (uint8_t)((neg << 7) | best);
+}
+
+static double load_elem(const void *base, int dtype, size_t i) {
+  switch (dtype) {
+    case OR_F32: {
+      float f;
+      memcpy(&f, (const char *)base + 4 * i, 4);
+      return (double)f;
+    }
+    case OR_F16: {
+      uint16_t h;
+      memcpy(&h, (const char *)base + 2 * i, 2);
+      return oracle_f16_to_double(h);
+    }
+    case OR_BF16: {
+      uint16_t h;
+      memcpy(&h, (const char *)base + 2 * i, 2);
+      return oracle_bf16_to_double(h);
+    }
+    case OR_E4M3:
+      return oracle_e4m3_to_double(((const uint8_t *)base)[i]);
+  }
+  return NAN;
+}
+
+static size_t elem_size(int dtype) {
+  return dtype == OR_F32 ? 4 : (dtype == OR_E4M3 ? 1 : 2);
+}
+
+/* Exact fp32 value of a 16/32-bit element (all of them are representable). */
+static float load_as_float(const void *base, int dtype, size_t i) {
+  return (float)load_elem(base, dtype, i);
+}
+
+/* ---------------------------------------------------------------------- */
+/* KV bytes per token: 2 * num_layers * num_kv_heads * head_dim * bytes     */
+/* ([P5] PART 02, "一行公式，算出单个 token 吃多少显存").                        */
+/* ---------------------------------------------------------------------- */
+double oracle_kv_bytes_per_token(int num_layers, int num_kv_heads, int head_dim,
+                                 double dtype_bytes) {
+  return 2.0 * num_layers * num_kv_heads * head_dim * dtype_bytes;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Append: write the new token's K and V into its slot.                     */
+/* [P4] §3.1 (Attention.forward step 2: cache_k[:, start_pos] = xk),          */
+/* [P5] PART 02 (new_k appended to k_cache), [P3] §2.2 (logical block =       */
+/* num_tokens // BLOCK_SIZE).  Cache layout [num_blocks][Hkv][bs][D].          */
+/* FP8: q8 = e4m3_rne_sat((float)x / scale) with an fp32 division; a token    */
+/* at offset 0 of its block opens the block and sets scale = amax/448 (1 if   */
+/* amax is 0).  Returns 0, or -1 for an unsupported dtype pair.               */
+/* ---------------------------------------------------------------------- */
+static void append_one(const void *src, int new_dtype, size_t src_off,
+                       void *cache, int cache_dtype, float *scales,
+                       size_t tile_elem, size_t scale_idx, int off, int D) {
+  if (cache_dtype == OR_E4M3) {
+    float sc;
+    if (off == 0) {
+      float amax = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float a = fabsf(load_as_float(src, new_dtype, src_off + d));
+        if (a > amax) amax = a;
+      }
+      sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+      scales[scale_idx] = sc;
+    } else {
+      sc = scales[scale_idx];
+    }
+    for (int d = 0; d < D; ++d) {
+      float x = load_as_float(src, new_dtype, src_off + d);
+      float r = x / sc;
+      ((uint8_t *)cache)[tile_elem + d] = oracle_e4m3_from_float(r);
+    }
+  } else {
+    size_t es = elem_size(cache_dtype);
+    memcpy((char *)cache + es * tile_elem, (const char *)src + es * src_off, es * D);
+  }
+}
+
+int oracle_append(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
+                  float *v_scale, const void *k_new, const void *v_new, int new_dtype,
+                  const int64_t *slot_mapping, int B, int Hkv, int D,
+                  int64_t num_blocks, int block_size) {
+  if (cache_dtype != OR_E4M3 && new_dtype != cache_dtype) return -1;
+  if (cache_dtype == OR_E4M3 && new_dtype == OR_E4M3) return -1;
+  for (int b = 0; b < B; ++b) {
+    int64_t slot = slot_mapping[b];
+    if (slot < 0) continue;
+    int64_t blk = slot / block_size;
+    int off = (int)(slot % block_size);
+    if (blk >= num_blocks) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      size_t tile = ((size_t)(blk * Hkv + h) * block_size + off) * D;
+      size_t src = ((size_t)b * Hkv + h) * D;
+      size_t sidx = (size_t)blk * Hkv + h;
+      append_one(k_new, new_dtype, src, k_cache, cache_dtype, k_scale, tile, sidx, off, D);
+      append_one(v_new, new_dtype, src, v_cache, cache_dtype, v_scale, tile, sidx, off, D);
+    }
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention over the paged cache.                                   */
+/* out[b,hq,:] = sum_t softmax_t(scale * q.K_t) V_t  ([P5] PART 02 formula     */
+/* Attention = softmax(QK^T/sqrt(d))V; [P3] §1.1 attention_step; [P4] §3.1     */
+/* scores = xq.keys^T / sqrt(d), softmax, .values).  For a single new query    */
+/* the causal mask of [P4] §2.1 admits every cached position, so it is empty. */
+/* K_t is gathered through the block table ([P3] §2.2; [P2] §三):              */
+/*   K_t = k_cache[block_table[b][t / bs]][h][t % bs][:],  h = hq / (Hq/Hkv)  */
+/* ([P4] §6.2 GQA: a group of query heads shares one K/V head).               */
+/* FP8 elements are decode(byte) * scale[block][h].  Positions t run over     */
+/* [t_begin[b], context_lens[b]) (t_begin NULL means 0), which lets tests      */
+/* build partial results over a sub-range.  lse_out (may be NULL) receives     */
+/* log(sum_t exp(s_t)) = m + log(l); a row with no positions gives out = 0    */
+/* and lse = -inf.                                                              */
+/* ---------------------------------------------------------------------- */
+int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
+                  const void *k_cache, const void *v_cache, int cache_dtype,
+                  const float *k_scale, const float *v_scale,
+                  const int32_t *block_table, int max_blocks,
+                  const int32_t *context_lens, const int32_t *t_begin,
+                  int B, int Hq, int Hkv, int D, int64_t num_blocks,
+                  int block_size, double scale, int nthreads) {
+  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+  int G = Hq / Hkv;
+  int err = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    for (int h = 0; h < Hkv; ++h) {
+      int t0 = t_begin ? t_begin[b] : 0;
+      int t1 = context_lens[b];
+      int n = t1 > t0 ? t1 - t0 : 0;
+      double *K = NULL, *V = NULL, *s = NULL, *qv = NULL;
+      if (n > 0) {
+        K = (double *)malloc(sizeof(double) * (size_t)n * D);
+        V = (double *)malloc(sizeof(double) * (size_t)n * D);
+        s = (double *)malloc(sizeof(double) * (size_t)n);
+      }
+      qv = (double *)malloc(sizeof(double) * D);
+      /* gather this (sequence, kv head)'s K and V contiguously */
+      for (int i = 0; i < n; ++i) {
+        int t = t0 + i;
+        int logical = t / block_size;
+        int64_t blk = logical < max_blocks ? block_table[(size_t)b * max_blocks + logical] : -1;
+        if (blk < 0 || blk >= num_blocks) {
+#pragma omp atomic write
+          err = -2;
+          blk = 0;
+        }
+        size_t base = ((size_t)(blk * Hkv + h) * block_size + (t % block_size)) * D;
+        double ks = 1.0, vs = 1.0;
+        if (cache_dtype == OR_E4M3) {
+          ks = k_scale[blk * Hkv + h];
+          vs = v_scale[blk * Hkv + h];
+        }
+        for (int d = 0; d < D; ++d) {
+          K[(size_t)i * D + d] = load_elem(k_cache, cache_dtype, base + d) * ks;
+          V[(size_t)i * D + d] = load_elem(v_cache, cache_dtype, base + d) * vs;
+        }
+      }
+      for (int g = 0; g < G; ++g) {
+        int hq = h * G + g;
+        double *o = out + ((size_t)b * Hq + hq) * D;
+        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, q_dtype, ((size_t)b * Hq + hq) * D + d);
+        if (n == 0) {
+          for (int d = 0; d < D; ++d) o[d] = 0.0;
+          if (lse_out) lse_out[(size_t)b * Hq + hq] = -INFINITY;
+          continue;
+        }
+        double m = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)i * D + d];
+          s[i] = scale * acc;
+          if (s[i] > m) m = s[i];
+        }
+        double l = 0.0;
+        for (int i = 0; i < n; ++i) {
+          s[i] = exp(s[i] - m);
+          l += s[i];
+        }
+        for (int d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int i = 0; i < n; ++i) acc += s[i] * V[(size_t)i * D + d];
+          o[d] = acc / l;
+        }
+        if (lse_out) lse_out[(size_t)b * Hq + hq] = m + log(l);
+      }
+      free(K);
+      free(V);
+      free(s);
+      free(qv);
+    }
+  }
+  return err;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Merge of partial results over disjoint position ranges.                  */
+/* From the online-softmax rescaling of [P3] §3.2 (O and l rescaled by        */
+/* exp(m_old - m_new) when the running max grows): with per-part lse_s and    */
+/* normalised o_s, out = sum_s exp(lse_s - M) o_s / sum_s exp(lse_s - M),     */
+/* M = max_s lse_s.  o_parts [R][S][D], lse_parts [R][S]; -inf = empty part.  */
+/* ---------------------------------------------------------------------- */
+void oracle_merge(double *out, const double *o_parts, const double *lse_parts,
+                  int R, int S, int D) {
+  for (int r = 0; r < R; ++r) {
+    double M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+      if (lse_parts[(size_t)r * S + s] > M) M = lse_parts[(size_t)r * S + s];
+    double *o = out + (size_t)r * D;
+    if (M == -INFINITY) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      continue;
+    }
+    double wsum = 0.0;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int s = 0; s < S; ++s) {
+      double lse = lse_parts[(size_t)r * S + s];
+      if (lse == -INFINITY) continue;
+      double w = exp(lse - M);
+      wsum += w;
+      for (int d = 0; d < D; ++d) o[d] += w * o_parts[((size_t)r * S + s) * D + d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= wsum;
+  }
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,75 @@
+"""Plants plausible mistakes in a COPY of the oracle source, builds it, and
+checks that at least one pin test fails for each — evidence that the pins
+constrain every part of the oracle.  Nothing here touches a GPU."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_append_and_formula as T_app
+import test_oracle_attention as T_att
+import test_oracle_formats as T_fmt
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original fragment, mutated fragment, pin tests expected to catch it)
+MUTANTS = [
+    ("drop softmax scale", "s[i] = scale * acc;", "s[i] = acc;",
+     [lambda: T_att.test_toy_incremental_step_equals_full_recompute(16)]),
+    ("interleaved head map", "int hq = h * G + g;", "int hq = g * Hkv + h;",
+     [T_att.test_scores_scale_and_head_mapping]),
+    ("scores against V", "acc += qv[d] * K[(size_t)i * D + d];",
+     "acc += qv[d] * V[(size_t)i * D + d];",
+     [lambda: T_att.test_bruteforce_matches_sdpa(3, 4, 2, 8, 16, 40)]),
+    ("offset from block index", "(t % block_size)) * D;", "(t / block_size)) * D;",
+     [lambda: T_att.test_bruteforce_matches_sdpa(3, 4, 2, 8, 16, 40)]),
+    ("no normalisation", "o[d] = acc / l;", "o[d] = acc;",
+     [T_att.test_closed_forms]),
+    ("K scale from V", "ks = k_scale[blk * Hkv + h];", "ks = v_scale[blk * Hkv + h];",
+     [T_att.test_fp8_cache_is_dequantised_bytes_times_scale]),
+    ("subnormal exponent", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);",
+     [T_fmt.test_e4m3_all_codes_match_torch]),
+    ("ties to odd", "(d == bestd && (code & 1) == 0)", "(d == bestd && (code & 1) == 1)",
+     [T_fmt.test_e4m3_encoder_matches_torch_round_to_nearest_even]),
+    ("merge weight sign", "double w = exp(lse - M);", "double w = exp(M - lse);",
+     [T_att.test_merge_of_partials_equals_full]),
+    ("lse sign", "lse_out[(size_t)b * Hq + hq] = m + log(l);",
+     "lse_out[(size_t)b * Hq + hq] = m - log(l);",
+     [T_att.test_merge_of_partials_equals_full]),
+    ("fresh block test", "if (off == 0) {", "if (off == 1) {",
+     [T_app.test_append_fp8_uses_block_scale_or_opens_block]),
+    ("f16 exponent bias", "v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
+     "v = ldexp(1.0 + (double)m / 1024.0, e - 14);",
+     [T_fmt.test_f16_all_codes_match_numpy]),
+    ("kv bytes drops the 2", "return 2.0 * num_layers", "return 1.0 * num_layers",
+     [T_app.test_kv_bytes_formula_matches_pages]),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut,tests", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, monkeypatch, name, orig, mut, tests):
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(orig) == 1, f"fragment for '{name}' not unique in oracle.c"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(orig, mut))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["cc", "-O1", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                    str(path), "-o", str(so), "-lm"], check=True)
+    import ctypes
+    real = oracle.lib()
+    mutant = ctypes.CDLL(str(so))
+    for fn in ("oracle_f16_to_double", "oracle_bf16_to_double", "oracle_e4m3_to_double",
+               "oracle_e4m3_from_float", "oracle_kv_bytes_per_token", "oracle_append",
+               "oracle_decode", "oracle_merge", "oracle_num_threads"):
+        getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
+        getattr(mutant, fn).restype = getattr(real, fn).restype
+    monkeypatch.setattr(oracle, "_lib", mutant)
+    caught = 0
+    for t in tests:
+        try:
+            t()
+        except (AssertionError, ValueError):
+            caught += 1
+    assert caught == len(tests), f"mutant '{name}' survived its pin tests"
