@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged GQA decode step on GB300.
+
+A step is the whole decode path over one batch: the host block manager's
+slot mapping (a1), copy-on-write copies when a block is shared (a2, none in
+these workloads), the KV append (a3) and paged attention with its split merge
+(a4-a8).  Default workload: the Llama-3.1-70B-shaped GQA decode layer (B=64,
+Hq=64, Hkv=8, D=128, bf16, every context 8192 tokens).  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--num-splits P]
+
+--impl reference times the CPU oracle (double precision, all host cores) on a
+bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
+an independent replica; only rank 0 prints.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attention: achieved HBM GB/s (% of GB300 peak); decode tok/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic():
+    """DRAM bytes per decode launch from the committed ncu capture, if the
+    kernel sources are unchanged since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for name in ("common.cuh", "decode.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("dram_bytes_per_launch_scaled")
+
+
+def oracle_sample_rate(w, seconds, threads=0):
+    """Times the oracle's append + decode on the first sequences of w until
+    about `seconds` of work; returns (GB/s of KV processed, description, cores)."""
+    import numpy as np
+    import oracle
+    from oracle.block_table import BlockTable
+
+    bt = BlockTable(w.num_blocks)
+    for b in range(w.B):
+        bt.adopt(b, w.tables[b], w.cached[b])
+    slots, _ = bt.append_slots(list(range(w.B)))
+    mb = w.max_blocks
+    table = np.full((w.B, mb), -1, dtype=np.int32)
+    for b in range(w.B):
+        table[b, :len(bt.seq_tables[b])] = bt.seq_tables[b]
+    lens = np.array([bt.seq_tokens[b] for b in range(w.B)], dtype=np.int32)
+    per_seq = [int(lens[b]) * 2 * w.Hkv * w.D * {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}[w.dtype]
+               for b in range(w.B)]
+    ks = None if w.k_scale is None else w.k_scale.numpy()   # views: the append writes through
+    vs = None if w.v_scale is None else w.v_scale.numpy()
+    done_bytes, elapsed, n = 0, 0.0, 1
+    b0 = 0
+    while elapsed < seconds:
+        rows = [(b0 + i) % w.B for i in range(n)]
+        t0 = time.perf_counter()
+        oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new[rows], w.v_new[rows], w.new_dtype,
+                      [slots[r] for r in rows], ks, vs, inplace=True)
+        oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table[rows], lens[rows],
+                      scale=w.scale, k_scale=ks, v_scale=vs, nthreads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_bytes += sum(per_seq[r] for r in rows)
+        b0 = (b0 + n) % w.B
+        if dt < seconds / 8:
+            n = min(w.B, n * 2)
+    cores = oracle.num_threads() if threads <= 0 else threads
+    desc = (f"oracle decode (fp64, OpenMP over sequence x kv-head) of {done_bytes / 1e9:.2f} GB of "
+            f"KV from the same workload's sequences, {elapsed:.1f} s")
+    return done_bytes / elapsed / 1e9, desc, cores
+
+
+def spot_check(w, out, step):
+    """Max-abs error of the timed run's output against the oracle on the first
+    and last sequence (the oracle applies the same append on the host copy)."""
+    import numpy as np
+    import oracle
+    rows = sorted({0, w.B - 1})
+    slots = step.h_slots.numpy()
+    ks = None if w.k_scale is None else w.k_scale.numpy()
+    vs = None if w.v_scale is None else w.v_scale.numpy()
+    oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new[rows], w.v_new[rows], w.new_dtype,
+                  slots[rows], ks, vs, inplace=True)
+    table = step.h_table.numpy()[rows]
+    lens = step.h_lens.numpy()[rows]
+    ref = oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table, lens,
+                        scale=w.scale, k_scale=ks, v_scale=vs)
+    got = out[rows].double().cpu().numpy()
+    return {"rows": rows, "max_abs_err": float(np.abs(got - ref).max())}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import workloads
+    w = workloads.config(args.workload)
+    budget = min(3.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, budget / 4)
+    rates, times = [], []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r, desc, cores = oracle_sample_rate(w, budget)
+        times.append(time.perf_counter() - t0)
+        rates.append(r)
+    total = time.perf_counter() - t_start
+    value = statistics.median(rates)
+    kv = w.kv_bytes()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(kv / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + f"; {args.steps} steps of ~{budget:.1f} s"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(total, 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w):
+    return {"workload": w.name, "index": w.seed - 1000, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+            "D": w.D, "kv_dtype": w.dtype, "q_dtype": w.q_dtype, "block_size": 16,
+            "context_lens": (w.context_lens[0] if len(set(w.context_lens)) == 1
+                             else f"{min(w.context_lens)}..{max(w.context_lens)}"),
+            "num_blocks": w.num_blocks,
+            "l2": f"KV read per step {w.kv_bytes() / 1e9:.2f} GB > 129 MB L2; no flush needed"}
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import workloads
+    import paged_kv_gqa_03_gb300 as pkv
+    from paged_kv_gqa_03_gb300.step import DecodeStep
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+           "fp8_e4m3": torch.float8_e4m3fn}
+    w = workloads.config(args.workload)
+    stream = torch.cuda.Stream(dev)
+    ks = None if w.k_scale is None else w.k_scale.to(dev)
+    vs = None if w.v_scale is None else w.v_scale.to(dev)
+    step = DecodeStep(w.k_cache.to(dev), w.v_cache.to(dev), w.Hq, tdt[w.q_dtype], w.max_blocks,
+                      ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale)
+    for b in range(w.B):
+        step.adopt(b, w.tables[b], w.cached[b])
+    t0 = time.perf_counter()
+    step.prepare()
+    host_a1_us = (time.perf_counter() - t0) * 1e6
+    step.upload()
+    q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
+    out = torch.empty_like(q)
+    kv = w.kv_bytes()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # warm-up
+    for _ in range(args.warmup):
+        step.launch(q, kn, vn, out)
+    stream.synchronize()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    sampler = ClockSampler(bus)
+    sampler.start()
+
+    # (1) device-timed steps: append + attention (+ merge), inputs resident in HBM
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.launch(q, kn, vn, out)
+    e1.record(stream)
+    e1.synchronize()
+    barrier()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+    # (2) the attention call alone, same stream, for the roofline of the dominant kernel
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for _ in range(args.steps):
+        step.attend(q, out)
+    a1.record(stream)
+    a1.synchronize()
+    ms_attn = max_over_ranks(a0.elapsed_time(a1) / args.steps)
+    clocks = sampler.stop()
+
+    # (3) end to end through the public API from pinned host buffers
+    hq = w.q.pin_memory()
+    hk, hv = w.k_new.pin_memory(), w.v_new.pin_memory()
+    hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    dq, dkn, dvn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dkn.copy_(hk, non_blocking=True)
+            dvn.copy_(hv, non_blocking=True)
+        step.upload()
+        step.launch(dq, dkn, dvn, out)
+        with torch.cuda.stream(stream):
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()             # the host reads the step's result
+        _ = float(hout.view(-1)[0])
+    x1.record(stream)
+    x1.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(x0.elapsed_time(x1) / args.steps)
+    h2d = (hq.numel() * hq.element_size() + hk.numel() * hk.element_size() * 2 + step.h2d_bytes())
+    d2h = hout.numel() * hout.element_size()
+
+    # a spot check of the timed outputs against the oracle on two sequences
+    check = spot_check(w, out, step) if rank == 0 else None
+
+    if rank != 0:
+        torch.distributed.destroy_process_group() if world > 1 else None
+        return
+    peak, peak_src = peak_hbm()
+    value = world * kv / (ms_step * 1e-3) / 1e9
+    attn_gbs = kv / (ms_attn * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        r, desc, cores = oracle_sample_rate(w, args.cpu_seconds)
+        cpu = {"value": round(r, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1), random block permutation)",
+        "config": _config(w) | {"parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "tok_per_s": round(world * w.B / (ms_step * 1e-3), 1),
+        "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + decode + merge)",
+                     "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
+                     "traffic": kernel_traffic(), "algorithmic_bytes_per_launch": kv,
+                     "ms_per_launch": round(ms_attn, 4)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * kv / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 4)},
+        "host_a1_us": round(host_a1_us, 1),
+        "clocks": clocks,
+        "gpu_launches": 4 * args.steps,
+        "num_splits": args.num_splits,
+        "check": check,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -115,17 +115,26 @@ def kv_bytes_per_token(num_layers, num_kv_heads, head_dim, dtype_bytes):
 
 
 def append(k_cache, v_cache, cache_dtype, k_new, v_new, new_dtype, slot_mapping,
-           k_scale=None, v_scale=None, block_size=16):
-    """Writes the new tokens into COPIES of the caches; returns
-    (k_cache, v_cache, k_scale, v_scale) after the append."""
-    kc = _raw(k_cache, cache_dtype).copy()
-    vc = _raw(v_cache, cache_dtype).copy()
+           k_scale=None, v_scale=None, block_size=16, inplace=False):
+    """Writes the new tokens into COPIES of the caches (into the given arrays
+    themselves when inplace=True); returns (k_cache, v_cache, k_scale, v_scale)
+    after the append."""
+    kc = _raw(k_cache, cache_dtype)
+    vc = _raw(v_cache, cache_dtype)
+    if not inplace:
+        kc, vc = kc.copy(), vc.copy()
     kn = _raw(k_new, new_dtype)
     vn = _raw(v_new, new_dtype)
     B, Hkv, D = kn.shape
     num_blocks = kc.shape[0]
-    ks = None if k_scale is None else np.array(k_scale, dtype=np.float32, copy=True)
-    vs = None if v_scale is None else np.array(v_scale, dtype=np.float32, copy=True)
+    def _scales(x):
+        if x is None:
+            return None
+        if inplace:
+            x = _raw(x, "f32")
+            return x
+        return np.array(x, dtype=np.float32, copy=True)
+    ks, vs = _scales(k_scale), _scales(v_scale)
     sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64))
     rc = lib().oracle_append(_ptr(kc), _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs),
                              _ptr(kn), _ptr(vn), DTYPES[new_dtype], _ptr(sm),

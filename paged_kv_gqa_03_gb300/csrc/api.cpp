@@ -1,0 +1,406 @@
+// api.cpp — the extern "C" boundary of libpagedkv.so: argument validation,
+// kernel selection, TMA descriptor encoding, workspace layout and launches.
+// Every check runs before the first launch, so a rejected call touches no
+// memory.  No function here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "pagedkv.h"
+
+namespace pkv {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return PKV_ECUDA;
+}
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout ws_layout(int B, int P, int D) {
+  WsLayout L;
+  size_t o = 0;
+  L.hdr = o;
+  o = align_up(o + sizeof(WsHeader), 256);
+  L.prefix = o;
+  o = align_up(o + sizeof(int32_t) * (size_t)(B + 1), 256);
+  L.starts = o;
+  o = align_up(o + sizeof(int4) * (size_t)(P + 1), 256);
+  L.part_o = o;
+  o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax * D, 256);
+  L.part_lse = o;
+  o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax, 256);
+  L.total = o;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel registry and per-device facts.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxKernels = 64;
+constexpr int kMaxDevices = 64;
+
+struct Registry {
+  DecodeKernel k[kMaxKernels];
+  int n = 0;
+};
+
+Registry &registry() {
+  static Registry r;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    r.n += register_decode_bf16(r.k + r.n);
+    r.n += register_decode_f16(r.k + r.n);
+    r.n += register_decode_fp8(r.k + r.n);
+    r.n += register_decode_f32(r.k + r.n);
+  });
+  return r;
+}
+
+struct DeviceFacts {
+  int sm_count = 0;
+  int ctas_per_sm[kMaxKernels] = {};  // 0 = not yet configured
+};
+std::mutex g_dev_mu;
+DeviceFacts g_dev[kMaxDevices];
+
+// Configures kernel `ki` on the current device (opt-in shared memory) and
+// returns its resident CTAs per SM and the SM count.
+int kernel_occupancy(int ki, int *ctas_per_sm, int *sm_count) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return PKV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceFacts &f = g_dev[dev];
+  if (f.sm_count == 0) {
+    e = cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (f.ctas_per_sm[ki] == 0) {
+    const DecodeKernel &k = registry().k[ki];
+    e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k.fn, k.warps * 32, k.smem_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (nb <= 0) return PKV_EUNSUPPORTED;
+    f.ctas_per_sm[ki] = nb;
+  }
+  *ctas_per_sm = f.ctas_per_sm[ki];
+  *sm_count = f.sm_count;
+  return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int esize_of(int dtype) {
+  switch (dtype) {
+    case PKV_F32: return 4;
+    case PKV_F16: return 2;
+    case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
+  }
+  return 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over a [num_blocks][Hkv][16][D] cache as 2-D rows of 128 bytes
+// wide boxes with the 128-byte swizzle; one box is 16 token rows x 128 bytes
+// (or 8 lines of two 64-byte tokens).
+int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int64_t num_blocks, int Hkv, int D) {
+  auto fn = encode_fn();
+  if (!fn) return cuda_status(cudaErrorNotSupported);
+  const int es = esize_of(dtype);
+  const int rowb = D * es;
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], estr[2] = {1, 1};
+  const cuuint64_t tiles = (cuuint64_t)num_blocks * Hkv;
+  if (rowb >= 128) {
+    dims[0] = (cuuint64_t)D;
+    dims[1] = tiles * kBlock;
+    strides[0] = (cuuint64_t)rowb;
+    box[0] = 128 / es;
+    box[1] = kBlock;
+  } else {
+    dims[0] = 128 / es;
+    dims[1] = tiles * kBlock * rowb / 128;
+    strides[0] = 128;
+    box[0] = 128 / es;
+    box[1] = kBlock * rowb / 128;
+  }
+  const CUtensorMapDataType dt = es == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+  return PKV_OK;
+}
+
+struct Choice {
+  int ki;   // registry index
+  int GC;   // heads per unit
+  int NC;   // units per kv head
+};
+
+// Picks the kernel for a shape: tensor cores for groups of >= 3 heads on
+// 16-bit and fp8 caches, CUDA cores otherwise.  PKV_FORCE_SIMT=1 selects the
+// CUDA-core kernels for every cache dtype (comparison runs).
+int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
+  static const bool force_simt = [] {
+    const char *v = std::getenv("PKV_FORCE_SIMT");
+    return v && v[0] == '1';
+  }();
+  const bool mma = cache_dtype != PKV_F32 && G >= 3 && !force_simt;
+  const int GC = mma ? 8 : (G >= 2 ? 2 : 1);
+  Registry &r = registry();
+  for (int i = 0; i < r.n; ++i) {
+    const DecodeKernel &k = r.k[i];
+    if (k.mma == (mma ? 1 : 0) && k.cache_dtype == cache_dtype && k.q_dtype == q_dtype && k.D == D && k.GC == GC) {
+      c->ki = i;
+      c->GC = GC;
+      c->NC = (G + GC - 1) / GC;
+      return PKV_OK;
+    }
+  }
+  return PKV_EUNSUPPORTED;
+}
+
+int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int Hq, int Hkv, int D, int64_t num_blocks,
+                           int max_blocks) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_blocks <= 0 || max_blocks <= 0) return PKV_EINVAL;
+  if (Hq % Hkv != 0) return PKV_EINVAL;
+  if (esize_of(cache_dtype) == 0 || esize_of(q_dtype) == 0 || q_dtype == PKV_FP8_E4M3) return PKV_EINVAL;
+  if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
+  if (cache_dtype == PKV_F32 && q_dtype != PKV_F32) return PKV_EUNSUPPORTED;
+  if ((cache_dtype == PKV_F16 || cache_dtype == PKV_BF16) && q_dtype != cache_dtype) return PKV_EUNSUPPORTED;
+  if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F32) return PKV_EUNSUPPORTED;
+  // TMA row coordinates and the work-item count are 32-bit
+  if ((double)num_blocks * Hkv * kBlock >= 2147483000.0) return PKV_EUNSUPPORTED;
+  const int G = Hq / Hkv;
+  const int NC = (G + 1) / 2;  // the most units per kv head any kernel uses
+  if ((double)B * max_blocks * Hkv * NC >= 2147483000.0) return PKV_EUNSUPPORTED;
+  return PKV_OK;
+}
+
+// Resolves the kernel and the partition count for a call.
+int plan_call(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, int D, int num_splits, Choice *c, int *P) {
+  int rc = choose_kernel(cache_dtype, q_dtype, D, Hq / Hkv, c);
+  if (rc != PKV_OK) return rc;
+  if (num_splits < 0) return PKV_EINVAL;
+  if (num_splits > 0) {
+    *P = num_splits;
+  } else {
+    int ctas = 0, sms = 0;
+    rc = kernel_occupancy(c->ki, &ctas, &sms);
+    if (rc != PKV_OK) return rc;
+    *P = sms * ctas * registry().k[c->ki].warps;
+  }
+  if (*P > (1 << 24)) return PKV_EINVAL;
+  (void)B;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_version(void) { return 10000; }
+
+int pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_EUNSUPPORTED: return "unsupported shape or dtype combination";
+    case PKV_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ECUDA: return "CUDA runtime error";
+    case PKV_ETIMEOUT: return "an in-kernel wait timed out";
+    case PKV_EOOM: return "no free physical block";
+    case PKV_ERANGE: return "value out of range";
+    case PKV_ENOTFOUND: return "unknown sequence id";
+  }
+  return "unknown status";
+}
+
+int paged_kv_append(const void *k_new, const void *v_new, int new_dtype, void *k_cache, void *v_cache,
+                    int cache_dtype, float *k_scale, float *v_scale, const int64_t *slot_mapping, int B, int Hkv,
+                    int D, int64_t num_blocks, pkv_stream_t stream) {
+  if (B < 0 || Hkv <= 0 || num_blocks <= 0) return PKV_EINVAL;
+  if (esize_of(cache_dtype) == 0 || esize_of(new_dtype) == 0) return PKV_EINVAL;
+  if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
+  if (B == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_EINVAL;
+  if (cache_dtype == PKV_FP8_E4M3) {
+    if (new_dtype == PKV_FP8_E4M3) return PKV_EUNSUPPORTED;
+    if (!k_scale || !v_scale) return PKV_EINVAL;
+  } else {
+    if (new_dtype != cache_dtype) return PKV_EUNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_EINVAL;
+  }
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+  return cuda_status(launch_append(k_new, v_new, new_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
+                                   slot_mapping, B, Hkv, D, num_blocks, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int cache_dtype, int q_dtype, int num_splits,
+                                 size_t *bytes_out) {
+  if (!bytes_out) return PKV_EINVAL;
+  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, Hq, Hkv, D, 1, 1);
+  if (rc != PKV_OK) return rc;
+  Choice c;
+  int P = 0;
+  rc = plan_call(cache_dtype, q_dtype, B, Hq, Hkv, D, num_splits, &c, &P);
+  if (rc != PKV_OK) return rc;
+  *bytes_out = ws_layout(B, P, D).total;
+  return PKV_OK;
+}
+
+int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                           int cache_dtype, const float *k_scale, const float *v_scale, const int32_t *block_table,
+                           int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                           int64_t num_blocks, float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                           pkv_stream_t stream) {
+  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, Hq, Hkv, D, num_blocks, max_blocks_per_seq);
+  if (rc != PKV_OK) return rc;
+  if (!std::isfinite(scale)) return PKV_EINVAL;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens) return PKV_EINVAL;
+  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+  Choice c;
+  int P = 0;
+  rc = plan_call(cache_dtype, q_dtype, B, Hq, Hkv, D, num_splits, &c, &P);
+  if (rc != PKV_OK) return rc;
+  const WsLayout L = ws_layout(B, P, D);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
+    return PKV_EWORKSPACE;
+  const DecodeKernel &k = registry().k[c.ki];
+  int ctas = 0, sms = 0;
+  rc = kernel_occupancy(c.ki, &ctas, &sms);  // also opts the kernel into its shared memory
+  if (rc != PKV_OK) return rc;
+
+  CUtensorMap tmK, tmV;
+  rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+  if (rc != PKV_OK) return rc;
+  rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+  if (rc != PKV_OK) return rc;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.out = out;
+  p.q = q;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.hdr = reinterpret_cast<WsHeader *>(ws + L.hdr);
+  p.prefix = reinterpret_cast<int32_t *>(ws + L.prefix);
+  p.starts = reinterpret_cast<int4 *>(ws + L.starts);
+  p.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  p.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+  p.num_blocks = num_blocks;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.G = Hq / Hkv;
+  p.GC = c.GC;
+  p.NC = c.NC;
+  p.HU = Hkv * c.NC;
+  p.P = P;
+  p.max_blocks = max_blocks_per_seq;
+  p.out_dtype = q_dtype;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = 4000000000ull;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool pdl = s != nullptr;  // programmatic launch on explicit streams only
+  cudaError_t e = launch_plan(p, s);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((P + k.warps - 1) / k.warps);
+  cfg.blockDim = dim3(k.warps * 32);
+  cfg.dynamicSmemBytes = k.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  void *args[3] = {&p, &tmK, &tmV};
+  e = cudaLaunchKernelExC(&cfg, k.fn, args);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_splitk_merge(p, s, pdl);
+  return cuda_status(e);
+}
+
+int paged_decode_status(const void *workspace, size_t workspace_bytes, pkv_stream_t stream, int *flags_out) {
+  if (!workspace || workspace_bytes < sizeof(WsHeader)) return PKV_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t status = 0;
+  cudaError_t e = cudaMemcpyAsync(&status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (flags_out) *flags_out = status;
+  if (status & PKV_FLAG_TIMEOUT) return PKV_ETIMEOUT;
+  if (status & (PKV_FLAG_BAD_LEN | PKV_FLAG_BAD_BLOCK)) return PKV_ERANGE;
+  return PKV_OK;
+}
+
+int paged_decode_merge(void *out, int out_dtype, const float *o_partial, const float *lse, int B, int Hq, int D,
+                       int S, pkv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || D <= 0 || S <= 0) return PKV_EINVAL;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16) return PKV_EINVAL;
+  if (B == 0) return PKV_OK;
+  if (!out || !o_partial || !lse) return PKV_EINVAL;
+  return cuda_status(launch_merge(out, out_dtype, o_partial, lse, B, Hq, D, S, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype, float *k_scale, float *v_scale,
+                         const int32_t *src_dst_pairs, int n_pairs, int Hkv, int D, int64_t num_blocks,
+                         pkv_stream_t stream) {
+  if (n_pairs < 0 || Hkv <= 0 || num_blocks <= 0) return PKV_EINVAL;
+  if (esize_of(cache_dtype) == 0) return PKV_EINVAL;
+  if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
+  if (n_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PKV_EINVAL;
+  if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_EINVAL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+  return cuda_status(launch_copy_blocks(k_cache, v_cache, cache_dtype, k_scale, v_scale, src_dst_pairs, n_pairs,
+                                        Hkv, D, num_blocks, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// append.cu — step a3 (append the new token's K/V through the slot mapping)
+// and step a2 (copy-on-write block copy).
+//
+// Append: k_cache[slot / 16][h][slot % 16][:] = k_new[b][h][:] — the cache
+// update of incremental decoding ("大模型推理加速——KV Cache篇" §3.1 step 2;
+// "苦猿的大模型日记 Day45" PART 02), addressed through the block table
+// ("LLM推理优化实战" §2.2).  FP8 caches store e4m3(x / scale) with CUDA's
+// saturating round-to-nearest-even conversion; a token at offset 0 opens its
+// block and sets the block's scale to max|x| / 448 first.
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+// One warp per (sequence, kv head, K-or-V).
+template <class NewT, bool kFp8>
+__global__ void __launch_bounds__(128)
+    append_kernel(const void *__restrict__ k_new, const void *__restrict__ v_new, void *k_cache,
+                  void *v_cache, float *k_scale, float *v_scale, const int64_t *__restrict__ slot_mapping,
+                  int B, int Hkv, int D, int64_t num_blocks, int cache_esize) {
+  const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= B * Hkv * 2) return;
+  const int kv = gw & 1, bh = gw >> 1;
+  const int b = bh / Hkv, h = bh % Hkv;
+  const int64_t slot = slot_mapping[b];
+  if (slot < 0) return;
+  const int64_t blk = slot / kBlock;
+  const int off = (int)(slot % kBlock);
+  if (blk >= num_blocks) return;
+  const void *src = kv ? v_new : k_new;
+  void *cache = kv ? v_cache : k_cache;
+  const size_t src_elem = ((size_t)b * Hkv + h) * D;
+  const size_t dst_elem = ((size_t)(blk * Hkv + h) * kBlock + off) * D;
+  if constexpr (!kFp8) {
+    // bit-exact copy of D * esize bytes, 16 bytes per lane-step
+    const uint4 *s16 = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(src) + src_elem * cache_esize);
+    uint4 *d16 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(cache) + dst_elem * cache_esize);
+    for (int i = lane; i < D * cache_esize / 16; i += 32) d16[i] = s16[i];
+  } else {
+    float *scales = kv ? v_scale : k_scale;
+    const size_t sidx = (size_t)blk * Hkv + h;
+    const int epl = D / 32;  // 2 or 4 elements per lane
+    float x[4];
+    float amax = 0.f;
+    for (int e = 0; e < epl; ++e) {
+      x[e] = load_scalar(NewT{}, src, src_elem + lane * epl + e);
+      amax = fmaxf(amax, fabsf(x[e]));
+    }
+    float scale;
+    if (off == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      scale = amax > 0.f ? amax / 448.0f : 1.0f;
+      if (lane == 0) scales[sidx] = scale;
+    } else {
+      scale = scales[sidx];
+    }
+    uint32_t packed = 0;
+    for (int e = 0; e < epl; ++e) {
+      const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(x[e] / scale, __NV_SATFINITE, __NV_E4M3);
+      packed |= (uint32_t)q << (8 * e);
+    }
+    uint8_t *dst = static_cast<uint8_t *>(cache) + dst_elem + lane * epl;
+    if (epl == 4)
+      *reinterpret_cast<uint32_t *>(dst) = packed;
+    else
+      *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed;
+  }
+}
+
+cudaError_t launch_append(const void *k_new, const void *v_new, int new_dtype, void *k_cache, void *v_cache,
+                          int cache_dtype, float *k_scale, float *v_scale, const int64_t *slot_mapping, int B,
+                          int Hkv, int D, int64_t num_blocks, cudaStream_t stream) {
+  const int warps = B * Hkv * 2;
+  if (warps == 0) return cudaSuccess;
+  const dim3 grid((warps + 3) / 4), block(128);
+  const int esize = cache_dtype == PKV_F32 ? 4 : (cache_dtype == PKV_FP8_E4M3 ? 1 : 2);
+  if (cache_dtype != PKV_FP8_E4M3) {
+    append_kernel<F32, false><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                                          slot_mapping, B, Hkv, D, num_blocks, esize);
+  } else if (new_dtype == PKV_F32) {
+    append_kernel<F32, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                                         slot_mapping, B, Hkv, D, num_blocks, esize);
+  } else if (new_dtype == PKV_F16) {
+    append_kernel<F16, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                                         slot_mapping, B, Hkv, D, num_blocks, esize);
+  } else {
+    append_kernel<BF16, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                                          slot_mapping, B, Hkv, D, num_blocks, esize);
+  }
+  return cudaGetLastError();
+}
+
+// Copy-on-write: cache[dst] = cache[src] for all kv heads (one CTA per pair
+// and K/V side), plus the block's fp8 scales.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                       const int32_t *__restrict__ pairs, int Hkv, size_t block_bytes, int64_t num_blocks) {
+  const int pair = blockIdx.x, kv = blockIdx.y;
+  const int src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+  if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks || src == dst) return;
+  uint8_t *base = kv ? v_cache : k_cache;
+  const uint4 *s = reinterpret_cast<const uint4 *>(base + (size_t)src * block_bytes);
+  uint4 *d = reinterpret_cast<uint4 *>(base + (size_t)dst * block_bytes);
+  for (size_t i = threadIdx.x; i < block_bytes / 16; i += blockDim.x) d[i] = s[i];
+  float *sc = kv ? v_scale : k_scale;
+  if (sc != nullptr)
+    for (int h = threadIdx.x; h < Hkv; h += blockDim.x) sc[(size_t)dst * Hkv + h] = sc[(size_t)src * Hkv + h];
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, int cache_dtype, float *k_scale, float *v_scale,
+                               const int32_t *pairs, int n_pairs, int Hkv, int D, int64_t num_blocks,
+                               cudaStream_t stream) {
+  if (n_pairs == 0) return cudaSuccess;
+  const int esize = cache_dtype == PKV_F32 ? 4 : (cache_dtype == PKV_FP8_E4M3 ? 1 : 2);
+  const size_t block_bytes = (size_t)Hkv * kBlock * D * esize;
+  const bool fp8 = cache_dtype == PKV_FP8_E4M3;
+  copy_blocks_kernel<<<dim3(n_pairs, 2), 256, 0, stream>>>(
+      static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), fp8 ? k_scale : nullptr,
+      fp8 ? v_scale : nullptr, pairs, Hkv, block_bytes, num_blocks);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

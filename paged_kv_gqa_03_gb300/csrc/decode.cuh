@@ -1,0 +1,710 @@
+// decode.cuh — the paged decode-attention kernel (steps a4–a8 up to the
+// partial results), templated on cache dtype, head dim and compute path.
+//
+// Work decomposition.  A "unit" is (sequence b, kv head h, head chunk c): the
+// query heads h*G + c*GC ... (at most GC of them) that share kv head h
+// ("大模型推理加速——KV Cache篇" §6.2 GQA).  Units are concatenated in the order
+// (b, h, c), each contributing ceil(ctx_b / 16) block items, and the item list
+// is cut into P equal contiguous ranges, one per warp (the "workers").  A
+// warp streams its range block by block, carrying the online-softmax state
+// across blocks of a unit ("LLM推理优化实战" §3.2 online softmax: running max
+// m, running sum l, accumulator rescaled by exp(m_old - m_new)); a unit cut by
+// a range boundary leaves normalised (o, lse) partials for the merge kernel.
+//
+// Data movement.  Each warp owns a ring of STAGES shared-memory slots; lane 0
+// issues 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of the block's
+// K tile and V tile — each a contiguous 16 x D run of [num_blocks][Hkv][16][D]
+// reached through the block table ("LLM推理优化实战" §2.2 block table) — onto
+// the slot's mbarrier, STAGES blocks ahead of the consumer.
+//
+// Compute.  MMA path (f16/bf16/fp8 caches, group >= 3): per 16-token block,
+// S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8] and O^T[D x 8] += V^T[D x 16] .
+// P^T[16 x 8] with mma.sync m16n8k16 (fp32 accumulate); P moves from the
+// score fragment to the B operand with movmatrix.  CUDA-core path (fp32
+// caches, groups of 1-2): lanes split tokens for q.K and head-dim slices for
+// p.V.  Scores use the scale of "苦猿的大模型日记 Day45" PART 02
+// (softmax(QK^T / sqrt(d))), applied in fp32 in the log2 domain.
+#pragma once
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+template <class CacheT, class QT, int D_, int GC_, bool MMA_, int WARPS_, int BUDGET_>
+struct DecodeCfg {
+  using Cache = CacheT;
+  using Q = QT;
+  static constexpr int D = D_, GC = GC_, WARPS = WARPS_;
+  static constexpr bool MMA = MMA_;
+  static constexpr bool FP8 = CacheT::kBytes == 1;
+  static constexpr int ROWB = D * CacheT::kBytes;           // bytes per token row
+  static constexpr int TILE = kBlock * ROWB;                // bytes per (block, head) tile
+  static constexpr int STAGES_RAW = BUDGET_ / (2 * TILE);
+  static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
+  static constexpr int NBOX = ROWB >= 128 ? ROWB / 128 : 1;  // TMA boxes per tile
+  static constexpr int BOX_ROWS = ROWB >= 128 ? kBlock : kBlock * ROWB / 128;
+  static constexpr int BOX_ELEMS = 128 / CacheT::kBytes;
+  static constexpr size_t TILES_BYTES = (size_t)WARPS * STAGES * 2 * TILE;
+  static constexpr size_t META_BYTES = (size_t)WARPS * STAGES * sizeof(StageMeta);
+  static constexpr size_t BAR_BYTES = (size_t)WARPS * STAGES * 8;
+  static constexpr size_t QBUF_BYTES = MMA ? 0 : (size_t)WARPS * GC * D * 4;
+  static constexpr size_t SMEM = 1024 + TILES_BYTES + META_BYTES + BAR_BYTES + QBUF_BYTES;
+  static_assert(TILE % 1024 == 0, "tiles must keep 1024-byte alignment for the swizzle");
+  static_assert(!MMA || GC == 8, "the MMA path serves 8-head chunks");
+  static_assert(D == 64 || D == 128, "head dim");
+};
+
+// ---------------------------------------------------------------------------
+// Producer: walks the worker's item range and issues TMA loads.
+// ---------------------------------------------------------------------------
+struct Producer {
+  int pi, e, s;          // next item, end of range, start of range
+  int b, hu, j, n, ctx;  // unit and block of item pi; blocks and length of sequence b
+  int seg_j0, seg_wfirst;
+  int win_b, win_hu, win_j0, win_id;  // lane-parallel window of 32 block-table entries
+  float win_ks, win_vs;
+};
+
+__device__ __forceinline__ void load_seq(Producer &pr, const DecodeParams &p) {
+  int ctx = __ldg(p.context_lens + pr.b);
+  ctx = ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
+  pr.ctx = ctx;
+  pr.n = (ctx + kBlock - 1) / kBlock;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, const CUtensorMap *tmK,
+                                        const CUtensorMap *tmV, uint8_t *tiles, StageMeta *meta,
+                                        uint64_t *bars, int stage, int lane) {
+  __syncwarp();
+  const int h = pr.hu / p.NC;
+  if (!(pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j >= pr.win_j0 && pr.j < pr.win_j0 + 32)) {
+    pr.win_b = pr.b;
+    pr.win_hu = pr.hu;
+    pr.win_j0 = pr.j;
+    const int jj = pr.j + lane;
+    int id = 0;
+    if (jj < pr.n) id = __ldg(p.block_table + (size_t)pr.b * p.max_blocks + jj);
+    pr.win_id = id;
+    if constexpr (Cfg::FP8) {
+      float ks = 0.f, vs = 0.f;
+      if (jj < pr.n && id >= 0 && (int64_t)id < p.num_blocks) {
+        ks = __ldg(p.k_scale + (size_t)id * p.Hkv + h);
+        vs = __ldg(p.v_scale + (size_t)id * p.Hkv + h);
+      }
+      pr.win_ks = ks;
+      pr.win_vs = vs;
+    }
+  }
+  const int blk = __shfl_sync(kFull, pr.win_id, pr.j - pr.win_j0);
+  float ks = 1.f, vs = 1.f;
+  if constexpr (Cfg::FP8) {
+    ks = __shfl_sync(kFull, pr.win_ks, pr.j - pr.win_j0);
+    vs = __shfl_sync(kFull, pr.win_vs, pr.j - pr.win_j0);
+  }
+  int flags = 0;
+  if (pr.pi == pr.s || pr.j == 0) {
+    flags |= kFirst;
+    pr.seg_j0 = pr.j;
+    pr.seg_wfirst = (pr.pi == pr.s);
+  }
+  if (pr.pi + 1 == pr.e || pr.j + 1 == pr.n) {
+    flags |= kLast;
+    if (pr.seg_j0 == 0 && pr.j + 1 == pr.n) flags |= kComplete;
+  }
+  if (pr.seg_wfirst) flags |= kWFirst;
+  const int nvalid = min(kBlock, pr.ctx - pr.j * kBlock);
+  if (lane == 0) {
+    const bool bad = blk < 0 || (int64_t)blk >= p.num_blocks;
+    // a bad id reads the tile just past the end of the tensor: TMA fills zeros
+    const int64_t tile_row = bad ? p.num_blocks * p.Hkv : (int64_t)blk * p.Hkv + h;
+    if (bad) atomicOr(&p.hdr->status, PKV_FLAG_BAD_BLOCK);
+    StageMeta m;
+    m.b = pr.b;
+    m.hu = pr.hu;
+    m.j = pr.j;
+    m.nvalid = nvalid;
+    m.ks = ks;
+    m.vs = vs;
+    m.flags = flags;
+    m.pad = 0;
+    meta[stage] = m;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&bars[stage], 2 * Cfg::TILE);
+    uint8_t *dk = tiles + (size_t)stage * 2 * Cfg::TILE;
+    uint8_t *dv = dk + Cfg::TILE;
+    const int y = (int)(tile_row * Cfg::BOX_ROWS);
+#pragma unroll
+    for (int bx = 0; bx < Cfg::NBOX; ++bx) {
+      tma_load_2d(dk + bx * 2048, tmK, bx * Cfg::BOX_ELEMS, y, &bars[stage]);
+      tma_load_2d(dv + bx * 2048, tmV, bx * Cfg::BOX_ELEMS, y, &bars[stage]);
+    }
+  }
+  // advance to the next item
+  ++pr.pi;
+  ++pr.j;
+  if (pr.j == pr.n && pr.pi < pr.e) {
+    pr.j = 0;
+    if (++pr.hu == p.HU) {
+      pr.hu = 0;
+      do {
+        ++pr.b;
+        load_seq(pr, p);
+      } while (pr.n == 0 && pr.b < p.B - 1);
+    }
+  }
+}
+
+// Zeroes token rows [nvalid, 16) of a tile so stale (possibly non-finite)
+// cache contents cannot leak into p.V through a zero weight.
+template <int ROWB>
+__device__ __forceinline__ void zero_tail_rows(uint8_t *tile, int nvalid, int lane) {
+  constexpr int CPR = ROWB / 16;  // 16-byte chunks per row
+  const uint32_t base = smem_u32(tile);
+  for (int idx = lane; idx < (kBlock - nvalid) * CPR; idx += 32) {
+    const int row = nvalid + idx / CPR, ch = idx % CPR;
+    sts128(base + tile_off<ROWB>(row, ch * 16), make_uint4(0, 0, 0, 0));
+  }
+  fence_proxy_async();
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// MMA path state and steps.
+// ---------------------------------------------------------------------------
+template <class Cfg>
+struct MmaState {
+  static constexpr int KS = Cfg::D / 16;  // k-steps of q.K
+  static constexpr int MT = Cfg::D / 16;  // m-tiles of V^T
+  uint32_t qb[KS][2];
+  float acc[MT][4];
+  float m0, m1, l0, l1;
+};
+
+template <class Cfg>
+__device__ __forceinline__ void mma_begin(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                          int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int h = m.hu / p.NC, c = m.hu % p.NC;
+  const int head0 = h * p.G + c * Cfg::GC;
+  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  const size_t row = ((size_t)m.b * p.Hq + head0 + gid) * Cfg::D;
+#pragma unroll
+  for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
+    uint32_t b0 = 0, b1 = 0;
+    if (gid < gc) {
+      if constexpr (Cfg::FP8) {
+        // k-slots 2t,2t+1 | 2t+8,2t+9 hold d = 16ks + 4t + {0,1} | {2,3}
+        const uint2 raw = *reinterpret_cast<const uint2 *>(
+            reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 4 * tig);
+        float2 x0, x1;
+        if constexpr (Cfg::Q::kCode == PKV_BF16) {
+          x0 = unpack2(BF16{}, raw.x);
+          x1 = unpack2(BF16{}, raw.y);
+        } else {
+          x0 = unpack2(F16{}, raw.x);
+          x1 = unpack2(F16{}, raw.y);
+        }
+        b0 = pack_f16x2(x0.x, x0.y);
+        b1 = pack_f16x2(x1.x, x1.y);
+      } else {
+        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 2 * tig;
+        b0 = *reinterpret_cast<const uint32_t *>(qr);
+        b1 = *reinterpret_cast<const uint32_t *>(qr + 8);
+      }
+    }
+    st.qb[ks][0] = b0;
+    st.qb[ks][1] = b1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) st.acc[mt][r] = 0.f;
+  st.m0 = st.m1 = -INFINITY;
+  st.l0 = st.l1 = 0.f;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                          uint8_t *tk, uint8_t *tv, int lane) {
+  constexpr int ROWB = Cfg::ROWB;
+  constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t kb = smem_u32(tk), vb = smem_u32(tv);
+  const int nvalid = m.nvalid;
+  if (nvalid < kBlock) zero_tail_rows<ROWB>(tv, nvalid, lane);
+
+  // ---- scores S^T = K . Q^T (16 tokens x 8 heads) ----
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (Cfg::FP8) {
+#pragma unroll
+    for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
+      const uint32_t w0 = lds32(kb + tile_off<ROWB>(gid, 16 * ks + 4 * tig));
+      const uint32_t w1 = lds32(kb + tile_off<ROWB>(gid + 8, 16 * ks + 4 * tig));
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff));
+      a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff));
+      a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
+      a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+      mma16816<false>(s, a, st.qb[ks][0], st.qb[ks][1]);
+    }
+  } else {
+    const int r = lane & 7, mi = lane >> 3;
+    const int krow = r + ((mi & 1) << 3), khi = mi >> 1;
+#pragma unroll
+    for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(kb + tile_off<ROWB>(krow, (2 * ks + khi) * 16), a);
+      mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
+    }
+  }
+
+  // ---- online softmax over the block (log2 domain) ----
+  const float sc = p.scale_log2 * m.ks;
+  float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
+  if (gid >= nvalid) x0 = x1 = -INFINITY;
+  if (gid + 8 >= nvalid) x2 = x3 = -INFINITY;
+  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  const float al0 = exp2f(st.m0 - mn0), al1 = exp2f(st.m1 - mn1);
+  const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+  const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+  st.l0 = st.l0 * al0 + (p0 + p2);
+  st.l1 = st.l1 * al1 + (p1 + p3);
+  st.m0 = mn0;
+  st.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+    st.acc[mt][0] *= al0;
+    st.acc[mt][1] *= al1;
+    st.acc[mt][2] *= al0;
+    st.acc[mt][3] *= al1;
+  }
+
+  // ---- O^T += V^T . P^T ----
+  uint32_t pb0, pb1;
+  if constexpr (Cfg::FP8) {
+    const float vs = m.vs;  // fold the V scale into the weights
+    pb0 = movmatrix_trans(pack_f16x2(p0 * vs, p1 * vs));
+    pb1 = movmatrix_trans(pack_f16x2(p2 * vs, p3 * vs));
+    constexpr int DPT = Cfg::D / 8;  // head-dim bytes owned by one row group
+    const int t0 = 2 * tig, t2 = 2 * tig + 8;
+    if constexpr (DPT == 16) {
+      const uint4 R0 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t0, 16 * gid));
+      const uint4 R1 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t0 + 1, 16 * gid));
+      const uint4 R2 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t2, 16 * gid));
+      const uint4 R3 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t2 + 1, 16 * gid));
+      const uint32_t w0[4] = {R0.x, R0.y, R0.z, R0.w}, w1[4] = {R1.x, R1.y, R1.z, R1.w};
+      const uint32_t w2[4] = {R2.x, R2.y, R2.z, R2.w}, w3[4] = {R3.x, R3.y, R3.z, R3.w};
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+        const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
+        a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
+        a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
+        a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
+        mma16816<false>(st.acc[mt], a, pb0, pb1);
+      }
+    } else {
+      const uint2 R0 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t0, 8 * gid));
+      const uint2 R1 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t0 + 1, 8 * gid));
+      const uint2 R2 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t2, 8 * gid));
+      const uint2 R3 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t2 + 1, 8 * gid));
+      const uint32_t w0[2] = {R0.x, R0.y}, w1[2] = {R1.x, R1.y};
+      const uint32_t w2[2] = {R2.x, R2.y}, w3[2] = {R3.x, R3.y};
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+        const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
+        a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
+        a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
+        a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
+        mma16816<false>(st.acc[mt], a, pb0, pb1);
+      }
+    }
+  } else {
+    if constexpr (kBF) {
+      pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+    } else {
+      pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+      pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+    }
+    const int r = lane & 7, mi = lane >> 3;
+    const int vtok = r + ((mi >> 1) << 3), vhi = mi & 1;
+#pragma unroll
+    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+      uint32_t a[4];
+      ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
+      mma16816<kBF>(st.acc[mt], a, pb0, pb1);
+    }
+  }
+}
+
+// Head-dim index held by accumulator row group `r` (0: gid, 1: gid + 8) of m-tile mt.
+template <class Cfg>
+__device__ __forceinline__ int mma_dim(int mt, int r, int gid) {
+  if constexpr (Cfg::FP8)
+    return gid * (Cfg::D / 8) + 2 * mt + r;
+  else
+    return 16 * mt + gid + 8 * r;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_finish(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                           int w, int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+  float l0 = st.l0, l1 = st.l1;
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, off);
+    l1 += __shfl_xor_sync(kFull, l1, off);
+  }
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+  const int h = m.hu / p.NC, c = m.hu % p.NC;
+  const int head0 = h * p.G + c * Cfg::GC;
+  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  const int hA = 2 * tig, hB = 2 * tig + 1;
+  if (m.flags & kComplete) {
+    const size_t baseA = ((size_t)m.b * p.Hq + head0 + hA) * Cfg::D;
+    const size_t baseB = baseA + Cfg::D;
+#pragma unroll
+    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int d = mma_dim<Cfg>(mt, r, gid);
+        if (hA < gc) store_scalar(typename Cfg::Q{}, p.out, baseA + d, st.acc[mt][2 * r] * inv0);
+        if (hB < gc) store_scalar(typename Cfg::Q{}, p.out, baseB + d, st.acc[mt][2 * r + 1] * inv1);
+      }
+  } else {
+    const int slot = (m.flags & kWFirst) ? 0 : 1;
+    const size_t base = ((size_t)w * 2 + slot) * kChunkMax;
+    float *oA = p.part_o + (base + hA) * Cfg::D;
+    float *oB = p.part_o + (base + hB) * Cfg::D;
+#pragma unroll
+    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int d = mma_dim<Cfg>(mt, r, gid);
+        if (hA < gc) oA[d] = st.acc[mt][2 * r] * inv0;
+        if (hB < gc) oB[d] = st.acc[mt][2 * r + 1] * inv1;
+      }
+    if (gid == 0) {
+      if (hA < gc) p.part_lse[base + hA] = st.m0 + log2f(l0);
+      if (hB < gc) p.part_lse[base + hB] = st.m1 + log2f(l1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core path state and steps (GC in {1, 2}).
+// ---------------------------------------------------------------------------
+template <class Cfg>
+struct SimtState {
+  static constexpr int DPL = Cfg::D / 32;  // head-dim elements per lane in p.V
+  float acc[Cfg::GC][DPL];
+  float m[Cfg::GC], l[Cfg::GC];
+};
+
+// 16 bytes of cache elements -> floats
+template <class T>
+__device__ __forceinline__ void cvt16(T, const uint4 &raw, float *f);
+template <>
+__device__ __forceinline__ void cvt16(F32, const uint4 &raw, float *f) {
+  f[0] = __uint_as_float(raw.x); f[1] = __uint_as_float(raw.y);
+  f[2] = __uint_as_float(raw.z); f[3] = __uint_as_float(raw.w);
+}
+template <>
+__device__ __forceinline__ void cvt16(F16, const uint4 &raw, float *f) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { const float2 v = unpack2(F16{}, w[i]); f[2 * i] = v.x; f[2 * i + 1] = v.y; }
+}
+template <>
+__device__ __forceinline__ void cvt16(BF16, const uint4 &raw, float *f) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { const float2 v = unpack2(BF16{}, w[i]); f[2 * i] = v.x; f[2 * i + 1] = v.y; }
+}
+template <>
+__device__ __forceinline__ void cvt16(E4M3, const uint4 &raw, float *f) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = unpack2_e4m3((uint16_t)(w[i] & 0xffff));
+    const float2 b = unpack2_e4m3((uint16_t)(w[i] >> 16));
+    f[4 * i] = a.x; f[4 * i + 1] = a.y; f[4 * i + 2] = b.x; f[4 * i + 3] = b.y;
+  }
+}
+
+// DPL elements of one V row owned by a lane -> floats
+template <class Cfg>
+__device__ __forceinline__ void load_vrow(uint32_t addr, float *f) {
+  using T = typename Cfg::Cache;
+  constexpr int DPL = SimtState<Cfg>::DPL;
+  constexpr int BYTES = DPL * T::kBytes;
+  if constexpr (BYTES == 16) {
+    cvt16(T{}, lds128(addr), f);
+  } else if constexpr (BYTES == 8) {
+    const uint2 v = lds64(addr);
+    if constexpr (T::kCode == PKV_F32) {
+      f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    } else {
+      const float2 a = unpack2(T{}, v.x), b = unpack2(T{}, v.y);
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+  } else if constexpr (BYTES == 4) {
+    const uint32_t v = lds32(addr);
+    if constexpr (T::kCode == PKV_FP8_E4M3) {
+      const float2 a = unpack2_e4m3((uint16_t)(v & 0xffff)), b = unpack2_e4m3((uint16_t)(v >> 16));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+      const float2 a = unpack2(T{}, v);
+      f[0] = a.x; f[1] = a.y;
+    }
+  } else {  // 2 bytes: two e4m3 values
+    const float2 a = unpack2_e4m3((uint16_t)lds16(addr));
+    f[0] = a.x; f[1] = a.y;
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void simt_begin(SimtState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                           float *qbuf, int lane) {
+  const int h = m.hu / p.NC, c = m.hu % p.NC;
+  const int head0 = h * p.G + c * Cfg::GC;
+  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  __syncwarp();
+  for (int idx = lane; idx < Cfg::GC * Cfg::D; idx += 32) {
+    const int g = idx / Cfg::D, d = idx % Cfg::D;
+    qbuf[idx] = g < gc ? load_scalar(typename Cfg::Q{}, p.q, ((size_t)m.b * p.Hq + head0 + g) * Cfg::D + d) : 0.f;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < Cfg::GC; ++g) {
+    st.m[g] = -INFINITY;
+    st.l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < SimtState<Cfg>::DPL; ++e) st.acc[g][e] = 0.f;
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void simt_block(SimtState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                           uint8_t *tk, uint8_t *tv, const float *qbuf, int lane) {
+  using T = typename Cfg::Cache;
+  constexpr int GC = Cfg::GC, D = Cfg::D, ROWB = Cfg::ROWB;
+  constexpr int HB = ROWB / 2;            // bytes of half a row
+  constexpr int EPC = 16 / T::kBytes;     // elements per 16-byte chunk
+  constexpr int DPL = SimtState<Cfg>::DPL;
+  const uint32_t kb = smem_u32(tk), vb = smem_u32(tv);
+  const int t = lane & 15, half = lane >> 4;
+  const int nvalid = m.nvalid;
+
+  // scores: lane (t, half) dots token t with half of q, then the halves add
+  float part[GC];
+#pragma unroll
+  for (int g = 0; g < GC; ++g) part[g] = 0.f;
+#pragma unroll
+  for (int i = 0; i < HB / 16; ++i) {
+    float kf[EPC];
+    cvt16(T{}, lds128(kb + tile_off<ROWB>(t, half * HB + 16 * i)), kf);
+    const float *qp = qbuf + half * (D / 2) + i * EPC;
+#pragma unroll
+    for (int g = 0; g < GC; ++g)
+#pragma unroll
+      for (int e = 0; e < EPC; e += 4) {
+        const float4 qv = *reinterpret_cast<const float4 *>(qp + g * D + e);
+        part[g] = fmaf(qv.x, kf[e], part[g]);
+        part[g] = fmaf(qv.y, kf[e + 1], part[g]);
+        part[g] = fmaf(qv.z, kf[e + 2], part[g]);
+        part[g] = fmaf(qv.w, kf[e + 3], part[g]);
+      }
+  }
+  const float sc = p.scale_log2 * m.ks;
+  float pw[GC];
+#pragma unroll
+  for (int g = 0; g < GC; ++g) {
+    float x = part[g] + __shfl_xor_sync(kFull, part[g], 16);
+    x = (t < nvalid) ? x * sc : -INFINITY;
+    float bm = x;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
+    const float mn = fmaxf(st.m[g], bm);
+    const float al = exp2f(st.m[g] - mn);
+    const float pg = exp2f(x - mn);
+    float bs = pg;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) bs += __shfl_xor_sync(kFull, bs, off);
+    st.l[g] = st.l[g] * al + bs;
+    st.m[g] = mn;
+    pw[g] = pg * m.vs;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) st.acc[g][e] *= al;
+  }
+  // p.V: lane owns head-dim elements [lane*DPL, lane*DPL + DPL)
+  const uint32_t vcol = lane * DPL * T::kBytes;
+  for (int tt = 0; tt < nvalid; ++tt) {
+    float vf[DPL];
+    load_vrow<Cfg>(vb + tile_off<ROWB>(tt, vcol), vf);
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+      const float pt = __shfl_sync(kFull, pw[g], tt);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) st.acc[g][e] = fmaf(pt, vf[e], st.acc[g][e]);
+    }
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                            int w, int lane) {
+  constexpr int DPL = SimtState<Cfg>::DPL;
+  const int h = m.hu / p.NC, c = m.hu % p.NC;
+  const int head0 = h * p.G + c * Cfg::GC;
+  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  if (m.flags & kComplete) {
+#pragma unroll
+    for (int g = 0; g < Cfg::GC; ++g) {
+      if (g >= gc) break;
+      const float inv = 1.f / st.l[g];
+      const size_t base = ((size_t)m.b * p.Hq + head0 + g) * Cfg::D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) store_scalar(typename Cfg::Q{}, p.out, base + e, st.acc[g][e] * inv);
+    }
+  } else {
+    const int slot = (m.flags & kWFirst) ? 0 : 1;
+    const size_t base = ((size_t)w * 2 + slot) * kChunkMax;
+#pragma unroll
+    for (int g = 0; g < Cfg::GC; ++g) {
+      if (g >= gc) break;
+      const float inv = 1.f / st.l[g];
+      float *o = p.part_o + (base + g) * Cfg::D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[e] = st.acc[g][e] * inv;
+      if (lane == 0) p.part_lse[base + g] = st.m[g] + log2f(st.l[g]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::WARPS * 32)
+    decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  uint8_t *tiles = smem + (size_t)wib * Cfg::STAGES * 2 * Cfg::TILE;
+  StageMeta *meta = reinterpret_cast<StageMeta *>(smem + Cfg::TILES_BYTES) + wib * Cfg::STAGES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES) + wib * Cfg::STAGES;
+  float *qbuf = reinterpret_cast<float *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES + Cfg::BAR_BYTES) +
+                wib * Cfg::GC * Cfg::D;
+  if (lane == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  __syncwarp();
+  grid_dep_wait();  // the plan kernel's outputs are visible from here on
+
+  const int w = blockIdx.x * Cfg::WARPS + wib;
+  if (w < p.P) {
+    const int4 st0 = p.starts[w];
+    const int e = p.starts[w + 1].x;
+    const int total = e - st0.x;
+    if (total > 0) {
+      Producer pr;
+      pr.pi = st0.x;
+      pr.e = e;
+      pr.s = st0.x;
+      pr.b = st0.y;
+      pr.hu = st0.z;
+      pr.j = st0.w;
+      pr.seg_j0 = 0;
+      pr.seg_wfirst = 0;
+      pr.win_b = -1;
+      pr.win_hu = -1;
+      pr.win_j0 = 0;
+      pr.win_id = 0;
+      pr.win_ks = pr.win_vs = 0.f;
+      load_seq(pr, p);
+      int issued = 0;
+      for (; issued < Cfg::STAGES && issued < total; ++issued)
+        produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, issued, lane);
+
+      typename std::conditional<Cfg::MMA, MmaState<Cfg>, SimtState<Cfg>>::type state;
+      for (int i = 0; i < total; ++i) {
+        const int stage = i % Cfg::STAGES;
+        const uint32_t parity = (uint32_t)(i / Cfg::STAGES) & 1u;
+        if (!mbar_wait_bounded(&bars[stage], parity, p.timeout_ns)) {
+          if (lane == 0) atomicOr(&p.hdr->status, PKV_FLAG_TIMEOUT);
+          // let the copies still in flight land before the CTA's memory goes away
+          for (int k = i; k < issued; ++k)
+            mbar_wait_bounded(&bars[k % Cfg::STAGES], (uint32_t)(k / Cfg::STAGES) & 1u, p.timeout_ns);
+          break;
+        }
+        const StageMeta m = meta[stage];
+        uint8_t *tk = tiles + (size_t)stage * 2 * Cfg::TILE;
+        uint8_t *tv = tk + Cfg::TILE;
+        if constexpr (Cfg::MMA) {
+          if (m.flags & kFirst) mma_begin<Cfg>(state, p, m, lane);
+          mma_block<Cfg>(state, p, m, tk, tv, lane);
+        } else {
+          if (m.flags & kFirst) simt_begin<Cfg>(state, p, m, qbuf, lane);
+          simt_block<Cfg>(state, p, m, tk, tv, qbuf, lane);
+        }
+        if (issued < total) {
+          produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane);
+          ++issued;
+        }
+        if (m.flags & kLast) {
+          if constexpr (Cfg::MMA)
+            mma_finish<Cfg>(state, p, m, w, lane);
+          else
+            simt_finish<Cfg>(state, p, m, w, lane);
+        }
+      }
+    }
+  }
+  grid_dep_launch();
+}
+
+template <class Cfg>
+DecodeKernel decode_entry() {
+  DecodeKernel k;
+  k.fn = reinterpret_cast<const void *>(&decode_kernel<Cfg>);
+  k.mma = Cfg::MMA ? 1 : 0;
+  k.cache_dtype = Cfg::Cache::kCode;
+  k.q_dtype = Cfg::Q::kCode;
+  k.D = Cfg::D;
+  k.GC = Cfg::GC;
+  k.warps = Cfg::WARPS;
+  k.stages = Cfg::STAGES;
+  k.smem_bytes = Cfg::SMEM;
+  return k;
+}
+
+constexpr int kWarps = 4;
+constexpr int kBudget = 24 * 1024;  // shared-memory pipeline bytes per warp
+
+}  // namespace pkv

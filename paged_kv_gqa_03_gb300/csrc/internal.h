@@ -1,0 +1,90 @@
+// internal.h — declarations shared by the C-ABI layer (api.cpp) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlock = 16;      // tokens per physical block (PKV_BLOCK_SIZE)
+constexpr int kChunkMax = 8;    // most query heads one work unit serves
+
+// Workspace header written by the plan kernel each call.
+struct WsHeader {
+  int32_t status;   // PKV_FLAG_* bits
+  int32_t P;        // partitions (warp workers)
+  int32_t W;        // total (unit, block) work items
+  int32_t B;
+  int32_t HU;       // units per sequence = Hkv * NC
+  int32_t pad[59];  // 256 bytes
+};
+
+// Per stage of a warp's pipeline: what the producer issued into it.
+struct StageMeta {
+  int32_t b, hu, j, nvalid;
+  float ks, vs;
+  int32_t flags;
+  int32_t pad;
+};
+enum : int32_t {
+  kFirst = 1,     // first block of a segment: reset state, load q
+  kLast = 2,      // last block of a segment: finalise
+  kComplete = 4,  // the segment is the whole unit: write the output directly
+  kWFirst = 8,    // the segment is its worker's first (partial slot 0, else 1)
+};
+
+struct DecodeParams {
+  void *out;
+  const void *q;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_table;
+  const int32_t *context_lens;
+  WsHeader *hdr;
+  int32_t *prefix;      // [B+1] exclusive prefix of blocks per sequence
+  int4 *starts;         // [P+1] {s, b, hu, j} of each worker's first item
+  float *part_o;        // [P][2][kChunkMax][D]
+  float *part_lse;      // [P][2][kChunkMax], log2 domain
+  int64_t num_blocks;
+  int B, Hq, Hkv, D, G, GC, NC, HU, P;
+  int max_blocks;
+  int out_dtype;
+  float scale_log2;     // softmax scale * log2(e)
+  uint64_t timeout_ns;
+};
+
+struct WsLayout {
+  size_t hdr, prefix, starts, part_o, part_lse, total;
+};
+WsLayout ws_layout(int B, int P, int D);
+
+// One compiled decode kernel variant.
+struct DecodeKernel {
+  const void *fn;       // __global__ void (DecodeParams, CUtensorMap, CUtensorMap)
+  int mma;              // 1 = tensor-core (mma.sync) path, 0 = CUDA-core path
+  int cache_dtype, q_dtype, D, GC;
+  int warps, stages;
+  size_t smem_bytes;
+};
+// Appends the variants a translation unit compiled; returns how many.
+int register_decode_bf16(DecodeKernel *out);
+int register_decode_f16(DecodeKernel *out);
+int register_decode_fp8(DecodeKernel *out);
+int register_decode_f32(DecodeKernel *out);
+
+cudaError_t launch_plan(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_splitk_merge(const DecodeParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_merge(void *out, int out_dtype, const float *o_partial, const float *lse,
+                         int B, int Hq, int D, int S, cudaStream_t stream);
+cudaError_t launch_append(const void *k_new, const void *v_new, int new_dtype, void *k_cache,
+                          void *v_cache, int cache_dtype, float *k_scale, float *v_scale,
+                          const int64_t *slot_mapping, int B, int Hkv, int D, int64_t num_blocks,
+                          cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
+                               float *v_scale, const int32_t *pairs, int n_pairs, int Hkv, int D,
+                               int64_t num_blocks, cudaStream_t stream);
+
+}  // namespace pkv
