@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller profiling cases)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -198,7 +200,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import workloads
-    w = workloads.config(args.workload)
+    w = _workload(args)
     budget = min(3.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample_rate(w, budget / 4)
@@ -227,6 +229,13 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _workload(args):
+    import workloads
+    if args.batch:
+        return workloads.config(args.workload, B=args.batch)
+    return workloads.config(args.workload)
+
+
 def _config(w):
     return {"workload": w.name, "index": w.seed - 1000, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
             "D": w.D, "kv_dtype": w.dtype, "q_dtype": w.q_dtype, "block_size": 16,
@@ -251,7 +260,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
            "fp8_e4m3": torch.float8_e4m3fn}
-    w = workloads.config(args.workload)
+    w = _workload(args)
     stream = torch.cuda.Stream(dev)
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
