@@ -163,6 +163,43 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
                            pkv_stream_t stream);
 
 /*
+ * paged_decode_attention for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers of
+ * this library.  Some of them cannot hand over a workspace: a plain C host
+ * program without a device allocator of its own, a plugin or custom operator
+ * whose host framework owns all device memory and offers no scratch, or a
+ * serving loop that must not call cudaMalloc once running (it can synchronise
+ * the device and can fail under a fixed memory budget).
+ *
+ * Same operation, arguments, layouts and results as paged_decode_attention,
+ * without `workspace` / `workspace_bytes`: the scratch comes from one array of
+ * PKV_STATIC_SCRATCH_BYTES bytes that the library keeps in device memory on
+ * every GPU that loads it, until the process exits.
+ *  - Limit: a shape whose paged_decode_workspace_bytes() exceeds
+ *    PKV_STATIC_SCRATCH_BYTES is rejected with PKV_EWORKSPACE before anything
+ *    runs (16 MiB holds D = 128 with ~2000 partitions, more than one per
+ *    resident warp of a GB300).
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *    first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's contents.  Nothing in it has to start at zero (each call writes
+ *    what it later reads), so it is never cleared.  Calls that overlap on the
+ *    GPU (several streams or host threads) race on the array: serialise them.
+ *  - paged_decode_status() does not apply (there is no workspace to pass).
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+int paged_decode_attention_static(void *out, const void *q, int q_dtype,
+                                  const void *k_cache, const void *v_cache, int cache_dtype,
+                                  const float *k_scale, const float *v_scale,
+                                  const int32_t *block_table, int max_blocks_per_seq,
+                                  const int32_t *context_lens,
+                                  int B, int Hq, int Hkv, int D, int64_t num_blocks,
+                                  float scale, int num_splits,
+                                  pkv_stream_t stream);
+
+/*
  * Synchronises `stream` and reads the status bits (PKV_FLAG_*) that the last
  * paged_decode_attention on `workspace` recorded.  Returns PKV_ETIMEOUT if
  * PKV_FLAG_TIMEOUT is set, PKV_ERANGE if a range flag is set, else PKV_OK;

@@ -24,6 +24,8 @@ static int cuda_status(cudaError_t e) {
   return PKV_ECUDA;
 }
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 WsLayout ws_layout(int B, int P, int D) {

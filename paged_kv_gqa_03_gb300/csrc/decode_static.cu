@@ -1,0 +1,75 @@
+// decode_static.cu — paged_decode_attention_static, the decode entry point for
+// callers that have no way to hand the library a device workspace.
+//
+// paged_decode_attention needs scratch memory (the partition plan, the
+// per-partition partial outputs and the status word) and asks its caller for
+// it.  Some callers cannot provide that: a plain C host program with no device
+// allocator of its own, a plugin or custom operator whose host framework owns
+// every byte of device memory and offers no scratch, or a serving loop that
+// must not call cudaMalloc once it is running (cudaMalloc can synchronise the
+// device and may fail under a fixed memory budget).  For them this file keeps
+// one fixed-size scratch array in the library's own device memory and runs the
+// ordinary entry point on it.  Nothing here allocates.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "pagedkv.h"
+
+namespace {
+
+// The scratch every call on a device shares.  Each GPU that loads the library
+// holds it until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name only stands in for the symbol; the address a kernel may use
+// comes from cudaGetSymbolAddress, looked up once per device.
+int scratch_on_current_device(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    pkv::record_cuda_error(e);
+    return PKV_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return PKV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      pkv::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+      return PKV_ECUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_decode_attention_static(void *out, const void *q, int q_dtype, const void *k_cache,
+                                             const void *v_cache, int cache_dtype, const float *k_scale,
+                                             const float *v_scale, const int32_t *block_table,
+                                             int max_blocks_per_seq, const int32_t *context_lens, int B,
+                                             int Hq, int Hkv, int D, int64_t num_blocks, float scale,
+                                             int num_splits, pkv_stream_t stream) {
+  size_t need = 0;
+  int rc = paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits, &need);
+  if (rc != PKV_OK) return rc;
+  if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_EWORKSPACE;  // beyond the fixed capacity
+  void *scratch = nullptr;
+  rc = scratch_on_current_device(&scratch);
+  if (rc != PKV_OK) return rc;
+  // Every byte the attention reads from its workspace is written earlier in the
+  // same call, so the scratch needs no clearing between calls.
+  return paged_decode_attention(out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale, block_table,
+                                max_blocks_per_seq, context_lens, B, Hq, Hkv, D, num_blocks, scale, num_splits,
+                                scratch, (size_t)PKV_STATIC_SCRATCH_BYTES, stream);
+}

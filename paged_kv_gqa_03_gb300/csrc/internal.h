@@ -56,6 +56,9 @@ struct DecodeParams {
   uint64_t timeout_ns;
 };
 
+// Records a CUDA error for pkv_last_cuda_error() on the calling thread.
+void record_cuda_error(cudaError_t e);
+
 struct WsLayout {
   size_t hdr, prefix, starts, part_o, part_lse, total;
 };
