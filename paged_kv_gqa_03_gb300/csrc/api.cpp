@@ -179,19 +179,35 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
     const char *v = std::getenv("PKV_FORCE_SIMT");
     return v && v[0] == '1';
   }();
+  // PKV_DECODE_WARPS / PKV_DECODE_STAGES pick an alternative pipeline shape
+  // where one is compiled (tuning runs); otherwise the first match is used.
+  static const int want_warps = [] {
+    const char *v = std::getenv("PKV_DECODE_WARPS");
+    return v ? std::atoi(v) : 0;
+  }();
+  static const int want_stages = [] {
+    const char *v = std::getenv("PKV_DECODE_STAGES");
+    return v ? std::atoi(v) : 0;
+  }();
   const bool mma = cache_dtype != PKV_F32 && G >= 3 && !force_simt;
   const int GC = mma ? 8 : (G >= 2 ? 2 : 1);
   Registry &r = registry();
+  int first = -1;
   for (int i = 0; i < r.n; ++i) {
     const DecodeKernel &k = r.k[i];
     if (k.mma == (mma ? 1 : 0) && k.cache_dtype == cache_dtype && k.q_dtype == q_dtype && k.D == D && k.GC == GC) {
-      c->ki = i;
-      c->GC = GC;
-      c->NC = (G + GC - 1) / GC;
-      return PKV_OK;
+      if (first < 0) first = i;
+      if ((want_warps == 0 || k.warps == want_warps) && (want_stages == 0 || k.stages == want_stages)) {
+        first = i;
+        break;
+      }
     }
   }
-  return PKV_EUNSUPPORTED;
+  if (first < 0) return PKV_EUNSUPPORTED;
+  c->ki = first;
+  c->GC = GC;
+  c->NC = (G + GC - 1) / GC;
+  return PKV_OK;
 }
 
 int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int Hq, int Hkv, int D, int64_t num_blocks,

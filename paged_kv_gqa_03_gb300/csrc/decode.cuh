@@ -9,7 +9,11 @@
 // warp streams its range block by block, carrying the online-softmax state
 // across blocks of a unit ("LLM推理优化实战" §3.2 online softmax: running max
 // m, running sum l, accumulator rescaled by exp(m_old - m_new)); a unit cut by
-// a range boundary leaves normalised (o, lse) partials for the merge kernel.
+// a range boundary leaves normalised (o, lse) partials that the merge kernel
+// combines (log-sum-exp rule).  (Letting the last warp of each split unit merge
+// it inside this kernel measured ~2 % slower on GB300: a unit's last partial
+// always lands at the end of some warp's range, so the fused merge only moved
+// serial work into the kernel's tail.)
 //
 // Data movement.  Each warp owns a ring of STAGES shared-memory slots; lane 0
 // issues 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of the block's
@@ -52,6 +56,10 @@ struct DecodeCfg {
   static constexpr size_t BAR_BYTES = (size_t)WARPS * STAGES * 8;
   static constexpr size_t QBUF_BYTES = MMA ? 0 : (size_t)WARPS * GC * D * 4;
   static constexpr size_t SMEM = 1024 + TILES_BYTES + META_BYTES + BAR_BYTES + QBUF_BYTES;
+  // CTAs that fit in an SM's 228 KiB of shared memory (1 KiB reserved per CTA);
+  // passed to __launch_bounds__ so registers never limit residency further
+  static constexpr int CTAS_RAW = (int)(233472 / (SMEM + 1024));
+  static constexpr int MIN_CTAS = CTAS_RAW < 1 ? 1 : (CTAS_RAW > 8 ? 8 : CTAS_RAW);
   static_assert(TILE % 1024 == 0, "tiles must keep 1024-byte alignment for the swizzle");
   static_assert(!MMA || GC == 8, "the MMA path serves 8-head chunks");
   static_assert(D == 64 || D == 128, "head dim");
@@ -65,6 +73,7 @@ struct Producer {
   int b, hu, j, n, ctx;  // unit and block of item pi; blocks and length of sequence b
   int seg_j0, seg_wfirst;
   int win_b, win_hu, win_j0, win_id;  // lane-parallel window of 32 block-table entries
+  int nxt_id;                         // the unit's next window, loaded one window ahead
   float win_ks, win_vs;
 };
 
@@ -82,14 +91,21 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
   __syncwarp();
   const int h = pr.hu / p.NC;
   if (!(pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j >= pr.win_j0 && pr.j < pr.win_j0 + 32)) {
+    const int32_t *row = p.block_table + (size_t)pr.b * p.max_blocks;
+    if (pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j == pr.win_j0 + 32) {
+      pr.win_id = pr.nxt_id;  // the window loaded ahead
+    } else {
+      const int jj = pr.j + lane;
+      pr.win_id = jj < pr.n ? __ldg(row + jj) : 0;
+    }
     pr.win_b = pr.b;
     pr.win_hu = pr.hu;
     pr.win_j0 = pr.j;
-    const int jj = pr.j + lane;
-    int id = 0;
-    if (jj < pr.n) id = __ldg(p.block_table + (size_t)pr.b * p.max_blocks + jj);
-    pr.win_id = id;
+    // load the following window now; it is first needed 32 blocks later
+    const int jn = pr.j + 32 + lane;
+    pr.nxt_id = jn < pr.n ? __ldg(row + jn) : 0;
     if constexpr (Cfg::FP8) {
+      const int jj = pr.j + lane, id = pr.win_id;
       float ks = 0.f, vs = 0.f;
       if (jj < pr.n && id >= 0 && (int64_t)id < p.num_blocks) {
         ks = __ldg(p.k_scale + (size_t)id * p.Hkv + h);
@@ -132,7 +148,8 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     m.flags = flags;
     m.pad = 0;
     meta[stage] = m;
-    fence_proxy_async();
+    // the warp's reads of this stage have completed (their results were
+    // consumed), so the TMA overwrite needs no proxy fence here
     mbar_arrive_expect_tx(&bars[stage], 2 * Cfg::TILE);
     uint8_t *dk = tiles + (size_t)stage * 2 * Cfg::TILE;
     uint8_t *dv = dk + Cfg::TILE;
@@ -240,6 +257,7 @@ __device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams 
   // ---- scores S^T = K . Q^T (16 tokens x 8 heads) ----
   float s[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (Cfg::FP8) {
+    float s1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain: odd k-steps
 #pragma unroll
     for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
       const uint32_t w0 = lds32(kb + tile_off<ROWB>(gid, 16 * ks + 4 * tig));
@@ -249,17 +267,28 @@ __device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams 
       a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff));
       a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
       a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
-      mma16816<false>(s, a, st.qb[ks][0], st.qb[ks][1]);
+      if (ks & 1)
+        mma16816<false>(s1, a, st.qb[ks][0], st.qb[ks][1]);
+      else
+        mma16816<false>(s, a, st.qb[ks][0], st.qb[ks][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += s1[i];
   } else {
     const int r = lane & 7, mi = lane >> 3;
     const int krow = r + ((mi & 1) << 3), khi = mi >> 1;
+    float s1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain: odd k-steps
 #pragma unroll
     for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(kb + tile_off<ROWB>(krow, (2 * ks + khi) * 16), a);
-      mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
+      if (ks & 1)
+        mma16816<kBF>(s1, a, st.qb[ks][0], st.qb[ks][1]);
+      else
+        mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += s1[i];
   }
 
   // ---- online softmax over the block (log2 domain) ----
@@ -605,11 +634,13 @@ __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodePara
 // The kernel.
 // ---------------------------------------------------------------------------
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::WARPS * 32)
+__global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment for the 128-byte swizzle, by pointer arithmetic on the
+  // shared array so every access stays a shared-memory access
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   uint8_t *tiles = smem + (size_t)wib * Cfg::STAGES * 2 * Cfg::TILE;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + Cfg::TILES_BYTES) + wib * Cfg::STAGES;
@@ -704,7 +735,10 @@ DecodeKernel decode_entry() {
   return k;
 }
 
-constexpr int kWarps = 4;
-constexpr int kBudget = 24 * 1024;  // shared-memory pipeline bytes per warp
+// Default pipeline shape: 5 warps per CTA, 16 KiB of stages per warp (two
+// bf16 D=128 blocks), two CTAs per SM — the fastest of the shapes measured on
+// GB300 for the GQA-8 layer (10 warps x 2 stages beat 8 x 3, 12 x 2 and 4 x 6).
+constexpr int kWarps = 5;
+constexpr int kBudget = 16 * 1024;  // shared-memory pipeline bytes per warp
 
 }  // namespace pkv

@@ -18,8 +18,11 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // Plan: prefix[b] = sum_{b' < b} ceil(ctx_b' / 16); W = HU * prefix[B];
 // partition w starts at item floor(w * W / P), decoded into (b, hu, j).
-// One CTA; context lengths are clamped to [0, 16 * max_blocks] (flagged).
+// Also writes the (zero) output of sequences with nothing to attend.  One CTA; context
+// lengths are clamped to [0, 16 * max_blocks] (flagged).
 // ---------------------------------------------------------------------------
+constexpr int kPlanSmemInts = 8192;  // prefix entries kept in shared memory (32 KiB)
+
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   grid_dep_launch();  // the decode kernel may start its prologue now
   __shared__ int32_t warp_tot[32];
@@ -57,7 +60,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     }
     __syncthreads();
     const int excl = carry + warp_tot[wid] + x - n;
-    if (b < p.B) p.prefix[b] = excl;
+    if (b < p.B) {
+      p.prefix[b] = excl;
+      if (n == 0)
+        for (size_t i = 0; i < (size_t)p.Hq * p.D; ++i) store_out(p.out_dtype, p.out, (size_t)b * p.Hq * p.D + i, 0.f);
+    }
     __syncthreads();
     if (tid == blockDim.x - 1) carry = excl + n;
     __syncthreads();
@@ -76,6 +83,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     p.hdr->B = p.B;
     p.hdr->HU = p.HU;
   }
+  // the binary searches read the prefix from shared memory when it fits
+  extern __shared__ int32_t s_prefix[];
+  const bool in_smem = p.B + 1 <= kPlanSmemInts;
+  if (in_smem) {
+    for (int b = tid; b <= p.B; b += blockDim.x) s_prefix[b] = p.prefix[b];
+    __syncthreads();
+  }
+  const int32_t *pre = in_smem ? s_prefix : p.prefix;
   for (int w = tid; w <= p.P; w += blockDim.x) {
     const int64_t s = W * w / p.P;
     int4 r;
@@ -85,13 +100,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       int lo = 0, hi = p.B - 1;  // largest b with HU * prefix[b] <= s
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)p.HU * p.prefix[mid] <= s)
+        if ((int64_t)p.HU * pre[mid] <= s)
           lo = mid;
         else
           hi = mid - 1;
       }
-      const int n = p.prefix[lo + 1] - p.prefix[lo];
-      const int64_t rr = s - (int64_t)p.HU * p.prefix[lo];
+      const int n = pre[lo + 1] - pre[lo];
+      const int64_t rr = s - (int64_t)p.HU * pre[lo];
       r = make_int4((int)s, lo, (int)(rr / n), (int)(rr % n));
     }
     p.starts[w] = r;
@@ -99,56 +114,110 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
 }
 
 cudaError_t launch_plan(const DecodeParams &p, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  const size_t smem = p.B + 1 <= kPlanSmemInts ? sizeof(int32_t) * (size_t)(p.B + 1) : 0;
+  plan_kernel<<<1, 1024, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Merge of the partials of units that a partition boundary cut.  One CTA per
-// unit; a unit processed whole by one warp was already written.  Units of
-// empty sequences are written as zeros here.
+// Merge kernel for the partials of units that a partition boundary cut (a8),
+// launched behind the decode kernel with programmatic dependent launch.  One
+// CTA per unit; a unit processed whole by one warp was already written.  Partition w covers
+// items [floor(w W / P), floor((w+1) W / P)) — the plan kernel's rule,
+// recomputed.  Segments are taken in chunks whose LSEs are staged in shared
+// memory; each thread keeps an online max / sum for its head and accumulates
+// 4 head-dim elements of every partial with one 16-byte load.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 v) {
+  if (dtype == PKV_F32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(p) + i) = v;
+  } else if (dtype == PKV_F16) {
+    const uint32_t lo = pack_f16x2(v.x, v.y), hi = pack_f16x2(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(p) + i) = make_uint2(lo, hi);
+  } else {
+    const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p) + i) = make_uint2(lo, hi);
+  }
+}
+
 __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p) {
+  constexpr int kSegChunk = 32;
+  constexpr int kVecPerThread = kChunkMax * 128 / 4 / 128;  // float4s per thread (D <= 128)
+  __shared__ float s_lse[kSegChunk][kChunkMax];
+  __shared__ int32_t s_base[kSegChunk];
   grid_dep_wait();
   const int u = blockIdx.x;
   const int b = u / p.HU, hu = u % p.HU;
   const int h = hu / p.NC, c = hu % p.NC;
   const int head0 = h * p.G + c * p.GC;
   const int gc = min(p.GC, p.G - c * p.GC);
+  const int D = p.D;
   const int pb = p.prefix[b];
   const int n = p.prefix[b + 1] - pb;
-  if (n == 0) {
-    for (int idx = threadIdx.x; idx < gc * p.D; idx += blockDim.x)
-      store_out(p.out_dtype, p.out, ((size_t)b * p.Hq + head0) * p.D + idx, 0.f);
-    return;
-  }
+  const int nvec = gc * D / 4;
+  const size_t out0 = ((size_t)b * p.Hq + head0) * D;
+  if (n == 0) return;  // written by the plan kernel
   const int64_t W = (int64_t)p.HU * p.prefix[p.B];
   const int64_t a = (int64_t)p.HU * pb + (int64_t)hu * n, e = a + n;
   const int wf = (int)(((a + 1) * p.P - 1) / W);
   const int wl = (int)((e * p.P - 1) / W);
   if (wf == wl) return;
-  for (int idx = threadIdx.x; idx < gc * p.D; idx += blockDim.x) {
-    const int g = idx / p.D, d = idx % p.D;
-    float M = -INFINITY;
-    for (int w = wf; w <= wl; ++w) {
-      const int64_t sw = p.starts[w].x, ew = p.starts[w + 1].x;
-      if ((a > sw ? a : sw) < (e < ew ? e : ew)) {
-        const int slot = sw >= a ? 0 : 1;
-        M = fmaxf(M, p.part_lse[((size_t)w * 2 + slot) * kChunkMax + g]);
-      }
+
+  float4 acc[kVecPerThread];
+  float M[kVecPerThread], den[kVecPerThread];
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    M[k] = -INFINITY;
+    den[k] = 0.f;
+  }
+  for (int cs = wf; cs <= wl; cs += kSegChunk) {
+    const int ns = min(kSegChunk, wl - cs + 1);
+    __syncthreads();  // the previous chunk's staging has been consumed
+    for (int i = threadIdx.x; i < ns * kChunkMax; i += blockDim.x) {
+      const int sgi = i / kChunkMax, g = i % kChunkMax;
+      const int w = cs + sgi;
+      const int64_t sw = W * w / p.P, ew = W * (w + 1) / p.P;
+      const bool valid = (a > sw ? a : sw) < (e < ew ? e : ew);
+      const int slot = sw >= a ? 0 : 1;
+      const int32_t base = (int32_t)(((int64_t)w * 2 + slot) * kChunkMax);
+      if (g == 0) s_base[sgi] = base;
+      s_lse[sgi][g] = (valid && g < gc) ? p.part_lse[base + g] : -INFINITY;
     }
-    float num = 0.f, den = 0.f;
-    for (int w = wf; w <= wl; ++w) {
-      const int64_t sw = p.starts[w].x, ew = p.starts[w + 1].x;
-      if ((a > sw ? a : sw) < (e < ew ? e : ew)) {
-        const int slot = sw >= a ? 0 : 1;
-        const size_t base = ((size_t)w * 2 + slot) * kChunkMax + g;
-        const float wt = exp2f(p.part_lse[base] - M);
-        num = fmaf(wt, p.part_o[base * p.D + d], num);
-        den += wt;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kVecPerThread; ++k) {
+      const int v = threadIdx.x + k * blockDim.x;
+      if (v >= nvec) continue;
+      const int g = (4 * v) / D, d = (4 * v) % D;
+      float cm = -INFINITY;
+      for (int sgi = 0; sgi < ns; ++sgi) cm = fmaxf(cm, s_lse[sgi][g]);
+      if (cm == -INFINITY) continue;
+      const float mn = fmaxf(M[k], cm);
+      const float rescale = exp2f(M[k] - mn);
+      acc[k].x *= rescale; acc[k].y *= rescale; acc[k].z *= rescale; acc[k].w *= rescale;
+      den[k] *= rescale;
+      for (int sgi = 0; sgi < ns; ++sgi) {
+        const float l = s_lse[sgi][g];
+        if (l == -INFINITY) continue;
+        const float wt = exp2f(l - mn);
+        const float4 o = *reinterpret_cast<const float4 *>(p.part_o + ((size_t)s_base[sgi] + g) * D + d);
+        acc[k].x = fmaf(wt, o.x, acc[k].x);
+        acc[k].y = fmaf(wt, o.y, acc[k].y);
+        acc[k].z = fmaf(wt, o.z, acc[k].z);
+        acc[k].w = fmaf(wt, o.w, acc[k].w);
+        den[k] += wt;
       }
+      M[k] = mn;
     }
-    store_out(p.out_dtype, p.out, ((size_t)b * p.Hq + head0 + g) * p.D + d, num / den);
+  }
+#pragma unroll
+  for (int k = 0; k < kVecPerThread; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v >= nvec) continue;
+    const float inv = 1.f / den[k];
+    store4_out(p.out_dtype, p.out, out0 + 4 * (size_t)v,
+               make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
   }
 }
 

@@ -119,3 +119,43 @@ class DecodeStep:
     @property
     def workspace(self):
         return self._ws
+
+    # -- whole step as one CUDA graph ----------------------------------------
+    def capture(self, h_q, h_k_new, h_v_new, h_out):
+        """Captures one full step — host->device copies of q, k_new, v_new
+        (pinned host tensors) and of the bookkeeping last written by
+        prepare(), the append, the attention, and the device->host copy of the
+        output into h_out — as a CUDA graph; replay() runs it.  Re-capture
+        after prepare() when the copy pairs or buffer sets change."""
+        dev = self.device
+        self.g_q = torch.empty(h_q.shape, dtype=h_q.dtype, device=dev)
+        self.g_k = torch.empty(h_k_new.shape, dtype=h_k_new.dtype, device=dev)
+        self.g_v = torch.empty(h_v_new.shape, dtype=h_v_new.dtype, device=dev)
+        self.g_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=dev)
+        # one eager run first: kernels are configured and tensor maps encoded
+        self._graph_body(h_q, h_k_new, h_v_new, h_out)
+        self.stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=self.stream):
+            self._graph_body(h_q, h_k_new, h_v_new, h_out)
+        self.graph = graph
+        return graph
+
+    def _graph_body(self, h_q, h_k_new, h_v_new, h_out):
+        s = self.stream
+        with torch.cuda.stream(s):
+            self.g_q.copy_(h_q, non_blocking=True)
+            self.g_k.copy_(h_k_new, non_blocking=True)
+            self.g_v.copy_(h_v_new, non_blocking=True)
+            self.d_slots.copy_(self.h_slots, non_blocking=True)
+            self.d_table.copy_(self.h_table, non_blocking=True)
+            self.d_lens.copy_(self.h_lens, non_blocking=True)
+            if self.ncow:
+                self.d_pairs[:2 * self.ncow].copy_(self.h_pairs[:2 * self.ncow], non_blocking=True)
+        self.launch(self.g_q, self.g_k, self.g_v, self.g_out)
+        with torch.cuda.stream(s):
+            h_out.copy_(self.g_out, non_blocking=True)
+
+    def replay(self):
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()

@@ -255,3 +255,21 @@ def test_exported_merge_matches_oracle():
         ref = oracle.merge(o.double().reshape(B * Hq, S, D).numpy(),
                            lse.double().reshape(B * Hq, S).numpy()).reshape(B, Hq, D)
         compare(out, ref, "f32" if name == "f32" else "bf16", "merge")
+
+
+def test_captured_step_graph_matches_eager_step():
+    """A whole step captured as a CUDA graph (copies, append, attention, copy
+    back) gives the eager step's output bit for bit and the same caches."""
+    w = workloads.config(3, B=4, ctx=[700, 17, 33, 1500], free_frac=0.3, min_free=4)
+    step, out = run_gpu_step(w)
+    eager_out = out.cpu()
+    eager_k = step.k_cache.cpu()
+    hq, hk, hv = w.q.pin_memory(), w.k_new.pin_memory(), w.v_new.pin_memory()
+    hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    step.capture(hq, hk, hv, hout)
+    for _ in range(2):
+        hout.zero_()
+        step.replay()
+        step.stream.synchronize()
+        assert torch.equal(hout, eager_out)
+    assert torch.equal(step.k_cache.cpu(), eager_k)
