@@ -41,6 +41,8 @@ WsLayout ws_layout(int B, int P, int D) {
   o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax * D, 256);
   L.part_lse = o;
   o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax, 256);
+  L.cta_flags = o;
+  o = align_up(o + sizeof(int32_t) * (size_t)P, 256);
   L.total = o;
   return L;
 }
@@ -171,16 +173,21 @@ struct Choice {
   int NC;   // units per kv head
 };
 
-// Picks the kernel for a shape: tensor cores for groups of >= 3 heads on
-// 16-bit and fp8 caches, CUDA cores otherwise.  PKV_FORCE_SIMT=1 selects the
-// CUDA-core kernels for every cache dtype (comparison runs).
+// Picks the kernel for a shape: tensor cores (8-head chunks, unused head
+// columns padded) for every group size on 16-bit and fp8 caches — even for
+// MHA the mma.sync block step measured faster on GB300 than the CUDA-core one
+// (5.83 vs 5.56 TB/s, fp16 MHA layer) — and CUDA cores for fp32 caches.
+// PKV_PATH=mma or =simt forces one path wherever it is compiled (comparison
+// runs); PKV_DECODE_WARPS / PKV_DECODE_STAGES pick an alternative pipeline
+// shape where one is compiled.
 int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
-  static const bool force_simt = [] {
-    const char *v = std::getenv("PKV_FORCE_SIMT");
-    return v && v[0] == '1';
+  static const int force = [] {
+    const char *v = std::getenv("PKV_PATH");
+    if (v && std::strcmp(v, "simt") == 0) return 1;
+    if (v && std::strcmp(v, "mma") == 0) return 2;
+    return 0;
   }();
-  // PKV_DECODE_WARPS / PKV_DECODE_STAGES pick an alternative pipeline shape
-  // where one is compiled (tuning runs); otherwise the first match is used.
+  // otherwise the first compiled match is the default shape
   static const int want_warps = [] {
     const char *v = std::getenv("PKV_DECODE_WARPS");
     return v ? std::atoi(v) : 0;
@@ -189,7 +196,7 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
     const char *v = std::getenv("PKV_DECODE_STAGES");
     return v ? std::atoi(v) : 0;
   }();
-  const bool mma = cache_dtype != PKV_F32 && G >= 3 && !force_simt;
+  const bool mma = cache_dtype != PKV_F32 && force != 1;
   const int GC = mma ? 8 : (G >= 2 ? 2 : 1);
   Registry &r = registry();
   int first = -1;
@@ -348,6 +355,7 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
   p.starts = reinterpret_cast<int4 *>(ws + L.starts);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+  p.cta_flags = reinterpret_cast<int32_t *>(ws + L.cta_flags);
   p.num_blocks = num_blocks;
   p.B = B;
   p.Hq = Hq;
@@ -363,13 +371,19 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = 4000000000ull;
 
+  p.inline_plan = B + 1 <= kInlinePrefix ? 1 : 0;
+  p.n_ctas = (P + k.warps - 1) / k.warps;
+
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool pdl = s != nullptr;  // programmatic launch on explicit streams only
-  cudaError_t e = launch_plan(p, s);
-  if (e != cudaSuccess) return cuda_status(e);
+  cudaError_t e = cudaSuccess;
+  if (!p.inline_plan) {
+    e = launch_plan(p, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((P + k.warps - 1) / k.warps);
+  cfg.gridDim = dim3(p.n_ctas);
   cfg.blockDim = dim3(k.warps * 32);
   cfg.dynamicSmemBytes = k.smem_bytes;
   cfg.stream = s;

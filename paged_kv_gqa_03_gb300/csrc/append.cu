@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(128)
     append_kernel(const void *__restrict__ k_new, const void *__restrict__ v_new, void *k_cache,
                   void *v_cache, float *k_scale, float *v_scale, const int64_t *__restrict__ slot_mapping,
                   int B, int Hkv, int D, int64_t num_blocks, int cache_esize) {
+  grid_dep_wait();  // launched early behind the previous kernel; its writes are visible now
   const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= B * Hkv * 2) return;
@@ -74,22 +75,27 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int new_dtype, v
                           int Hkv, int D, int64_t num_blocks, cudaStream_t stream) {
   const int warps = B * Hkv * 2;
   if (warps == 0) return cudaSuccess;
-  const dim3 grid((warps + 3) / 4), block(128);
   const int esize = cache_dtype == PKV_F32 ? 4 : (cache_dtype == PKV_FP8_E4M3 ? 1 : 2);
-  if (cache_dtype != PKV_FP8_E4M3) {
-    append_kernel<F32, false><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
-                                                          slot_mapping, B, Hkv, D, num_blocks, esize);
-  } else if (new_dtype == PKV_F32) {
-    append_kernel<F32, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
-                                                         slot_mapping, B, Hkv, D, num_blocks, esize);
-  } else if (new_dtype == PKV_F16) {
-    append_kernel<F16, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
-                                                         slot_mapping, B, Hkv, D, num_blocks, esize);
-  } else {
-    append_kernel<BF16, true><<<grid, block, 0, stream>>>(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
-                                                          slot_mapping, B, Hkv, D, num_blocks, esize);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = stream != nullptr ? 1 : 0;  // early launch on explicit streams only
+  if (cache_dtype != PKV_FP8_E4M3)
+    return cudaLaunchKernelEx(&cfg, append_kernel<F32, false>, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                              slot_mapping, B, Hkv, D, num_blocks, esize);
+  if (new_dtype == PKV_F32)
+    return cudaLaunchKernelEx(&cfg, append_kernel<F32, true>, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                              slot_mapping, B, Hkv, D, num_blocks, esize);
+  if (new_dtype == PKV_F16)
+    return cudaLaunchKernelEx(&cfg, append_kernel<F16, true>, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                              slot_mapping, B, Hkv, D, num_blocks, esize);
+  return cudaLaunchKernelEx(&cfg, append_kernel<BF16, true>, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                            slot_mapping, B, Hkv, D, num_blocks, esize);
 }
 
 // Copy-on-write: cache[dst] = cache[src] for all kv heads (one CTA per pair

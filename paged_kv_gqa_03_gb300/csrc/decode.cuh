@@ -55,7 +55,8 @@ struct DecodeCfg {
   static constexpr size_t META_BYTES = (size_t)WARPS * STAGES * sizeof(StageMeta);
   static constexpr size_t BAR_BYTES = (size_t)WARPS * STAGES * 8;
   static constexpr size_t QBUF_BYTES = MMA ? 0 : (size_t)WARPS * GC * D * 4;
-  static constexpr size_t SMEM = 1024 + TILES_BYTES + META_BYTES + BAR_BYTES + QBUF_BYTES;
+  static constexpr size_t PREFIX_BYTES = (size_t)kInlinePrefix * 4;  // inline plan
+  static constexpr size_t SMEM = 1024 + TILES_BYTES + META_BYTES + BAR_BYTES + QBUF_BYTES + PREFIX_BYTES;
   // CTAs that fit in an SM's 228 KiB of shared memory (1 KiB reserved per CTA);
   // passed to __launch_bounds__ so registers never limit residency further
   static constexpr int CTAS_RAW = (int)(233472 / (SMEM + 1024));
@@ -87,7 +88,7 @@ __device__ __forceinline__ void load_seq(Producer &pr, const DecodeParams &p) {
 template <class Cfg>
 __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, const CUtensorMap *tmK,
                                         const CUtensorMap *tmV, uint8_t *tiles, StageMeta *meta,
-                                        uint64_t *bars, int stage, int lane) {
+                                        uint64_t *bars, int stage, int lane, int *cta_flags) {
   __syncwarp();
   const int h = pr.hu / p.NC;
   if (!(pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j >= pr.win_j0 && pr.j < pr.win_j0 + 32)) {
@@ -137,7 +138,7 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     const bool bad = blk < 0 || (int64_t)blk >= p.num_blocks;
     // a bad id reads the tile just past the end of the tensor: TMA fills zeros
     const int64_t tile_row = bad ? p.num_blocks * p.Hkv : (int64_t)blk * p.Hkv + h;
-    if (bad) atomicOr(&p.hdr->status, PKV_FLAG_BAD_BLOCK);
+    if (bad) atomicOr(cta_flags, PKV_FLAG_BAD_BLOCK);
     StageMeta m;
     m.b = pr.b;
     m.hu = pr.hu;
@@ -366,20 +367,34 @@ __device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams 
       }
     }
   } else {
+    const int r = lane & 7, mi = lane >> 3;
+    const int vtok = r + ((mi >> 1) << 3), vhi = mi & 1;
     if constexpr (kBF) {
-      pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      // bf16 keeps 8 significant bits; short contexts give weights near 1
+      // whose rounding would show in the output, so P goes in as a bf16 high
+      // part plus a bf16 residual (two MMAs on the same V fragments)
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h01));
+      pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h23));
+      const uint32_t lb0 = movmatrix_trans(pack_bf16x2(p0 - f01.x, p1 - f01.y));
+      const uint32_t lb1 = movmatrix_trans(pack_bf16x2(p2 - f23.x, p3 - f23.y));
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
+        mma16816<true>(st.acc[mt], a, pb0, pb1);
+        mma16816<true>(st.acc[mt], a, lb0, lb1);
+      }
     } else {
       pb0 = movmatrix_trans(pack_f16x2(p0, p1));
       pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-    }
-    const int r = lane & 7, mi = lane >> 3;
-    const int vtok = r + ((mi >> 1) << 3), vhi = mi & 1;
 #pragma unroll
-    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-      uint32_t a[4];
-      ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
-      mma16816<kBF>(st.acc[mt], a, pb0, pb1);
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
+        mma16816<false>(st.acc[mt], a, pb0, pb1);
+      }
     }
   }
 }
@@ -631,6 +646,80 @@ __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodePara
 }
 
 // ---------------------------------------------------------------------------
+// Inline plan (batches of up to kInlinePrefix - 1 sequences): every CTA scans
+// context_lens into a shared-memory prefix of blocks per sequence,
+// prefix[b] = sum_{b' < b} ceil(ctx_b' / 16), so no separate plan launch is
+// needed; CTA 0 also stores it for the merge kernel.  Lengths are clamped to
+// [0, 16 * max_blocks] and flagged.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int clamp_len(const DecodeParams &p, int ctx, int *flags) {
+  if (ctx < 0 || ctx > p.max_blocks * kBlock) *flags |= PKV_FLAG_BAD_LEN;
+  return ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
+}
+
+__device__ __forceinline__ void inline_plan(const DecodeParams &p, int32_t *s_prefix, int32_t *s_scan,
+                                            int *cta_flags) {
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = T >> 5;
+  const int k = (p.B + T - 1) / T;  // consecutive sequences per thread
+  const int b0 = tid * k;
+  int sum = 0, flags = 0;
+  for (int i = 0; i < k; ++i)
+    if (b0 + i < p.B) sum += (clamp_len(p, __ldg(p.context_lens + b0 + i), &flags) + kBlock - 1) / kBlock;
+  int x = sum;  // inclusive scan within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_scan[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = lane < nw ? s_scan[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane < nw) s_scan[lane] = incl - v;
+  }
+  __syncthreads();
+  int run = s_scan[wid] + x - sum;
+  int unused = 0;
+  for (int i = 0; i < k; ++i) {
+    const int b = b0 + i;
+    if (b < p.B) {
+      s_prefix[b] = run;
+      run += (clamp_len(p, __ldg(p.context_lens + b), &unused) + kBlock - 1) / kBlock;
+      if (b == p.B - 1) s_prefix[p.B] = run;
+    }
+  }
+  if (flags) atomicOr(cta_flags, flags);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int b = tid; b <= p.B; b += T) p.prefix[b] = s_prefix[b];
+}
+
+// Partition w's first item {s, b, hu, j} and its end, from the prefix.
+__device__ __forceinline__ int4 locate(const DecodeParams &p, const int32_t *pre, int w, int *end) {
+  const int64_t W = (int64_t)p.HU * pre[p.B];
+  const int64_t s = W * w / p.P;
+  *end = (int)(W * (w + 1) / p.P);
+  if (s >= W) return make_int4((int)W, p.B, 0, 0);
+  int lo = 0, hi = p.B - 1;  // largest b with HU * prefix[b] <= s
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)p.HU * pre[mid] <= s)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int n = pre[lo + 1] - pre[lo];
+  const int64_t rr = s - (int64_t)p.HU * pre[lo];
+  return make_int4((int)s, lo, (int)(rr / n), (int)(rr % n));
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <class Cfg>
@@ -647,6 +736,11 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES) + wib * Cfg::STAGES;
   float *qbuf = reinterpret_cast<float *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES + Cfg::BAR_BYTES) +
                 wib * Cfg::GC * Cfg::D;
+  int32_t *s_prefix =
+      reinterpret_cast<int32_t *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES + Cfg::BAR_BYTES + Cfg::QBUF_BYTES);
+  __shared__ int32_t s_scan[32];
+  __shared__ int cta_flags;
+  if (threadIdx.x == 0) cta_flags = 0;
   if (lane == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -656,12 +750,19 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
     tma_prefetch_desc(&tmV);
   }
   __syncwarp();
-  grid_dep_wait();  // the plan kernel's outputs are visible from here on
+  grid_dep_wait();  // the previous kernel's writes are visible from here on
+  if (p.inline_plan) inline_plan(p, s_prefix, s_scan, &cta_flags);
 
   const int w = blockIdx.x * Cfg::WARPS + wib;
   if (w < p.P) {
-    const int4 st0 = p.starts[w];
-    const int e = p.starts[w + 1].x;
+    int e;
+    int4 st0;
+    if (p.inline_plan) {
+      st0 = locate(p, s_prefix, w, &e);
+    } else {
+      st0 = p.starts[w];
+      e = p.starts[w + 1].x;
+    }
     const int total = e - st0.x;
     if (total > 0) {
       Producer pr;
@@ -681,14 +782,14 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       load_seq(pr, p);
       int issued = 0;
       for (; issued < Cfg::STAGES && issued < total; ++issued)
-        produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, issued, lane);
+        produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, issued, lane, &cta_flags);
 
       typename std::conditional<Cfg::MMA, MmaState<Cfg>, SimtState<Cfg>>::type state;
       for (int i = 0; i < total; ++i) {
         const int stage = i % Cfg::STAGES;
         const uint32_t parity = (uint32_t)(i / Cfg::STAGES) & 1u;
         if (!mbar_wait_bounded(&bars[stage], parity, p.timeout_ns)) {
-          if (lane == 0) atomicOr(&p.hdr->status, PKV_FLAG_TIMEOUT);
+          if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
           // let the copies still in flight land before the CTA's memory goes away
           for (int k = i; k < issued; ++k)
             mbar_wait_bounded(&bars[k % Cfg::STAGES], (uint32_t)(k / Cfg::STAGES) & 1u, p.timeout_ns);
@@ -705,7 +806,7 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
           simt_block<Cfg>(state, p, m, tk, tv, qbuf, lane);
         }
         if (issued < total) {
-          produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane);
+          produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane, &cta_flags);
           ++issued;
         }
         if (m.flags & kLast) {
@@ -717,6 +818,8 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       }
     }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) p.cta_flags[blockIdx.x] = cta_flags;
   grid_dep_launch();
 }
 

@@ -11,6 +11,10 @@ int register_decode_f16(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<F16, F16, 64, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 64, 1, false, kWarps, kBudget>>();
+  // alternative pipeline shapes (PKV_DECODE_WARPS / PKV_DECODE_STAGES)
+  out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 4, 16 * 1024>>();
+  out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 6, 16 * 1024>>();
+  out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 4, 24 * 1024>>();
   return n;
 }
 

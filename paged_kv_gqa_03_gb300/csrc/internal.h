@@ -13,14 +13,22 @@ constexpr int kBlock = 16;      // tokens per physical block (PKV_BLOCK_SIZE)
 constexpr int kChunkMax = 8;    // most query heads one work unit serves
 
 // Workspace header written by the plan kernel each call.
+// Workspace header.  `status` is published by the merge kernel at the end of
+// every call: the OR of the plan's flags (when the plan kernel ran) and of
+// every decode CTA's flags.
 struct WsHeader {
-  int32_t status;   // PKV_FLAG_* bits
-  int32_t P;        // partitions (warp workers)
-  int32_t W;        // total (unit, block) work items
+  int32_t status;      // PKV_FLAG_* bits of the last call
+  int32_t plan_flags;  // written by the plan kernel
+  int32_t P;           // partitions (warp workers)
+  int32_t W;           // total (unit, block) work items
   int32_t B;
-  int32_t HU;       // units per sequence = Hkv * NC
-  int32_t pad[59];  // 256 bytes
+  int32_t HU;          // units per sequence = Hkv * NC
+  int32_t pad[58];     // 256 bytes
 };
+
+// Batches up to this size are planned inside the decode kernel (each CTA
+// scans context_lens into shared memory); larger ones use the plan kernel.
+constexpr int kInlinePrefix = 2048;
 
 // Per stage of a warp's pipeline: what the producer issued into it.
 struct StageMeta {
@@ -48,19 +56,22 @@ struct DecodeParams {
   int4 *starts;         // [P+1] {s, b, hu, j} of each worker's first item
   float *part_o;        // [P][2][kChunkMax][D]
   float *part_lse;      // [P][2][kChunkMax], log2 domain
+  int32_t *cta_flags;   // [decode CTAs] PKV_FLAG_* bits of each decode CTA
   int64_t num_blocks;
   int B, Hq, Hkv, D, G, GC, NC, HU, P;
   int max_blocks;
   int out_dtype;
   float scale_log2;     // softmax scale * log2(e)
   uint64_t timeout_ns;
+  int inline_plan;      // 1: the decode kernel computes prefix and partition starts itself
+  int n_ctas;           // decode grid size
 };
 
 // Records a CUDA error for pkv_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);
 
 struct WsLayout {
-  size_t hdr, prefix, starts, part_o, part_lse, total;
+  size_t hdr, prefix, starts, part_o, part_lse, cta_flags, total;
 };
 WsLayout ws_layout(int B, int P, int D);
 

@@ -16,19 +16,22 @@
 namespace pkv {
 
 // ---------------------------------------------------------------------------
-// Plan: prefix[b] = sum_{b' < b} ceil(ctx_b' / 16); W = HU * prefix[B];
-// partition w starts at item floor(w * W / P), decoded into (b, hu, j).
-// Also writes the (zero) output of sequences with nothing to attend.  One CTA; context
-// lengths are clamped to [0, 16 * max_blocks] (flagged).
+// Plan kernel, for batches too large to plan inside the decode kernel:
+// prefix[b] = sum_{b' < b} ceil(ctx_b' / 16); W = HU * prefix[B]; partition w
+// starts at item floor(w * W / P), decoded into (b, hu, j).  One CTA; context
+// lengths are clamped to [0, 16 * max_blocks] (flagged in plan_flags).
 // ---------------------------------------------------------------------------
 constexpr int kPlanSmemInts = 8192;  // prefix entries kept in shared memory (32 KiB)
 
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   grid_dep_launch();  // the decode kernel may start its prologue now
   __shared__ int32_t warp_tot[32];
-  __shared__ int32_t carry;
+  __shared__ int32_t carry, s_flags;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
-  if (tid == 0) carry = 0;
+  if (tid == 0) {
+    carry = 0;
+    s_flags = 0;
+  }
   __syncthreads();
   int flags = 0;
   for (int base = 0; base < p.B; base += blockDim.x) {
@@ -60,22 +63,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     }
     __syncthreads();
     const int excl = carry + warp_tot[wid] + x - n;
-    if (b < p.B) {
-      p.prefix[b] = excl;
-      if (n == 0)
-        for (size_t i = 0; i < (size_t)p.Hq * p.D; ++i) store_out(p.out_dtype, p.out, (size_t)b * p.Hq * p.D + i, 0.f);
-    }
+    if (b < p.B) p.prefix[b] = excl;
     __syncthreads();
     if (tid == blockDim.x - 1) carry = excl + n;
     __syncthreads();
   }
   const int total_blocks = carry;
+  if (flags) atomicOr(&s_flags, flags);
+  __syncthreads();
   if (tid == 0) {
     p.prefix[p.B] = total_blocks;
-    p.hdr->status = 0;
+    p.hdr->plan_flags = s_flags;
   }
-  __syncthreads();
-  if (flags) atomicOr(&p.hdr->status, flags);
+  __syncthreads();  // prefix[B] is read below by other threads
   const int64_t W = (int64_t)p.HU * total_blocks;
   if (tid == 0) {
     p.hdr->P = p.P;
@@ -146,6 +146,19 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p)
   __shared__ float s_lse[kSegChunk][kChunkMax];
   __shared__ int32_t s_base[kSegChunk];
   grid_dep_wait();
+  if (blockIdx.x == 0 && threadIdx.x < 32) {  // publish the call's status bits
+    int f = p.inline_plan ? 0 : p.hdr->plan_flags;
+    for (int c = threadIdx.x; c < p.n_ctas; c += 32) f |= p.cta_flags[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) f |= __shfl_xor_sync(kFull, f, off);
+    if (threadIdx.x == 0) {
+      p.hdr->status = f;
+      p.hdr->P = p.P;
+      p.hdr->W = p.HU * p.prefix[p.B];
+      p.hdr->B = p.B;
+      p.hdr->HU = p.HU;
+    }
+  }
   const int u = blockIdx.x;
   const int b = u / p.HU, hu = u % p.HU;
   const int h = hu / p.NC, c = hu % p.NC;
@@ -156,7 +169,11 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p)
   const int n = p.prefix[b + 1] - pb;
   const int nvec = gc * D / 4;
   const size_t out0 = ((size_t)b * p.Hq + head0) * D;
-  if (n == 0) return;  // written by the plan kernel
+  if (n == 0) {  // nothing to attend: the output is zero
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x)
+      store4_out(p.out_dtype, p.out, out0 + 4 * (size_t)v, make_float4(0.f, 0.f, 0.f, 0.f));
+    return;
+  }
   const int64_t W = (int64_t)p.HU * p.prefix[p.B];
   const int64_t a = (int64_t)p.HU * pb + (int64_t)hu * n, e = a + n;
   const int wf = (int)(((a + 1) * p.P - 1) / W);

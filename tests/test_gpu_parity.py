@@ -273,3 +273,36 @@ def test_captured_step_graph_matches_eager_step():
         step.stream.synchronize()
         assert torch.equal(hout, eager_out)
     assert torch.equal(step.k_cache.cpu(), eager_k)
+
+
+def test_large_batch_is_planned_by_the_plan_kernel():
+    """Batches of 2048 sequences and more are planned by a separate kernel
+    (smaller ones inside the decode kernel); both give the oracle's result and
+    flag a bad context length."""
+    spec = dict(B=2100, Hq=8, Hkv=2, D=64, dtype="bf16", ctx_range=(1, 40), free_frac=0.2, min_free=64)
+    _check_step(workloads.make(spec, seed=21))
+    pkv = _pkv()
+    w = workloads.make(dict(spec, B=2050), seed=22)
+    dev = "cuda"
+    table = np.full((w.B, 3), 0, dtype=np.int32)
+    for b in range(w.B):
+        table[b, :len(w.tables[b])] = w.tables[b]
+    lens = np.array(w.cached, dtype=np.int32)
+    lens[7] = 10_000                       # beyond 16 * max_blocks: clamped and flagged
+    out, ws = _attend(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), torch.from_numpy(table).to(dev),
+                      torch.from_numpy(lens).to(dev), w.scale)
+    rc, flags = pkv.paged_decode_status(ws)
+    assert rc == pkv.PKV_ERANGE and flags == 2
+    lens[7] = 48
+    ref = oracle.decode(w.q, "bf16", w.k_cache, w.v_cache, "bf16", table, np.maximum(lens, 0), scale=w.scale)
+    compare(out, ref, "bf16", "large batch")
+
+
+@pytest.mark.parametrize("dtype,q_dtype", [("bf16", "bf16"), ("f16", "f16"), ("fp8_e4m3", "bf16")])
+def test_short_contexts_many_sequences(dtype, q_dtype):
+    """Contexts of 1-8 tokens put single softmax weights near 1, where the
+    rounding of the weights fed to the tensor cores would show directly."""
+    spec = dict(B=1024, Hq=16, Hkv=2, D=128, dtype=dtype, q_dtype=q_dtype, ctx_range=(1, 8),
+                free_frac=0.5, min_free=256)
+    stats = _check_step(workloads.make(spec, seed=31))
+    print(dtype, stats)
