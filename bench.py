@@ -56,6 +56,29 @@ def dist_setup(args):
     return world, rank, local
 
 
+# --- replica aggregation (one process per GPU; no data-path collective) -----
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's time: every rank's number, MAX-reduced."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank, world, ms):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -274,16 +297,6 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(q)
     kv = w.kv_bytes()
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
 
     # warm-up
     for _ in range(args.warmup):
@@ -300,15 +313,15 @@ def run_ours(args, world, rank, local):
 
     # (1) device-timed steps: append + attention (+ merge), inputs resident in HBM
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         step.launch(q, kn, vn, out)
     e1.record(stream)
     e1.synchronize()
-    barrier()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    barrier(world)
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # (2) the attention call alone, same stream, for the roofline of the dominant kernel
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -318,21 +331,22 @@ def run_ours(args, world, rank, local):
         step.attend(q, out)
     a1.record(stream)
     a1.synchronize()
-    ms_attn = max_over_ranks(a0.elapsed_time(a1) / args.steps)
+    ms_attn = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
     clocks = sampler.stop()
 
     # (3) end to end through the public API from pinned host buffers: each step
     # copies q, k_new, v_new and the bookkeeping to the device, runs append +
     # attention and copies the output back (one captured CUDA graph per step),
     # then the host reads the result
-    hq = w.q.pin_memory()
-    hk, hv = w.k_new.pin_memory(), w.v_new.pin_memory()
+    step.h_q.copy_(w.q)           # the step's inputs sit in the pinned staging buffer
+    step.h_k_new.copy_(w.k_new)
+    step.h_v_new.copy_(w.v_new)
     hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
-    step.capture(hq, hk, hv, hout)
+    step.capture(hout)
     for _ in range(3):
         step.replay()
         stream.synchronize()
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(stream)
@@ -342,9 +356,9 @@ def run_ours(args, world, rank, local):
         _ = float(hout.view(-1)[0])
     x1.record(stream)
     x1.synchronize()
-    barrier()
-    ms_e2e = max_over_ranks(x0.elapsed_time(x1) / args.steps)
-    h2d = (hq.numel() * hq.element_size() + hk.numel() * hk.element_size() * 2 + step.h2d_bytes())
+    barrier(world)
+    ms_e2e = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, dev)
+    h2d = step.h2d_bytes(with_inputs=True)
     d2h = hout.numel() * hout.element_size()
     out = step.g_out
 
@@ -369,7 +383,7 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group() if world > 1 else None
         return
     peak, peak_src = peak_hbm()
-    value = world * kv / (ms_step * 1e-3) / 1e9
+    value = job_gbs(kv, world, ms_step)
     attn_gbs = kv / (ms_attn * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
@@ -389,7 +403,7 @@ def run_ours(args, world, rank, local):
                      "traffic": kernel_traffic(), "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * kv / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(kv, world, ms_e2e), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
         "host_a1_us": round(host_a1_us, 1),

@@ -6,15 +6,37 @@
   a3  paged_kv_append of the new token's K/V at its slot;
   a4-a8  paged_decode_attention (gather, scores, online softmax, p.V, merge).
 
-Device state (caches, scales, tables, workspace) stays resident; per step
-only q, k_new, v_new and the host-produced slot mapping / tables / lengths
-cross to the device.  Everything is asynchronous on `stream`.
+Device state (caches, scales, workspace) stays resident.  Per step only q,
+k_new, v_new and the host-produced slot mapping / copy pairs / tables /
+lengths cross to the device, all from ONE pinned staging buffer with one copy
+(two staging buffers alternate so the host can prepare step n+1 while step n's
+copy is in flight).  Everything is asynchronous on `stream`.
 """
 import numpy as np
 import torch
 
 from . import (BlockManager, lib, paged_decode_attention, paged_decode_workspace_bytes,
                paged_kv_append, paged_kv_copy_blocks)
+
+_ALIGN = 256
+
+
+class _Staging:
+    """One contiguous byte buffer with typed sections at 256-byte offsets."""
+
+    def __init__(self, layout, total, device, pin):
+        if device.type == "cuda":
+            self.buf = torch.empty(total, dtype=torch.uint8, device=device)
+        else:
+            self.buf = torch.empty(total, dtype=torch.uint8, pin_memory=pin)
+        self.views = {}
+        for name, (off, shape, dtype) in layout.items():
+            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+            self.views[name] = self.buf[off:off + n].view(dtype).view(shape)
+        self.done = None   # event recorded after the last copy out of this buffer
+
+    def __getitem__(self, name):
+        return self.views[name]
 
 
 class DecodeStep:
@@ -24,6 +46,7 @@ class DecodeStep:
         self.k_scale, self.v_scale = k_scale, v_scale
         self.num_blocks, self.Hkv, _, self.D = k_cache.shape
         self.Hq, self.q_dtype, self.max_blocks = Hq, q_dtype, max_blocks
+        self.new_dtype = q_dtype if k_cache.dtype == torch.float8_e4m3fn else k_cache.dtype
         self.num_splits = num_splits
         self.scale = 1.0 / float(np.sqrt(self.D)) if scale is None else float(scale)
         self.device = k_cache.device
@@ -32,48 +55,67 @@ class DecodeStep:
         self.seqs = []
         self._ws = None
         self._B = None
-        self._sets = []     # two pinned host buffer sets, used alternately
         self._turn = 0
         self.ncow = 0
+        self.graph = None
 
-    # -- a1 ---------------------------------------------------------------
-    def adopt(self, seq, blocks, num_tokens):
-        self.bm.adopt(seq, blocks, num_tokens)
-        self.seqs.append(seq)
+    # -- buffers ---------------------------------------------------------------
+    def _layout(self, B):
+        sections = [("q", (B, self.Hq, self.D), self.q_dtype),
+                    ("k_new", (B, self.Hkv, self.D), self.new_dtype),
+                    ("v_new", (B, self.Hkv, self.D), self.new_dtype),
+                    ("slots", (B,), torch.int64),
+                    ("pairs", (2 * B,), torch.int32),
+                    ("table", (B, self.max_blocks), torch.int32),
+                    ("lens", (B,), torch.int32)]
+        layout, off = {}, 0
+        for name, shape, dtype in sections:
+            layout[name] = (off, shape, dtype)
+            n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+            off = (off + n + _ALIGN - 1) // _ALIGN * _ALIGN
+        self._io_bytes = layout["slots"][0]           # q, k_new, v_new
+        self._book_bytes = off - layout["slots"][0]   # slots .. lens
+        return layout, off
 
     def _buffers(self, B):
         if self._B == B:
             return
-        dev, pin = self.device, torch.cuda.is_available()
         self._B = B
+        layout, total = self._layout(B)
+        pin = torch.cuda.is_available()
+        self._host = [_Staging(layout, total, torch.device("cpu"), pin) for _ in range(2)]
+        self._dev = _Staging(layout, total, self.device, False)
         self.h_seqs = np.empty(B, dtype=np.int64)
-        self._sets = []
-        for _ in range(2):
-            self._sets.append(dict(
-                slots=torch.empty(B, dtype=torch.int64, pin_memory=pin),
-                pairs=torch.empty(2 * B, dtype=torch.int32, pin_memory=pin),
-                table=torch.empty((B, self.max_blocks), dtype=torch.int32, pin_memory=pin),
-                lens=torch.empty(B, dtype=torch.int32, pin_memory=pin),
-                done=None))
-        self.d_slots = torch.empty(B, dtype=torch.int64, device=dev)
-        self.d_pairs = torch.empty(2 * B, dtype=torch.int32, device=dev)
-        self.d_table = torch.empty((B, self.max_blocks), dtype=torch.int32, device=dev)
-        self.d_lens = torch.empty(B, dtype=torch.int32, device=dev)
+        self.d_q, self.d_k_new, self.d_v_new = self._dev["q"], self._dev["k_new"], self._dev["v_new"]
+        self.d_slots, self.d_pairs = self._dev["slots"], self._dev["pairs"]
+        self.d_table, self.d_lens = self._dev["table"], self._dev["lens"]
+        self._select(self._turn)
         n = paged_decode_workspace_bytes(B, self.Hq, self.Hkv, self.D, self.k_cache.dtype,
                                          self.q_dtype, self.num_splits)
-        self._ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def _select(self, turn):
+        hs = self._host[turn]
+        self.h_q, self.h_k_new, self.h_v_new = hs["q"], hs["k_new"], hs["v_new"]
+        self.h_slots, self.h_pairs = hs["slots"], hs["pairs"]
+        self.h_table, self.h_lens = hs["table"], hs["lens"]
+
+    # -- a1 ----------------------------------------------------------------------
+    def adopt(self, seq, blocks, num_tokens):
+        self.bm.adopt(seq, blocks, num_tokens)
+        self.seqs.append(seq)
 
     def prepare(self, seqs=None):
-        """Host part: slots, copy pairs, tables and lengths into pinned buffers.
-        Returns the number of copy-on-write pairs (raises on OOM)."""
+        """Host part of a step: switches to the other staging buffer (waiting
+        for the copy that last read it), then writes the slots, copy pairs,
+        tables and lengths of one new token per sequence into it.  Returns the
+        number of copy-on-write pairs (raises on OOM)."""
         seqs = self.seqs if seqs is None else seqs
         self._buffers(len(seqs))
         self._turn ^= 1
-        hs = self._sets[self._turn]
-        if hs["done"] is not None:      # the copies that last read this set have finished
-            hs["done"].synchronize()
-        self.h_slots, self.h_pairs, self.h_table, self.h_lens = (
-            hs["slots"], hs["pairs"], hs["table"], hs["lens"])
+        if self._host[self._turn].done is not None:
+            self._host[self._turn].done.synchronize()
+        self._select(self._turn)
         self.h_seqs[:] = seqs
         ncow = self.bm.append_slots_into(self.h_seqs, self.h_slots.numpy(), self.h_pairs.numpy())
         if ncow < 0:
@@ -85,24 +127,30 @@ class DecodeStep:
             raise RuntimeError(f"export failed [{rc}]")
         return ncow
 
-    def upload(self):
-        """Host -> device copies of the step's bookkeeping (async on stream)."""
+    def _copy_in(self, with_inputs):
+        """One host->device copy of the current staging buffer (the step's
+        bookkeeping, and q / k_new / v_new when with_inputs)."""
+        hs = self._host[self._turn]
+        lo = 0 if with_inputs else self._io_bytes
+        hi = self._io_bytes + self._book_bytes
         with torch.cuda.stream(self.stream):
-            self.d_slots.copy_(self.h_slots, non_blocking=True)
-            self.d_table.copy_(self.h_table, non_blocking=True)
-            self.d_lens.copy_(self.h_lens, non_blocking=True)
-            if self.ncow:
-                self.d_pairs[:2 * self.ncow].copy_(self.h_pairs[:2 * self.ncow], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(self.stream)
-            self._sets[self._turn]["done"] = ev
+            self._dev.buf[lo:hi].copy_(hs.buf[lo:hi], non_blocking=True)
+            if not torch.cuda.is_current_stream_capturing():
+                ev = torch.cuda.Event()
+                ev.record(self.stream)
+                hs.done = ev
 
-    def h2d_bytes(self):
-        return (self.h_slots.numel() * 8 + self.h_table.numel() * 4 + self.h_lens.numel() * 4
-                + 8 * self.ncow)
+    def upload(self):
+        """Copies the bookkeeping written by prepare() to the device."""
+        self._copy_in(with_inputs=False)
 
-    # -- a2..a8 -----------------------------------------------------------
+    def h2d_bytes(self, with_inputs=True):
+        return (self._io_bytes if with_inputs else 0) + self._book_bytes
+
+    # -- a2..a8 ------------------------------------------------------------------
     def launch(self, q, k_new, v_new, out):
+        """Runs a2..a8 with device tensors q, k_new, v_new (bookkeeping from
+        the last upload())."""
         s = self.stream
         if self.ncow:
             paged_kv_copy_blocks(self.k_cache, self.v_cache, self.d_pairs[:2 * self.ncow].view(-1, 2),
@@ -120,40 +168,27 @@ class DecodeStep:
     def workspace(self):
         return self._ws
 
-    # -- whole step as one CUDA graph ----------------------------------------
-    def capture(self, h_q, h_k_new, h_v_new, h_out):
-        """Captures one full step — host->device copies of q, k_new, v_new
-        (pinned host tensors) and of the bookkeeping last written by
-        prepare(), the append, the attention, and the device->host copy of the
-        output into h_out — as a CUDA graph; replay() runs it.  Re-capture
-        after prepare() when the copy pairs or buffer sets change."""
-        dev = self.device
-        self.g_q = torch.empty(h_q.shape, dtype=h_q.dtype, device=dev)
-        self.g_k = torch.empty(h_k_new.shape, dtype=h_k_new.dtype, device=dev)
-        self.g_v = torch.empty(h_v_new.shape, dtype=h_v_new.dtype, device=dev)
-        self.g_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=dev)
-        # one eager run first: kernels are configured and tensor maps encoded
-        self._graph_body(h_q, h_k_new, h_v_new, h_out)
+    # -- a whole step from host memory as one CUDA graph ---------------------------
+    def capture(self, h_out):
+        """Captures one full step from the current staging buffer — one
+        host->device copy of q, k_new, v_new (written into h_q / h_k_new /
+        h_v_new) and the bookkeeping, the append, the attention, and one
+        device->host copy of the output into the pinned tensor h_out — as a
+        CUDA graph; replay() runs it.  Re-capture after a prepare() that
+        switches staging buffers or changes the copy pairs."""
+        self.g_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=self.device)
+        self._graph_body(h_out)          # eager once: kernels configured, tensor maps encoded
         self.stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=self.stream):
-            self._graph_body(h_q, h_k_new, h_v_new, h_out)
+            self._graph_body(h_out)
         self.graph = graph
         return graph
 
-    def _graph_body(self, h_q, h_k_new, h_v_new, h_out):
-        s = self.stream
-        with torch.cuda.stream(s):
-            self.g_q.copy_(h_q, non_blocking=True)
-            self.g_k.copy_(h_k_new, non_blocking=True)
-            self.g_v.copy_(h_v_new, non_blocking=True)
-            self.d_slots.copy_(self.h_slots, non_blocking=True)
-            self.d_table.copy_(self.h_table, non_blocking=True)
-            self.d_lens.copy_(self.h_lens, non_blocking=True)
-            if self.ncow:
-                self.d_pairs[:2 * self.ncow].copy_(self.h_pairs[:2 * self.ncow], non_blocking=True)
-        self.launch(self.g_q, self.g_k, self.g_v, self.g_out)
-        with torch.cuda.stream(s):
+    def _graph_body(self, h_out):
+        self._copy_in(with_inputs=True)
+        self.launch(self.d_q, self.d_k_new, self.d_v_new, self.g_out)
+        with torch.cuda.stream(self.stream):
             h_out.copy_(self.g_out, non_blocking=True)
 
     def replay(self):

@@ -264,9 +264,11 @@ def test_captured_step_graph_matches_eager_step():
     step, out = run_gpu_step(w)
     eager_out = out.cpu()
     eager_k = step.k_cache.cpu()
-    hq, hk, hv = w.q.pin_memory(), w.k_new.pin_memory(), w.v_new.pin_memory()
+    step.h_q.copy_(w.q)
+    step.h_k_new.copy_(w.k_new)
+    step.h_v_new.copy_(w.v_new)
     hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
-    step.capture(hq, hk, hv, hout)
+    step.capture(hout)
     for _ in range(2):
         hout.zero_()
         step.replay()
