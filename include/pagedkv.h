@@ -244,6 +244,21 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype,
                          pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Staging copy.                                                            */
+/* ------------------------------------------------------------------------ */
+/*
+ * dst[0:bytes] = src[0:bytes], performed by the SMs (a kernel on `stream`)
+ * rather than a copy engine.  Either pointer may be pinned host memory
+ * (cudaHostAlloc / torch pin_memory), which the GPU addresses directly under
+ * unified addressing — over NVLink-C2C on Grace-based systems — so this is the
+ * host<->device staging copy of a decode step (its inputs in, its output
+ * out): for the ~1-2 MB a step moves, many CTAs issuing 16-byte accesses beat
+ * one copy-engine transfer.  Both pointers and `bytes` must be 16-byte
+ * aligned; the ranges must not overlap.
+ */
+int pkv_copy(void *dst, const void *src, size_t bytes, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Step a1 — host block manager: allocate / fork / free / slot mapping.     */
 /* ------------------------------------------------------------------------ */
 /*

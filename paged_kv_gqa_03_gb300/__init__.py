@@ -14,7 +14,7 @@ import os
 __all__ = [
     "PagedKVError", "paged_kv_append", "paged_decode_workspace_bytes",
     "paged_decode_attention", "paged_decode_status", "paged_decode_merge",
-    "paged_kv_copy_blocks", "pkv_status_string", "pkv_version", "BlockManager",
+    "paged_kv_copy_blocks", "pkv_copy", "pkv_status_string", "pkv_version", "BlockManager",
     "DTYPE_CODES", "LIB_PATH", "lib",
 ]
 
@@ -44,6 +44,7 @@ _sig("paged_decode_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i3
 _sig("paged_decode_status", _i32, _P, _sz, _P, ctypes.POINTER(_i32))
 _sig("paged_decode_merge", _i32, _P, _i32, _P, _P, _i32, _i32, _i32, _i32, _P)
 _sig("paged_kv_copy_blocks", _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
+_sig("pkv_copy", _i32, _P, _P, _sz, _P)
 _sig("pkv_status_string", ctypes.c_char_p, _i32)
 _sig("pkv_last_cuda_error", _i32)
 _sig("pkv_version", _i32)
@@ -200,6 +201,18 @@ def paged_decode_merge(out, o_partial, lse, stream=None):
                                  _dev(o_partial, "o_partial", torch.float32),
                                  _dev(lse, "lse", torch.float32), B, Hq, D, S, _stream(stream)),
            "paged_decode_merge")
+
+
+def pkv_copy(dst, src, nbytes=None, stream=None):
+    """SM-driven copy of nbytes (default: all of src) between CUDA tensors
+    and/or pinned host tensors (see include/pagedkv.h)."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    n = src.numel() * src.element_size() if nbytes is None else nbytes
+    _check(_L.pkv_copy(dst.data_ptr(), src.data_ptr(), n, _stream(stream)), "pkv_copy")
 
 
 def paged_kv_copy_blocks(k_cache, v_cache, src_dst_pairs, k_scale=None, v_scale=None, stream=None):

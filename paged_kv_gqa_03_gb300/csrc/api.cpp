@@ -435,4 +435,14 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype, float *k
                                         Hkv, D, num_blocks, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int pkv_copy(void *dst, const void *src, size_t bytes, pkv_stream_t stream) {
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src || (bytes & 15u) != 0 || !aligned16(dst) || !aligned16(src)) return PKV_EINVAL;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_copy(dst, src, bytes, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

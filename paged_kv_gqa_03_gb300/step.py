@@ -16,7 +16,7 @@ import numpy as np
 import torch
 
 from . import (BlockManager, lib, paged_decode_attention, paged_decode_workspace_bytes,
-               paged_kv_append, paged_kv_copy_blocks)
+               paged_kv_append, paged_kv_copy_blocks, pkv_copy)
 
 _ALIGN = 256
 
@@ -133,8 +133,8 @@ class DecodeStep:
         hs = self._host[self._turn]
         lo = 0 if with_inputs else self._io_bytes
         hi = self._io_bytes + self._book_bytes
+        pkv_copy(self._dev.buf[lo:hi], hs.buf[lo:hi], stream=self.stream)
         with torch.cuda.stream(self.stream):
-            self._dev.buf[lo:hi].copy_(hs.buf[lo:hi], non_blocking=True)
             if not torch.cuda.is_current_stream_capturing():
                 ev = torch.cuda.Event()
                 ev.record(self.stream)
@@ -188,8 +188,7 @@ class DecodeStep:
     def _graph_body(self, h_out):
         self._copy_in(with_inputs=True)
         self.launch(self.d_q, self.d_k_new, self.d_v_new, self.g_out)
-        with torch.cuda.stream(self.stream):
-            h_out.copy_(self.g_out, non_blocking=True)
+        pkv_copy(h_out, self.g_out, stream=self.stream)
 
     def replay(self):
         with torch.cuda.stream(self.stream):

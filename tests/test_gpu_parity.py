@@ -308,3 +308,20 @@ def test_short_contexts_many_sequences(dtype, q_dtype):
                 free_frac=0.5, min_free=256)
     stats = _check_step(workloads.make(spec, seed=31))
     print(dtype, stats)
+
+
+def test_sm_copy_between_pinned_host_and_device_is_exact():
+    pkv = _pkv()
+    g = torch.Generator().manual_seed(8)
+    n = 3 * 1024 * 1024 + 48                    # not a multiple of the per-thread stride
+    src_host = torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(n, dtype=torch.uint8, device="cuda")
+    back = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    pkv.pkv_copy(dev, src_host)                 # host -> device
+    dev2 = torch.empty_like(dev)
+    pkv.pkv_copy(dev2, dev)                     # device -> device
+    pkv.pkv_copy(back, dev2)                    # device -> host
+    torch.cuda.synchronize()
+    assert torch.equal(back, src_host)
+    with pytest.raises(pkv.PagedKVError):
+        pkv.pkv_copy(dev, src_host, nbytes=7)   # not a multiple of 16 bytes
