@@ -245,52 +245,81 @@ __device__ __forceinline__ void mma_begin(MmaState<Cfg> &st, const DecodeParams 
   st.l0 = st.l1 = 0.f;
 }
 
+// A block's K and V operands in registers (MMA fragments, or raw fp8 words).
 template <class Cfg>
-__device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
-                                          uint8_t *tk, uint8_t *tv, int lane) {
+struct MmaFrags {
+  static constexpr int KS = Cfg::D / 16, MT = Cfg::D / 16;
+  static constexpr int KW = Cfg::FP8 ? 2 : 4;            // words per k-step
+  static constexpr int VW = Cfg::FP8 ? Cfg::D / 32 : 4;  // words per token row (fp8) / m-tile
+  static constexpr int VN = Cfg::FP8 ? 4 : MT;           // fp8: 4 token rows
+  uint32_t k[KS][KW];
+  uint32_t v[VN][VW];
+};
+
+template <class Cfg>
+__device__ __forceinline__ void mma_load(MmaFrags<Cfg> &f, uint8_t *tk, uint8_t *tv, int nvalid, int lane) {
   constexpr int ROWB = Cfg::ROWB;
-  constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
   const int gid = lane >> 2, tig = lane & 3;
   const uint32_t kb = smem_u32(tk), vb = smem_u32(tv);
-  const int nvalid = m.nvalid;
   if (nvalid < kBlock) zero_tail_rows<ROWB>(tv, nvalid, lane);
-
-  // ---- scores S^T = K . Q^T (16 tokens x 8 heads) ----
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (Cfg::FP8) {
-    float s1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain: odd k-steps
 #pragma unroll
-    for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
-      const uint32_t w0 = lds32(kb + tile_off<ROWB>(gid, 16 * ks + 4 * tig));
-      const uint32_t w1 = lds32(kb + tile_off<ROWB>(gid + 8, 16 * ks + 4 * tig));
-      uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff));
-      a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff));
-      a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
-      a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
-      if (ks & 1)
-        mma16816<false>(s1, a, st.qb[ks][0], st.qb[ks][1]);
-      else
-        mma16816<false>(s, a, st.qb[ks][0], st.qb[ks][1]);
+    for (int ks = 0; ks < MmaFrags<Cfg>::KS; ++ks) {
+      f.k[ks][0] = lds32(kb + tile_off<ROWB>(gid, 16 * ks + 4 * tig));
+      f.k[ks][1] = lds32(kb + tile_off<ROWB>(gid + 8, 16 * ks + 4 * tig));
     }
+    constexpr int DPT = Cfg::D / 8;  // head-dim bytes owned by one row group
+    const int trow[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] += s1[i];
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (DPT == 16) {
+        const uint4 r = lds128(vb + tile_off<ROWB>(trow[i], 16 * gid));
+        f.v[i][0] = r.x; f.v[i][1] = r.y; f.v[i][2] = r.z; f.v[i][3] = r.w;
+      } else {
+        const uint2 r = lds64(vb + tile_off<ROWB>(trow[i], 8 * gid));
+        f.v[i][0] = r.x; f.v[i][1] = r.y;
+      }
+    }
   } else {
     const int r = lane & 7, mi = lane >> 3;
     const int krow = r + ((mi & 1) << 3), khi = mi >> 1;
-    float s1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain: odd k-steps
+    const int vtok = r + ((mi >> 1) << 3), vhi = mi & 1;
 #pragma unroll
-    for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(kb + tile_off<ROWB>(krow, (2 * ks + khi) * 16), a);
-      if (ks & 1)
-        mma16816<kBF>(s1, a, st.qb[ks][0], st.qb[ks][1]);
-      else
-        mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
-    }
+    for (int ks = 0; ks < MmaFrags<Cfg>::KS; ++ks) ldsm_x4(kb + tile_off<ROWB>(krow, (2 * ks + khi) * 16), f.k[ks]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] += s1[i];
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt)
+      ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), f.v[mt]);
   }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cfg> &f, const DecodeParams &p,
+                                            const StageMeta &m, int lane) {
+  constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
+  const int gid = lane >> 2;
+  const int nvalid = m.nvalid;
+
+  // ---- scores S^T = K . Q^T (16 tokens x 8 heads), two independent chains ----
+  float s[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < MmaFrags<Cfg>::KS; ++ks) {
+    uint32_t a[4];
+    if constexpr (Cfg::FP8) {
+      // k-slots 2t,2t+1 | 2t+8,2t+9 of row gid (+8) hold d = 16ks + 4t + {0,1} | {2,3}
+      a[0] = e4m3x2_to_f16x2((uint16_t)(f.k[ks][0] & 0xffff));
+      a[1] = e4m3x2_to_f16x2((uint16_t)(f.k[ks][1] & 0xffff));
+      a[2] = e4m3x2_to_f16x2((uint16_t)(f.k[ks][0] >> 16));
+      a[3] = e4m3x2_to_f16x2((uint16_t)(f.k[ks][1] >> 16));
+    } else {
+      a[0] = f.k[ks][0]; a[1] = f.k[ks][1]; a[2] = f.k[ks][2]; a[3] = f.k[ks][3];
+    }
+    if (ks & 1)
+      mma16816<kBF>(s1, a, st.qb[ks][0], st.qb[ks][1]);
+    else
+      mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] += s1[i];
 
   // ---- online softmax over the block (log2 domain) ----
   const float sc = p.scale_log2 * m.ks;
@@ -312,7 +341,7 @@ __device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams 
   st.m0 = mn0;
   st.m1 = mn1;
 #pragma unroll
-  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+  for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
     st.acc[mt][0] *= al0;
     st.acc[mt][1] *= al1;
     st.acc[mt][2] *= al0;
@@ -320,82 +349,44 @@ __device__ __forceinline__ void mma_block(MmaState<Cfg> &st, const DecodeParams 
   }
 
   // ---- O^T += V^T . P^T ----
-  uint32_t pb0, pb1;
   if constexpr (Cfg::FP8) {
     const float vs = m.vs;  // fold the V scale into the weights
-    pb0 = movmatrix_trans(pack_f16x2(p0 * vs, p1 * vs));
-    pb1 = movmatrix_trans(pack_f16x2(p2 * vs, p3 * vs));
-    constexpr int DPT = Cfg::D / 8;  // head-dim bytes owned by one row group
-    const int t0 = 2 * tig, t2 = 2 * tig + 8;
-    if constexpr (DPT == 16) {
-      const uint4 R0 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t0, 16 * gid));
-      const uint4 R1 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t0 + 1, 16 * gid));
-      const uint4 R2 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t2, 16 * gid));
-      const uint4 R3 = *reinterpret_cast<const uint4 *>(tv + tile_off<ROWB>(t2 + 1, 16 * gid));
-      const uint32_t w0[4] = {R0.x, R0.y, R0.z, R0.w}, w1[4] = {R1.x, R1.y, R1.z, R1.w};
-      const uint32_t w2[4] = {R2.x, R2.y, R2.z, R2.w}, w3[4] = {R3.x, R3.y, R3.z, R3.w};
+    const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0 * vs, p1 * vs));
+    const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2 * vs, p3 * vs));
 #pragma unroll
-      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-        const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
-        const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
-        uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
-        a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
-        a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
-        a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
-        mma16816<false>(st.acc[mt], a, pb0, pb1);
-      }
-    } else {
-      const uint2 R0 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t0, 8 * gid));
-      const uint2 R1 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t0 + 1, 8 * gid));
-      const uint2 R2 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t2, 8 * gid));
-      const uint2 R3 = *reinterpret_cast<const uint2 *>(tv + tile_off<ROWB>(t2 + 1, 8 * gid));
-      const uint32_t w0[2] = {R0.x, R0.y}, w1[2] = {R1.x, R1.y};
-      const uint32_t w2[2] = {R2.x, R2.y}, w3[2] = {R3.x, R3.y};
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
+      // bytes 2mt, 2mt+1 of the thread's head-dim run, from token rows
+      // (2t, 2t+1) and (2t+8, 2t+9), paired for the f16x2 conversion
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+      const uint32_t x = __byte_perm(f.v[0][mt >> 1], f.v[1][mt >> 1], sel);
+      const uint32_t y = __byte_perm(f.v[2][mt >> 1], f.v[3][mt >> 1], sel);
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
+      a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
+      a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
+      a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
+      mma16816<false>(st.acc[mt], a, pb0, pb1);
+    }
+  } else if constexpr (kBF) {
+    // bf16 keeps 8 significant bits; short contexts give weights near 1
+    // whose rounding would show in the output, so P goes in as a bf16 high
+    // part plus a bf16 residual (two MMAs on the same V fragments)
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const uint32_t pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h01));
+    const uint32_t pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h23));
+    const uint32_t lb0 = movmatrix_trans(pack_bf16x2(p0 - f01.x, p1 - f01.y));
+    const uint32_t lb1 = movmatrix_trans(pack_bf16x2(p2 - f23.x, p3 - f23.y));
 #pragma unroll
-      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-        const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
-        const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
-        uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
-        a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
-        a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
-        a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
-        mma16816<false>(st.acc[mt], a, pb0, pb1);
-      }
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
+      mma16816<true>(st.acc[mt], f.v[mt], pb0, pb1);
+      mma16816<true>(st.acc[mt], f.v[mt], lb0, lb1);
     }
   } else {
-    const int r = lane & 7, mi = lane >> 3;
-    const int vtok = r + ((mi >> 1) << 3), vhi = mi & 1;
-    if constexpr (kBF) {
-      // bf16 keeps 8 significant bits; short contexts give weights near 1
-      // whose rounding would show in the output, so P goes in as a bf16 high
-      // part plus a bf16 residual (two MMAs on the same V fragments)
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
-      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      pb0 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h01));
-      pb1 = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&h23));
-      const uint32_t lb0 = movmatrix_trans(pack_bf16x2(p0 - f01.x, p1 - f01.y));
-      const uint32_t lb1 = movmatrix_trans(pack_bf16x2(p2 - f23.x, p3 - f23.y));
+    const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
 #pragma unroll
-      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
-        mma16816<true>(st.acc[mt], a, pb0, pb1);
-        mma16816<true>(st.acc[mt], a, lb0, lb1);
-      }
-    } else {
-      pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-      pb1 = movmatrix_trans(pack_f16x2(p2, p3));
-#pragma unroll
-      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_trans(vb + tile_off<ROWB>(vtok, (2 * mt + vhi) * 16), a);
-        mma16816<false>(st.acc[mt], a, pb0, pb1);
-      }
-    }
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) mma16816<false>(st.acc[mt], f.v[mt], pb0, pb1);
   }
 }
 
@@ -799,15 +790,25 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
         uint8_t *tk = tiles + (size_t)stage * 2 * Cfg::TILE;
         uint8_t *tv = tk + Cfg::TILE;
         if constexpr (Cfg::MMA) {
+          // The stage is refilled after the block is computed: every fragment
+          // has been consumed by then, so the TMA overwrite needs no proxy
+          // fence.  (Refilling it right after the fragments reach registers
+          // measured 1-2 % slower on GB300.)
           if (m.flags & kFirst) mma_begin<Cfg>(state, p, m, lane);
-          mma_block<Cfg>(state, p, m, tk, tv, lane);
+          MmaFrags<Cfg> frags;
+          mma_load<Cfg>(frags, tk, tv, m.nvalid, lane);
+          mma_compute<Cfg>(state, frags, p, m, lane);
+          if (issued < total) {
+            produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane, &cta_flags);
+            ++issued;
+          }
         } else {
           if (m.flags & kFirst) simt_begin<Cfg>(state, p, m, qbuf, lane);
           simt_block<Cfg>(state, p, m, tk, tv, qbuf, lane);
-        }
-        if (issued < total) {
-          produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane, &cta_flags);
-          ++issued;
+          if (issued < total) {
+            produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane, &cta_flags);
+            ++issued;
+          }
         }
         if (m.flags & kLast) {
           if constexpr (Cfg::MMA)
