@@ -48,6 +48,9 @@ def lib():
         L.oracle_decode.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
                                     i32, i32, i32, i32, i64, i32, f64, i32]
         L.oracle_decode.restype = i32
+        L.oracle_decode_multi.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
+                                          i32, i32, i32, i32, i32, i64, i32, f64, i32]
+        L.oracle_decode_multi.restype = i32
         L.oracle_merge.argtypes = [P, P, P, i32, i32, i32]
         L.oracle_merge.restype = None
         L.oracle_num_threads.argtypes = []
@@ -149,11 +152,18 @@ def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
            nthreads=0, with_lse=False):
     """Exact attention of each query row over its sequence's gathered cache.
 
-    Returns out as float64 [B, Hq, D] (and lse [B, Hq] when with_lse)."""
+    q [B, Hq, D]: one new token per sequence -> out float64 [B, Hq, D] (and
+    lse [B, Hq] when with_lse).  q [B, q_len, Hq, D]: q_len new tokens per
+    sequence, each seeing the positions up to its own -> out [B, q_len, Hq, D]
+    (lse [B, q_len, Hq])."""
     qr = _raw(q, q_dtype)
     kc = _raw(k_cache, cache_dtype)
     vc = _raw(v_cache, cache_dtype)
-    B, Hq, D = qr.shape
+    multi = qr.ndim == 4
+    if multi:
+        B, q_len, Hq, D = qr.shape
+    else:
+        (B, Hq, D), q_len = qr.shape, 1
     num_blocks, Hkv = kc.shape[0], kc.shape[1]
     if kc.shape[2] != block_size or kc.shape[3] != D:
         raise ValueError("cache shape must be [num_blocks, Hkv, block_size, D]")
@@ -166,12 +176,18 @@ def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
         raise ValueError("fp8 cache needs k_scale and v_scale")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    out = np.empty((B, Hq, D), dtype=np.float64)
-    lse = np.empty((B, Hq), dtype=np.float64)
-    rc = lib().oracle_decode(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
-                             _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),
-                             bt.shape[1], _ptr(cl), _ptr(tb), B, Hq, Hkv, D, num_blocks,
-                             block_size, float(scale), int(nthreads))
+    out = np.empty(qr.shape, dtype=np.float64)
+    lse = np.empty(qr.shape[:-1], dtype=np.float64)
+    if multi:
+        rc = lib().oracle_decode_multi(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
+                                       _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),
+                                       bt.shape[1], _ptr(cl), _ptr(tb), B, q_len, Hq, Hkv, D,
+                                       num_blocks, block_size, float(scale), int(nthreads))
+    else:
+        rc = lib().oracle_decode(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
+                                 _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),
+                                 bt.shape[1], _ptr(cl), _ptr(tb), B, Hq, Hkv, D, num_blocks,
+                                 block_size, float(scale), int(nthreads))
     if rc == -1:
         raise ValueError("oracle_decode: Hq must be a multiple of Hkv")
     if rc == -2:

@@ -207,15 +207,22 @@ int oracle_append(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
 /* build partial results over a sub-range.  lse_out (may be NULL) receives     */
 /* log(sum_t exp(s_t)) = m + log(l); a row with no positions gives out = 0    */
 /* and lse = -inf.                                                              */
+/*                                                                          */
+/* Several new queries per sequence (q_len > 1, the verify step of           */
+/* speculative decoding, [P3] §4): the q_len newest positions are the new     */
+/* tokens, and new token i (0-based) sees positions up to its own, i.e. the   */
+/* first ctx - (q_len - 1 - i) of them — the causal mask                      */
+/* tril(diagonal = kv_len - q_len) of [P5] PART 04 naive_attention.           */
+/* q and out are then [B][q_len][Hq][D], lse [B][q_len][Hq].                  */
 /* ---------------------------------------------------------------------- */
-int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
-                  const void *k_cache, const void *v_cache, int cache_dtype,
-                  const float *k_scale, const float *v_scale,
-                  const int32_t *block_table, int max_blocks,
-                  const int32_t *context_lens, const int32_t *t_begin,
-                  int B, int Hq, int Hkv, int D, int64_t num_blocks,
-                  int block_size, double scale, int nthreads) {
-  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
+                       const void *k_cache, const void *v_cache, int cache_dtype,
+                       const float *k_scale, const float *v_scale,
+                       const int32_t *block_table, int max_blocks,
+                       const int32_t *context_lens, const int32_t *t_begin,
+                       int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                       int block_size, double scale, int nthreads) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || q_len <= 0) return -1;
   int G = Hq / Hkv;
   int err = 0;
 #ifdef _OPENMP
@@ -257,33 +264,39 @@ int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
           V[(size_t)i * D + d] = load_elem(v_cache, cache_dtype, base + d) * vs;
         }
       }
-      for (int g = 0; g < G; ++g) {
-        int hq = h * G + g;
-        double *o = out + ((size_t)b * Hq + hq) * D;
-        for (int d = 0; d < D; ++d) qv[d] = load_elem(q, q_dtype, ((size_t)b * Hq + hq) * D + d);
-        if (n == 0) {
-          for (int d = 0; d < D; ++d) o[d] = 0.0;
-          if (lse_out) lse_out[(size_t)b * Hq + hq] = -INFINITY;
-          continue;
+      for (int qi = 0; qi < q_len; ++qi) {
+        /* new token qi sees the first nq of the n positions */
+        int nq = n - (q_len - 1 - qi);
+        if (nq < 0) nq = 0;
+        size_t row = (size_t)b * q_len + qi;
+        for (int g = 0; g < G; ++g) {
+          int hq = h * G + g;
+          double *o = out + (row * Hq + hq) * D;
+          for (int d = 0; d < D; ++d) qv[d] = load_elem(q, q_dtype, (row * Hq + hq) * D + d);
+          if (nq == 0) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            if (lse_out) lse_out[row * Hq + hq] = -INFINITY;
+            continue;
+          }
+          double m = -INFINITY;
+          for (int i = 0; i < nq; ++i) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)i * D + d];
+            s[i] = scale * acc;
+            if (s[i] > m) m = s[i];
+          }
+          double l = 0.0;
+          for (int i = 0; i < nq; ++i) {
+            s[i] = exp(s[i] - m);
+            l += s[i];
+          }
+          for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int i = 0; i < nq; ++i) acc += s[i] * V[(size_t)i * D + d];
+            o[d] = acc / l;
+          }
+          if (lse_out) lse_out[row * Hq + hq] = m + log(l);
         }
-        double m = -INFINITY;
-        for (int i = 0; i < n; ++i) {
-          double acc = 0.0;
-          for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)i * D + d];
-          s[i] = scale * acc;
-          if (s[i] > m) m = s[i];
-        }
-        double l = 0.0;
-        for (int i = 0; i < n; ++i) {
-          s[i] = exp(s[i] - m);
-          l += s[i];
-        }
-        for (int d = 0; d < D; ++d) {
-          double acc = 0.0;
-          for (int i = 0; i < n; ++i) acc += s[i] * V[(size_t)i * D + d];
-          o[d] = acc / l;
-        }
-        if (lse_out) lse_out[(size_t)b * Hq + hq] = m + log(l);
       }
       free(K);
       free(V);
@@ -292,6 +305,30 @@ int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
     }
   }
   return err;
+}
+
+int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
+                  const void *k_cache, const void *v_cache, int cache_dtype,
+                  const float *k_scale, const float *v_scale,
+                  const int32_t *block_table, int max_blocks,
+                  const int32_t *context_lens, const int32_t *t_begin,
+                  int B, int Hq, int Hkv, int D, int64_t num_blocks,
+                  int block_size, double scale, int nthreads) {
+  return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
+                     block_table, max_blocks, context_lens, t_begin, B, 1, Hq, Hkv, D, num_blocks,
+                     block_size, scale, nthreads);
+}
+
+int oracle_decode_multi(double *out, double *lse_out, const void *q, int q_dtype,
+                        const void *k_cache, const void *v_cache, int cache_dtype,
+                        const float *k_scale, const float *v_scale,
+                        const int32_t *block_table, int max_blocks,
+                        const int32_t *context_lens, const int32_t *t_begin,
+                        int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                        int block_size, double scale, int nthreads) {
+  return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
+                     block_table, max_blocks, context_lens, t_begin, B, q_len, Hq, Hkv, D, num_blocks,
+                     block_size, scale, nthreads);
 }
 
 /* ---------------------------------------------------------------------- */

@@ -245,3 +245,85 @@ def test_fp8_cache_is_dequantised_bytes_times_scale():
     vs = [torch.stack([vd[tables[b][t // bs], :, t % bs] for t in range(ctx[b])]) for b in range(B)]
     ref = sdpa_reference(q.double(), ks, vs, 0.25).numpy()
     assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def _multi_case(seed, B, q_len, Hq, Hkv, D, bs, max_ctx):
+    g = torch.Generator().manual_seed(seed)
+    ctx = torch.randint(q_len, max_ctx + 1, (B,), generator=g).tolist()
+    ks = [torch.randn((c, Hkv, D), generator=g, dtype=torch.float64).float().double() for c in ctx]
+    vs = [torch.randn((c, Hkv, D), generator=g, dtype=torch.float64).float().double() for c in ctx]
+    q = torch.randn((B, q_len, Hq, D), generator=g, dtype=torch.float64).float().double()
+    nb = sum((c + bs - 1) // bs for c in ctx) + 2
+    perm = torch.randperm(nb, generator=g).numpy()
+    pk, tables, mb = scatter(ks, Hkv, D, bs, nb, perm)
+    pv, _, _ = scatter(vs, Hkv, D, bs, nb, perm)
+    return ctx, ks, vs, q, pk, pv, tables, mb
+
+
+@pytest.mark.parametrize("B,q_len,Hq,Hkv,D,bs,max_ctx", [
+    (3, 2, 8, 2, 16, 16, 40),
+    (2, 4, 8, 1, 8, 4, 37),      # MQA, small blocks
+    (2, 5, 16, 2, 64, 16, 70),   # group 8
+    (2, 3, 3, 3, 8, 2, 9),       # MHA, contexts down to q_len
+])
+def test_multi_query_matches_masked_sdpa(B, q_len, Hq, Hkv, D, bs, max_ctx):
+    """q_len new tokens per sequence (the verify step of speculative decoding,
+    'LLM推理优化实战' §4): new token i sees the cache up to its own position, the
+    mask tril(ones(q_len, kv_len), diagonal = kv_len - q_len) of the
+    naive_attention of '苦猿的大模型日记 Day45' PART 04, given to torch SDPA as a
+    boolean mask."""
+    ctx, ks, vs, q, pk, pv, tables, mb = _multi_case(7 + q_len * B, B, q_len, Hq, Hkv, D, bs,
+                                                     max_ctx)
+    scale = 1.0 / math.sqrt(D)
+    got, lse = oracle.decode(q.float().numpy(), "f32", pk.float().numpy(), pv.float().numpy(),
+                             "f32", dense_table(tables, mb), ctx, scale=scale, block_size=bs,
+                             with_lse=True)
+    assert got.shape == (B, q_len, Hq, D) and lse.shape == (B, q_len, Hq)
+    G = Hq // Hkv
+    for b in range(B):
+        T = ctx[b]
+        mask = torch.tril(torch.ones((q_len, T), dtype=torch.bool), diagonal=T - q_len)
+        Kx = ks[b].permute(1, 0, 2).repeat_interleave(G, dim=0)      # [Hq, T, D]
+        Vx = vs[b].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Qx = q[b].permute(1, 0, 2)                                     # [Hq, q_len, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(Qx, Kx, Vx, attn_mask=mask,
+                                                               scale=scale)
+        assert np.allclose(got[b], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        s = (Qx @ Kx.transpose(1, 2)) * scale
+        ref_lse = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)   # [Hq, q_len]
+        assert np.allclose(lse[b], ref_lse.T.numpy(), rtol=0, atol=1e-12)
+
+
+def test_multi_query_rows_are_single_queries_over_shorter_contexts():
+    """Token i of q_len equals a one-query decode whose context stops at its
+    own position; q_len = 1 in the 4-D form equals the 3-D form bit for bit."""
+    B, q_len, Hq, Hkv, D, bs = 3, 4, 4, 2, 8, 4
+    ctx, ks, vs, q, pk, pv, tables, mb = _multi_case(19, B, q_len, Hq, Hkv, D, bs, 30)
+    bt = dense_table(tables, mb)
+    args = (pk.float().numpy(), pv.float().numpy(), "f32", bt)
+    multi = oracle.decode(q.float().numpy(), "f32", *args, ctx, scale=0.3, block_size=bs)
+    for i in range(q_len):
+        one = oracle.decode(q[:, i].float().numpy(), "f32", *args,
+                            [c - (q_len - 1 - i) for c in ctx], scale=0.3, block_size=bs)
+        assert np.array_equal(multi[:, i], one)
+    single = oracle.decode(q[:, :1].float().numpy(), "f32", *args, ctx, scale=0.3, block_size=bs)
+    plain = oracle.decode(q[:, 0].float().numpy(), "f32", *args, ctx, scale=0.3, block_size=bs)
+    assert np.array_equal(single[:, 0], plain)
+
+
+def test_multi_query_toy_rows_of_full_masked_computation():
+    """Page 'KV Cache篇' §2.1: with '天' cached and '气真' both new, the two new
+    rows are rows 1 and 2 of the full causally masked computation."""
+    t = _toy()
+    X2 = _f64(t["X_step2"])
+    WQ, WK, WV = _f64(t["W_Q"]), _f64(t["W_K"]), _f64(t["W_V"])
+    div = t["scale_divisor"]
+    Q2, K2, V2 = [(X2 @ W).float().double() for W in (WQ, WK, WV)]
+    mask = torch.triu(torch.full((3, 3), float("-inf"), dtype=torch.float64), diagonal=1)
+    full = torch.softmax(Q2 @ K2.T / div + mask, dim=-1) @ V2
+    pk, tables, mb = scatter([K2[:, None, :]], 1, 4, 2, 2, [1, 0])
+    pv, _, _ = scatter([V2[:, None, :]], 1, 4, 2, 2, [1, 0])
+    q = Q2[1:3][None, :, None, :]                                         # [1, 2, 1, 4]
+    out = oracle.decode(q.float().numpy(), "f32", pk.float().numpy(), pv.float().numpy(), "f32",
+                        dense_table(tables, mb), [3], scale=1.0 / div, block_size=2)
+    assert np.allclose(out[0, :, 0], full[1:3].numpy(), rtol=0, atol=1e-12)

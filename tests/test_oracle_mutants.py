@@ -34,14 +34,22 @@ MUTANTS = [
      [T_fmt.test_e4m3_encoder_matches_torch_round_to_nearest_even]),
     ("merge weight sign", "double w = exp(lse - M);", "double w = exp(M - lse);",
      [T_att.test_merge_of_partials_equals_full]),
-    ("lse sign", "lse_out[(size_t)b * Hq + hq] = m + log(l);",
-     "lse_out[(size_t)b * Hq + hq] = m - log(l);",
+    ("lse sign", "lse_out[row * Hq + hq] = m + log(l);",
+     "lse_out[row * Hq + hq] = m - log(l);",
      [T_att.test_merge_of_partials_equals_full]),
     ("fresh block test", "if (off == 0) {", "if (off == 1) {",
      [T_app.test_append_fp8_uses_block_scale_or_opens_block]),
     ("f16 exponent bias", "v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
      "v = ldexp(1.0 + (double)m / 1024.0, e - 14);",
      [T_fmt.test_f16_all_codes_match_numpy]),
+    ("causal limit off by one", "int nq = n - (q_len - 1 - qi);", "int nq = n - (q_len - qi);",
+     [lambda: T_att.test_multi_query_matches_masked_sdpa(3, 2, 8, 2, 16, 16, 40),
+      T_att.test_multi_query_toy_rows_of_full_masked_computation]),
+    ("causal limit reversed", "int nq = n - (q_len - 1 - qi);", "int nq = n - qi;",
+     [T_att.test_multi_query_rows_are_single_queries_over_shorter_contexts]),
+    ("query row ignores token", "size_t row = (size_t)b * q_len + qi;",
+     "size_t row = (size_t)b * q_len;",
+     [lambda: T_att.test_multi_query_matches_masked_sdpa(2, 4, 8, 1, 8, 4, 37)]),
     ("kv bytes drops the 2", "return 2.0 * num_layers", "return 1.0 * num_layers",
      [T_app.test_kv_bytes_formula_matches_pages]),
 ]
@@ -62,7 +70,7 @@ def test_planted_mistake_is_caught(tmp_path, monkeypatch, name, orig, mut, tests
     mutant = ctypes.CDLL(str(so))
     for fn in ("oracle_f16_to_double", "oracle_bf16_to_double", "oracle_e4m3_to_double",
                "oracle_e4m3_from_float", "oracle_kv_bytes_per_token", "oracle_append",
-               "oracle_decode", "oracle_merge", "oracle_num_threads"):
+               "oracle_decode", "oracle_decode_multi", "oracle_merge", "oracle_num_threads"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)
