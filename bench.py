@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="new tokens per sequence per step (multi-query decode, causal)")
     return ap.parse_args()
 
 
@@ -169,7 +171,10 @@ def oracle_sample_rate(w, seconds, threads=0):
     bt = BlockTable(w.num_blocks)
     for b in range(w.B):
         bt.adopt(b, w.tables[b], w.cached[b])
-    slots, _ = bt.append_slots(list(range(w.B)))
+    L = w.q_len
+    slots, _ = bt.append_slots([b for b in range(w.B) for _ in range(L)])
+    k_new = w.k_new.reshape(w.B, L, w.Hkv, w.D)
+    v_new = w.v_new.reshape(w.B, L, w.Hkv, w.D)
     mb = w.max_blocks
     table = np.full((w.B, mb), -1, dtype=np.int32)
     for b in range(w.B):
@@ -184,8 +189,9 @@ def oracle_sample_rate(w, seconds, threads=0):
     while elapsed < seconds:
         rows = [(b0 + i) % w.B for i in range(n)]
         t0 = time.perf_counter()
-        oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new[rows], w.v_new[rows], w.new_dtype,
-                      [slots[r] for r in rows], ks, vs, inplace=True)
+        oracle.append(w.k_cache, w.v_cache, w.dtype, k_new[rows].reshape(-1, w.Hkv, w.D),
+                      v_new[rows].reshape(-1, w.Hkv, w.D), w.new_dtype,
+                      [slots[r * L + t] for r in rows for t in range(L)], ks, vs, inplace=True)
         oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table[rows], lens[rows],
                       scale=w.scale, k_scale=ks, v_scale=vs, nthreads=threads)
         dt = time.perf_counter() - t0
@@ -206,11 +212,13 @@ def spot_check(w, out, step):
     import numpy as np
     import oracle
     rows = sorted({0, w.B - 1})
-    slots = step.h_slots.numpy()
+    L = w.q_len
+    slots = step.h_slots.numpy().reshape(w.B, L)
     ks = None if w.k_scale is None else w.k_scale.numpy()
     vs = None if w.v_scale is None else w.v_scale.numpy()
-    oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new[rows], w.v_new[rows], w.new_dtype,
-                  slots[rows], ks, vs, inplace=True)
+    oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new[rows].reshape(-1, w.Hkv, w.D),
+                  w.v_new[rows].reshape(-1, w.Hkv, w.D), w.new_dtype,
+                  slots[rows].reshape(-1), ks, vs, inplace=True)
     table = step.h_table.numpy()[rows]
     lens = step.h_lens.numpy()[rows]
     ref = oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table, lens,
@@ -254,13 +262,17 @@ def run_reference(args, world, rank):
 
 def _workload(args):
     import workloads
+    over = {}
     if args.batch:
-        return workloads.config(args.workload, B=args.batch)
-    return workloads.config(args.workload)
+        over["B"] = args.batch
+    if args.q_len > 1:
+        over["q_len"] = args.q_len
+    return workloads.config(args.workload, **over)
 
 
 def _config(w):
-    return {"workload": w.name, "index": w.seed - 1000, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+    extra = {} if w.q_len == 1 else {"q_len": w.q_len}
+    return extra | {"workload": w.name, "index": w.seed - 1000, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
             "D": w.D, "kv_dtype": w.dtype, "q_dtype": w.q_dtype, "block_size": 16,
             "context_lens": (w.context_lens[0] if len(set(w.context_lens)) == 1
                              else f"{min(w.context_lens)}..{max(w.context_lens)}"),
@@ -288,7 +300,8 @@ def run_ours(args, world, rank, local):
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
     step = DecodeStep(w.k_cache.to(dev), w.v_cache.to(dev), w.Hq, tdt[w.q_dtype], w.max_blocks,
-                      ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale)
+                      ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
+                      q_len=w.q_len)
     for b in range(w.B):
         step.adopt(b, w.tables[b], w.cached[b])
     step.prepare()
@@ -367,7 +380,8 @@ def run_ours(args, world, rank, local):
     host_a1 = []
     for _ in range(max(5, min(args.steps, 20))):
         probe = DecodeStep(step.k_cache, step.v_cache, w.Hq, tdt[w.q_dtype], w.max_blocks,
-                           ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale)
+                           ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
+                           q_len=w.q_len)
         for b in range(w.B):
             probe.adopt(b, w.tables[b], w.cached[b])
         probe._buffers(w.B)
@@ -395,7 +409,10 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1), random block permutation)",
         "config": _config(w) | {"parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "tok_per_s": round(world * w.B / (ms_step * 1e-3), 1),
+        "tok_per_s": round(world * w.B * w.q_len / (ms_step * 1e-3), 1),
+        "attn_tflops": round(4.0 * w.Hq * w.D * sum(
+            max(0, c - w.q_len + 1 + i) for c in w.context_lens for i in range(w.q_len))
+            / (ms_attn * 1e-3) / 1e12, 2),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + decode + merge)",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,

@@ -101,7 +101,14 @@ typedef enum {
  * fresh block): then scale = max_d |x_d| / 448 (1.0 if that is 0) is computed
  * from the token and written to k_scale/v_scale first.  k_scale and v_scale are
  * required (non-NULL) exactly when cache_dtype is PKV_FP8_E4M3.
- * Slots must be distinct within one call.
+ * Slots must be distinct within one call.  Several tokens of one sequence may
+ * be appended in one call (q_len new tokens, see paged_decode_attention_multi)
+ * when they are consecutive entries of slot_mapping in position order (what
+ * pkv_bm_append_slots returns for an id repeated consecutively): a token of a
+ * block opened earlier in the same call then uses the opener's scale, exactly
+ * as if the tokens had been appended one call at a time.  With an FP8 cache,
+ * other orders that put a block's opener and a later token of it in one call
+ * are not supported.
  */
 int paged_kv_append(const void *k_new, const void *v_new, int new_dtype,
                     void *k_cache, void *v_cache, int cache_dtype,
@@ -161,6 +168,39 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
                            float scale, int num_splits,
                            void *workspace, size_t workspace_bytes,
                            pkv_stream_t stream);
+
+/*
+ * Decode attention for q_len new query tokens per sequence (the verify step
+ * of speculative decoding, "LLM推理优化实战" §4, or a chunked decode step).
+ * The q_len tokens are the newest q_len positions of each sequence and are
+ * already in the cache (appended with paged_kv_append, slots in order), so
+ * context_lens[b] counts them.  New token i (0-based) attends positions
+ * 0 .. ctx_b - q_len + i: the causal mask tril(ones(q_len, ctx), diagonal =
+ * ctx - q_len) of the naive_attention in "苦猿的大模型日记 Day45" PART 04.
+ * A row that sees no position (ctx_b < q_len - i) gives out = 0.
+ *
+ *   q, out     [B][q_len][Hq][D] (q_len = 1 is paged_decode_attention)
+ *   q_len      1 .. PKV_MAX_Q_LEN
+ * Everything else, including the workspace rule, is as for
+ * paged_decode_attention; the workspace size comes from
+ * paged_decode_multi_workspace_bytes.  Each kv head's q_len * G query rows
+ * are served in chunks of 8 (the 8 columns of one MMA tile), so the K/V of a
+ * (sequence, kv head) is read from memory once per chunk (re-reads of the
+ * same blocks mostly hit L2).
+ */
+#define PKV_MAX_Q_LEN 64
+int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
+                                       int cache_dtype, int q_dtype, int num_splits,
+                                       size_t *bytes_out);
+int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
+                                 const void *k_cache, const void *v_cache, int cache_dtype,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *block_table, int max_blocks_per_seq,
+                                 const int32_t *context_lens,
+                                 int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                                 float scale, int num_splits,
+                                 void *workspace, size_t workspace_bytes,
+                                 pkv_stream_t stream);
 
 /*
  * paged_decode_attention for callers that cannot allocate device memory.

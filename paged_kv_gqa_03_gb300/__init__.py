@@ -41,6 +41,10 @@ _sig("paged_decode_workspace_bytes", _i32, _i32, _i32, _i32, _i32, _i32, _i32, _
      ctypes.POINTER(_sz))
 _sig("paged_decode_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
      _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _sz, _P)
+_sig("paged_decode_multi_workspace_bytes", _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+     ctypes.POINTER(_sz))
+_sig("paged_decode_attention_multi", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
+     _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _sz, _P)
 _sig("paged_decode_status", _i32, _P, _sz, _P, ctypes.POINTER(_i32))
 _sig("paged_decode_merge", _i32, _P, _i32, _P, _P, _i32, _i32, _i32, _i32, _P)
 _sig("paged_kv_copy_blocks", _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
@@ -148,14 +152,18 @@ def paged_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale=None, 
         _stream(stream)), "paged_kv_append")
 
 
-def paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits=0):
-    """Workspace size for paged_decode_attention on the current device.
-    dtypes are torch dtypes or C codes."""
+def paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits=0, q_len=1):
+    """Workspace size for paged_decode_attention (q_len new tokens per
+    sequence) on the current device.  dtypes are torch dtypes or C codes."""
     conv = lambda d: d if isinstance(d, int) else _code(_torch().empty(0, dtype=d))
     out = _sz(0)
-    _check(_L.paged_decode_workspace_bytes(B, Hq, Hkv, D, conv(cache_dtype), conv(q_dtype),
-                                           num_splits, ctypes.byref(out)),
-           "paged_decode_workspace_bytes")
+    if q_len == 1:
+        rc = _L.paged_decode_workspace_bytes(B, Hq, Hkv, D, conv(cache_dtype), conv(q_dtype),
+                                             num_splits, ctypes.byref(out))
+    else:
+        rc = _L.paged_decode_multi_workspace_bytes(B, q_len, Hq, Hkv, D, conv(cache_dtype),
+                                                   conv(q_dtype), num_splits, ctypes.byref(out))
+    _check(rc, "paged_decode_workspace_bytes")
     return out.value
 
 
@@ -163,21 +171,36 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
                            k_scale=None, v_scale=None, num_splits=0, workspace=None, stream=None):
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over the paged cache.
 
+    q, out [B, Hq, D]: one new token per sequence (paged_decode_attention).
+    q, out [B, q_len, Hq, D]: q_len new tokens per sequence, token i seeing
+    the cache up to its own position (paged_decode_attention_multi).
     workspace: a uint8 CUDA tensor of paged_decode_workspace_bytes(...) bytes;
     allocated here (by torch) when None."""
     torch = _torch()
-    B, Hq, D = q.shape
+    if q.dim() == 4:
+        B, q_len, Hq, D = q.shape
+    else:
+        (B, Hq, D), q_len = q.shape, 1
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out shape {tuple(out.shape)} != q shape {tuple(q.shape)}")
     num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
     if workspace is None:
-        n = paged_decode_workspace_bytes(B, Hq, Hkv, D, _code(k_cache), _code(q), num_splits)
+        n = paged_decode_workspace_bytes(B, Hq, Hkv, D, _code(k_cache), _code(q), num_splits,
+                                         q_len=q_len)
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
-    _check(_L.paged_decode_attention(
-        _dev(out, "out"), _dev(q, "q"), _code(q), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        _code(k_cache), _dev(k_scale, "k_scale", torch.float32),
-        _dev(v_scale, "v_scale", torch.float32), _dev(block_table, "block_table", torch.int32),
-        block_table.shape[1], _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D,
-        num_blocks, float(scale), num_splits, _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _stream(stream)), "paged_decode_attention")
+    args = (_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _code(k_cache), _dev(k_scale, "k_scale", torch.float32),
+            _dev(v_scale, "v_scale", torch.float32), _dev(block_table, "block_table", torch.int32),
+            block_table.shape[1], _dev(context_lens, "context_lens", torch.int32))
+    tail = (num_blocks, float(scale), num_splits, _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if q.dim() == 4:
+        _check(_L.paged_decode_attention_multi(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
+                                               B, q_len, Hq, Hkv, D, *tail),
+               "paged_decode_attention_multi")
+    else:
+        _check(_L.paged_decode_attention(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
+                                         B, Hq, Hkv, D, *tail), "paged_decode_attention")
     return workspace
 
 

@@ -180,7 +180,7 @@ struct Choice {
 // PKV_PATH=mma or =simt forces one path wherever it is compiled (comparison
 // runs); PKV_DECODE_WARPS / PKV_DECODE_STAGES pick an alternative pipeline
 // shape where one is compiled.
-int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
+int choose_kernel(int cache_dtype, int q_dtype, int D, int R, Choice *c) {
   static const int force = [] {
     const char *v = std::getenv("PKV_PATH");
     if (v && std::strcmp(v, "simt") == 0) return 1;
@@ -197,7 +197,7 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
     return v ? std::atoi(v) : 0;
   }();
   const bool mma = cache_dtype != PKV_F32 && force != 1;
-  const int GC = mma ? 8 : (G >= 2 ? 2 : 1);
+  const int GC = mma ? 8 : (R >= 2 ? 2 : 1);
   Registry &r = registry();
   int first = -1;
   for (int i = 0; i < r.n; ++i) {
@@ -213,13 +213,14 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int G, Choice *c) {
   if (first < 0) return PKV_EUNSUPPORTED;
   c->ki = first;
   c->GC = GC;
-  c->NC = (G + GC - 1) / GC;
+  c->NC = (R + GC - 1) / GC;
   return PKV_OK;
 }
 
-int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int Hq, int Hkv, int D, int64_t num_blocks,
-                           int max_blocks) {
+int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int q_len, int Hq, int Hkv, int D,
+                           int64_t num_blocks, int max_blocks) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_blocks <= 0 || max_blocks <= 0) return PKV_EINVAL;
+  if (q_len < 1 || q_len > PKV_MAX_Q_LEN) return PKV_EINVAL;
   if (Hq % Hkv != 0) return PKV_EINVAL;
   if (esize_of(cache_dtype) == 0 || esize_of(q_dtype) == 0 || q_dtype == PKV_FP8_E4M3) return PKV_EINVAL;
   if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
@@ -228,15 +229,15 @@ int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int Hq, int Hkv,
   if (cache_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F32) return PKV_EUNSUPPORTED;
   // TMA row coordinates and the work-item count are 32-bit
   if ((double)num_blocks * Hkv * kBlock >= 2147483000.0) return PKV_EUNSUPPORTED;
-  const int G = Hq / Hkv;
-  const int NC = (G + 1) / 2;  // the most units per kv head any kernel uses
-  if ((double)B * max_blocks * Hkv * NC >= 2147483000.0) return PKV_EUNSUPPORTED;
+  const int R = q_len * (Hq / Hkv);  // query rows per kv head; units per kv head <= R
+  if ((double)B * max_blocks * Hkv * R >= 2147483000.0) return PKV_EUNSUPPORTED;
   return PKV_OK;
 }
 
 // Resolves the kernel and the partition count for a call.
-int plan_call(int cache_dtype, int q_dtype, int B, int Hq, int Hkv, int D, int num_splits, Choice *c, int *P) {
-  int rc = choose_kernel(cache_dtype, q_dtype, D, Hq / Hkv, c);
+int plan_call(int cache_dtype, int q_dtype, int B, int q_len, int Hq, int Hkv, int D, int num_splits, Choice *c,
+              int *P) {
+  int rc = choose_kernel(cache_dtype, q_dtype, D, q_len * (Hq / Hkv), c);
   if (rc != PKV_OK) return rc;
   if (num_splits < 0) return PKV_EINVAL;
   if (num_splits > 0) {
@@ -298,17 +299,22 @@ int paged_kv_append(const void *k_new, const void *v_new, int new_dtype, void *k
                                    slot_mapping, B, Hkv, D, num_blocks, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int cache_dtype, int q_dtype, int num_splits,
-                                 size_t *bytes_out) {
+int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D, int cache_dtype, int q_dtype,
+                                       int num_splits, size_t *bytes_out) {
   if (!bytes_out) return PKV_EINVAL;
-  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, Hq, Hkv, D, 1, 1);
+  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, q_len, Hq, Hkv, D, 1, 1);
   if (rc != PKV_OK) return rc;
   Choice c;
   int P = 0;
-  rc = plan_call(cache_dtype, q_dtype, B, Hq, Hkv, D, num_splits, &c, &P);
+  rc = plan_call(cache_dtype, q_dtype, B, q_len, Hq, Hkv, D, num_splits, &c, &P);
   if (rc != PKV_OK) return rc;
   *bytes_out = ws_layout(B, P, D).total;
   return PKV_OK;
+}
+
+int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int cache_dtype, int q_dtype, int num_splits,
+                                 size_t *bytes_out) {
+  return paged_decode_multi_workspace_bytes(B, 1, Hq, Hkv, D, cache_dtype, q_dtype, num_splits, bytes_out);
 }
 
 int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
@@ -316,7 +322,17 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
                            int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq, int Hkv, int D,
                            int64_t num_blocks, float scale, int num_splits, void *workspace, size_t workspace_bytes,
                            pkv_stream_t stream) {
-  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, Hq, Hkv, D, num_blocks, max_blocks_per_seq);
+  return paged_decode_attention_multi(out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale, block_table,
+                                      max_blocks_per_seq, context_lens, B, 1, Hq, Hkv, D, num_blocks, scale,
+                                      num_splits, workspace, workspace_bytes, stream);
+}
+
+int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                                 int cache_dtype, const float *k_scale, const float *v_scale,
+                                 const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
+                                 int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks, float scale,
+                                 int num_splits, void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, q_len, Hq, Hkv, D, num_blocks, max_blocks_per_seq);
   if (rc != PKV_OK) return rc;
   if (!std::isfinite(scale)) return PKV_EINVAL;
   if (B == 0) return PKV_OK;
@@ -325,7 +341,7 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
   Choice c;
   int P = 0;
-  rc = plan_call(cache_dtype, q_dtype, B, Hq, Hkv, D, num_splits, &c, &P);
+  rc = plan_call(cache_dtype, q_dtype, B, q_len, Hq, Hkv, D, num_splits, &c, &P);
   if (rc != PKV_OK) return rc;
   const WsLayout L = ws_layout(B, P, D);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
@@ -365,6 +381,8 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
   p.GC = c.GC;
   p.NC = c.NC;
   p.HU = Hkv * c.NC;
+  p.q_len = q_len;
+  p.R = q_len * p.G;
   p.P = P;
   p.max_blocks = max_blocks_per_seq;
   p.out_dtype = q_dtype;

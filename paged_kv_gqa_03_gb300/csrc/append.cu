@@ -6,7 +6,11 @@
 // "苦猿的大模型日记 Day45" PART 02), addressed through the block table
 // ("LLM推理优化实战" §2.2).  FP8 caches store e4m3(x / scale) with CUDA's
 // saturating round-to-nearest-even conversion; a token at offset 0 opens its
-// block and sets the block's scale to max|x| / 448 first.
+// block and sets the block's scale to max|x| / 448 first.  When one call
+// appends several tokens of a sequence (consecutive entries, positions in
+// order), a later token of a block opened in the same call finds its opener at
+// entry b - offset and derives the same scale from the opener's values, so it
+// never reads the scale while the opener writes it.
 #include "common.cuh"
 #include "internal.h"
 
@@ -54,6 +58,14 @@ __global__ void __launch_bounds__(128)
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
       scale = amax > 0.f ? amax / 448.0f : 1.0f;
       if (lane == 0) scales[sidx] = scale;
+    } else if (b >= off && slot_mapping[b - off] == blk * kBlock) {
+      // the block's opener is entry b - off of this call: same scale, from its values
+      const size_t osrc = ((size_t)(b - off) * Hkv + h) * D;
+      float oa = 0.f;
+      for (int e = 0; e < epl; ++e) oa = fmaxf(oa, fabsf(load_scalar(NewT{}, src, osrc + lane * epl + e)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) oa = fmaxf(oa, __shfl_xor_sync(kFull, oa, o));
+      scale = oa > 0.f ? oa / 448.0f : 1.0f;
     } else {
       scale = scales[sidx];
     }

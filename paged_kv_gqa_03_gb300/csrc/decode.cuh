@@ -2,8 +2,13 @@
 // partial results), templated on cache dtype, head dim and compute path.
 //
 // Work decomposition.  A "unit" is (sequence b, kv head h, head chunk c): the
-// query heads h*G + c*GC ... (at most GC of them) that share kv head h
-// ("大模型推理加速——KV Cache篇" §6.2 GQA).  Units are concatenated in the order
+// query rows c*GC ... (at most GC of them) of the R = q_len * G rows that
+// share kv head h ("大模型推理加速——KV Cache篇" §6.2 GQA).  Row r is query head
+// h*G + r % G of new token r / G; with q_len > 1 (several new tokens per
+// sequence, the verify step of speculative decoding, "LLM推理优化实战" §4) new
+// token i sees only the first ctx - (q_len - 1 - i) positions, the causal mask
+// tril(diagonal = kv_len - q_len) of "苦猿的大模型日记 Day45" PART 04, applied
+// per score column.  Units are concatenated in the order
 // (b, h, c), each contributing ceil(ctx_b / 16) block items, and the item list
 // is cut into P equal contiguous ranges, one per warp (the "workers").  A
 // warp streams its range block by block, carrying the online-softmax state
@@ -133,7 +138,8 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     if (pr.seg_j0 == 0 && pr.j + 1 == pr.n) flags |= kComplete;
   }
   if (pr.seg_wfirst) flags |= kWFirst;
-  const int nvalid = min(kBlock, pr.ctx - pr.j * kBlock);
+  const int rem = pr.ctx - pr.j * kBlock;
+  const int nvalid = min(kBlock, rem);
   if (lane == 0) {
     const bool bad = blk < 0 || (int64_t)blk >= p.num_blocks;
     // a bad id reads the tile just past the end of the tensor: TMA fills zeros
@@ -147,7 +153,7 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     m.ks = ks;
     m.vs = vs;
     m.flags = flags;
-    m.pad = 0;
+    m.rem = rem;
     meta[stage] = m;
     // the warp's reads of this stage have completed (their results were
     // consumed), so the TMA overwrite needs no proxy fence here
@@ -190,6 +196,19 @@ __device__ __forceinline__ void zero_tail_rows(uint8_t *tile, int nvalid, int la
   __syncwarp();
 }
 
+// Row r (0 <= r < R) of kv head h of sequence b: its offset in q / out,
+// [B][q_len][Hq][D] (q_len = 1: [B][Hq][D]), in elements.
+__device__ __forceinline__ size_t query_row(const DecodeParams &p, int b, int h, int r) {
+  const int i = r / p.G;
+  return (((size_t)b * p.q_len + i) * p.Hq + h * p.G + (r - i * p.G)) * (size_t)p.D;
+}
+
+// Positions hidden from row r at the end of the sequence: the newer tokens of
+// its step, q_len - 1 - r / G (0 for rows past R, which are padding).
+__device__ __forceinline__ int row_back(const DecodeParams &p, int r) {
+  return max(0, p.q_len - 1 - r / p.G);
+}
+
 // ---------------------------------------------------------------------------
 // MMA path state and steps.
 // ---------------------------------------------------------------------------
@@ -200,16 +219,18 @@ struct MmaState {
   uint32_t qb[KS][2];
   float acc[MT][4];
   float m0, m1, l0, l1;
+  int back0, back1;  // row_back of the score columns 2 tig, 2 tig + 1
 };
 
 template <class Cfg>
 __device__ __forceinline__ void mma_begin(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
                                           int lane) {
   const int gid = lane >> 2, tig = lane & 3;
-  const int h = m.hu / p.NC, c = m.hu % p.NC;
-  const int head0 = h * p.G + c * Cfg::GC;
-  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
-  const size_t row = ((size_t)m.b * p.Hq + head0 + gid) * Cfg::D;
+  const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
+  const int gc = min(Cfg::GC, p.R - r0);
+  const size_t row = gid < gc ? query_row(p, m.b, h, r0 + gid) : 0;
+  st.back0 = row_back(p, r0 + 2 * tig);
+  st.back1 = row_back(p, r0 + 2 * tig + 1);
 #pragma unroll
   for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
     uint32_t b0 = 0, b1 = 0;
@@ -297,7 +318,8 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
                                             const StageMeta &m, int lane) {
   constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
   const int gid = lane >> 2;
-  const int nvalid = m.nvalid;
+  // token rows of the block visible to score columns 2 tig, 2 tig + 1
+  const int lim0 = m.rem - st.back0, lim1 = m.rem - st.back1;
 
   // ---- scores S^T = K . Q^T (16 tokens x 8 heads), two independent chains ----
   float s[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -324,8 +346,10 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
   // ---- online softmax over the block (log2 domain) ----
   const float sc = p.scale_log2 * m.ks;
   float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
-  if (gid >= nvalid) x0 = x1 = -INFINITY;
-  if (gid + 8 >= nvalid) x2 = x3 = -INFINITY;
+  if (gid >= lim0) x0 = -INFINITY;
+  if (gid >= lim1) x1 = -INFINITY;
+  if (gid + 8 >= lim0) x2 = -INFINITY;
+  if (gid + 8 >= lim1) x3 = -INFINITY;
   float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -333,9 +357,11 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
     mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
   }
   const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-  const float al0 = exp2f(st.m0 - mn0), al1 = exp2f(st.m1 - mn1);
-  const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-  const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+  // a column that has seen no visible position yet keeps weight 0 (not NaN)
+  const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = exp2f(st.m0 - mb0), al1 = exp2f(st.m1 - mb1);
+  const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1);
+  const float p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
   st.l0 = st.l0 * al0 + (p0 + p2);
   st.l1 = st.l1 * al1 + (p1 + p3);
   st.m0 = mn0;
@@ -409,14 +435,14 @@ __device__ __forceinline__ void mma_finish(MmaState<Cfg> &st, const DecodeParams
     l0 += __shfl_xor_sync(kFull, l0, off);
     l1 += __shfl_xor_sync(kFull, l1, off);
   }
-  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-  const int h = m.hu / p.NC, c = m.hu % p.NC;
-  const int head0 = h * p.G + c * Cfg::GC;
-  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  // a row with no visible position (context shorter than q_len) gives 0
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
+  const int gc = min(Cfg::GC, p.R - r0);
   const int hA = 2 * tig, hB = 2 * tig + 1;
   if (m.flags & kComplete) {
-    const size_t baseA = ((size_t)m.b * p.Hq + head0 + hA) * Cfg::D;
-    const size_t baseB = baseA + Cfg::D;
+    const size_t baseA = hA < gc ? query_row(p, m.b, h, r0 + hA) : 0;
+    const size_t baseB = hB < gc ? query_row(p, m.b, h, r0 + hB) : 0;
 #pragma unroll
     for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
 #pragma unroll
@@ -453,6 +479,7 @@ struct SimtState {
   static constexpr int DPL = Cfg::D / 32;  // head-dim elements per lane in p.V
   float acc[Cfg::GC][DPL];
   float m[Cfg::GC], l[Cfg::GC];
+  int back[Cfg::GC];
 };
 
 // 16 bytes of cache elements -> floats
@@ -520,17 +547,17 @@ __device__ __forceinline__ void load_vrow(uint32_t addr, float *f) {
 template <class Cfg>
 __device__ __forceinline__ void simt_begin(SimtState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
                                            float *qbuf, int lane) {
-  const int h = m.hu / p.NC, c = m.hu % p.NC;
-  const int head0 = h * p.G + c * Cfg::GC;
-  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
+  const int gc = min(Cfg::GC, p.R - r0);
   __syncwarp();
   for (int idx = lane; idx < Cfg::GC * Cfg::D; idx += 32) {
     const int g = idx / Cfg::D, d = idx % Cfg::D;
-    qbuf[idx] = g < gc ? load_scalar(typename Cfg::Q{}, p.q, ((size_t)m.b * p.Hq + head0 + g) * Cfg::D + d) : 0.f;
+    qbuf[idx] = g < gc ? load_scalar(typename Cfg::Q{}, p.q, query_row(p, m.b, h, r0 + g) + d) : 0.f;
   }
   __syncwarp();
 #pragma unroll
   for (int g = 0; g < Cfg::GC; ++g) {
+    st.back[g] = row_back(p, r0 + g);
     st.m[g] = -INFINITY;
     st.l[g] = 0.f;
 #pragma unroll
@@ -549,6 +576,9 @@ __device__ __forceinline__ void simt_block(SimtState<Cfg> &st, const DecodeParam
   const uint32_t kb = smem_u32(tk), vb = smem_u32(tv);
   const int t = lane & 15, half = lane >> 4;
   const int nvalid = m.nvalid;
+  int vis = 0;  // rows visible to some column: p.V skips the rest
+#pragma unroll
+  for (int g = 0; g < GC; ++g) vis = max(vis, min(nvalid, m.rem - st.back[g]));
 
   // scores: lane (t, half) dots token t with half of q, then the halves add
   float part[GC];
@@ -575,13 +605,14 @@ __device__ __forceinline__ void simt_block(SimtState<Cfg> &st, const DecodeParam
 #pragma unroll
   for (int g = 0; g < GC; ++g) {
     float x = part[g] + __shfl_xor_sync(kFull, part[g], 16);
-    x = (t < nvalid) ? x * sc : -INFINITY;
+    x = (t < m.rem - st.back[g]) ? x * sc : -INFINITY;
     float bm = x;
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
     const float mn = fmaxf(st.m[g], bm);
-    const float al = exp2f(st.m[g] - mn);
-    const float pg = exp2f(x - mn);
+    const float mb = mn == -INFINITY ? 0.f : mn;  // no visible position yet: weight 0
+    const float al = exp2f(st.m[g] - mb);
+    const float pg = exp2f(x - mb);
     float bs = pg;
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) bs += __shfl_xor_sync(kFull, bs, off);
@@ -593,7 +624,7 @@ __device__ __forceinline__ void simt_block(SimtState<Cfg> &st, const DecodeParam
   }
   // p.V: lane owns head-dim elements [lane*DPL, lane*DPL + DPL)
   const uint32_t vcol = lane * DPL * T::kBytes;
-  for (int tt = 0; tt < nvalid; ++tt) {
+  for (int tt = 0; tt < vis; ++tt) {
     float vf[DPL];
     load_vrow<Cfg>(vb + tile_off<ROWB>(tt, vcol), vf);
 #pragma unroll
@@ -609,15 +640,14 @@ template <class Cfg>
 __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
                                             int w, int lane) {
   constexpr int DPL = SimtState<Cfg>::DPL;
-  const int h = m.hu / p.NC, c = m.hu % p.NC;
-  const int head0 = h * p.G + c * Cfg::GC;
-  const int gc = min(Cfg::GC, p.G - c * Cfg::GC);
+  const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
+  const int gc = min(Cfg::GC, p.R - r0);
   if (m.flags & kComplete) {
 #pragma unroll
     for (int g = 0; g < Cfg::GC; ++g) {
       if (g >= gc) break;
-      const float inv = 1.f / st.l[g];
-      const size_t base = ((size_t)m.b * p.Hq + head0 + g) * Cfg::D + lane * DPL;
+      const float inv = st.l[g] > 0.f ? 1.f / st.l[g] : 0.f;
+      const size_t base = query_row(p, m.b, h, r0 + g) + lane * DPL;
 #pragma unroll
       for (int e = 0; e < DPL; ++e) store_scalar(typename Cfg::Q{}, p.out, base + e, st.acc[g][e] * inv);
     }
@@ -627,7 +657,7 @@ __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodePara
 #pragma unroll
     for (int g = 0; g < Cfg::GC; ++g) {
       if (g >= gc) break;
-      const float inv = 1.f / st.l[g];
+      const float inv = st.l[g] > 0.f ? 1.f / st.l[g] : 0.f;
       float *o = p.part_o + (base + g) * Cfg::D + lane * DPL;
 #pragma unroll
       for (int e = 0; e < DPL; ++e) o[e] = st.acc[g][e] * inv;

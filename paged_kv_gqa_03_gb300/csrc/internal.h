@@ -32,10 +32,10 @@ constexpr int kInlinePrefix = 2048;
 
 // Per stage of a warp's pipeline: what the producer issued into it.
 struct StageMeta {
-  int32_t b, hu, j, nvalid;
+  int32_t b, hu, j, nvalid;  // nvalid = min(16, rem): cache rows of the block inside ctx
   float ks, vs;
   int32_t flags;
-  int32_t pad;
+  int32_t rem;               // ctx - 16 j: positions of the sequence from this block on
 };
 enum : int32_t {
   kFirst = 1,     // first block of a segment: reset state, load q
@@ -59,6 +59,8 @@ struct DecodeParams {
   int32_t *cta_flags;   // [decode CTAs] PKV_FLAG_* bits of each decode CTA
   int64_t num_blocks;
   int B, Hq, Hkv, D, G, GC, NC, HU, P;
+  int q_len;            // new query tokens per sequence (1 = plain decode)
+  int R;                // query rows per kv head = q_len * G, cut into NC chunks of GC
   int max_blocks;
   int out_dtype;
   float scale_log2;     // softmax scale * log2(e)

@@ -161,17 +161,20 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p)
   }
   const int u = blockIdx.x;
   const int b = u / p.HU, hu = u % p.HU;
-  const int h = hu / p.NC, c = hu % p.NC;
-  const int head0 = h * p.G + c * p.GC;
-  const int gc = min(p.GC, p.G - c * p.GC);
+  const int h = hu / p.NC, r0 = (hu % p.NC) * p.GC;
+  const int gc = min(p.GC, p.R - r0);
   const int D = p.D;
   const int pb = p.prefix[b];
   const int n = p.prefix[b + 1] - pb;
   const int nvec = gc * D / 4;
-  const size_t out0 = ((size_t)b * p.Hq + head0) * D;
+  // output offset of row r0 + g of this unit ([B][q_len][Hq][D])
+  auto out_row = [&](int g) {
+    const int r = r0 + g, i = r / p.G;
+    return (((size_t)b * p.q_len + i) * p.Hq + h * p.G + (r - i * p.G)) * (size_t)D;
+  };
   if (n == 0) {  // nothing to attend: the output is zero
     for (int v = threadIdx.x; v < nvec; v += blockDim.x)
-      store4_out(p.out_dtype, p.out, out0 + 4 * (size_t)v, make_float4(0.f, 0.f, 0.f, 0.f));
+      store4_out(p.out_dtype, p.out, out_row(4 * v / D) + (4 * v) % D, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
   const int64_t W = (int64_t)p.HU * p.prefix[p.B];
@@ -232,8 +235,8 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p)
   for (int k = 0; k < kVecPerThread; ++k) {
     const int v = threadIdx.x + k * blockDim.x;
     if (v >= nvec) continue;
-    const float inv = 1.f / den[k];
-    store4_out(p.out_dtype, p.out, out0 + 4 * (size_t)v,
+    const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;  // no visible position: 0
+    store4_out(p.out_dtype, p.out, out_row(4 * v / D) + (4 * v) % D,
                make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
   }
 }

@@ -6,6 +6,10 @@
   a3  paged_kv_append of the new token's K/V at its slot;
   a4-a8  paged_decode_attention (gather, scores, online softmax, p.V, merge).
 
+With q_len > 1 every sequence appends q_len tokens per step (slots in order)
+and attends them causally (the verify step of speculative decoding): q, out
+are [B, q_len, Hq, D] and k_new, v_new [B, q_len, Hkv, D].
+
 Device state (caches, scales, workspace) stays resident.  Per step only q,
 k_new, v_new and the host-produced slot mapping / copy pairs / tables /
 lengths cross to the device, all from ONE pinned staging buffer with one copy
@@ -41,13 +45,14 @@ class _Staging:
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, Hq, q_dtype, max_blocks, k_scale=None, v_scale=None,
-                 num_splits=0, stream=None, scale=None):
+                 num_splits=0, stream=None, scale=None, q_len=1):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
         self.num_blocks, self.Hkv, _, self.D = k_cache.shape
         self.Hq, self.q_dtype, self.max_blocks = Hq, q_dtype, max_blocks
         self.new_dtype = q_dtype if k_cache.dtype == torch.float8_e4m3fn else k_cache.dtype
         self.num_splits = num_splits
+        self.q_len = q_len
         self.scale = 1.0 / float(np.sqrt(self.D)) if scale is None else float(scale)
         self.device = k_cache.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -61,11 +66,14 @@ class DecodeStep:
 
     # -- buffers ---------------------------------------------------------------
     def _layout(self, B):
-        sections = [("q", (B, self.Hq, self.D), self.q_dtype),
-                    ("k_new", (B, self.Hkv, self.D), self.new_dtype),
-                    ("v_new", (B, self.Hkv, self.D), self.new_dtype),
-                    ("slots", (B,), torch.int64),
-                    ("pairs", (2 * B,), torch.int32),
+        L = self.q_len
+        rows = (B, self.Hq, self.D) if L == 1 else (B, L, self.Hq, self.D)
+        kv = (B, self.Hkv, self.D) if L == 1 else (B, L, self.Hkv, self.D)
+        sections = [("q", rows, self.q_dtype),
+                    ("k_new", kv, self.new_dtype),
+                    ("v_new", kv, self.new_dtype),
+                    ("slots", (B * L,), torch.int64),
+                    ("pairs", (2 * B * L,), torch.int32),
                     ("table", (B, self.max_blocks), torch.int32),
                     ("lens", (B,), torch.int32)]
         layout, off = {}, 0
@@ -86,12 +94,13 @@ class DecodeStep:
         self._host = [_Staging(layout, total, torch.device("cpu"), pin) for _ in range(2)]
         self._dev = _Staging(layout, total, self.device, False)
         self.h_seqs = np.empty(B, dtype=np.int64)
+        self.h_tok_seqs = np.empty(B * self.q_len, dtype=np.int64)
         self.d_q, self.d_k_new, self.d_v_new = self._dev["q"], self._dev["k_new"], self._dev["v_new"]
         self.d_slots, self.d_pairs = self._dev["slots"], self._dev["pairs"]
         self.d_table, self.d_lens = self._dev["table"], self._dev["lens"]
         self._select(self._turn)
         n = paged_decode_workspace_bytes(B, self.Hq, self.Hkv, self.D, self.k_cache.dtype,
-                                         self.q_dtype, self.num_splits)
+                                         self.q_dtype, self.num_splits, q_len=self.q_len)
         self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
 
     def _select(self, turn):
@@ -108,8 +117,8 @@ class DecodeStep:
     def prepare(self, seqs=None):
         """Host part of a step: switches to the other staging buffer (waiting
         for the copy that last read it), then writes the slots, copy pairs,
-        tables and lengths of one new token per sequence into it.  Returns the
-        number of copy-on-write pairs (raises on OOM)."""
+        tables and lengths of q_len new tokens per sequence into it.  Returns
+        the number of copy-on-write pairs (raises on OOM)."""
         seqs = self.seqs if seqs is None else seqs
         self._buffers(len(seqs))
         self._turn ^= 1
@@ -117,7 +126,12 @@ class DecodeStep:
             self._host[self._turn].done.synchronize()
         self._select(self._turn)
         self.h_seqs[:] = seqs
-        ncow = self.bm.append_slots_into(self.h_seqs, self.h_slots.numpy(), self.h_pairs.numpy())
+        if self.q_len == 1:
+            tok_seqs = self.h_seqs
+        else:
+            tok_seqs = self.h_tok_seqs
+            tok_seqs.reshape(-1, self.q_len)[:] = self.h_seqs[:, None]
+        ncow = self.bm.append_slots_into(tok_seqs, self.h_slots.numpy(), self.h_pairs.numpy())
         if ncow < 0:
             raise MemoryError("block manager out of blocks")
         self.ncow = ncow
@@ -155,6 +169,9 @@ class DecodeStep:
         if self.ncow:
             paged_kv_copy_blocks(self.k_cache, self.v_cache, self.d_pairs[:2 * self.ncow].view(-1, 2),
                                  self.k_scale, self.v_scale, stream=s)
+        if self.q_len > 1:
+            k_new = k_new.view(-1, self.Hkv, self.D)
+            v_new = v_new.view(-1, self.Hkv, self.D)
         paged_kv_append(k_new, v_new, self.k_cache, self.v_cache, self.d_slots, self.k_scale,
                         self.v_scale, stream=s)
         self.attend(q, out)

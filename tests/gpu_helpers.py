@@ -50,7 +50,7 @@ def run_gpu_step(w, num_splits=0, stream=None):
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
     step = DecodeStep(kc, vc, w.Hq, TORCH[w.q_dtype], w.max_blocks, ks, vs,
-                      num_splits=num_splits, stream=stream, scale=w.scale)
+                      num_splits=num_splits, stream=stream, scale=w.scale, q_len=w.q_len)
     for b in range(w.B):
         step.adopt(b, w.tables[b], w.cached[b])
     step.prepare()
@@ -67,7 +67,7 @@ def run_oracle_step(w):
     bt = BlockTable(w.num_blocks)
     for b in range(w.B):
         bt.adopt(b, w.tables[b], w.cached[b])
-    slots, cow = bt.append_slots(list(range(w.B)))
+    slots, cow = bt.append_slots([b for b in range(w.B) for _ in range(w.q_len)])
     assert cow == []
     mb = w.max_blocks
     table = np.full((w.B, mb), -1, dtype=np.int32)
@@ -75,7 +75,9 @@ def run_oracle_step(w):
         t = bt.seq_tables[b]
         table[b, :len(t)] = t
     lens = np.array([bt.seq_tokens[b] for b in range(w.B)], dtype=np.int32)
-    kc, vc, ks, vs = oracle.append(w.k_cache, w.v_cache, w.dtype, w.k_new, w.v_new, w.new_dtype,
+    k_new = w.k_new.reshape(-1, w.Hkv, w.D)
+    v_new = w.v_new.reshape(-1, w.Hkv, w.D)
+    kc, vc, ks, vs = oracle.append(w.k_cache, w.v_cache, w.dtype, k_new, v_new, w.new_dtype,
                                    slots, None if w.k_scale is None else w.k_scale.numpy(),
                                    None if w.v_scale is None else w.v_scale.numpy())
     out = oracle.decode(w.q, w.q_dtype, kc, vc, w.dtype, table, lens, scale=w.scale,

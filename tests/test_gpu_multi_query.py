@@ -1,0 +1,186 @@
+"""GPU parity of multi-query paged decode: q_len new tokens per sequence
+appended in one step and attended causally (new token i sees the cache up to
+its own position — the verify step of speculative decoding, "LLM推理优化实战"
+§4, with the mask tril(diagonal = kv_len - q_len) of "苦猿的大模型日记 Day45"
+PART 04), through the C ABI against the oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import compare, run_gpu_step, run_oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _pkv():
+    import paged_kv_gqa_03_gb300 as pkv
+    return pkv
+
+
+def _bytes(t):
+    return t.detach().cpu().contiguous().view(torch.uint8).numpy()
+
+
+def _check_step(w, num_splits=0):
+    step, out = run_gpu_step(w, num_splits=num_splits)
+    slots, table, lens, (kc, vc, ks, vs), ref = run_oracle_step(w)
+    assert step.h_slots.tolist() == slots
+    assert np.array_equal(step.h_table.numpy(), table)
+    assert np.array_equal(step.h_lens.numpy(), lens)
+    assert np.array_equal(_bytes(step.k_cache).reshape(-1), kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(_bytes(step.v_cache).reshape(-1), vc.view(np.uint8).reshape(-1))
+    if ks is not None:
+        assert np.array_equal(step.k_scale.cpu().numpy(), ks)
+        assert np.array_equal(step.v_scale.cpu().numpy(), vs)
+    rc, flags = _pkv().paged_decode_status(step.workspace, step.stream)
+    assert rc == 0 and flags == 0
+    assert out.shape == (w.B, w.q_len, w.Hq, w.D)
+    return compare(out, ref, w.dtype, f"{w.name} q_len {w.q_len}")
+
+
+@pytest.mark.parametrize("spec", [
+    dict(Hq=16, Hkv=2, D=128, dtype="bf16", q_len=2, ctx=[40, 300, 2, 17]),
+    dict(Hq=16, Hkv=2, D=128, dtype="bf16", q_len=4, ctx=[4, 16, 33, 700]),
+    dict(Hq=16, Hkv=2, D=64, dtype="bf16", q_len=8, ctx=[8, 100, 250]),
+    dict(Hq=8, Hkv=1, D=128, dtype="bf16", q_len=5, ctx=[5, 21, 160]),           # MQA, R = 40
+    dict(Hq=6, Hkv=2, D=128, dtype="bf16", q_len=3, ctx=[3, 47, 129]),           # R = 9: 8 + 1
+    dict(Hq=4, Hkv=4, D=128, dtype="f16", q_len=3, ctx=[3, 47, 129]),            # MHA, R = 3
+    dict(Hq=8, Hkv=2, D=128, dtype="f16", q_len=6, ctx=[6, 90, 512]),
+    dict(Hq=8, Hkv=2, D=128, dtype="fp8_e4m3", q_dtype="bf16", q_len=4, ctx=[19, 35, 4, 200]),
+    dict(Hq=8, Hkv=2, D=64, dtype="fp8_e4m3", q_dtype="f16", q_len=2, ctx=[17, 2, 63]),
+    dict(Hq=8, Hkv=2, D=128, dtype="f32", q_len=3, ctx=[3, 40, 177]),            # CUDA cores, GC 2
+    dict(Hq=2, Hkv=2, D=64, dtype="f32", q_len=2, ctx=[2, 18, 33]),              # group 1, R = 2
+], ids=lambda s: f"{s['dtype']}-q{s['Hq']}-kv{s['Hkv']}-d{s['D']}-L{s['q_len']}")
+def test_multi_query_shapes_and_dtypes(spec):
+    """Contexts cover ctx == q_len (nothing cached), tokens that open one or
+    two blocks inside the step (fp8: a block's scale set by a token of the
+    same call), ragged tails and several partition counts."""
+    spec = dict(spec)
+    spec.setdefault("q_dtype", spec["dtype"])
+    spec["B"] = len(spec["ctx"])
+    spec.update(free_frac=0.5, min_free=8)
+    for seed, splits in ((5, 0), (6, 5), (7, 1000)):
+        _check_step(workloads.make(spec, seed=seed), num_splits=splits)
+
+
+@pytest.mark.parametrize("q_len", [2, 4, 8])
+def test_multi_query_llama70b_layer(q_len):
+    """The Llama-3.1-70B-shaped GQA-8 bf16 layer (Hq 64, Hkv 8, D 128) at
+    context 8192 with q_len new tokens per sequence, 16 sequences, every
+    output compared."""
+    w = workloads.config(3, B=16, q_len=q_len)
+    stats = _check_step(w)
+    print(f"q_len {q_len}: {stats}")
+
+
+def test_multi_query_full_size_workload():
+    """64 sequences of 8192 positions (the bench's multi-query workload at
+    q_len 4), every output compared."""
+    stats = _check_step(workloads.config(3, q_len=4))
+    print(stats)
+
+
+def test_rows_that_see_nothing_are_zero():
+    """A context shorter than q_len leaves the first rows of that sequence
+    with no visible position: their output is 0, the others are exact."""
+    pkv = _pkv()
+    dev = "cuda"
+    g = torch.Generator().manual_seed(12)
+    B, L, Hq, Hkv, D, nb = 3, 4, 8, 2, 128, 6
+    q = torch.randn((B, L, Hq, D), generator=g).to(torch.bfloat16)
+    kc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    table = torch.tensor([[0, 1], [2, 3], [4, 5]], dtype=torch.int32)
+    lens = torch.tensor([2, 0, 20], dtype=torch.int32)
+    for splits in (0, 1, 7):
+        out = torch.empty_like(q, device=dev)
+        ws = pkv.paged_decode_attention(out, q.to(dev), kc.to(dev), vc.to(dev), table.to(dev),
+                                        lens.to(dev), 0.1, num_splits=splits)
+        rc, flags = pkv.paged_decode_status(ws)
+        assert rc == 0 and flags == 0
+        got = out.cpu()
+        assert torch.all(got[0, :2] == 0) and torch.all(got[1] == 0)
+        ref = oracle.decode(q, "bf16", kc, vc, "bf16", table.numpy(), lens.numpy(), scale=0.1)
+        compare(out, ref, "bf16", f"short contexts, splits {splits}")
+
+
+def test_q_len_one_in_4d_form_is_the_plain_decode():
+    w = workloads.make(dict(B=5, Hq=16, Hkv=2, D=128, dtype="bf16", ctx_range=(1, 400),
+                            free_frac=0.3), seed=41)
+    pkv = _pkv()
+    dev = "cuda"
+    table = np.full((w.B, w.max_blocks), -1, dtype=np.int32)
+    for b in range(w.B):
+        table[b, :len(w.tables[b])] = w.tables[b]
+    lens = torch.tensor(w.cached, dtype=torch.int32, device=dev)
+    args = (w.k_cache.to(dev), w.v_cache.to(dev), torch.from_numpy(table).to(dev), lens, w.scale)
+    q = w.q.to(dev)
+    o3 = torch.empty_like(q)
+    o4 = torch.empty_like(q)[:, None]
+    pkv.paged_decode_attention(o3, q, *args)
+    pkv.paged_decode_attention(o4, q[:, None].contiguous(), *args)
+    torch.cuda.synchronize()
+    assert torch.equal(o3, o4[:, 0])
+
+
+def test_multi_token_append_into_shared_partial_block():
+    """Two forks of a 390-token parent (24 full blocks + 6 tokens) append 3
+    tokens each in one step: each copies the shared partial block once, then
+    writes all three tokens into its copy; the parent is untouched
+    ("LLM推理优化实战" §2.2 copy-on-write)."""
+    from oracle.block_table import BlockTable
+    from paged_kv_gqa_03_gb300.step import DecodeStep
+    dev = "cuda"
+    L, Hq, Hkv, D, nb = 3, 32, 8, 128, 40
+    g = torch.Generator().manual_seed(19)
+    kc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    q = torch.randn((2, L, Hq, D), generator=g).to(torch.bfloat16)
+    kn = torch.randn((2, L, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = torch.randn((2, L, Hkv, D), generator=g).to(torch.bfloat16)
+    step = DecodeStep(kc.to(dev), vc.to(dev), Hq, torch.bfloat16, 32, scale=0.09, q_len=L)
+    ref_bt = BlockTable(nb)
+    for bm in (step.bm, ref_bt):
+        bm.allocate(0, 390)
+        bm.fork(0, 1)
+        bm.fork(0, 2)
+    ncow = step.prepare([1, 2])
+    step.upload()
+    assert ncow == 2
+    slots_ref, cow_ref = ref_bt.append_slots([1, 1, 1, 2, 2, 2])
+    assert step.h_slots.tolist() == slots_ref
+    assert [tuple(step.h_pairs[2 * i:2 * i + 2].tolist()) for i in range(2)] == cow_ref
+    out = torch.empty((2, L, Hq, D), dtype=torch.bfloat16, device=dev)
+    step.launch(q.to(dev), kn.to(dev), vn.to(dev), out)
+    step.stream.synchronize()
+    kr, vr = kc.clone(), vc.clone()
+    for src, dst in cow_ref:
+        kr[dst], vr[dst] = kr[src], vr[src]
+    kr, vr, _, _ = oracle.append(kr, vr, "bf16", kn.reshape(-1, Hkv, D), vn.reshape(-1, Hkv, D),
+                                 "bf16", slots_ref)
+    assert np.array_equal(_bytes(step.k_cache), kr.view(np.uint8).reshape(_bytes(step.k_cache).shape))
+    assert np.array_equal(_bytes(step.v_cache), vr.view(np.uint8).reshape(_bytes(step.v_cache).shape))
+    table, lens = step.bm.export([1, 2], 32)
+    assert lens.tolist() == [393, 393]
+    ref = oracle.decode(q, "bf16", kr, vr, "bf16", table, lens, scale=0.09)
+    compare(out, ref, "bf16", "multi-token cow")
+
+
+def test_captured_multi_query_step_matches_eager():
+    w = workloads.config(3, B=4, ctx=[700, 17, 33, 1500], free_frac=0.3, min_free=8, q_len=3)
+    step, out = run_gpu_step(w)
+    eager_out = out.cpu()
+    eager_k = step.k_cache.cpu()
+    step.h_q.copy_(w.q)
+    step.h_k_new.copy_(w.k_new)
+    step.h_v_new.copy_(w.v_new)
+    hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    step.capture(hout)
+    for _ in range(2):
+        hout.zero_()
+        step.replay()
+        step.stream.synchronize()
+        assert torch.equal(hout, eager_out)
+    assert torch.equal(step.k_cache.cpu(), eager_k)

@@ -23,6 +23,12 @@ Recipe (the same for every workload):
     the tile is stored as e4m3 of x / scale (torch's float8_e4m3fn cast).
 
 `context_lens` of a workload are attended lengths, i.e. cached + 1.
+
+A spec with `q_len` = L > 1 (several new tokens per sequence, as in the verify
+step of speculative decoding) appends L tokens per sequence: `ctx` still
+gives attended lengths, cached = ctx - L, q is [B, L, Hq, D] and k_new / v_new
+are [B, L, Hkv, D] (token t of sequence b at position cached_b + t), each taken
+from the pool and zeroed as above.  Without `q_len` the draws are unchanged.
 """
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -76,6 +82,7 @@ class Workload:
     prefix_blocks: int = 0
     seed: int = 0
     extra: dict = field(default_factory=dict)
+    q_len: int = 1               # new tokens per sequence
 
     @property
     def new_dtype(self):
@@ -83,7 +90,7 @@ class Workload:
 
     @property
     def context_lens(self):
-        return [c + 1 for c in self.cached]
+        return [c + self.q_len for c in self.cached]
 
     @property
     def scale(self):
@@ -108,8 +115,8 @@ class Workload:
             nb = (c + BLOCK - 1) // BLOCK
             for j in range(min(nb, len(self.tables[b]))):
                 blocks.add(self.tables[b][j])
-        nb_new = sum(1 for b, c in enumerate(self.context_lens)
-                     if (c + BLOCK - 1) // BLOCK > len(self.tables[b]))
+        nb_new = sum(max(0, (c + BLOCK - 1) // BLOCK - len(self.tables[b]))
+                     for b, c in enumerate(self.context_lens))
         per_block = 2 * self.Hkv * BLOCK * self.D * ITEMSIZE[self.dtype]
         return (len(blocks) + nb_new) * per_block
 
@@ -143,7 +150,10 @@ def make(spec, seed: int) -> Workload:
     else:
         lo, hi = spec["suffix_range"]
         ctx = [prefix + s + 1 for s in torch.randint(lo, hi + 1, (B,), generator=g).tolist()]
-    cached = [c - 1 for c in ctx]
+    L = spec.get("q_len", 1)
+    cached = [c - L for c in ctx]
+    if min(cached, default=0) < 0:
+        raise ValueError("context shorter than q_len")
 
     # (2) physical blocks
     pblocks = prefix // BLOCK
@@ -185,31 +195,35 @@ def make(spec, seed: int) -> Workload:
         k_scale = v_scale = None
 
     # (5) queries
-    q = torch.randn((B, Hq, D), generator=g, dtype=torch.float32).to(_TORCH[q_dtype])
+    qshape = (B, Hq, D) if "q_len" not in spec else (B, L, Hq, D)
+    q = torch.randn(qshape, generator=g, dtype=torch.float32).to(_TORCH[q_dtype])
 
-    # appended tokens: the pool value at position `cached`, then zeroed
-    k_new = torch.empty((B, Hkv, D), dtype=_TORCH[new_dtype])
-    v_new = torch.empty((B, Hkv, D), dtype=_TORCH[new_dtype])
+    # appended tokens: the pool value at positions cached .. cached + L - 1, then zeroed
+    k_new = torch.empty((B, L, Hkv, D), dtype=_TORCH[new_dtype])
+    v_new = torch.empty((B, L, Hkv, D), dtype=_TORCH[new_dtype])
     for b in range(B):
-        pos = cached[b]
-        j, off = pos // BLOCK, pos % BLOCK
-        if j < len(tables[b]):
-            blk = tables[b][j]
-        else:  # the token opens a block the block manager will pick; draw from a
-            blk = perm[(used + b) % num_blocks]  # deterministic spare tile instead
-        if dtype == "fp8_e4m3":
-            k_new[b] = k_vals[blk, :, off, :].to(k_new.dtype)
-            v_new[b] = v_vals[blk, :, off, :].to(v_new.dtype)
-        else:
-            k_new[b] = k_cache[blk, :, off, :]
-            v_new[b] = v_cache[blk, :, off, :]
-        if j < len(tables[b]):
-            k_cache[blk, :, off, :] = 0
-            v_cache[blk, :, off, :] = 0
+        for t in range(L):
+            pos = cached[b] + t
+            j, off = pos // BLOCK, pos % BLOCK
+            if j < len(tables[b]):
+                blk = tables[b][j]
+            else:  # the token opens a block the block manager will pick; draw from a
+                blk = perm[(used + b * L + t) % num_blocks]  # deterministic spare tile instead
+            if dtype == "fp8_e4m3":
+                k_new[b, t] = k_vals[blk, :, off, :].to(k_new.dtype)
+                v_new[b, t] = v_vals[blk, :, off, :].to(v_new.dtype)
+            else:
+                k_new[b, t] = k_cache[blk, :, off, :]
+                v_new[b, t] = v_cache[blk, :, off, :]
+            if j < len(tables[b]):
+                k_cache[blk, :, off, :] = 0
+                v_cache[blk, :, off, :] = 0
+    if "q_len" not in spec:
+        k_new, v_new = k_new[:, 0], v_new[:, 0]
     return Workload(name=spec.get("name", "custom"), B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
                     q_dtype=q_dtype, num_blocks=num_blocks, q=q, k_new=k_new, v_new=v_new,
                     k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
-                    tables=tables, cached=cached, prefix_blocks=pblocks, seed=seed)
+                    tables=tables, cached=cached, prefix_blocks=pblocks, seed=seed, q_len=L)
 
 
 def config(index: int, **overrides) -> Workload:
