@@ -144,9 +144,9 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_traffic():
+def kernel_traffic(q_len=1):
     """DRAM bytes per decode launch from the committed ncu capture, if the
-    kernel sources are unchanged since it was taken."""
+    kernel sources are unchanged since it was taken and it covers q_len."""
     try:
         with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
             rec = json.load(f)
@@ -156,7 +156,7 @@ def kernel_traffic():
     for name in ("common.cuh", "decode.cuh", "internal.h"):
         with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
-    if rec.get("source_sha256") != h.hexdigest():
+    if rec.get("source_sha256") != h.hexdigest() or rec.get("q_len", 1) != q_len:
         return None
     return rec.get("dram_bytes_per_launch_scaled")
 
@@ -417,7 +417,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + decode + merge)",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": kernel_traffic(), "algorithmic_bytes_per_launch": kv,
+                     "traffic": kernel_traffic(w.q_len), "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_gbs(kv, world, ms_e2e), 2), "unit": "GB/s",
