@@ -337,6 +337,20 @@ int pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child);
 /* free(seq): refcount - 1 per block, blocks at 0 go back to the free list. */
 int pkv_bm_free(pkv_block_manager *bm, int64_t seq);
 
+/* Sliding window (KV eviction, "苦猿的大模型日记 Day45" PART 02: a fixed cache
+ * bound in exchange for visible history): with window W >= 1 the sequence's
+ * next token (position tokens(seq)) and every later one see only positions
+ * >= tokens(seq) + 1 - W, so every block whose 16 positions all lie below that
+ * is released: refcount - 1 (back to the end of the free list at 0, in table
+ * order) and its table entry becomes -1 (exported as -1; fork and free skip
+ * it).  The table keeps its length, so logical block j stays entry j.  Call it
+ * before a step's pkv_bm_append_slots with the window that step's
+ * paged_decode_attention_multi uses; *released_out (may be NULL) receives the
+ * number of entries released.  PKV_EINVAL for W < 1, PKV_ENOTFOUND for an
+ * unknown id. */
+int pkv_bm_release_window(pkv_block_manager *bm, int64_t seq, int64_t window,
+                          int64_t *released_out);
+
 /*
  * Reserves the slot of one new token for each of the n sequences seqs[i]:
  *   pos = tokens(seq); if pos % 16 == 0 a fresh block is appended to the table;

@@ -49,7 +49,7 @@ def lib():
                                     i32, i32, i32, i32, i64, i32, f64, i32]
         L.oracle_decode.restype = i32
         L.oracle_decode_multi.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
-                                          i32, i32, i32, i32, i32, i64, i32, f64, i32]
+                                          i32, i32, i32, i32, i32, i32, i64, i32, f64, i32]
         L.oracle_decode_multi.restype = i32
         L.oracle_merge.argtypes = [P, P, P, i32, i32, i32]
         L.oracle_merge.restype = None
@@ -149,13 +149,14 @@ def append(k_cache, v_cache, cache_dtype, k_new, v_new, new_dtype, slot_mapping,
 
 def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
            scale=None, k_scale=None, v_scale=None, block_size=16, t_begin=None,
-           nthreads=0, with_lse=False):
+           nthreads=0, with_lse=False, window=0):
     """Exact attention of each query row over its sequence's gathered cache.
 
     q [B, Hq, D]: one new token per sequence -> out float64 [B, Hq, D] (and
     lse [B, Hq] when with_lse).  q [B, q_len, Hq, D]: q_len new tokens per
     sequence, each seeing the positions up to its own -> out [B, q_len, Hq, D]
-    (lse [B, q_len, Hq])."""
+    (lse [B, q_len, Hq]).  window > 0: each row sees only the `window` most
+    recent positions up to its own."""
     qr = _raw(q, q_dtype)
     kc = _raw(k_cache, cache_dtype)
     vc = _raw(v_cache, cache_dtype)
@@ -178,11 +179,11 @@ def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
         scale = 1.0 / math.sqrt(D)
     out = np.empty(qr.shape, dtype=np.float64)
     lse = np.empty(qr.shape[:-1], dtype=np.float64)
-    if multi:
+    if multi or window:
         rc = lib().oracle_decode_multi(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
                                        _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),
-                                       bt.shape[1], _ptr(cl), _ptr(tb), B, q_len, Hq, Hkv, D,
-                                       num_blocks, block_size, float(scale), int(nthreads))
+                                       bt.shape[1], _ptr(cl), _ptr(tb), B, q_len, int(window), Hq,
+                                       Hkv, D, num_blocks, block_size, float(scale), int(nthreads))
     else:
         rc = lib().oracle_decode(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc),
                                  _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt),

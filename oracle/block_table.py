@@ -24,6 +24,14 @@ copied only when a request modifies them).  New tokens go to position
 num_tokens // BLOCK_SIZE); a fresh block is needed only when that position
 starts a block.  ``adopt`` (not on the page) registers a table built elsewhere,
 removing its blocks from the free list while keeping the order of the rest.
+
+``release_outside_window`` (not on the page; the sliding window / KV eviction
+of "苦猿的大模型日记 Day45" PART 02 keeps a fixed cache bound by giving up
+history): with window W, the next token (position num_tokens) and every later
+one see positions >= num_tokens + 1 - W only, so every block whose 16
+positions all lie below that is released — its reference dropped (free list
+end when it reaches 0, in table order) and its table entry set to -1.  fork
+and free skip -1 entries.
 """
 
 
@@ -81,17 +89,40 @@ class BlockTable:
         self.seq_tables[child_id] = list(parent_blocks)
         self.seq_tokens[child_id] = self.seq_tokens[parent_id]
         for blk in parent_blocks:
-            self.block_refcount[blk] += 1
+            if blk >= 0:
+                self.block_refcount[blk] += 1
         return True
 
     def free(self, seq_id):
         self._compact()
         for blk in self.seq_tables[seq_id]:
+            if blk < 0:
+                continue
             self.block_refcount[blk] -= 1
             if self.block_refcount[blk] == 0:
                 self.free_blocks.append(blk)
         del self.seq_tables[seq_id]
         del self.seq_tokens[seq_id]
+
+    def release_outside_window(self, seq_id, window):
+        """Releases the blocks no later token can see; returns how many."""
+        if window < 1:
+            raise ValueError("window must be >= 1")
+        self._compact()
+        table = self.seq_tables[seq_id]
+        first_visible = self.seq_tokens[seq_id] + 1 - window
+        n = min(len(table), max(0, first_visible) // self.block_size)
+        released = 0
+        for j in range(n):
+            blk = table[j]
+            if blk < 0:
+                continue
+            self.block_refcount[blk] -= 1
+            if self.block_refcount[blk] == 0:
+                self.free_blocks.append(blk)
+            table[j] = -1
+            released += 1
+        return released
 
     def append_slots(self, seq_ids):
         """One new token per sequence.  Returns (slots, cow_pairs) or None on

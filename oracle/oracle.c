@@ -214,15 +214,21 @@ int oracle_append(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
 /* first ctx - (q_len - 1 - i) of them — the causal mask                      */
 /* tril(diagonal = kv_len - q_len) of [P5] PART 04 naive_attention.           */
 /* q and out are then [B][q_len][Hq][D], lse [B][q_len][Hq].                  */
+/*                                                                          */
+/* Sliding window (window W > 0; 0 means none): a row sees only the W most    */
+/* recent positions up to its own, [lim - W, lim) with lim its causal limit   */
+/* above — the fixed-size visible history of [P5] PART 02 (third advanced     */
+/* direction, sliding window / KV eviction).  Positions no row can see are    */
+/* not gathered at all, so their blocks may have been released.              */
 /* ---------------------------------------------------------------------- */
 static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
                        const void *k_cache, const void *v_cache, int cache_dtype,
                        const float *k_scale, const float *v_scale,
                        const int32_t *block_table, int max_blocks,
                        const int32_t *context_lens, const int32_t *t_begin,
-                       int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                       int B, int q_len, int window, int Hq, int Hkv, int D, int64_t num_blocks,
                        int block_size, double scale, int nthreads) {
-  if (Hkv <= 0 || Hq % Hkv != 0 || q_len <= 0) return -1;
+  if (Hkv <= 0 || Hq % Hkv != 0 || q_len <= 0 || window < 0) return -1;
   int G = Hq / Hkv;
   int err = 0;
 #ifdef _OPENMP
@@ -235,6 +241,8 @@ static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
     for (int h = 0; h < Hkv; ++h) {
       int t0 = t_begin ? t_begin[b] : 0;
       int t1 = context_lens[b];
+      /* the earliest position any row sees: row 0's window start */
+      if (window > 0 && t1 - (q_len - 1) - window > t0) t0 = t1 - (q_len - 1) - window;
       int n = t1 > t0 ? t1 - t0 : 0;
       double *K = NULL, *V = NULL, *s = NULL, *qv = NULL;
       if (n > 0) {
@@ -265,9 +273,11 @@ static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
         }
       }
       for (int qi = 0; qi < q_len; ++qi) {
-        /* new token qi sees the first nq of the n positions */
-        int nq = n - (q_len - 1 - qi);
-        if (nq < 0) nq = 0;
+        /* new token qi sees gathered positions [lo, hi) */
+        int hi = n - (q_len - 1 - qi);
+        if (hi < 0) hi = 0;
+        int lo = (window > 0 && hi - window > 0) ? hi - window : 0;
+        int nq = hi - lo;
         size_t row = (size_t)b * q_len + qi;
         for (int g = 0; g < G; ++g) {
           int hq = h * G + g;
@@ -279,20 +289,20 @@ static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
             continue;
           }
           double m = -INFINITY;
-          for (int i = 0; i < nq; ++i) {
+          for (int i = lo; i < hi; ++i) {
             double acc = 0.0;
             for (int d = 0; d < D; ++d) acc += qv[d] * K[(size_t)i * D + d];
             s[i] = scale * acc;
             if (s[i] > m) m = s[i];
           }
           double l = 0.0;
-          for (int i = 0; i < nq; ++i) {
+          for (int i = lo; i < hi; ++i) {
             s[i] = exp(s[i] - m);
             l += s[i];
           }
           for (int d = 0; d < D; ++d) {
             double acc = 0.0;
-            for (int i = 0; i < nq; ++i) acc += s[i] * V[(size_t)i * D + d];
+            for (int i = lo; i < hi; ++i) acc += s[i] * V[(size_t)i * D + d];
             o[d] = acc / l;
           }
           if (lse_out) lse_out[row * Hq + hq] = m + log(l);
@@ -315,7 +325,7 @@ int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
                   int B, int Hq, int Hkv, int D, int64_t num_blocks,
                   int block_size, double scale, int nthreads) {
   return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
-                     block_table, max_blocks, context_lens, t_begin, B, 1, Hq, Hkv, D, num_blocks,
+                     block_table, max_blocks, context_lens, t_begin, B, 1, 0, Hq, Hkv, D, num_blocks,
                      block_size, scale, nthreads);
 }
 
@@ -324,11 +334,11 @@ int oracle_decode_multi(double *out, double *lse_out, const void *q, int q_dtype
                         const float *k_scale, const float *v_scale,
                         const int32_t *block_table, int max_blocks,
                         const int32_t *context_lens, const int32_t *t_begin,
-                        int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                        int B, int q_len, int window, int Hq, int Hkv, int D, int64_t num_blocks,
                         int block_size, double scale, int nthreads) {
   return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
-                     block_table, max_blocks, context_lens, t_begin, B, q_len, Hq, Hkv, D, num_blocks,
-                     block_size, scale, nthreads);
+                     block_table, max_blocks, context_lens, t_begin, B, q_len, window, Hq, Hkv, D,
+                     num_blocks, block_size, scale, nthreads);
 }
 
 /* ---------------------------------------------------------------------- */

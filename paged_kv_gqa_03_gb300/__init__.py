@@ -58,6 +58,7 @@ _sig("pkv_bm_allocate", _i32, _P, _i64, _i64)
 _sig("pkv_bm_adopt", _i32, _P, _i64, _P, _i32, _i64)
 _sig("pkv_bm_fork", _i32, _P, _i64, _i64)
 _sig("pkv_bm_free", _i32, _P, _i64)
+_sig("pkv_bm_release_window", _i32, _P, _i64, _i64, ctypes.POINTER(_i64))
 _sig("pkv_bm_append_slots", _i32, _P, _P, _i32, _P, _P, ctypes.POINTER(_i32))
 _sig("pkv_bm_export", _i32, _P, _P, _i32, _P, _i32, _P)
 _sig("pkv_bm_num_free", _i64, _P)
@@ -285,6 +286,14 @@ class BlockManager:
 
     def free(self, seq):
         _check(_L.pkv_bm_free(self._h, seq), "free")
+
+    def release_outside_window(self, seq, window):
+        """Releases the blocks of seq that no later token sees with this
+        sliding window; returns how many table entries were released."""
+        n = _i64(0)
+        _check(_L.pkv_bm_release_window(self._h, seq, window, ctypes.byref(n)),
+               "release_outside_window")
+        return n.value
 
     def append_slots(self, seqs):
         """One new token per sequence: (slots list, [(src, dst), ...]) or None on OOM."""

@@ -11,6 +11,7 @@
 // token lands in a block whose count is above one.
 #include <stdint.h>
 
+#include <algorithm>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -101,7 +102,8 @@ int pkv_bm_fork(pkv_block_manager *bm, int64_t parent, int64_t child) {
   if (it == bm->seqs.end()) return PKV_ENOTFOUND;
   if (bm->seqs.count(child)) return PKV_EINVAL;
   pkv_block_manager::Seq s = it->second;
-  for (int32_t blk : s.table) bm->refcount[blk] += 1;
+  for (int32_t blk : s.table)
+    if (blk >= 0) bm->refcount[blk] += 1;
   bm->seqs.emplace(child, std::move(s));
   return PKV_OK;
 }
@@ -112,8 +114,28 @@ int pkv_bm_free(pkv_block_manager *bm, int64_t seq) {
   if (it == bm->seqs.end()) return PKV_ENOTFOUND;
   bm->compact();
   for (int32_t blk : it->second.table)
-    if (--bm->refcount[blk] == 0) bm->free_list.push_back(blk);
+    if (blk >= 0 && --bm->refcount[blk] == 0) bm->free_list.push_back(blk);
   bm->seqs.erase(it);
+  return PKV_OK;
+}
+
+int pkv_bm_release_window(pkv_block_manager *bm, int64_t seq, int64_t window, int64_t *released_out) {
+  if (!bm || window < 1) return PKV_EINVAL;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PKV_ENOTFOUND;
+  bm->compact();
+  std::vector<int32_t> &table = it->second.table;
+  const int64_t first_visible = it->second.tokens + 1 - window;
+  const int64_t n = std::min<int64_t>((int64_t)table.size(), first_visible > 0 ? first_visible / kBS : 0);
+  int64_t released = 0;
+  for (int64_t j = 0; j < n; ++j) {
+    const int32_t blk = table[(size_t)j];
+    if (blk < 0) continue;
+    if (--bm->refcount[blk] == 0) bm->free_list.push_back(blk);
+    table[(size_t)j] = -1;
+    ++released;
+  }
+  if (released_out) *released_out = released;
   return PKV_OK;
 }
 

@@ -41,7 +41,11 @@ def test_native_matches_oracle_on_random_ops(seed):
             s = live.pop(rng.randrange(len(live)))
             ref.free(s)
             bm.free(s)
-        elif op < 0.6:
+        elif op < 0.62 and live:
+            s = rng.choice(live)
+            w = rng.randrange(1, 50)
+            assert ref.release_outside_window(s, w) == bm.release_outside_window(s, w)
+        elif op < 0.67:
             blocks = rng.sample(range(N), rng.randrange(0, 4))
             ntok = len(blocks) * 16 - rng.randrange(0, 16) if blocks else 0
             ref.adopt(next_id, blocks, ntok)
@@ -62,6 +66,34 @@ def test_native_matches_oracle_on_random_ops(seed):
                 assert lens[i] == ref.seq_tokens[s]
         for blk in range(N):
             assert ref.block_refcount[blk] == bm.refcount(blk)
+
+
+def test_release_outside_window_bounds_the_cache():
+    """Decoding one sequence for 400 tokens with window 40 keeps at most
+    ceil(40 / 16) + 1 blocks; a fork shares the kept blocks only."""
+    pkv = _pkv()
+    bm, ref = pkv.BlockManager(64), BlockTable(64)
+    for m in (bm, ref):
+        assert m.allocate(0, 5)
+    for step in range(400):
+        assert bm.release_outside_window(0, 40) == ref.release_outside_window(0, 40)
+        assert bm.append_slots([0]) == ref.append_slots([0])
+        table, lens = bm.export([0], 64)
+        held = [b for b in table[0] if b >= 0]
+        assert len(held) <= 4 and bm.num_free() == 64 - len(held)
+        assert list(table[0, :len(ref.seq_tables[0])]) == ref.seq_tables[0]
+    first = (int(lens[0]) - 40) // 16                 # released logical blocks stay -1
+    assert all(table[0, :first] == -1)
+    assert bm.fork(0, 1) and ref.fork(0, 1)
+    for blk in held:
+        assert bm.refcount(blk) == 2 == ref.block_refcount[blk]
+    bm.free(0), ref.free(0), bm.free(1), ref.free(1)
+    assert bm.num_free() == 64 == ref.num_free()
+    with pytest.raises(pkv.PagedKVError):
+        bm.release_outside_window(5, 40)            # unknown sequence
+    assert bm.allocate(5, 1)
+    with pytest.raises(pkv.PagedKVError):
+        bm.release_outside_window(5, 0)             # window must be >= 1
 
 
 def test_errors():

@@ -327,3 +327,65 @@ def test_multi_query_toy_rows_of_full_masked_computation():
     out = oracle.decode(q.float().numpy(), "f32", pk.float().numpy(), pv.float().numpy(), "f32",
                         dense_table(tables, mb), [3], scale=1.0 / div, block_size=2)
     assert np.allclose(out[0, :, 0], full[1:3].numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("B,q_len,window,Hq,Hkv,D,bs,max_ctx", [
+    (3, 1, 5, 8, 2, 16, 16, 60),
+    (3, 1, 17, 4, 2, 8, 4, 70),
+    (2, 4, 6, 8, 1, 8, 4, 37),       # several new tokens, each with its own window
+    (2, 3, 16, 16, 2, 64, 16, 90),
+])
+def test_sliding_window_matches_band_masked_sdpa(B, q_len, window, Hq, Hkv, D, bs, max_ctx):
+    """Sliding window ('苦猿的大模型日记 Day45' PART 02, third advanced
+    direction): a row sees the `window` most recent positions up to its own,
+    i.e. the causal mask of PART 04 intersected with triu(diagonal =
+    kv_len - q_len - window + 1); compared with torch SDPA on that mask."""
+    ctx, ks, vs, q, pk, pv, tables, mb = _multi_case(3 + window + q_len, B, q_len, Hq, Hkv, D, bs,
+                                                     max_ctx)
+    scale = 1.0 / math.sqrt(D)
+    got, lse = oracle.decode(q.float().numpy(), "f32", pk.float().numpy(), pv.float().numpy(),
+                             "f32", dense_table(tables, mb), ctx, scale=scale, block_size=bs,
+                             with_lse=True, window=window)
+    G = Hq // Hkv
+    for b in range(B):
+        T = ctx[b]
+        causal = torch.tril(torch.ones((q_len, T), dtype=torch.bool), diagonal=T - q_len)
+        band = torch.triu(torch.ones((q_len, T), dtype=torch.bool), diagonal=T - q_len - window + 1)
+        mask = causal & band
+        Kx = ks[b].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Vx = vs[b].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Qx = q[b].permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(Qx, Kx, Vx, attn_mask=mask,
+                                                               scale=scale)
+        assert np.allclose(got[b], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        s = (Qx @ Kx.transpose(1, 2)) * scale
+        ref_lse = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)
+        assert np.allclose(lse[b], ref_lse.T.numpy(), rtol=0, atol=1e-12)
+
+
+def test_sliding_window_special_cases():
+    """A window covering the context is no window (bit for bit); a window of
+    one gives each row its own position's V exactly; blocks wholly before
+    every row's window are never read (their table entries may be -1)."""
+    B, q_len, Hq, Hkv, D, bs = 3, 2, 4, 2, 8, 4
+    ctx, ks, vs, q, pk, pv, tables, mb = _multi_case(29, B, q_len, Hq, Hkv, D, bs, 45)
+    bt = dense_table(tables, mb)
+    args = (pk.float().numpy(), pv.float().numpy(), "f32")
+    qf = q.float().numpy()
+    full = oracle.decode(qf, "f32", *args, bt, ctx, scale=0.3, block_size=bs)
+    wide = oracle.decode(qf, "f32", *args, bt, ctx, scale=0.3, block_size=bs, window=max(ctx))
+    assert np.array_equal(full, wide)
+    one = oracle.decode(qf, "f32", *args, bt, ctx, scale=0.3, block_size=bs, window=1)
+    for b in range(B):
+        for i in range(q_len):
+            pos = ctx[b] - q_len + i
+            for hq in range(Hq):
+                assert np.array_equal(one[b, i, hq], vs[b][pos, hq // (Hq // Hkv)].numpy())
+    W = 5
+    ref = oracle.decode(qf, "f32", *args, bt, ctx, scale=0.3, block_size=bs, window=W)
+    holed = bt.copy()
+    for b in range(B):
+        first = max(0, ctx[b] - (q_len - 1) - W)       # earliest position any row sees
+        holed[b, :first // bs] = -1
+    got = oracle.decode(qf, "f32", *args, holed, ctx, scale=0.3, block_size=bs, window=W)
+    assert np.array_equal(got, ref)

@@ -42,11 +42,18 @@ MUTANTS = [
     ("f16 exponent bias", "v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
      "v = ldexp(1.0 + (double)m / 1024.0, e - 14);",
      [T_fmt.test_f16_all_codes_match_numpy]),
-    ("causal limit off by one", "int nq = n - (q_len - 1 - qi);", "int nq = n - (q_len - qi);",
+    ("causal limit off by one", "int hi = n - (q_len - 1 - qi);", "int hi = n - (q_len - qi);",
      [lambda: T_att.test_multi_query_matches_masked_sdpa(3, 2, 8, 2, 16, 16, 40),
       T_att.test_multi_query_toy_rows_of_full_masked_computation]),
-    ("causal limit reversed", "int nq = n - (q_len - 1 - qi);", "int nq = n - qi;",
+    ("causal limit reversed", "int hi = n - (q_len - 1 - qi);", "int hi = n - qi;",
      [T_att.test_multi_query_rows_are_single_queries_over_shorter_contexts]),
+    ("window start off by one", "? hi - window : 0;", "? hi - window + 1 : 0;",
+     [lambda: T_att.test_sliding_window_matches_band_masked_sdpa(2, 4, 6, 8, 1, 8, 4, 37),
+      T_att.test_sliding_window_special_cases]),
+    ("window gather ignores q_len",
+     "if (window > 0 && t1 - (q_len - 1) - window > t0) t0 = t1 - (q_len - 1) - window;",
+     "if (window > 0 && t1 - window > t0) t0 = t1 - window;",
+     [lambda: T_att.test_sliding_window_matches_band_masked_sdpa(2, 4, 6, 8, 1, 8, 4, 37)]),
     ("query row ignores token", "size_t row = (size_t)b * q_len + qi;",
      "size_t row = (size_t)b * q_len;",
      [lambda: T_att.test_multi_query_matches_masked_sdpa(2, 4, 8, 1, 8, 4, 37)]),
