@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence per step (multi-query decode, causal)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window: each row attends its W most recent positions")
     return ap.parse_args()
 
 
@@ -180,8 +182,8 @@ def oracle_sample_rate(w, seconds, threads=0):
     for b in range(w.B):
         table[b, :len(bt.seq_tables[b])] = bt.seq_tables[b]
     lens = np.array([bt.seq_tokens[b] for b in range(w.B)], dtype=np.int32)
-    per_seq = [int(lens[b]) * 2 * w.Hkv * w.D * {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}[w.dtype]
-               for b in range(w.B)]
+    per_seq = [w.attended(int(lens[b])) * 2 * w.Hkv * w.D
+               * {"f32": 4, "f16": 2, "bf16": 2, "fp8_e4m3": 1}[w.dtype] for b in range(w.B)]
     ks = None if w.k_scale is None else w.k_scale.numpy()   # views: the append writes through
     vs = None if w.v_scale is None else w.v_scale.numpy()
     done_bytes, elapsed, n = 0, 0.0, 1
@@ -193,7 +195,7 @@ def oracle_sample_rate(w, seconds, threads=0):
                       v_new[rows].reshape(-1, w.Hkv, w.D), w.new_dtype,
                       [slots[r * L + t] for r in rows for t in range(L)], ks, vs, inplace=True)
         oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table[rows], lens[rows],
-                      scale=w.scale, k_scale=ks, v_scale=vs, nthreads=threads)
+                      scale=w.scale, k_scale=ks, v_scale=vs, nthreads=threads, window=w.window)
         dt = time.perf_counter() - t0
         elapsed += dt
         done_bytes += sum(per_seq[r] for r in rows)
@@ -222,7 +224,7 @@ def spot_check(w, out, step):
     table = step.h_table.numpy()[rows]
     lens = step.h_lens.numpy()[rows]
     ref = oracle.decode(w.q[rows], w.q_dtype, w.k_cache, w.v_cache, w.dtype, table, lens,
-                        scale=w.scale, k_scale=ks, v_scale=vs)
+                        scale=w.scale, k_scale=ks, v_scale=vs, window=w.window)
     got = out[rows].double().cpu().numpy()
     return {"rows": rows, "max_abs_err": float(np.abs(got - ref).max())}
 
@@ -267,11 +269,15 @@ def _workload(args):
         over["B"] = args.batch
     if args.q_len > 1:
         over["q_len"] = args.q_len
+    if args.window:
+        over["window"] = args.window
     return workloads.config(args.workload, **over)
 
 
 def _config(w):
     extra = {} if w.q_len == 1 else {"q_len": w.q_len}
+    if w.window:
+        extra["window"] = w.window
     return extra | {"workload": w.name, "index": w.seed - 1000, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
             "D": w.D, "kv_dtype": w.dtype, "q_dtype": w.q_dtype, "block_size": 16,
             "context_lens": (w.context_lens[0] if len(set(w.context_lens)) == 1
@@ -301,7 +307,7 @@ def run_ours(args, world, rank, local):
     vs = None if w.v_scale is None else w.v_scale.to(dev)
     step = DecodeStep(w.k_cache.to(dev), w.v_cache.to(dev), w.Hq, tdt[w.q_dtype], w.max_blocks,
                       ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
-                      q_len=w.q_len)
+                      q_len=w.q_len, window=w.window)
     for b in range(w.B):
         step.adopt(b, w.tables[b], w.cached[b])
     step.prepare()
@@ -381,7 +387,7 @@ def run_ours(args, world, rank, local):
     for _ in range(max(5, min(args.steps, 20))):
         probe = DecodeStep(step.k_cache, step.v_cache, w.Hq, tdt[w.q_dtype], w.max_blocks,
                            ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
-                           q_len=w.q_len)
+                           q_len=w.q_len, window=w.window)
         for b in range(w.B):
             probe.adopt(b, w.tables[b], w.cached[b])
         probe._buffers(w.B)
@@ -411,13 +417,14 @@ def run_ours(args, world, rank, local):
         "config": _config(w) | {"parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "tok_per_s": round(world * w.B * w.q_len / (ms_step * 1e-3), 1),
         "attn_tflops": round(4.0 * w.Hq * w.D * sum(
-            max(0, c - w.q_len + 1 + i) for c in w.context_lens for i in range(w.q_len))
-            / (ms_attn * 1e-3) / 1e12, 2),
+            min(max(0, c - w.q_len + 1 + i), w.window or 1 << 30)
+            for c in w.context_lens for i in range(w.q_len)) / (ms_attn * 1e-3) / 1e12, 2),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + decode + merge)",
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": kernel_traffic(w.q_len), "algorithmic_bytes_per_launch": kv,
+                     "traffic": None if w.window else kernel_traffic(w.q_len),
+                     "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_gbs(kv, world, ms_e2e), 2), "unit": "GB/s",

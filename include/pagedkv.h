@@ -179,8 +179,18 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  * ctx - q_len) of the naive_attention in "苦猿的大模型日记 Day45" PART 04.
  * A row that sees no position (ctx_b < q_len - i) gives out = 0.
  *
+ * Sliding window (window W > 0; 0 = none): each row sees only the W most
+ * recent positions up to its own, [lim - W, lim) with lim = ctx_b - q_len + i
+ * + 1 — the fixed visible history of "苦猿的大模型日记 Day45" PART 02 (sliding
+ * window / KV eviction).  Only blocks that hold a position some row of the
+ * sequence sees are read (the first is the block of ctx_b - q_len + 1 - W), so
+ * entries of block_table before it may be -1 (see pkv_bm_release_window).
+ *
  *   q, out     [B][q_len][Hq][D] (q_len = 1 is paged_decode_attention)
  *   q_len      1 .. PKV_MAX_Q_LEN
+ *   window     0 (no window) or W >= 1 (W >= 2^30 acts as no window)
+ *   max_blocks_per_seq  at most 2^26 (PKV_EUNSUPPORTED above), for every
+ *              decode entry point
  * Everything else, including the workspace rule, is as for
  * paged_decode_attention; the workspace size comes from
  * paged_decode_multi_workspace_bytes.  Each kv head's q_len * G query rows
@@ -197,8 +207,8 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
                                  const float *k_scale, const float *v_scale,
                                  const int32_t *block_table, int max_blocks_per_seq,
                                  const int32_t *context_lens,
-                                 int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks,
-                                 float scale, int num_splits,
+                                 int B, int q_len, int window, int Hq, int Hkv, int D,
+                                 int64_t num_blocks, float scale, int num_splits,
                                  void *workspace, size_t workspace_bytes,
                                  pkv_stream_t stream);
 

@@ -44,7 +44,7 @@ _sig("paged_decode_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i3
 _sig("paged_decode_multi_workspace_bytes", _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
      ctypes.POINTER(_sz))
 _sig("paged_decode_attention_multi", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
-     _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _sz, _P)
+     _i32, _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _sz, _P)
 _sig("paged_decode_status", _i32, _P, _sz, _P, ctypes.POINTER(_i32))
 _sig("paged_decode_merge", _i32, _P, _i32, _P, _P, _i32, _i32, _i32, _i32, _P)
 _sig("paged_kv_copy_blocks", _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
@@ -169,12 +169,14 @@ def paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits
 
 
 def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, scale,
-                           k_scale=None, v_scale=None, num_splits=0, workspace=None, stream=None):
+                           k_scale=None, v_scale=None, num_splits=0, workspace=None, stream=None,
+                           window=0):
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over the paged cache.
 
     q, out [B, Hq, D]: one new token per sequence (paged_decode_attention).
     q, out [B, q_len, Hq, D]: q_len new tokens per sequence, token i seeing
     the cache up to its own position (paged_decode_attention_multi).
+    window > 0: each row sees only its `window` most recent positions.
     workspace: a uint8 CUDA tensor of paged_decode_workspace_bytes(...) bytes;
     allocated here (by torch) when None."""
     torch = _torch()
@@ -195,9 +197,9 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
             block_table.shape[1], _dev(context_lens, "context_lens", torch.int32))
     tail = (num_blocks, float(scale), num_splits, _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _stream(stream))
-    if q.dim() == 4:
+    if q.dim() == 4 or window:
         _check(_L.paged_decode_attention_multi(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
-                                               B, q_len, Hq, Hkv, D, *tail),
+                                               B, q_len, int(window), Hq, Hkv, D, *tail),
                "paged_decode_attention_multi")
     else:
         _check(_L.paged_decode_attention(_dev(out, "out"), _dev(q, "q"), _code(q), *args,

@@ -221,6 +221,7 @@ int validate_decode_shapes(int q_dtype, int cache_dtype, int B, int q_len, int H
                            int64_t num_blocks, int max_blocks) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_blocks <= 0 || max_blocks <= 0) return PKV_EINVAL;
   if (q_len < 1 || q_len > PKV_MAX_Q_LEN) return PKV_EINVAL;
+  if (max_blocks > (1 << 26)) return PKV_EUNSUPPORTED;  // 16 * max_blocks stays below 2^30
   if (Hq % Hkv != 0) return PKV_EINVAL;
   if (esize_of(cache_dtype) == 0 || esize_of(q_dtype) == 0 || q_dtype == PKV_FP8_E4M3) return PKV_EINVAL;
   if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
@@ -323,17 +324,19 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
                            int64_t num_blocks, float scale, int num_splits, void *workspace, size_t workspace_bytes,
                            pkv_stream_t stream) {
   return paged_decode_attention_multi(out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale, block_table,
-                                      max_blocks_per_seq, context_lens, B, 1, Hq, Hkv, D, num_blocks, scale,
+                                      max_blocks_per_seq, context_lens, B, 1, 0, Hq, Hkv, D, num_blocks, scale,
                                       num_splits, workspace, workspace_bytes, stream);
 }
 
 int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
                                  int cache_dtype, const float *k_scale, const float *v_scale,
                                  const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
-                                 int B, int q_len, int Hq, int Hkv, int D, int64_t num_blocks, float scale,
-                                 int num_splits, void *workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                                 int B, int q_len, int window, int Hq, int Hkv, int D, int64_t num_blocks,
+                                 float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                                 pkv_stream_t stream) {
   int rc = validate_decode_shapes(q_dtype, cache_dtype, B, q_len, Hq, Hkv, D, num_blocks, max_blocks_per_seq);
   if (rc != PKV_OK) return rc;
+  if (window < 0) return PKV_EINVAL;
   if (!std::isfinite(scale)) return PKV_EINVAL;
   if (B == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens) return PKV_EINVAL;
@@ -383,6 +386,9 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   p.HU = Hkv * c.NC;
   p.q_len = q_len;
   p.R = q_len * p.G;
+  // a window of 2^30 positions or more covers any context this call accepts
+  p.window = window < (1 << 30) ? window : 0;
+  p.wlen = p.window > 0 ? p.window : (1 << 30);
   p.P = P;
   p.max_blocks = max_blocks_per_seq;
   p.out_dtype = q_dtype;

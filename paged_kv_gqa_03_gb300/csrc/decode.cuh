@@ -8,7 +8,10 @@
 // sequence, the verify step of speculative decoding, "LLM推理优化实战" §4) new
 // token i sees only the first ctx - (q_len - 1 - i) positions, the causal mask
 // tril(diagonal = kv_len - q_len) of "苦猿的大模型日记 Day45" PART 04, applied
-// per score column.  Units are concatenated in the order
+// per score column.  With a sliding window W (the same page, PART 02: a fixed
+// visible history) a row sees only [lim - W, lim); a unit then streams only
+// the blocks from the first one row 0's window reaches.  Units are
+// concatenated in the order
 // (b, h, c), each contributing ceil(ctx_b / 16) block items, and the item list
 // is cut into P equal contiguous ranges, one per warp (the "workers").  A
 // warp streams its range block by block, carrying the online-softmax state
@@ -77,6 +80,7 @@ struct DecodeCfg {
 struct Producer {
   int pi, e, s;          // next item, end of range, start of range
   int b, hu, j, n, ctx;  // unit and block of item pi; blocks and length of sequence b
+  int j0;                // first block of sequence b inside some row's window
   int seg_j0, seg_wfirst;
   int win_b, win_hu, win_j0, win_id;  // lane-parallel window of 32 block-table entries
   int nxt_id;                         // the unit's next window, loaded one window ahead
@@ -84,10 +88,10 @@ struct Producer {
 };
 
 __device__ __forceinline__ void load_seq(Producer &pr, const DecodeParams &p) {
-  int ctx = __ldg(p.context_lens + pr.b);
-  ctx = ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
+  const int ctx = clamped_len(p, __ldg(p.context_lens + pr.b));
   pr.ctx = ctx;
   pr.n = (ctx + kBlock - 1) / kBlock;
+  pr.j0 = first_block(p, ctx);
 }
 
 template <class Cfg>
@@ -128,14 +132,14 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     vs = __shfl_sync(kFull, pr.win_vs, pr.j - pr.win_j0);
   }
   int flags = 0;
-  if (pr.pi == pr.s || pr.j == 0) {
+  if (pr.pi == pr.s || pr.j == pr.j0) {
     flags |= kFirst;
     pr.seg_j0 = pr.j;
     pr.seg_wfirst = (pr.pi == pr.s);
   }
   if (pr.pi + 1 == pr.e || pr.j + 1 == pr.n) {
     flags |= kLast;
-    if (pr.seg_j0 == 0 && pr.j + 1 == pr.n) flags |= kComplete;
+    if (pr.seg_j0 == pr.j0 && pr.j + 1 == pr.n) flags |= kComplete;
   }
   if (pr.seg_wfirst) flags |= kWFirst;
   const int rem = pr.ctx - pr.j * kBlock;
@@ -171,7 +175,6 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
   ++pr.pi;
   ++pr.j;
   if (pr.j == pr.n && pr.pi < pr.e) {
-    pr.j = 0;
     if (++pr.hu == p.HU) {
       pr.hu = 0;
       do {
@@ -179,6 +182,7 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
         load_seq(pr, p);
       } while (pr.n == 0 && pr.b < p.B - 1);
     }
+    pr.j = pr.j0;
   }
 }
 
@@ -318,8 +322,10 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
                                             const StageMeta &m, int lane) {
   constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
   const int gid = lane >> 2;
-  // token rows of the block visible to score columns 2 tig, 2 tig + 1
-  const int lim0 = m.rem - st.back0, lim1 = m.rem - st.back1;
+  // token rows r of the block visible to score column c: base_c <= r < base_c + W,
+  // base_c = rem - back_c - W (one unsigned compare; W = 2^30 without a window)
+  const int base0 = m.rem - st.back0 - p.wlen, base1 = m.rem - st.back1 - p.wlen;
+  const uint32_t wl = (uint32_t)p.wlen;
 
   // ---- scores S^T = K . Q^T (16 tokens x 8 heads), two independent chains ----
   float s[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -346,10 +352,10 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
   // ---- online softmax over the block (log2 domain) ----
   const float sc = p.scale_log2 * m.ks;
   float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
-  if (gid >= lim0) x0 = -INFINITY;
-  if (gid >= lim1) x1 = -INFINITY;
-  if (gid + 8 >= lim0) x2 = -INFINITY;
-  if (gid + 8 >= lim1) x3 = -INFINITY;
+  if ((uint32_t)(gid - base0) >= wl) x0 = -INFINITY;
+  if ((uint32_t)(gid - base1) >= wl) x1 = -INFINITY;
+  if ((uint32_t)(gid + 8 - base0) >= wl) x2 = -INFINITY;
+  if ((uint32_t)(gid + 8 - base1) >= wl) x3 = -INFINITY;
   float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -605,7 +611,7 @@ __device__ __forceinline__ void simt_block(SimtState<Cfg> &st, const DecodeParam
 #pragma unroll
   for (int g = 0; g < GC; ++g) {
     float x = part[g] + __shfl_xor_sync(kFull, part[g], 16);
-    x = (t < m.rem - st.back[g]) ? x * sc : -INFINITY;
+    x = ((uint32_t)(t - (m.rem - st.back[g] - p.wlen)) < (uint32_t)p.wlen) ? x * sc : -INFINITY;
     float bm = x;
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
@@ -669,13 +675,13 @@ __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodePara
 // ---------------------------------------------------------------------------
 // Inline plan (batches of up to kInlinePrefix - 1 sequences): every CTA scans
 // context_lens into a shared-memory prefix of blocks per sequence,
-// prefix[b] = sum_{b' < b} ceil(ctx_b' / 16), so no separate plan launch is
+// prefix[b] = sum_{b' < b} items_b' (seq_items: blocks inside the windows), so no separate plan launch is
 // needed; CTA 0 also stores it for the merge kernel.  Lengths are clamped to
 // [0, 16 * max_blocks] and flagged.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int clamp_len(const DecodeParams &p, int ctx, int *flags) {
   if (ctx < 0 || ctx > p.max_blocks * kBlock) *flags |= PKV_FLAG_BAD_LEN;
-  return ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
+  return clamped_len(p, ctx);
 }
 
 __device__ __forceinline__ void inline_plan(const DecodeParams &p, int32_t *s_prefix, int32_t *s_scan,
@@ -685,7 +691,7 @@ __device__ __forceinline__ void inline_plan(const DecodeParams &p, int32_t *s_pr
   const int b0 = tid * k;
   int sum = 0, flags = 0;
   for (int i = 0; i < k; ++i)
-    if (b0 + i < p.B) sum += (clamp_len(p, __ldg(p.context_lens + b0 + i), &flags) + kBlock - 1) / kBlock;
+    if (b0 + i < p.B) sum += seq_items(p, clamp_len(p, __ldg(p.context_lens + b0 + i), &flags));
   int x = sum;  // inclusive scan within the warp
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -711,7 +717,7 @@ __device__ __forceinline__ void inline_plan(const DecodeParams &p, int32_t *s_pr
     const int b = b0 + i;
     if (b < p.B) {
       s_prefix[b] = run;
-      run += (clamp_len(p, __ldg(p.context_lens + b), &unused) + kBlock - 1) / kBlock;
+      run += seq_items(p, clamp_len(p, __ldg(p.context_lens + b), &unused));
       if (b == p.B - 1) s_prefix[p.B] = run;
     }
   }
@@ -737,7 +743,8 @@ __device__ __forceinline__ int4 locate(const DecodeParams &p, const int32_t *pre
   }
   const int n = pre[lo + 1] - pre[lo];
   const int64_t rr = s - (int64_t)p.HU * pre[lo];
-  return make_int4((int)s, lo, (int)(rr / n), (int)(rr % n));
+  const int j0 = first_block(p, clamped_len(p, __ldg(p.context_lens + lo)));
+  return make_int4((int)s, lo, (int)(rr / n), j0 + (int)(rr % n));
 }
 
 // ---------------------------------------------------------------------------

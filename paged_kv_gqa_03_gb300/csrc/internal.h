@@ -61,6 +61,8 @@ struct DecodeParams {
   int B, Hq, Hkv, D, G, GC, NC, HU, P;
   int q_len;            // new query tokens per sequence (1 = plain decode)
   int R;                // query rows per kv head = q_len * G, cut into NC chunks of GC
+  int window;           // sliding window W (0 = none): a row sees [lim - W, lim)
+  int wlen;             // W, or 1 << 30 without a window (visible-range width)
   int max_blocks;
   int out_dtype;
   float scale_log2;     // softmax scale * log2(e)
@@ -68,6 +70,23 @@ struct DecodeParams {
   int inline_plan;      // 1: the decode kernel computes prefix and partition starts itself
   int n_ctas;           // decode grid size
 };
+
+#ifdef __CUDACC__
+// Context length clamped to [0, 16 * max_blocks].
+__device__ __forceinline__ int clamped_len(const DecodeParams &p, int ctx) {
+  return ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
+}
+// First block any row of a sequence of (clamped) length ctx can see: with a
+// window, row 0's window starts at ctx - (q_len - 1) - W.
+__device__ __forceinline__ int first_block(const DecodeParams &p, int ctx) {
+  const int lo = p.window > 0 ? ctx - (p.q_len - 1) - p.window : 0;
+  return lo > 0 ? lo / kBlock : 0;
+}
+// Work items (blocks streamed per unit) of a sequence of (clamped) length ctx.
+__device__ __forceinline__ int seq_items(const DecodeParams &p, int ctx) {
+  return (ctx + kBlock - 1) / kBlock - first_block(p, ctx);
+}
+#endif
 
 // Records a CUDA error for pkv_last_cuda_error() on the calling thread.
 void record_cuda_error(cudaError_t e);

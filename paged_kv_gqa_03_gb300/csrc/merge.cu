@@ -17,8 +17,9 @@ namespace pkv {
 
 // ---------------------------------------------------------------------------
 // Plan kernel, for batches too large to plan inside the decode kernel:
-// prefix[b] = sum_{b' < b} ceil(ctx_b' / 16); W = HU * prefix[B]; partition w
-// starts at item floor(w * W / P), decoded into (b, hu, j).  One CTA; context
+// prefix[b] = sum_{b' < b} items_b' (ceil(ctx_b' / 16) blocks, less those
+// before every row's sliding window); W = HU * prefix[B]; partition w starts at
+// item floor(w * W / P), decoded into (b, hu, j).  One CTA; context
 // lengths are clamped to [0, 16 * max_blocks] (flagged in plan_flags).
 // ---------------------------------------------------------------------------
 constexpr int kPlanSmemInts = 8192;  // prefix entries kept in shared memory (32 KiB)
@@ -38,10 +39,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     const int b = base + tid;
     int n = 0;
     if (b < p.B) {
-      int ctx = p.context_lens[b];
+      const int ctx = p.context_lens[b];
       if (ctx < 0 || ctx > p.max_blocks * kBlock) flags |= PKV_FLAG_BAD_LEN;
-      ctx = ctx < 0 ? 0 : (ctx > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx);
-      n = (ctx + kBlock - 1) / kBlock;
+      n = seq_items(p, clamped_len(p, ctx));
     }
     int x = n;  // inclusive scan within the warp
 #pragma unroll
@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       }
       const int n = pre[lo + 1] - pre[lo];
       const int64_t rr = s - (int64_t)p.HU * pre[lo];
-      r = make_int4((int)s, lo, (int)(rr / n), (int)(rr % n));
+      const int j0 = first_block(p, clamped_len(p, p.context_lens[lo]));
+      r = make_int4((int)s, lo, (int)(rr / n), j0 + (int)(rr % n));
     }
     p.starts[w] = r;
   }

@@ -8,7 +8,10 @@
 
 With q_len > 1 every sequence appends q_len tokens per step (slots in order)
 and attends them causally (the verify step of speculative decoding): q, out
-are [B, q_len, Hq, D] and k_new, v_new [B, q_len, Hkv, D].
+are [B, q_len, Hq, D] and k_new, v_new [B, q_len, Hkv, D].  With a sliding
+window W each row attends its W most recent positions, and a1 first releases
+the blocks that no token of the step (or later) can see, so a sequence holds
+at most ceil((W + q_len - 1) / 16) + 1 blocks.
 
 Device state (caches, scales, workspace) stays resident.  Per step only q,
 k_new, v_new and the host-produced slot mapping / copy pairs / tables /
@@ -45,7 +48,7 @@ class _Staging:
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, Hq, q_dtype, max_blocks, k_scale=None, v_scale=None,
-                 num_splits=0, stream=None, scale=None, q_len=1):
+                 num_splits=0, stream=None, scale=None, q_len=1, window=0):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
         self.num_blocks, self.Hkv, _, self.D = k_cache.shape
@@ -53,6 +56,7 @@ class DecodeStep:
         self.new_dtype = q_dtype if k_cache.dtype == torch.float8_e4m3fn else k_cache.dtype
         self.num_splits = num_splits
         self.q_len = q_len
+        self.window = window
         self.scale = 1.0 / float(np.sqrt(self.D)) if scale is None else float(scale)
         self.device = k_cache.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -126,6 +130,9 @@ class DecodeStep:
             self._host[self._turn].done.synchronize()
         self._select(self._turn)
         self.h_seqs[:] = seqs
+        if self.window:
+            for seq in seqs:
+                self.bm.release_outside_window(int(seq), self.window)
         if self.q_len == 1:
             tok_seqs = self.h_seqs
         else:
@@ -179,7 +186,8 @@ class DecodeStep:
     def attend(self, q, out):
         paged_decode_attention(out, q, self.k_cache, self.v_cache, self.d_table, self.d_lens,
                                self.scale, self.k_scale, self.v_scale,
-                               num_splits=self.num_splits, workspace=self._ws, stream=self.stream)
+                               num_splits=self.num_splits, workspace=self._ws, stream=self.stream,
+                               window=self.window)
 
     @property
     def workspace(self):

@@ -50,7 +50,8 @@ def run_gpu_step(w, num_splits=0, stream=None):
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
     step = DecodeStep(kc, vc, w.Hq, TORCH[w.q_dtype], w.max_blocks, ks, vs,
-                      num_splits=num_splits, stream=stream, scale=w.scale, q_len=w.q_len)
+                      num_splits=num_splits, stream=stream, scale=w.scale, q_len=w.q_len,
+                      window=w.window)
     for b in range(w.B):
         step.adopt(b, w.tables[b], w.cached[b])
     step.prepare()
@@ -67,6 +68,9 @@ def run_oracle_step(w):
     bt = BlockTable(w.num_blocks)
     for b in range(w.B):
         bt.adopt(b, w.tables[b], w.cached[b])
+    if w.window:
+        for b in range(w.B):
+            bt.release_outside_window(b, w.window)
     slots, cow = bt.append_slots([b for b in range(w.B) for _ in range(w.q_len)])
     assert cow == []
     mb = w.max_blocks
@@ -81,5 +85,5 @@ def run_oracle_step(w):
                                    slots, None if w.k_scale is None else w.k_scale.numpy(),
                                    None if w.v_scale is None else w.v_scale.numpy())
     out = oracle.decode(w.q, w.q_dtype, kc, vc, w.dtype, table, lens, scale=w.scale,
-                        k_scale=ks, v_scale=vs)
+                        k_scale=ks, v_scale=vs, window=w.window)
     return slots, table, lens, (kc, vc, ks, vs), out

@@ -81,12 +81,13 @@ def test_multi_query_argument_errors_without_gpu():
         a = dict(B=2, Hq=8, Hkv=2, D=128, ws=256, wsb=1 << 30)
         a.update(kw)
         return L.paged_decode_attention_multi(16, 16, 2, 16, 16, 2, NULL, NULL, 16, 4, 16, a["B"],
-                                              q_len, a["Hq"], a["Hkv"], a["D"], 10, 0.1, 3,
-                                              a["ws"], a["wsb"], NULL)
+                                              q_len, a.get("window", 0), a["Hq"], a["Hkv"], a["D"],
+                                              10, 0.1, 3, a["ws"], a["wsb"], NULL)
     assert multi(0) == pkv.PKV_EINVAL
     assert multi(65) == pkv.PKV_EINVAL                        # above PKV_MAX_Q_LEN
     assert multi(4, Hq=6, Hkv=4) == pkv.PKV_EINVAL
     assert multi(4, ws=NULL) == pkv.PKV_EWORKSPACE
+    assert multi(4, window=-1) == pkv.PKV_EINVAL
     assert multi(4, B=0) == pkv.PKV_OK
     size = ctypes.c_size_t(0)
     assert L.paged_decode_multi_workspace_bytes(2, 0, 8, 2, 128, 2, 2, 5, ctypes.byref(size)) == pkv.PKV_EINVAL

@@ -29,6 +29,9 @@ step of speculative decoding) appends L tokens per sequence: `ctx` still
 gives attended lengths, cached = ctx - L, q is [B, L, Hq, D] and k_new / v_new
 are [B, L, Hkv, D] (token t of sequence b at position cached_b + t), each taken
 from the pool and zeroed as above.  Without `q_len` the draws are unchanged.
+(`q_len` = 1 given explicitly keeps the 4-D shapes with L = 1.)  A spec's
+`window` (sliding window, 0 = none) changes no draw; it is carried to the
+attention call and to kv_bytes.
 """
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -83,6 +86,7 @@ class Workload:
     seed: int = 0
     extra: dict = field(default_factory=dict)
     q_len: int = 1               # new tokens per sequence
+    window: int = 0              # sliding window (0 = none)
 
     @property
     def new_dtype(self):
@@ -100,12 +104,20 @@ class Workload:
     def max_blocks(self):
         return max(1, max((c + BLOCK - 1) // BLOCK for c in self.context_lens))
 
+    def attended(self, ctx):
+        """Positions some row of a sequence of length ctx attends."""
+        if self.window:
+            return min(ctx, self.window + self.q_len - 1)
+        return ctx
+
     def kv_bytes(self):
-        """Logical bytes of K and V attention reads (+ fp8 scales)."""
+        """Logical bytes of K and V attention reads (+ fp8 scales): the
+        positions attended (inside the window, if any)."""
         per_tok = 2 * self.Hkv * self.D * ITEMSIZE[self.dtype]
-        total = sum(self.context_lens) * per_tok
+        total = sum(self.attended(c) for c in self.context_lens) * per_tok
         if self.dtype == "fp8_e4m3":
-            total += sum((c + BLOCK - 1) // BLOCK for c in self.context_lens) * self.Hkv * 2 * 4
+            total += sum((c + BLOCK - 1) // BLOCK - (c - self.attended(c)) // BLOCK
+                         for c in self.context_lens) * self.Hkv * 2 * 4
         return total
 
     def unique_kv_bytes(self):
@@ -223,7 +235,8 @@ def make(spec, seed: int) -> Workload:
     return Workload(name=spec.get("name", "custom"), B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype,
                     q_dtype=q_dtype, num_blocks=num_blocks, q=q, k_new=k_new, v_new=v_new,
                     k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
-                    tables=tables, cached=cached, prefix_blocks=pblocks, seed=seed, q_len=L)
+                    tables=tables, cached=cached, prefix_blocks=pblocks, seed=seed, q_len=L,
+                    window=spec.get("window", 0))
 
 
 def config(index: int, **overrides) -> Workload:
