@@ -51,6 +51,9 @@ def lib():
         L.oracle_decode_multi.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
                                           i32, i32, i32, i32, i32, i32, i64, i32, f64, i32]
         L.oracle_decode_multi.restype = i32
+        L.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
+                                     i32, i32, i32, i32, i32, i64, i32, f64, i32]
+        L.oracle_prefill.restype = i32
         L.oracle_merge.argtypes = [P, P, P, i32, i32, i32]
         L.oracle_merge.restype = None
         L.oracle_num_threads.argtypes = []
@@ -193,6 +196,45 @@ def decode(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens,
         raise ValueError("oracle_decode: Hq must be a multiple of Hkv")
     if rc == -2:
         raise ValueError("oracle_decode: block table entry out of range")
+    return (out, lse) if with_lse else out
+
+
+def prefill(q, q_dtype, k_cache, v_cache, cache_dtype, block_table, context_lens, q_start,
+            scale=None, k_scale=None, v_scale=None, block_size=16, nthreads=0, with_lse=False,
+            window=0):
+    """Causal attention of each sequence's new tokens: q [total, Hq, D] holds
+    sequence b's n_b = q_start[b+1] - q_start[b] new tokens from row
+    q_start[b]; they are its n_b newest positions.  Returns out float64
+    [total, Hq, D] (and lse [total, Hq])."""
+    qr = _raw(q, q_dtype)
+    kc = _raw(k_cache, cache_dtype)
+    vc = _raw(v_cache, cache_dtype)
+    total, Hq, D = qr.shape
+    num_blocks, Hkv = kc.shape[0], kc.shape[1]
+    if kc.shape[2] != block_size or kc.shape[3] != D:
+        raise ValueError("cache shape must be [num_blocks, Hkv, block_size, D]")
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    qs = np.ascontiguousarray(np.asarray(q_start, dtype=np.int32))
+    B = len(cl)
+    if len(qs) != B + 1 or qs[0] != 0 or qs[-1] != total or np.any(np.diff(qs) < 0):
+        raise ValueError("q_start must be [B+1] offsets from 0 to the row count")
+    ks = None if k_scale is None else np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32))
+    vs = None if v_scale is None else np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32))
+    if cache_dtype == "fp8_e4m3" and (ks is None or vs is None):
+        raise ValueError("fp8 cache needs k_scale and v_scale")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.empty(qr.shape, dtype=np.float64)
+    lse = np.empty(qr.shape[:-1], dtype=np.float64)
+    rc = lib().oracle_prefill(_ptr(out), _ptr(lse), _ptr(qr), DTYPES[q_dtype], _ptr(kc), _ptr(vc),
+                              DTYPES[cache_dtype], _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
+                              _ptr(cl), _ptr(qs), B, int(window), Hq, Hkv, D, num_blocks,
+                              block_size, float(scale), int(nthreads))
+    if rc == -1:
+        raise ValueError("oracle_prefill: Hq must be a multiple of Hkv")
+    if rc == -2:
+        raise ValueError("oracle_prefill: block table entry out of range")
     return (out, lse) if with_lse else out
 
 

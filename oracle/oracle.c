@@ -220,15 +220,23 @@ int oracle_append(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
 /* above — the fixed-size visible history of [P5] PART 02 (third advanced     */
 /* direction, sliding window / KV eviction).  Positions no row can see are    */
 /* not gathered at all, so their blocks may have been released.              */
+/*                                                                          */
+/* Prefill (q_start != NULL): sequence b has its own number of new tokens,    */
+/* n_b = q_start[b+1] - q_start[b], packed in q / out from row q_start[b]     */
+/* ([total][Hq][D]); they are the n_b newest of its ctx_b positions and       */
+/* attend causally as above — the masked attention of a prompt over itself    */
+/* and any cached prefix ([P3] §3.2 flash_attention over Q, K, V blocks;      */
+/* [P5] PART 04 causal naive_attention).                                     */
 /* ---------------------------------------------------------------------- */
 static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
                        const void *k_cache, const void *v_cache, int cache_dtype,
                        const float *k_scale, const float *v_scale,
                        const int32_t *block_table, int max_blocks,
                        const int32_t *context_lens, const int32_t *t_begin,
+                       const int32_t *q_start,
                        int B, int q_len, int window, int Hq, int Hkv, int D, int64_t num_blocks,
                        int block_size, double scale, int nthreads) {
-  if (Hkv <= 0 || Hq % Hkv != 0 || q_len <= 0 || window < 0) return -1;
+  if (Hkv <= 0 || Hq % Hkv != 0 || (!q_start && q_len <= 0) || window < 0) return -1;
   int G = Hq / Hkv;
   int err = 0;
 #ifdef _OPENMP
@@ -241,8 +249,11 @@ static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
     for (int h = 0; h < Hkv; ++h) {
       int t0 = t_begin ? t_begin[b] : 0;
       int t1 = context_lens[b];
+      /* this sequence's new tokens and its first row in q / out */
+      const int nl = q_start ? q_start[b + 1] - q_start[b] : q_len;
+      const size_t row0 = q_start ? (size_t)q_start[b] : (size_t)b * q_len;
       /* the earliest position any row sees: row 0's window start */
-      if (window > 0 && t1 - (q_len - 1) - window > t0) t0 = t1 - (q_len - 1) - window;
+      if (window > 0 && t1 - (nl - 1) - window > t0) t0 = t1 - (nl - 1) - window;
       int n = t1 > t0 ? t1 - t0 : 0;
       double *K = NULL, *V = NULL, *s = NULL, *qv = NULL;
       if (n > 0) {
@@ -272,13 +283,13 @@ static int decode_impl(double *out, double *lse_out, const void *q, int q_dtype,
           V[(size_t)i * D + d] = load_elem(v_cache, cache_dtype, base + d) * vs;
         }
       }
-      for (int qi = 0; qi < q_len; ++qi) {
+      for (int qi = 0; qi < nl; ++qi) {
         /* new token qi sees gathered positions [lo, hi) */
-        int hi = n - (q_len - 1 - qi);
+        int hi = n - (nl - 1 - qi);
         if (hi < 0) hi = 0;
         int lo = (window > 0 && hi - window > 0) ? hi - window : 0;
         int nq = hi - lo;
-        size_t row = (size_t)b * q_len + qi;
+        size_t row = row0 + qi;
         for (int g = 0; g < G; ++g) {
           int hq = h * G + g;
           double *o = out + (row * Hq + hq) * D;
@@ -325,8 +336,8 @@ int oracle_decode(double *out, double *lse_out, const void *q, int q_dtype,
                   int B, int Hq, int Hkv, int D, int64_t num_blocks,
                   int block_size, double scale, int nthreads) {
   return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
-                     block_table, max_blocks, context_lens, t_begin, B, 1, 0, Hq, Hkv, D, num_blocks,
-                     block_size, scale, nthreads);
+                     block_table, max_blocks, context_lens, t_begin, NULL, B, 1, 0, Hq, Hkv, D,
+                     num_blocks, block_size, scale, nthreads);
 }
 
 int oracle_decode_multi(double *out, double *lse_out, const void *q, int q_dtype,
@@ -337,7 +348,19 @@ int oracle_decode_multi(double *out, double *lse_out, const void *q, int q_dtype
                         int B, int q_len, int window, int Hq, int Hkv, int D, int64_t num_blocks,
                         int block_size, double scale, int nthreads) {
   return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
-                     block_table, max_blocks, context_lens, t_begin, B, q_len, window, Hq, Hkv, D,
+                     block_table, max_blocks, context_lens, t_begin, NULL, B, q_len, window, Hq, Hkv, D,
+                     num_blocks, block_size, scale, nthreads);
+}
+
+int oracle_prefill(double *out, double *lse_out, const void *q, int q_dtype,
+                   const void *k_cache, const void *v_cache, int cache_dtype,
+                   const float *k_scale, const float *v_scale,
+                   const int32_t *block_table, int max_blocks,
+                   const int32_t *context_lens, const int32_t *q_start,
+                   int B, int window, int Hq, int Hkv, int D, int64_t num_blocks,
+                   int block_size, double scale, int nthreads) {
+  return decode_impl(out, lse_out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale,
+                     block_table, max_blocks, context_lens, NULL, q_start, B, 0, window, Hq, Hkv, D,
                      num_blocks, block_size, scale, nthreads);
 }
 

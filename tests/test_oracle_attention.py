@@ -389,3 +389,72 @@ def test_sliding_window_special_cases():
         holed[b, :first // bs] = -1
     got = oracle.decode(qf, "f32", *args, holed, ctx, scale=0.3, block_size=bs, window=W)
     assert np.array_equal(got, ref)
+
+
+def test_prefill_matches_causal_sdpa_over_the_prompt():
+    """Prefill with nothing cached: each sequence's whole prompt attends
+    causally to itself — torch SDPA with is_causal on the contiguous K/V
+    ('LLM推理优化实战' §3.2 flash_attention computes exactly this), with GQA."""
+    g = torch.Generator().manual_seed(41)
+    Hq, Hkv, D, bs = 8, 2, 16, 4
+    n = [1, 7, 16, 23]
+    ks = [torch.randn((t, Hkv, D), generator=g, dtype=torch.float64).float().double() for t in n]
+    vs = [torch.randn((t, Hkv, D), generator=g, dtype=torch.float64).float().double() for t in n]
+    q = torch.randn((sum(n), Hq, D), generator=g, dtype=torch.float64).float().double()
+    nb = sum((t + bs - 1) // bs for t in n) + 1
+    perm = torch.randperm(nb, generator=g).numpy()
+    pk, tables, mb = scatter(ks, Hkv, D, bs, nb, perm)
+    pv, _, _ = scatter(vs, Hkv, D, bs, nb, perm)
+    q_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    got = oracle.prefill(q.float().numpy(), "f32", pk.float().numpy(), pv.float().numpy(), "f32",
+                         dense_table(tables, mb), n, q_start, scale=0.25, block_size=bs)
+    G = Hq // Hkv
+    for b in range(len(n)):
+        Qx = q[q_start[b]:q_start[b + 1]].permute(1, 0, 2)
+        Kx = ks[b].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        Vx = vs[b].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(Qx, Kx, Vx, is_causal=True, scale=0.25)
+        assert np.allclose(got[q_start[b]:q_start[b + 1]], ref.permute(1, 0, 2).numpy(), rtol=0,
+                           atol=1e-12)
+
+
+def test_prefill_with_cached_prefix_equals_multi_query_rows():
+    """A prompt chunk after a cached prefix (chunked prefill): with every n_b
+    equal to L the packed prefill equals the multi-query decode bit for bit;
+    ragged n_b equal per-sequence multi-query calls, windows included."""
+    B, L, Hq, Hkv, D, bs = 3, 5, 4, 2, 8, 4
+    ctx, ks, vs, q, pk, pv, tables, mb = _multi_case(53, B, L, Hq, Hkv, D, bs, 60)
+    bt = dense_table(tables, mb)
+    args = (pk.float().numpy(), pv.float().numpy(), "f32", bt, ctx)
+    for W in (0, 7):
+        multi = oracle.decode(q.float().numpy(), "f32", *args, scale=0.3, block_size=bs, window=W)
+        packed = oracle.prefill(q.reshape(B * L, Hq, D).float().numpy(), "f32", *args,
+                                np.arange(0, B * L + 1, L), scale=0.3, block_size=bs, window=W)
+        assert np.array_equal(packed.reshape(B, L, Hq, D), multi)
+    n = [2, 5, 1]
+    q_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    rows = torch.cat([q[b, L - n[b]:] for b in range(B)])       # the last n_b new tokens
+    got = oracle.prefill(rows.float().numpy(), "f32", *args, q_start, scale=0.3, block_size=bs)
+    for b in range(B):
+        one = oracle.decode(q[b:b + 1, L - n[b]:].float().numpy(), "f32", pk.float().numpy(),
+                            pv.float().numpy(), "f32", bt[b:b + 1], ctx[b:b + 1], scale=0.3,
+                            block_size=bs)
+        assert np.array_equal(got[q_start[b]:q_start[b + 1]], one[0])
+
+
+def test_prefill_toy_example_is_the_full_masked_computation():
+    """Page 'KV Cache篇' §2.1: prefilling all three tokens of '天气真' gives the
+    page's full causally masked computation, row for row."""
+    t = _toy()
+    X2 = _f64(t["X_step2"])
+    WQ, WK, WV = _f64(t["W_Q"]), _f64(t["W_K"]), _f64(t["W_V"])
+    div = t["scale_divisor"]
+    Q2, K2, V2 = [(X2 @ W).float().double() for W in (WQ, WK, WV)]
+    mask = torch.triu(torch.full((3, 3), float("-inf"), dtype=torch.float64), diagonal=1)
+    full = torch.softmax(Q2 @ K2.T / div + mask, dim=-1) @ V2
+    pk, tables, mb = scatter([K2[:, None, :]], 1, 4, 2, 2, [1, 0])
+    pv, _, _ = scatter([V2[:, None, :]], 1, 4, 2, 2, [1, 0])
+    out = oracle.prefill(Q2[:, None, :].float().numpy(), "f32", pk.float().numpy(),
+                         pv.float().numpy(), "f32", dense_table(tables, mb), [3], [0, 3],
+                         scale=1.0 / div, block_size=2)
+    assert np.allclose(out[:, 0], full.numpy(), rtol=0, atol=1e-12)

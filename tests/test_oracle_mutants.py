@@ -42,21 +42,28 @@ MUTANTS = [
     ("f16 exponent bias", "v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
      "v = ldexp(1.0 + (double)m / 1024.0, e - 14);",
      [T_fmt.test_f16_all_codes_match_numpy]),
-    ("causal limit off by one", "int hi = n - (q_len - 1 - qi);", "int hi = n - (q_len - qi);",
+    ("causal limit off by one", "int hi = n - (nl - 1 - qi);", "int hi = n - (nl - qi);",
      [lambda: T_att.test_multi_query_matches_masked_sdpa(3, 2, 8, 2, 16, 16, 40),
       T_att.test_multi_query_toy_rows_of_full_masked_computation]),
-    ("causal limit reversed", "int hi = n - (q_len - 1 - qi);", "int hi = n - qi;",
+    ("causal limit reversed", "int hi = n - (nl - 1 - qi);", "int hi = n - qi;",
      [T_att.test_multi_query_rows_are_single_queries_over_shorter_contexts]),
     ("window start off by one", "? hi - window : 0;", "? hi - window + 1 : 0;",
      [lambda: T_att.test_sliding_window_matches_band_masked_sdpa(2, 4, 6, 8, 1, 8, 4, 37),
       T_att.test_sliding_window_special_cases]),
     ("window gather ignores q_len",
-     "if (window > 0 && t1 - (q_len - 1) - window > t0) t0 = t1 - (q_len - 1) - window;",
+     "if (window > 0 && t1 - (nl - 1) - window > t0) t0 = t1 - (nl - 1) - window;",
      "if (window > 0 && t1 - window > t0) t0 = t1 - window;",
      [lambda: T_att.test_sliding_window_matches_band_masked_sdpa(2, 4, 6, 8, 1, 8, 4, 37)]),
-    ("query row ignores token", "size_t row = (size_t)b * q_len + qi;",
-     "size_t row = (size_t)b * q_len;",
+    ("query row ignores token", "size_t row = row0 + qi;",
+     "size_t row = row0;",
      [lambda: T_att.test_multi_query_matches_masked_sdpa(2, 4, 8, 1, 8, 4, 37)]),
+    ("prefill rows from the wrong offset", "const size_t row0 = q_start ? (size_t)q_start[b] : (size_t)b * q_len;",
+     "const size_t row0 = q_start ? (size_t)q_start[b] * 0 : (size_t)b * q_len;",
+     [T_att.test_prefill_matches_causal_sdpa_over_the_prompt]),
+    # (mutants must not write outside the caller's arrays: they run in-process)
+    ("prefill token count of the first sequence", "const int nl = q_start ? q_start[b + 1] - q_start[b] : q_len;",
+     "const int nl = q_start ? q_start[1] - q_start[0] : q_len;",
+     [T_att.test_prefill_matches_causal_sdpa_over_the_prompt]),
     ("kv bytes drops the 2", "return 2.0 * num_layers", "return 1.0 * num_layers",
      [T_app.test_kv_bytes_formula_matches_pages]),
 ]
@@ -77,7 +84,8 @@ def test_planted_mistake_is_caught(tmp_path, monkeypatch, name, orig, mut, tests
     mutant = ctypes.CDLL(str(so))
     for fn in ("oracle_f16_to_double", "oracle_bf16_to_double", "oracle_e4m3_to_double",
                "oracle_e4m3_from_float", "oracle_kv_bytes_per_token", "oracle_append",
-               "oracle_decode", "oracle_decode_multi", "oracle_merge", "oracle_num_threads"):
+               "oracle_decode", "oracle_decode_multi", "oracle_prefill", "oracle_merge",
+               "oracle_num_threads"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)
