@@ -50,6 +50,8 @@ def parse():
                     help="new tokens per sequence per step (multi-query decode, causal)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window: each row attends its W most recent positions")
+    ap.add_argument("--prefill", default="",
+                    help="time paged prefill (tensor cores) on a prefill workload: page, llama70b, chunked")
     return ap.parse_args()
 
 
@@ -441,11 +443,152 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, world, rank, local):
+    """Paged prefill on the tensor cores: each launch attends every new token
+    of the workload causally; value = useful TFLOP/s (4 * D per query head and
+    visible position), L2 flushed before every timed launch."""
+    import numpy as np
+    import torch
+
+    import workloads
+    import paged_kv_gqa_03_gb300 as pkv
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = dict(workloads.PREFILL_SPECS[args.prefill])
+    c = workloads.make_prefill(2000 + list(workloads.PREFILL_SPECS).index(args.prefill), **spec,
+                               free=8, window=args.window)
+    flops = workloads.prefill_flops(c)
+    q, kc, vc = c["q"].to(dev), c["kc"].to(dev), c["vc"].to(dev)
+    table = torch.from_numpy(c["table"]).to(dev)
+    lens = torch.from_numpy(c["ctx"]).to(dev)
+    q_start = torch.from_numpy(c["q_start"]).to(dev)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    scale = 1.0 / math.sqrt(c["D"])
+    max_n = max(c["n"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+
+    def launch():
+        pkv.paged_prefill_attention(out, q, kc, vc, table, lens, q_start, max_n, scale,
+                                    window=args.window, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch()
+    stream.synchronize()
+    sampler = ClockSampler(torch.cuda.get_device_properties(dev).pci_bus_id)
+    sampler.start()
+    times = []
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+    ms = max_over_ranks(statistics.median(times), world, dev)
+    tflops = flops / (ms * 1e-3) / 1e12
+    assert int(status.item()) == 0
+
+    # end to end: q from pinned host memory, the launch, out back to pinned host memory
+    hq = c["q"].pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    e2e = []
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            x0.record(stream)
+            pkv.pkv_copy(q, hq, stream=stream)
+            launch()
+            pkv.pkv_copy(hout, out, stream=stream)
+            x1.record(stream)
+        x1.synchronize()
+        e2e.append(x0.elapsed_time(x1))
+    ms_e2e = statistics.median(e2e)
+
+    # context: torch SDPA (a library kernel) on the same prompts stored contiguously, when
+    # nothing is cached and no window is set
+    sdpa = None
+    if not any(c["prefix"]) and not args.window:
+        G = c["Hq"] // c["Hkv"]
+        qs = [q[c["q_start"][b]:c["q_start"][b + 1]].transpose(0, 1)[None] for b in range(len(c["n"]))]
+        qq = torch.cat(qs)                                                   # [B, Hq, n, D]
+        kk = torch.randn((qq.shape[0], c["Hkv"], qq.shape[2], c["D"]), device=dev, dtype=q.dtype)
+        vv = torch.randn_like(kk)
+        F = torch.nn.functional
+        kx = kk.repeat_interleave(G, 1) if G > 1 else kk
+        vx = vv.repeat_interleave(G, 1) if G > 1 else vv
+        for _ in range(3):
+            F.scaled_dot_product_attention(qq, kx, vx, is_causal=True)
+        st = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            F.scaled_dot_product_attention(qq, kx, vx, is_causal=True)
+            e1.record()
+            e1.synchronize()
+            st.append(e0.elapsed_time(e1))
+        sdpa = {"tflops": round(flops / (statistics.median(st) * 1e-3) / 1e12, 1),
+                "ms": round(statistics.median(st), 4),
+                "what": "torch scaled_dot_product_attention, is_causal, contiguous K/V (GQA heads expanded), same shapes"}
+
+    # oracle sample on the host cores: the first 64 rows' worth of one sequence
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        import oracle
+        rows = np.arange(min(64, c["n"][0]))
+        lens = np.array([c["ctx"][0] - c["n"][0] + r + 1 for r in rows], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode(c["q"][rows], c["dtype"], c["kc"], c["vc"], c["dtype"], c["table"][np.zeros_like(rows)],
+                      lens, scale=scale, window=args.window)
+        dt = time.perf_counter() - t0
+        f = 4.0 * c["D"] * c["Hq"] * sum(min(l, args.window) if args.window else l for l in lens)
+        cpu = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"oracle (fp64) on {len(rows)} rows of sequence 0, {dt:.1f} s"}
+    if rank != 0:
+        return
+    peak, src = peak_bf16()
+    line = {
+        "metric": "paged prefill attention throughput (causal, useful FLOPs)", "value": round(tflops, 1),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": c["dtype"], "data": "synthetic (seeded N(0,1), random block permutation)",
+        "config": {"workload": f"prefill {args.prefill}", "B": len(c["n"]), "new_tokens": c["n"][0],
+                   "cached_prefix": c["prefix"][0], "Hq": c["Hq"], "Hkv": c["Hkv"], "D": c["D"],
+                   "window": args.window, "block_size": 16, "l2": "flushed (256 MB write) before every timed launch"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(tflops, 1),
+                     "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "note": "bf16 P is split into high + residual parts (1.5x the MMA work of one P)"},
+        "e2e": {"value": round(flops / (ms_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": q.numel() * q.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": round(ms_e2e, 4)},
+        "sdpa_contiguous": sdpa, "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.prefill:
+        run_prefill(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

@@ -213,6 +213,39 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
                                  pkv_stream_t stream);
 
 /*
+ * Paged prefill attention on the tensor cores (tcgen05): sequence b's
+ * n_b = q_start[b+1] - q_start[b] new tokens — its prompt, or a chunk of it
+ * after a cached prefix — attend causally over its paged cache.  The tokens
+ * are already appended (paged_kv_append, slots in order) and are the n_b
+ * newest of ctx_b = context_lens[b] positions: new token i (position
+ * ctx_b - n_b + i) attends positions 0 .. ctx_b - n_b + i, or only the
+ * `window` most recent of them when window > 0.  This is FlashAttention's
+ * tiled computation ("LLM推理优化实战" §3.2 flash_attention: row blocks of Q,
+ * blocks of K / V, online softmax) with the causal mask of "苦猿的大模型日记
+ * Day45" PART 04; a row that sees nothing gives 0.
+ *
+ *   q, out       [total][Hq][D], total = q_start[B]; rows of sequence b start
+ *                at q_start[b] (int32 [B+1], device, non-decreasing, q_start[0] = 0)
+ *   q_dtype      must equal cache_dtype, which is PKV_F16 or PKV_BF16
+ *                (PKV_EUNSUPPORTED otherwise; FP8 caches use the decode path)
+ *   max_q_len    >= every n_b (host value; sizes the grid); a larger n_b sets
+ *                PKV_FLAG_BAD_LEN and rows past max_q_len are not written
+ *   scale        > 0 (PKV_EINVAL otherwise)
+ *   window       0 (none) or W >= 1
+ *   status       device int32 or NULL: zeroed by the call, then the OR of
+ *                PKV_FLAG_* bits (bad block id, bad length, in-kernel timeout)
+ *   D            64 or 128; B <= 65535
+ * Other arguments as for paged_decode_attention.  Asynchronous on `stream`;
+ * needs no workspace.
+ */
+int paged_prefill_attention(void *out, const void *q, int q_dtype,
+                            const void *k_cache, const void *v_cache, int cache_dtype,
+                            const int32_t *block_table, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *q_start,
+                            int B, int max_q_len, int Hq, int Hkv, int D, int64_t num_blocks,
+                            float scale, int window, int32_t *status, pkv_stream_t stream);
+
+/*
  * paged_decode_attention for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point; it exists for callers of
  * this library.  Some of them cannot hand over a workspace: a plain C host

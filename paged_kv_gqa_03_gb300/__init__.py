@@ -13,7 +13,7 @@ import os
 
 __all__ = [
     "PagedKVError", "paged_kv_append", "paged_decode_workspace_bytes",
-    "paged_decode_attention", "paged_decode_status", "paged_decode_merge",
+    "paged_decode_attention", "paged_prefill_attention", "paged_decode_status", "paged_decode_merge",
     "paged_kv_copy_blocks", "pkv_copy", "pkv_status_string", "pkv_version", "BlockManager",
     "DTYPE_CODES", "LIB_PATH", "lib",
 ]
@@ -45,6 +45,8 @@ _sig("paged_decode_multi_workspace_bytes", _i32, _i32, _i32, _i32, _i32, _i32, _
      ctypes.POINTER(_sz))
 _sig("paged_decode_attention_multi", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
      _i32, _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _sz, _P)
+_sig("paged_prefill_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _i32, _P, _P,
+     _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _P)
 _sig("paged_decode_status", _i32, _P, _sz, _P, ctypes.POINTER(_i32))
 _sig("paged_decode_merge", _i32, _P, _i32, _P, _P, _i32, _i32, _i32, _i32, _P)
 _sig("paged_kv_copy_blocks", _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
@@ -67,6 +69,7 @@ _sig("pkv_bm_num_tokens", _i64, _P, _i64)
 
 PKV_OK, PKV_EINVAL, PKV_EUNSUPPORTED, PKV_EWORKSPACE = 0, -1, -2, -3
 PKV_ECUDA, PKV_ETIMEOUT, PKV_EOOM, PKV_ERANGE, PKV_ENOTFOUND = -4, -5, -6, -7, -8
+PKV_FLAG_TIMEOUT, PKV_FLAG_BAD_LEN, PKV_FLAG_BAD_BLOCK = 1, 2, 4
 
 
 def lib():
@@ -205,6 +208,26 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
         _check(_L.paged_decode_attention(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
                                          B, Hq, Hkv, D, *tail), "paged_decode_attention")
     return workspace
+
+
+def paged_prefill_attention(out, q, k_cache, v_cache, block_table, context_lens, q_start, max_q_len,
+                            scale, window=0, status=None, stream=None):
+    """Causal attention of each sequence's new tokens over its paged cache
+    (tensor cores).  q, out [total, Hq, D]; q_start int32 [B+1] row offsets;
+    max_q_len >= every sequence's new-token count; status: optional int32
+    CUDA tensor that receives the PKV_FLAG_* bits."""
+    torch = _torch()
+    total, Hq, D = q.shape
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out shape {tuple(out.shape)} != q shape {tuple(q.shape)}")
+    B = q_start.shape[0] - 1
+    num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
+    _check(_L.paged_prefill_attention(
+        _dev(out, "out"), _dev(q, "q"), _code(q), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _code(k_cache), _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), _dev(q_start, "q_start", torch.int32),
+        B, int(max_q_len), Hq, Hkv, D, num_blocks, float(scale), int(window),
+        _dev(status, "status", torch.int32), _stream(stream)), "paged_prefill_attention")
 
 
 def paged_decode_status(workspace, stream=None):

@@ -423,6 +423,55 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   return cuda_status(e);
 }
 
+int paged_prefill_attention(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
+                            int cache_dtype, const int32_t *block_table, int max_blocks_per_seq,
+                            const int32_t *context_lens, const int32_t *q_start, int B, int max_q_len, int Hq,
+                            int Hkv, int D, int64_t num_blocks, float scale, int window, int32_t *status,
+                            pkv_stream_t stream) {
+  int rc = validate_decode_shapes(q_dtype, cache_dtype, B, 1, Hq, Hkv, D, num_blocks, max_blocks_per_seq);
+  if (rc != PKV_OK) return rc;
+  if (cache_dtype != PKV_F16 && cache_dtype != PKV_BF16) return PKV_EUNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale) || window < 0 || max_q_len < 0) return PKV_EINVAL;
+  if (B > 65535 || Hkv > 65535) return PKV_EUNSUPPORTED;
+  const int G = Hq / Hkv;
+  const int64_t tiles = ((int64_t)max_q_len * G + 127) / 128;
+  if (tiles > INT32_MAX) return PKV_EUNSUPPORTED;
+  if (B == 0 || tiles == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || !q_start) return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+  CUtensorMap tmK, tmV;
+  rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+  if (rc != PKV_OK) return rc;
+  rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+  if (rc != PKV_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (status) {
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.out = out;
+  p.q = q;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.q_start = q_start;
+  p.status = status;
+  p.num_blocks = num_blocks;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.G = G;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_q_len = max_q_len;
+  p.max_tiles = (int)tiles;
+  p.window = window < (1 << 30) ? window : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = 4000000000ull;
+  return cuda_status(launch_prefill(p, cache_dtype, tmK, tmV, s));
+}
+
 int paged_decode_status(const void *workspace, size_t workspace_bytes, pkv_stream_t stream, int *flags_out) {
   if (!workspace || workspace_bytes < sizeof(WsHeader)) return PKV_EWORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -110,6 +110,25 @@ int register_decode_f16(DecodeKernel *out);
 int register_decode_fp8(DecodeKernel *out);
 int register_decode_f32(DecodeKernel *out);
 
+// Paged prefill (tcgen05): each sequence's new tokens attend causally.
+struct PrefillParams {
+  void *out;
+  const void *q;
+  const int32_t *block_table;
+  const int32_t *context_lens;
+  const int32_t *q_start;   // [B+1] row offsets of each sequence's new tokens in q / out
+  int32_t *status;          // PKV_FLAG_* bits (may be null)
+  int64_t num_blocks;
+  int B, Hq, Hkv, D, G, max_blocks, max_q_len, max_tiles;
+  int window;               // 0 = none
+  float scale_log2;         // softmax scale * log2(e), > 0
+  uint64_t timeout_ns;
+};
+// Launches the prefill kernel for (cache dtype, D); cudaErrorNotSupported for
+// a combination that is not compiled.
+cudaError_t launch_prefill(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                           cudaStream_t stream);
+
 cudaError_t launch_plan(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_splitk_merge(const DecodeParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge(void *out, int out_dtype, const float *o_partial, const float *lse,

@@ -245,3 +245,61 @@ def config(index: int, **overrides) -> Workload:
     spec = dict(SPECS[index])
     spec.update(overrides)
     return make(spec, 1000 + index)
+
+
+# Prefill workloads (a prompt, or a prompt chunk after a cached prefix, per
+# sequence; every new token attends causally).  "page": the pages' prefill
+# benchmark shape (fp16, 16 heads, D 64, 2048 tokens, one sequence);
+# "llama70b": the Llama-3.1-70B-shaped GQA layer with four 2048-token prompts;
+# "chunked": four 1024-token chunks after 4096 cached positions.
+PREFILL_SPECS = {
+    "page": dict(n=[2048], prefix=[0], Hq=16, Hkv=16, D=64, dtype="f16"),
+    "llama70b": dict(n=[2048] * 4, prefix=[0] * 4, Hq=64, Hkv=8, D=128, dtype="bf16"),
+    "chunked": dict(n=[1024] * 4, prefix=[4096] * 4, Hq=64, Hkv=8, D=128, dtype="bf16"),
+}
+
+
+def make_prefill(seed, n, prefix, Hq, Hkv, D, dtype, free=4, stale_nan=True, window=0):
+    """Paged caches holding sequences of ctx_b = prefix_b + n_b positions
+    (block ids a random permutation, every value N(0,1) rounded to dtype),
+    packed q [sum n, Hq, D] for the n_b new tokens with row offsets q_start,
+    and NaN in every stale position past ctx_b inside a sequence's last block
+    (stale_nan).  Draw order: permutation, K, V, q."""
+    import numpy as np
+    g = torch.Generator().manual_seed(seed)
+    B = len(n)
+    ctx = [p + m for p, m in zip(prefix, n)]
+    need = [(c + BLOCK - 1) // BLOCK for c in ctx]
+    nb = sum(need) + free
+    perm = torch.randperm(nb, generator=g).tolist()
+    tables, k = [], 0
+    for b in range(B):
+        tables.append(perm[k:k + need[b]])
+        k += need[b]
+    table = np.full((B, max(1, max(need))), -1, dtype=np.int32)
+    for b in range(B):
+        table[b, :need[b]] = tables[b]
+    t = _TORCH[dtype]
+    kc = _fill_normal(torch.empty((nb, Hkv, BLOCK, D), dtype=t), g, dtype)
+    vc = _fill_normal(torch.empty((nb, Hkv, BLOCK, D), dtype=t), g, dtype)
+    if stale_nan:
+        for b in range(B):
+            if ctx[b] % BLOCK:
+                kc[tables[b][-1], :, ctx[b] % BLOCK:] = float("nan")
+                vc[tables[b][-1], :, ctx[b] % BLOCK:] = float("nan")
+    q = _fill_normal(torch.empty((sum(n), Hq, D), dtype=t), g, dtype)
+    q_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    return dict(q=q, kc=kc, vc=vc, table=table, ctx=np.array(ctx, dtype=np.int32), q_start=q_start,
+                n=list(n), prefix=list(prefix), dtype=dtype, Hq=Hq, Hkv=Hkv, D=D, window=window)
+
+
+def prefill_flops(c):
+    """Useful FLOPs of a prefill: 4 * D per (query head, visible position)."""
+    total = 0
+    for b, m in enumerate(c["n"]):
+        ctx = int(c["ctx"][b])
+        for i in range(m):
+            lim = ctx - m + i + 1
+            vis = min(lim, c["window"]) if c["window"] else lim
+            total += max(0, vis)
+    return 4.0 * c["D"] * c["Hq"] * total
