@@ -11,14 +11,17 @@
 //    token i, query head g) of the kv head's group, token-major, so GQA heads
 //    share every K / V tile;
 //  * K / V tiles of 128 positions = 8 paged blocks, fetched by TMA through the
-//    block table (one 2 KiB box per block and 64-element panel) into a
-//    STAGES-deep ring;
-//  * S = Q . K^T (128 x 128, f32) and O += P . V (128 x D, f32) are tcgen05.mma
-//    with operands in shared memory (128-byte swizzle; V as an MN-major
-//    operand) and accumulators in tensor memory; S is double-buffered so the
-//    MMA of tile j+1 overlaps the softmax of tile j;
-//  * four softmax warps own one query row per thread (tcgen05.ld 32x32b): the
-//    row max needs no shuffles; P goes back to shared memory as the A operand;
+//    block table (one 2 KiB box per block and 64-element panel) into a 3-deep
+//    K ring and a 2-deep V ring: a K slot frees as soon as S = Q . K^T has
+//    read it, a V slot when P . V has;
+//  * S (128 x 128, f32) and O (128 x D, f32) live in tensor memory; S has three
+//    buffers, and each buffer's P (the 16-bit weights) is written back over
+//    the S columns its thread has read, so P . V takes A from tensor memory
+//    (tcgen05.mma A-in-TMEM) and B = V from shared memory (128-byte swizzle,
+//    MN-major); Q and K are 128-byte-swizzled K-major operands;
+//  * eight softmax warps: thread (row, half) owns half of one query row's
+//    columns (tcgen05.ld / st 32x32b; warps w and w + 4 share a lane
+//    quarter); the halves exchange their partial row max once per tile;
 //  * O is rescaled in tensor memory only when a row's running max grows by
 //    more than 8 (log2 units): the result is exact either way, since P and l
 //    share the stale max, and p <= 2^8 keeps P well inside 16-bit range;
@@ -26,7 +29,7 @@
 //    11 significant bits, enough for the 2e-3 output bound; bf16 keeps 8, so a
 //    bf16 P goes in as a high part plus its bf16 residual, two MMAs on the
 //    same V tile (the weights then carry ~16 bits);
-//  * warp roles: 0-3 softmax + epilogue, 4 TMA producer, 5 MMA issue and
+//  * warp roles: 0-7 softmax + epilogue, 8 TMA producer, 9 MMA issue and
 //    tensor-memory allocation.  Every wait is bounded; a timeout sets
 //    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
 //    memory.
@@ -42,26 +45,28 @@ template <class T, int D_>
 struct PrefillCfg {
   static constexpr int D = D_;
   static constexpr bool BF = T::kCode == PKV_BF16;
+  static constexpr bool SPLIT = BF;                     // P as bf16 high + residual
   static constexpr int M = 128;                         // query rows per CTA
   static constexpr int N = 128;                         // cache positions per K / V tile
   static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
   static constexpr int PANELS = D / 64;                 // 128-byte panels per row
-  static constexpr int PANEL_Q = M * 128;               // one Q or P panel (128 rows)
+  static constexpr int PANEL_Q = M * 128;               // one Q panel (128 rows)
   static constexpr int PANEL_KV = N * 128;              // one K or V panel (128 positions)
   static constexpr int Q_BYTES = PANELS * PANEL_Q;
-  static constexpr int KV_BYTES = PANELS * PANEL_KV;    // the K (or V) half of a stage
-  static constexpr int STAGES = D == 64 ? 3 : 2;
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr bool SPLIT = BF;                      // P as bf16 high + residual
-  static constexpr int P_PART = 2 * PANEL_Q;            // 128 rows x 128 positions
-  static constexpr int P_BYTES = (SPLIT ? 2 : 1) * P_PART;
-  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)STAGES * STAGE_BYTES + P_BYTES;
+  static constexpr int KV_BYTES = PANELS * PANEL_KV;    // one K (or V) tile
+  static constexpr int KSTAGES = 3, VSTAGES = 2;
+  static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
+  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int SBUF = 3;                        // S / P buffers in tensor memory
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;                  // S buffers at columns 0 and 128
-  static constexpr uint32_t COL_O = 256;                // O at columns 256 .. 256 + D
-  static constexpr int THREADS = 192;
+  static constexpr uint32_t COL_O = SBUF * N;           // O after the S buffers
+  static constexpr int SOFTMAX = 256;                   // threads: 128 rows x 2 halves
+  static constexpr int THREADS = SOFTMAX + 64;          // + producer warp + MMA warp
+  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1;  // warp ids
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
+  static_assert(LOADS <= 32, "one box per producer lane");
+  static_assert(SMEM + 4096 <= 232448, "shared memory");
 };
 
 // A bounded wait whose outcome is the same for every lane of the warp (the
@@ -93,12 +98,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *sQ = smem;
-  uint8_t *sKV = sQ + Cfg::Q_BYTES;
-  uint8_t *sP = sKV + (size_t)Cfg::STAGES * Cfg::STAGE_BYTES;
-  __shared__ __align__(8) uint64_t full[Cfg::STAGES], empty[Cfg::STAGES];
-  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full, pv_done, fin;
+  uint8_t *sK = sQ + Cfg::Q_BYTES;
+  uint8_t *sV = sK + (size_t)Cfg::KSTAGES * Cfg::KV_BYTES;
+  __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
+  __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
+  // per S buffer: S written, P written, P . V done.  (One P barrier per buffer:
+  // the softmax may finish tile j + 1 before the MMA warp waits for tile j, but
+  // it cannot finish tile j + SBUF before that.)
+  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
+  __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
+  __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag, cta_flags, consumed, issued;
+  __shared__ int abort_flag, cta_flags, k_consumed, v_consumed, k_issued, v_issued;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = p.max_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) row tiles first
@@ -121,38 +132,47 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (tid == 0) {
 #pragma unroll
-    for (int s = 0; s < Cfg::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < Cfg::KSTAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], 4);
-    mbar_init(&s_free[1], 4);
-    mbar_init(&p_full, 4);
-    mbar_init(&pv_done, 1);
+#pragma unroll
+    for (int s = 0; s < Cfg::VSTAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+#pragma unroll
+    for (int s = 0; s < Cfg::SBUF; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], Cfg::SOFTMAX / 32);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(&xch[0], Cfg::SOFTMAX / 32);
+    mbar_init(&xch[1], Cfg::SOFTMAX / 32);
+    mbar_init(&xl, Cfg::SOFTMAX / 32);
     mbar_init(&fin, 1);
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = ctx_raw != ctx ? PKV_FLAG_BAD_LEN : 0;
-    consumed = 0;
-    issued = 0;
+    k_consumed = v_consumed = k_issued = v_issued = 0;
   }
-  if (warp == 5) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
-  if (warp == 4 && lane == 0) {
+  if (warp == Cfg::ISSUER) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
+  if (warp == Cfg::PRODUCER && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (tid < Cfg::M) {  // Q tile: each softmax thread stages its own row (zeros past R)
-    const int r = r0 + tid;
+  if (tid < Cfg::SOFTMAX) {  // Q tile: thread (row, half) stages half of its row (zeros past R)
+    const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
+    const int r = r0 + row;
     const int ii = r / p.G, g = r - ii * p.G;
     const uint4 *src = r < R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
                                                              ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D)
                              : nullptr;
 #pragma unroll
-    for (int c = 0; c < Cfg::D / 8; ++c) {
+    for (int k = 0; k < Cfg::D / 16; ++k) {
+      const int c = half * (Cfg::D / 16) + k;
       const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      sts128(smem_u32(sQ + (c >> 3) * Cfg::PANEL_Q + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)), v);
+      sts128(smem_u32(sQ + (c >> 3) * Cfg::PANEL_Q + row * 128 + (((c & 7) ^ (row & 7)) << 4)), v);
     }
     fence_proxy_async();
   }
@@ -161,68 +181,68 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc::fence_after();
   const uint32_t tbase = tmem_base;
 
-  if (warp == 4) {
+  if (warp == Cfg::PRODUCER) {
     // ---------------- TMA producer ----------------
+    // lane l fetches block (l % 8) of a tile, panel l / 8; the ids of the next
+    // tile are read one tile ahead
+    const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
+    auto block_row = [&](int jj, int *bad) -> int64_t {
+      const int lb = (j_first + jj) * Cfg::BLOCKS + slot;
+      if (jj >= T || lb >= nblk) return p.num_blocks * p.Hkv;  // past the tensor: zero fill
+      const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
+      if (id >= 0 && (int64_t)id < p.num_blocks) return (int64_t)id * p.Hkv + h;
+      *bad = 1;
+      return p.num_blocks * p.Hkv;
+    };
+    int bad = 0;
+    int64_t trow = block_row(0, &bad);
     for (int j = 0; j < T; ++j) {
-      const int st = j % Cfg::STAGES;
-      if (j >= Cfg::STAGES &&
-          !warp_wait(&empty[st], (uint32_t)((j / Cfg::STAGES) - 1) & 1u, p.timeout_ns)) {
-        if (lane == 0) {
-          atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
-          abort_flag = 1;
-        }
+      const int64_t next = block_row(j + 1, &bad);
+      const int ks = j % Cfg::KSTAGES, vs = j % Cfg::VSTAGES;
+      if (j >= Cfg::KSTAGES &&
+          !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
         break;
-      }
       if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
-      const int lb = (j_first + j) * Cfg::BLOCKS + (lane & (Cfg::BLOCKS - 1));
-      int64_t trow = p.num_blocks * p.Hkv;  // past the tensor: TMA fills zeros
-      if (lb < nblk) {
-        const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
-        if (id >= 0 && (int64_t)id < p.num_blocks)
-          trow = (int64_t)id * p.Hkv + h;
-        else
-          atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], Cfg::STAGE_BYTES);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
       __syncwarp();
-      if (lane < 2 * Cfg::BLOCKS * Cfg::PANELS) {  // one box per lane: (block, K or V, panel)
-        const int blk = lane & (Cfg::BLOCKS - 1), kv = (lane / Cfg::BLOCKS) & 1, panel = lane / (2 * Cfg::BLOCKS);
-        uint8_t *dst = sKV + (size_t)st * Cfg::STAGE_BYTES + kv * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + blk * 2048;
-        tma_load_2d(dst, kv ? &tmV : &tmK, panel * 64, (int)(trow * kBlock), &full[st]);
-      }
-      if (lane == 0) issued = j + 1;
+      if (lane < Cfg::LOADS)
+        tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
+                    (int)(trow * kBlock), &k_full[ks]);
+      if (lane == 0) k_issued = j + 1;
+      if (j >= Cfg::VSTAGES &&
+          !warp_wait(&v_empty[vs], (uint32_t)((j / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
+      __syncwarp();
+      if (lane < Cfg::LOADS)
+        tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
+                    (int)(trow * kBlock), &v_full[vs]);
+      if (lane == 0) v_issued = j + 1;
+      trow = next;
     }
-  } else if (warp == 5) {
+    if (bad) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
+    if (__any_sync(kFull, k_issued < T || v_issued < T) && lane == 0 && !*(volatile int *)&abort_flag) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
+    }
+  } else if (warp == Cfg::ISSUER) {
     // ---------------- MMA issue ----------------
     constexpr uint32_t idS = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::N, false);
     constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
-    const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
+    const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
     for (int j = 0; j <= T && ok; ++j) {
       if (j < T) {
-        const int st = j % Cfg::STAGES;
-        ok = warp_wait(&full[st], (uint32_t)(j / Cfg::STAGES) & 1u, p.timeout_ns);
-        if (ok && j >= 2) ok = warp_wait(&s_free[j & 1], (uint32_t)((j >> 1) - 1) & 1u, p.timeout_ns);
+        const int ks = j % Cfg::KSTAGES, sb = j % Cfg::SBUF;
+        ok = warp_wait(&k_full[ks], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
+        // S buffer sb last held P of tile j - SBUF: its P . V must be done
+        if (ok && j >= Cfg::SBUF) ok = warp_wait(&pv_done[sb], (uint32_t)((j / Cfg::SBUF) - 1) & 1u, p.timeout_ns);
         if (!ok) break;
-        if (lane == 0) consumed = j + 1;
-        uint8_t *kt = sKV + (size_t)st * Cfg::STAGE_BYTES;
-        // stale cache rows past ctx inside the sequence's last block: zero them in V
-        // (their weights are 0, but 0 * NaN would still poison P . V)
-        const int kv0 = (j_first + j) * Cfg::N;
-        const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
-        if (z0 >= 0 && z0 < z1) {
-          for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
-            const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
-            sts128(smem_u32(kt + Cfg::KV_BYTES + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16),
-                   make_uint4(0, 0, 0, 0));
-          }
-          fence_proxy_async();
-        }
-        __syncwarp();
+        if (lane == 0) k_consumed = j + 1;
         tc::fence_after();
         if (lane == 0) {
-          const uint32_t k0 = smem_u32(kt);
-          const uint32_t dS = tbase + Cfg::COL_S + (uint32_t)(j & 1) * Cfg::N;
+          const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
+          const uint32_t dS = tbase + (uint32_t)(sb * Cfg::N);
 #pragma unroll
           for (int k = 0; k < Cfg::D / 16; ++k) {
             const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
@@ -230,28 +250,44 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
                         k > 0 ? 1u : 0u);
           }
-          tc::commit(&s_full[j & 1]);
+          tc::commit(&s_full[sb]);
+          tc::commit(&k_empty[ks]);
         }
         __syncwarp();
       }
       if (j >= 1) {
-        const int jp = j - 1, stp = jp % Cfg::STAGES;
-        ok = warp_wait(&p_full, (uint32_t)jp & 1u, p.timeout_ns);
+        const int jp = j - 1, vs = jp % Cfg::VSTAGES, sb = jp % Cfg::SBUF;
+        ok = warp_wait(&v_full[vs], (uint32_t)(jp / Cfg::VSTAGES) & 1u, p.timeout_ns);
+        if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(jp / Cfg::SBUF) & 1u, p.timeout_ns);
         if (!ok) break;
+        if (lane == 0) v_consumed = jp + 1;
+        uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
+        // stale cache rows past ctx inside the sequence's last block: zero them in V
+        // (their weights are 0, but 0 * NaN would still poison P . V)
+        const int kv0 = (j_first + jp) * Cfg::N;
+        const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
+        if (z0 >= 0 && z0 < z1) {
+          for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
+            const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
+            sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
+          }
+          fence_proxy_async();
+        }
+        __syncwarp();
         tc::fence_after();
         if (lane == 0) {
-          const uint32_t v0 = smem_u32(sKV + (size_t)stp * Cfg::STAGE_BYTES + Cfg::KV_BYTES);
+          const uint32_t v0 = smem_u32(vt);
+          const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
 #pragma unroll
           for (int k = 0; k < Cfg::N / 16; ++k) {
-            const uint32_t offp = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
+            // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+            const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
             const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
-            tc::mma_f16(tbase + Cfg::COL_O, tc::desc_sw128(p0 + offp, 16, 1024), dv, idO,
-                        (jp > 0 || k > 0) ? 1u : 0u);
-            if constexpr (Cfg::SPLIT)
-              tc::mma_f16(tbase + Cfg::COL_O, tc::desc_sw128(p0 + Cfg::P_PART + offp, 16, 1024), dv, idO, 1u);
+            tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (jp > 0 || k > 0) ? 1u : 0u);
+            if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
           }
-          tc::commit(&pv_done);
-          tc::commit(&empty[stp]);
+          tc::commit(&pv_done[sb]);
+          tc::commit(&v_empty[vs]);
         }
         __syncwarp();
       }
@@ -262,31 +298,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       abort_flag = 1;
     }
   } else {
-    // ---------------- softmax + epilogue (one query row per thread) ----------------
-    const int r = r0 + tid;
+    // ---------------- softmax + epilogue: thread (row, half) ----------------
+    constexpr int SC = Cfg::N / 2;  // S columns of a thread (its half of the row)
+    constexpr int OC = Cfg::D / 2;  // O columns of a thread
+    const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
+    const int r = r0 + row;
     const bool valid = r < R;
     const int lim = valid ? ctx - n + r / p.G + 1 : 0;  // visible positions [lo, lim)
     const int lo = (valid && p.window > 0) ? max(0, lim - p.window) : 0;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     float m_run = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      ok = warp_wait(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
+      const int sb = j % Cfg::SBUF;
+      ok = warp_wait(&s_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
       if (!ok) break;
       tc::fence_after();
-      uint32_t s[Cfg::N / 32][32];
+      const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
+      uint32_t s[SC / 32][32];
 #pragma unroll
-      for (int q = 0; q < Cfg::N / 32; ++q)
-        tc::ld32(tbase + lane_base + Cfg::COL_S + (uint32_t)(j & 1) * Cfg::N + (uint32_t)q * 32, s[q]);
-      tc::wait_ld();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[j & 1]);
-      const int kv0 = (j_first + j) * Cfg::N;
-      if (!(kv0 >= lo && kv0 + Cfg::N <= lim)) {  // a mask edge crosses this tile
+      for (int q = 0; q < SC / 32; ++q) tc::ld32(scol + (uint32_t)(q * 32), s[q]);
+      const int kv0 = (j_first + j) * Cfg::N + half * SC;
+      if (!(kv0 >= lo && kv0 + SC <= lim)) {  // a mask edge crosses these columns
 #pragma unroll
-        for (int q = 0; q < Cfg::N / 32; ++q)
+        for (int q = 0; q < SC / 32; ++q)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int pos = kv0 + q * 32 + e;
@@ -295,61 +331,70 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < Cfg::N / 32; ++q)
+      for (int q = 0; q < SC / 32; ++q)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
+      // the row max over both halves (double-buffered exchange, bounded wait)
+      red[j & 1][half][row] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xch[j & 1]);
+      ok = warp_wait(&xch[j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
+      if (!ok) break;
+      mx = fmaxf(mx, red[j & 1][half ^ 1][row]);
       const float m_new = fmaxf(m_run, mx * c);
-      const bool need = m_new > m_run + 8.f;
-      if (j > 0) {  // P . V of the previous tile has finished reading P and writing O
-        ok = warp_wait(&pv_done, (uint32_t)(j - 1) & 1u, p.timeout_ns);
-        if (!ok) break;
-        tc::fence_after();
-      }
-      if (__any_sync(kFull, need)) {
-        const float alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
-        if (j > 0) {
-#pragma unroll
-          for (int q = 0; q < Cfg::D / 32; ++q) {
-            uint32_t o[32];
-            tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)q * 32, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::st32(tbase + lane_base + Cfg::COL_O + (uint32_t)q * 32, o);
-          }
-          tc::wait_st();
-        }
-        l *= alpha;
+      // warps w and w + 4 hold the same rows and the same m_new: same decision
+      const bool rescale = __any_sync(kFull, m_new > m_run + 8.f);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
         m_run = m_new;
       }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       float sum = 0.f;
+      uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
 #pragma unroll
-      for (int ch = 0; ch < Cfg::N / 8; ++ch) {  // 16-byte chunks of the P row
-        uint32_t w[4], wl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = ch * 8 + 2 * e;
-          const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
-          const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
-          sum += a0 + a1;
-          w[e] = pack2<Cfg::BF>(a0, a1);
-          if constexpr (Cfg::SPLIT) {
-            const float2 hi = unpack2(BF16{}, w[e]);
-            wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
-          }
+      for (int e = 0; e < SC / 2; ++e) {
+        const int col = 2 * e;
+        const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
+        const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
+        sum += a0 + a1;
+        w[e] = pack2<Cfg::BF>(a0, a1);
+        if constexpr (Cfg::SPLIT) {
+          const float2 hi = unpack2(BF16{}, w[e]);
+          wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
         }
-        const uint32_t off = (uint32_t)((ch >> 3) * Cfg::PANEL_Q + tid * 128 + (((ch & 7) ^ (tid & 7)) << 4));
-        sts128(smem_u32(sP + off), make_uint4(w[0], w[1], w[2], w[3]));
-        if constexpr (Cfg::SPLIT) sts128(smem_u32(sP + Cfg::P_PART + off), make_uint4(wl[0], wl[1], wl[2], wl[3]));
       }
-      l += sum;
-      fence_proxy_async();
+      if (rescale && j > 0) {  // O must hold P . V of the previous tile before it is scaled
+        ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+        if (!ok) break;
+        tc::fence_after();
+#pragma unroll
+        for (int q = 0; q < OC / 32; ++q) {
+          uint32_t o[32];
+          const uint32_t ta = tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32);
+          tc::ld32(ta, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st32(ta, o);
+        }
+      }
+      l = l * alpha + sum;
+      // P over this thread's own (already read) S columns: high part, then residual
+      tc::st32(scol, w);
+      if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
-    if (ok && T > 0) ok = warp_wait(&pv_done, (uint32_t)(T - 1) & 1u, p.timeout_ns);
+    if (ok && T > 0)
+      ok = warp_wait(&pv_done[(T - 1) % Cfg::SBUF], (uint32_t)((T - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+    if (ok) {  // the row sum over both halves
+      red_l[half][row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xl);
+      ok = warp_wait(&xl, 0, p.timeout_ns);
+    }
     if (!ok) {
       if (lane == 0) {
         atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
@@ -357,17 +402,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
     } else {
       tc::fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that sees nothing gives 0
+      const float lt = l + red_l[half ^ 1][row];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
       const int ii = r / p.G, g = r - ii * p.G;
       uint4 *dst = valid ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                     ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D)
+                                                     ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D + half * OC)
                          : nullptr;
 #pragma unroll
-      for (int q = 0; q < Cfg::D / 32; ++q) {
+      for (int q = 0; q < OC / 32; ++q) {
         uint32_t o[32];
         if (T > 0) {
-          tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)q * 32, o);
-          tc::wait_ld();
+          tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
@@ -375,11 +420,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (dst) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+            uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv, __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
-            dst[q * 4 + v] = make_uint4(w[0], w[1], w[2], w[3]);
+              wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                     __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+            dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
       }
@@ -389,18 +435,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // ---------------- drain, then free tensor memory ----------------
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == Cfg::ISSUER) {
     if (lane == 0) tc::commit(&fin);  // completes once every issued MMA has
     __syncwarp();
     if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
-  } else if (warp == 4 && lane == 0) {
-    for (int j = consumed; j < issued; ++j)  // copies issued but never consumed (abort only)
-      mbar_wait_bounded(&full[j % Cfg::STAGES], (uint32_t)(j / Cfg::STAGES) & 1u, p.timeout_ns);
+  } else if (warp == Cfg::PRODUCER && lane == 0) {  // copies issued but never consumed (abort only)
+    for (int j = k_consumed; j < k_issued; ++j)
+      mbar_wait_bounded(&k_full[j % Cfg::KSTAGES], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
+    for (int j = v_consumed; j < v_issued; ++j)
+      mbar_wait_bounded(&v_full[j % Cfg::VSTAGES], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 5) tc::dealloc(tbase, Cfg::TMEM_COLS);
+  if (warp == Cfg::ISSUER) tc::dealloc(tbase, Cfg::TMEM_COLS);
   if (tid == 0 && cta_flags && p.status) atomicOr(p.status, cta_flags);
 }
 
