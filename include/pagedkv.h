@@ -193,10 +193,13 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  *              decode entry point
  * Everything else, including the workspace rule, is as for
  * paged_decode_attention; the workspace size comes from
- * paged_decode_multi_workspace_bytes.  Each kv head's q_len * G query rows
- * are served in chunks of 8 (the 8 columns of one MMA tile), so the K/V of a
- * (sequence, kv head) is read from memory once per chunk (re-reads of the
- * same blocks mostly hit L2).
+ * paged_decode_multi_workspace_bytes.  Kernels: with q_len >= 2, an F16 or
+ * BF16 cache, num_splits = 0, scale > 0 and at least one (sequence, kv head,
+ * 128-row tile) per SM, the call runs the tensor-core prefill kernel (see
+ * paged_prefill_attention), which reads each (sequence, kv head)'s K/V once
+ * for all its q_len * G rows; otherwise each kv head's rows are served in
+ * 8-row units by the decode kernel (K/V read once per unit, re-reads mostly
+ * from L2) with the split-KV merge.  Both meet the same error bound.
  */
 #define PKV_MAX_Q_LEN 64
 int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,

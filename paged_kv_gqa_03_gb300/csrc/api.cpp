@@ -349,6 +349,53 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   const WsLayout L = ws_layout(B, P, D);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
     return PKV_EWORKSPACE;
+  if (q_len >= 2 && num_splits == 0) {
+    // Several new tokens per sequence on a 16-bit cache: the tensor-core
+    // prefill kernel streams each (sequence, kv head)'s K/V once for all of
+    // its q_len * G rows (the 8-row units below stream it once per unit).
+    // Used when its grid of (sequence, kv head, 128-row tile) CTAs fills the
+    // GPU; it has no split over the context.
+    int sms = 0, dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    const int G = Hq / Hkv;
+    const int64_t tiles = ((int64_t)q_len * G + 127) / 128;
+    if ((cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && B <= 65535 &&
+        (int64_t)B * Hkv * tiles >= sms) {
+      CUtensorMap tmK, tmV;
+      rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+      if (rc != PKV_OK) return rc;
+      rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+      if (rc != PKV_OK) return rc;
+      cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+      WsHeader *hdr = reinterpret_cast<WsHeader *>(static_cast<uint8_t *>(workspace) + L.hdr);
+      e = cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s);
+      if (e != cudaSuccess) return cuda_status(e);
+      PrefillParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      pp.out = out;
+      pp.q = q;
+      pp.block_table = block_table;
+      pp.context_lens = context_lens;
+      pp.q_start = nullptr;
+      pp.uniform_q_len = q_len;
+      pp.status = &hdr->status;
+      pp.num_blocks = num_blocks;
+      pp.B = B;
+      pp.Hq = Hq;
+      pp.Hkv = Hkv;
+      pp.D = D;
+      pp.G = G;
+      pp.max_blocks = max_blocks_per_seq;
+      pp.max_q_len = q_len;
+      pp.max_tiles = (int)tiles;
+      pp.window = window < (1 << 30) ? window : 0;
+      pp.scale_log2 = scale * 1.4426950408889634f;
+      pp.timeout_ns = 4000000000ull;
+      return cuda_status(launch_prefill(pp, cache_dtype, tmK, tmV, s));
+    }
+  }
   const DecodeKernel &k = registry().k[c.ki];
   int ctas = 0, sms = 0;
   rc = kernel_occupancy(c.ki, &ctas, &sms);  // also opts the kernel into its shared memory

@@ -116,7 +116,9 @@ struct PrefillParams {
   const void *q;
   const int32_t *block_table;
   const int32_t *context_lens;
-  const int32_t *q_start;   // [B+1] row offsets of each sequence's new tokens in q / out
+  const int32_t *q_start;   // [B+1] row offsets of each sequence's new tokens in q / out,
+                            // or null: every sequence has uniform_q_len new tokens
+  int uniform_q_len;
   int32_t *status;          // PKV_FLAG_* bits (may be null)
   int64_t num_blocks;
   int B, Hq, Hkv, D, G, max_blocks, max_q_len, max_tiles;

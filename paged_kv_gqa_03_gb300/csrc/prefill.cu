@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = p.max_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) row tiles first
   const int h = blockIdx.y, b = blockIdx.z;
-  const int qs = __ldg(p.q_start + b);
-  const int n = __ldg(p.q_start + b + 1) - qs;
+  const int qs = p.q_start ? __ldg(p.q_start + b) : b * p.uniform_q_len;
+  const int n = p.q_start ? __ldg(p.q_start + b + 1) - qs : p.uniform_q_len;
   if (tid == 0 && tile == 0 && (n > p.max_q_len || n < 0) && p.status) atomicOr(p.status, PKV_FLAG_BAD_LEN);
   const int R = n * p.G;  // query rows of this kv head
   const int r0 = tile * Cfg::M;
@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
     auto block_row = [&](int jj, int *bad) -> int64_t {
       const int lb = (j_first + jj) * Cfg::BLOCKS + slot;
-      if (jj >= T || lb >= nblk) return p.num_blocks * p.Hkv;  // past the tensor: zero fill
+      // past the context, or wholly before every row's window (such blocks may
+      // have been released): nothing to read, the box past the tensor fills zeros
+      if (jj >= T || lb >= nblk || (lb + 1) * kBlock <= first) return p.num_blocks * p.Hkv;
       const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
       if (id >= 0 && (int64_t)id < p.num_blocks) return (int64_t)id * p.Hkv + h;
       *bad = 1;
@@ -231,66 +233,72 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
     const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
-    for (int j = 0; j <= T && ok; ++j) {
-      if (j < T) {
-        const int ks = j % Cfg::KSTAGES, sb = j % Cfg::SBUF;
-        ok = warp_wait(&k_full[ks], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
-        // S buffer sb last held P of tile j - SBUF: its P . V must be done
-        if (ok && j >= Cfg::SBUF) ok = warp_wait(&pv_done[sb], (uint32_t)((j / Cfg::SBUF) - 1) & 1u, p.timeout_ns);
-        if (!ok) break;
-        if (lane == 0) k_consumed = j + 1;
-        tc::fence_after();
-        if (lane == 0) {
-          const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
-          const uint32_t dS = tbase + (uint32_t)(sb * Cfg::N);
+    // S = Q . K^T of tile jj into S buffer jj % SBUF (free once P . V of tile
+    // jj - SBUF, which read P from it, is done)
+    auto issue_s = [&](int jj) -> bool {
+      const int ks = jj % Cfg::KSTAGES, sb = jj % Cfg::SBUF;
+      if (!warp_wait(&k_full[ks], (uint32_t)(jj / Cfg::KSTAGES) & 1u, p.timeout_ns)) return false;
+      if (jj >= Cfg::SBUF &&
+          !warp_wait(&pv_done[sb], (uint32_t)((jj / Cfg::SBUF) - 1) & 1u, p.timeout_ns))
+        return false;
+      if (lane == 0) k_consumed = jj + 1;
+      tc::fence_after();
+      if (lane == 0) {
+        const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
+        const uint32_t dS = tbase + (uint32_t)(sb * Cfg::N);
 #pragma unroll
-          for (int k = 0; k < Cfg::D / 16; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
-            const uint32_t offk = (uint32_t)((k >> 2) * Cfg::PANEL_KV + (k & 3) * 32);
-            tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
-                        k > 0 ? 1u : 0u);
-          }
-          tc::commit(&s_full[sb]);
-          tc::commit(&k_empty[ks]);
+        for (int k = 0; k < Cfg::D / 16; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
+          const uint32_t offk = (uint32_t)((k >> 2) * Cfg::PANEL_KV + (k & 3) * 32);
+          tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
+                      k > 0 ? 1u : 0u);
         }
-        __syncwarp();
+        tc::commit(&s_full[sb]);
+        tc::commit(&k_empty[ks]);
       }
-      if (j >= 1) {
-        const int jp = j - 1, vs = jp % Cfg::VSTAGES, sb = jp % Cfg::SBUF;
-        ok = warp_wait(&v_full[vs], (uint32_t)(jp / Cfg::VSTAGES) & 1u, p.timeout_ns);
-        if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(jp / Cfg::SBUF) & 1u, p.timeout_ns);
-        if (!ok) break;
-        if (lane == 0) v_consumed = jp + 1;
-        uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-        // stale cache rows past ctx inside the sequence's last block: zero them in V
-        // (their weights are 0, but 0 * NaN would still poison P . V)
-        const int kv0 = (j_first + jp) * Cfg::N;
-        const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
-        if (z0 >= 0 && z0 < z1) {
-          for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
-            const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
-            sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
-          }
-          fence_proxy_async();
+      __syncwarp();
+      return true;
+    };
+    // S runs one tile ahead of P . V (tensor-pipe order ... S(j+1), P . V(j)).
+    // (Two ahead measured much slower: S(j+2) reuses the buffer of P . V(j-1),
+    // so its issue waits for that P . V to complete and the pipe drains.)
+    if (T > 0) ok = issue_s(0);
+    for (int j = 0; j < T && ok; ++j) {
+      if (j + 1 < T && !(ok = issue_s(j + 1))) break;
+      const int vs = j % Cfg::VSTAGES, sb = j % Cfg::SBUF;
+      ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+      if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
+      if (!ok) break;
+      if (lane == 0) v_consumed = j + 1;
+      uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
+      // stale cache rows past ctx inside the sequence's last block: zero them in V
+      // (their weights are 0, but 0 * NaN would still poison P . V)
+      const int kv0 = (j_first + j) * Cfg::N;
+      const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
+      if (z0 >= 0 && z0 < z1) {
+        for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
+          const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
+          sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
         }
-        __syncwarp();
-        tc::fence_after();
-        if (lane == 0) {
-          const uint32_t v0 = smem_u32(vt);
-          const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
+        fence_proxy_async();
+      }
+      __syncwarp();
+      tc::fence_after();
+      if (lane == 0) {
+        const uint32_t v0 = smem_u32(vt);
+        const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
 #pragma unroll
-          for (int k = 0; k < Cfg::N / 16; ++k) {
-            // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
-            const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
-            const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
-            tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (jp > 0 || k > 0) ? 1u : 0u);
-            if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
-          }
-          tc::commit(&pv_done[sb]);
-          tc::commit(&v_empty[vs]);
+        for (int k = 0; k < Cfg::N / 16; ++k) {
+          // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+          const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
+          const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
+          tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (j > 0 || k > 0) ? 1u : 0u);
+          if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
         }
-        __syncwarp();
+        tc::commit(&pv_done[sb]);
+        tc::commit(&v_empty[vs]);
       }
+      __syncwarp();
       if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
     }
     if (!ok && lane == 0) {
