@@ -45,6 +45,8 @@ def lib():
         L.oracle_kv_bytes_per_token.restype = f64
         L.oracle_append.argtypes = [P, P, i32, P, P, P, P, i32, P, i32, i32, i32, i64, i32]
         L.oracle_append.restype = i32
+        L.oracle_append_calibrated.argtypes = L.oracle_append.argtypes
+        L.oracle_append_calibrated.restype = i32
         L.oracle_decode.argtypes = [P, P, P, i32, P, P, i32, P, P, P, i32, P, P,
                                     i32, i32, i32, i32, i64, i32, f64, i32]
         L.oracle_decode.restype = i32
@@ -121,10 +123,11 @@ def kv_bytes_per_token(num_layers, num_kv_heads, head_dim, dtype_bytes):
 
 
 def append(k_cache, v_cache, cache_dtype, k_new, v_new, new_dtype, slot_mapping,
-           k_scale=None, v_scale=None, block_size=16, inplace=False):
+           k_scale=None, v_scale=None, block_size=16, inplace=False, calibrated=False):
     """Writes the new tokens into COPIES of the caches (into the given arrays
     themselves when inplace=True); returns (k_cache, v_cache, k_scale, v_scale)
-    after the append."""
+    after the append.  calibrated=True: FP8 block scales follow the running
+    max of the block's tokens, earlier tokens re-quantised when it grows."""
     kc = _raw(k_cache, cache_dtype)
     vc = _raw(v_cache, cache_dtype)
     if not inplace:
@@ -142,7 +145,8 @@ def append(k_cache, v_cache, cache_dtype, k_new, v_new, new_dtype, slot_mapping,
         return np.array(x, dtype=np.float32, copy=True)
     ks, vs = _scales(k_scale), _scales(v_scale)
     sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64))
-    rc = lib().oracle_append(_ptr(kc), _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs),
+    fn = lib().oracle_append_calibrated if calibrated else lib().oracle_append
+    rc = fn(_ptr(kc), _ptr(vc), DTYPES[cache_dtype], _ptr(ks), _ptr(vs),
                              _ptr(kn), _ptr(vn), DTYPES[new_dtype], _ptr(sm),
                              B, Hkv, D, num_blocks, block_size)
     if rc != 0:

@@ -194,6 +194,91 @@ int oracle_append(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Calibrated FP8 append.  [P2] §四 and [P5] PART 02 (first advanced          */
+/* direction) warn that an FP8 cache's quality depends on how its scales are  */
+/* calibrated.  Here a block's scale follows the running maximum of its       */
+/* tokens and is a power of two: cand(x) = the smallest 2^k with              */
+/* max|x| <= 448 * 2^k (1 if x is all zero).  A token at offset 0 sets        */
+/* scale = cand; a later token with cand > scale first raises the scale to    */
+/* cand and re-quantises the block's earlier tokens,                          */
+/*   q' = e4m3_rne_sat( fp32( decode(q) * scale_old ) / scale_new ),           */
+/* then every token is stored as e4m3_rne_sat(x / scale) (fp32 ops).  No      */
+/* stored value saturates, and since scales are powers of two the            */
+/* re-quantisation only shifts exponents: exact for values that stay in the   */
+/* e4m3 normal range.  Tokens are applied in order b = 0 .. B-1.  Other       */
+/* cache types: the plain append.                                             */
+/* ---------------------------------------------------------------------- */
+static float pow2_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  int e;
+  float m = frexpf(amax, &e); /* amax = m * 2^e, 0.5 <= m < 1 */
+  /* amax <= 448 * 2^k = 0.875 * 2^(9 + k) */
+  int k = (m <= 0.875f) ? e - 9 : e - 8;
+  return ldexpf(1.0f, k);
+}
+
+static void append_one_calibrated(const void *src, int new_dtype, size_t src_off,
+                                  uint8_t *cache, float *scales, size_t tile_elem,
+                                  size_t scale_idx, int off, int D) {
+  float amax = 0.0f;
+  for (int d = 0; d < D; ++d) {
+    float a = fabsf(load_as_float(src, new_dtype, src_off + d));
+    if (a > amax) amax = a;
+  }
+  float cand = pow2_scale(amax);
+  float sc;
+  if (off == 0) {
+    sc = cand;
+  } else {
+    sc = scales[scale_idx];
+    if (cand > sc) {
+      /* earlier tokens of the block: rows off-1 .. 0 of the same tile */
+      for (int t = 0; t < off; ++t) {
+        uint8_t *row = cache + tile_elem - (size_t)(off - t) * D;
+        for (int d = 0; d < D; ++d) {
+          float v = (float)oracle_e4m3_to_double(row[d]);
+          float y = v * sc;
+          float r = y / cand;
+          row[d] = oracle_e4m3_from_float(r);
+        }
+      }
+      sc = cand;
+    }
+  }
+  scales[scale_idx] = sc;
+  for (int d = 0; d < D; ++d) {
+    float x = load_as_float(src, new_dtype, src_off + d);
+    float r = x / sc;
+    cache[tile_elem + d] = oracle_e4m3_from_float(r);
+  }
+}
+
+int oracle_append_calibrated(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
+                             float *v_scale, const void *k_new, const void *v_new, int new_dtype,
+                             const int64_t *slot_mapping, int B, int Hkv, int D,
+                             int64_t num_blocks, int block_size) {
+  if (cache_dtype != OR_E4M3)
+    return oracle_append(k_cache, v_cache, cache_dtype, k_scale, v_scale, k_new, v_new, new_dtype,
+                         slot_mapping, B, Hkv, D, num_blocks, block_size);
+  if (new_dtype == OR_E4M3) return -1;
+  for (int b = 0; b < B; ++b) {
+    int64_t slot = slot_mapping[b];
+    if (slot < 0) continue;
+    int64_t blk = slot / block_size;
+    int off = (int)(slot % block_size);
+    if (blk >= num_blocks) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      size_t tile = ((size_t)(blk * Hkv + h) * block_size + off) * D;
+      size_t src = ((size_t)b * Hkv + h) * D;
+      size_t sidx = (size_t)blk * Hkv + h;
+      append_one_calibrated(k_new, new_dtype, src, (uint8_t *)k_cache, k_scale, tile, sidx, off, D);
+      append_one_calibrated(v_new, new_dtype, src, (uint8_t *)v_cache, v_scale, tile, sidx, off, D);
+    }
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Decode attention over the paged cache.                                   */
 /* out[b,hq,:] = sum_t softmax_t(scale * q.K_t) V_t  ([P5] PART 02 formula     */
 /* Attention = softmax(QK^T/sqrt(d))V; [P3] §1.1 attention_step; [P4] §3.1     */

@@ -119,3 +119,75 @@ def test_block_table_adopt_keeps_free_order():
     slots, cow = bt.append_slots(["p", "q"])
     # p: pos 20 in shared? block 1 (refcount 1) -> no copy; q: pos 17 in block 2
     assert cow == [] and slots == [1 * 16 + 4, 2 * 16 + 1]
+
+
+def _stream_into_fresh_blocks(calibrated, mags, D=32, Hkv=2, seed=6):
+    """Appends len(mags) tokens one call at a time into fresh blocks (token t
+    scaled by mags[t]); returns (k cache bytes, k scales, the tokens as fp32)."""
+    g = torch.Generator().manual_seed(seed)
+    n = len(mags)
+    nb = (n + 15) // 16
+    kc = np.zeros((nb, Hkv, 16, D), dtype=np.uint8)
+    vc = kc.copy()
+    ks = np.zeros((nb, Hkv), dtype=np.float32)
+    vs = ks.copy()
+    toks = (torch.randn((n, Hkv, D), generator=g) * torch.tensor(mags)[:, None, None]).to(torch.bfloat16)
+    for t in range(n):
+        kc, vc, ks, vs = oracle.append(kc, vc, "fp8_e4m3", toks[t:t + 1], toks[t:t + 1], "bf16", [t],
+                                       k_scale=ks, v_scale=vs, calibrated=calibrated)
+    return kc, ks, toks.float()
+
+
+def _pow2_scale(amax):
+    """Smallest power of two p with amax <= 448 p (1 for amax 0), from the
+    exact search over exponents."""
+    out = np.ones_like(amax, dtype=np.float32)
+    for i, a in np.ndenumerate(amax):
+        if a > 0:
+            k = -160
+            while float(a) > 448.0 * 2.0 ** k:
+                k += 1
+            out[i] = np.float32(2.0 ** k)
+    return out
+
+
+def test_calibrated_append_scale_is_the_block_max_power_of_two_and_nothing_saturates():
+    """Growing magnitudes ('苦猿的大模型日记 Day45' PART 02: calibration decides
+    FP8 quality): every block's scale is the smallest power of two covering
+    max|x| / 448 over its tokens, the newest token is the RNE cast of
+    x / scale, and every stored value dequantises within one e4m3 rounding
+    (2^-4 relative) plus half a subnormal step (2^-10 scale) of its token —
+    re-quantisation by a power of two is exact in the normal range.  The
+    opener-only rule saturates the same stream."""
+    mags = [0.5 * 1.3 ** t for t in range(20)]            # each token larger than the last
+    kc, ks, x = _stream_into_fresh_blocks(True, mags)
+    xk = x.numpy()
+    for blk in range(kc.shape[0]):
+        t0, t1 = 16 * blk, min(len(mags), 16 * blk + 16)
+        amax = np.abs(xk[t0:t1]).max(axis=(0, 2))               # per kv head
+        assert np.array_equal(ks[blk], _pow2_scale(amax))
+        last = t1 - 1
+        r = torch.from_numpy(xk[last] / ks[blk][:, None])
+        assert np.array_equal(kc[blk, :, last - t0], r.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        deq = torch.from_numpy(kc[blk, :, :t1 - t0]).view(torch.float8_e4m3fn).float().numpy() \
+            * ks[blk][:, None, None]
+        tru = np.transpose(xk[t0:t1], (1, 0, 2))
+        assert np.all(np.abs(deq - tru) <= 2.0 ** -4 * np.abs(tru) + 2.0 ** -10 * ks[blk][:, None, None])
+    kc_p, ks_p, _ = _stream_into_fresh_blocks(False, mags)
+    deq_p = torch.from_numpy(kc_p[0, :, :16]).view(torch.float8_e4m3fn).float().numpy() * ks_p[0][:, None, None]
+    tru = np.transpose(xk[:16], (1, 0, 2))
+    assert np.any(np.abs(deq_p - tru) > 0.3 * np.abs(tru))
+
+
+def test_calibrated_rescale_shifts_exponents_exactly():
+    """A token four times larger than the block's first raises the scale by
+    2^2; the first token's bytes then dequantise to the same values as
+    before whenever they stay in the normal range."""
+    base = [1.0, 4.0]
+    kc1, ks1, _ = _stream_into_fresh_blocks(True, base[:1], seed=9)
+    kc2, ks2, _ = _stream_into_fresh_blocks(True, base, seed=9)
+    assert np.all(ks2[0] > ks1[0])
+    before = torch.from_numpy(kc1[0, :, 0]).view(torch.float8_e4m3fn).float().numpy() * ks1[0][:, None]
+    after = torch.from_numpy(kc2[0, :, 0]).view(torch.float8_e4m3fn).float().numpy() * ks2[0][:, None]
+    normal = np.abs(after) >= 2.0 ** -6 * ks2[0][:, None]
+    assert normal.sum() > 20 and np.array_equal(before[normal], after[normal])

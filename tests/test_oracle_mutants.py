@@ -37,7 +37,7 @@ MUTANTS = [
     ("lse sign", "lse_out[row * Hq + hq] = m + log(l);",
      "lse_out[row * Hq + hq] = m - log(l);",
      [T_att.test_merge_of_partials_equals_full]),
-    ("fresh block test", "if (off == 0) {", "if (off == 1) {",
+    ("fresh block test", "    if (off == 0) {\n      float amax", "    if (off == 1) {\n      float amax",
      [T_app.test_append_fp8_uses_block_scale_or_opens_block]),
     ("f16 exponent bias", "v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
      "v = ldexp(1.0 + (double)m / 1024.0, e - 14);",
@@ -64,6 +64,15 @@ MUTANTS = [
     ("prefill token count of the first sequence", "const int nl = q_start ? q_start[b + 1] - q_start[b] : q_len;",
      "const int nl = q_start ? q_start[1] - q_start[0] : q_len;",
      [T_att.test_prefill_matches_causal_sdpa_over_the_prompt]),
+    ("calibration skips re-quantising", "          row[d] = oracle_e4m3_from_float(r);",
+     "          (void)r;",
+     [T_app.test_calibrated_append_scale_is_the_block_max_power_of_two_and_nothing_saturates]),
+    ("calibration keeps the opener's scale", "      sc = cand;\n    }\n  }",
+     "      (void)cand;\n    }\n  }",
+     [T_app.test_calibrated_append_scale_is_the_block_max_power_of_two_and_nothing_saturates]),
+    ("calibration scale off by a power of two", "  int k = (m <= 0.875f) ? e - 9 : e - 8;",
+     "  int k = (m <= 0.875f) ? e - 8 : e - 7;",
+     [T_app.test_calibrated_append_scale_is_the_block_max_power_of_two_and_nothing_saturates]),
     ("kv bytes drops the 2", "return 2.0 * num_layers", "return 1.0 * num_layers",
      [T_app.test_kv_bytes_formula_matches_pages]),
 ]
@@ -84,6 +93,7 @@ def test_planted_mistake_is_caught(tmp_path, monkeypatch, name, orig, mut, tests
     mutant = ctypes.CDLL(str(so))
     for fn in ("oracle_f16_to_double", "oracle_bf16_to_double", "oracle_e4m3_to_double",
                "oracle_e4m3_from_float", "oracle_kv_bytes_per_token", "oracle_append",
+               "oracle_append_calibrated",
                "oracle_decode", "oracle_decode_multi", "oracle_prefill", "oracle_merge",
                "oracle_num_threads"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
