@@ -117,6 +117,29 @@ int paged_kv_append(const void *k_new, const void *v_new, int new_dtype,
                     int B, int Hkv, int D, int64_t num_blocks,
                     pkv_stream_t stream);
 
+/*
+ * paged_kv_append with calibrated FP8 block scales (the FP8 calibration that
+ * "苦猿的大模型日记 Day45" PART 02 and "大模型推理加速核心KV Cache 复用机制与内存
+ * 布局优化" §四 say decides an FP8 cache's quality).  Same arguments.  For an
+ * FP8 cache a block's scale is the smallest power of two p with
+ * max|x| <= 448 p over the tokens written to the block so far: a token at
+ * offset 0 sets it; a later token whose own p is larger raises the scale and
+ * first re-quantises the block's earlier bytes to
+ *   e4m3_rne_sat( fp32( decode(q) * p_old ) / p_new ),
+ * an exact exponent shift for values in the e4m3 normal range; each token is
+ * stored as e4m3_rne_sat(x / p) (fp32 division).  No stored value saturates.
+ * Tokens are applied in slot_mapping order; several tokens of one block in one
+ * call must be consecutive entries in position order (pkv_bm_append_slots
+ * order).  Blocks written with the plain rule may be continued with this one
+ * (their scale is then raised to a power of two only if a token outgrows it).
+ * Other cache types: exactly paged_kv_append.
+ */
+int paged_kv_append_calibrated(const void *k_new, const void *v_new, int new_dtype,
+                               void *k_cache, void *v_cache, int cache_dtype,
+                               float *k_scale, float *v_scale,
+                               const int64_t *slot_mapping, int B, int Hkv, int D,
+                               int64_t num_blocks, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Steps a4–a8 — paged gather, scores, online softmax, PV, split-KV merge.  */
 /* ------------------------------------------------------------------------ */

@@ -37,6 +37,7 @@ def _sig(name, res, *args):
 
 
 _sig("paged_kv_append", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
+_sig("paged_kv_append_calibrated", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
 _sig("paged_decode_workspace_bytes", _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
      ctypes.POINTER(_sz))
 _sig("paged_decode_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
@@ -143,12 +144,14 @@ def _stream(stream):
 
 
 def paged_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
-                    stream=None):
+                    stream=None, calibrated=False):
     """Writes k_new/v_new [B, Hkv, D] into the caches [num_blocks, Hkv, 16, D]
-    at slot_mapping[b] (int64; < 0 skips)."""
+    at slot_mapping[b] (int64; < 0 skips).  calibrated=True: FP8 block scales
+    follow the block's running max (paged_kv_append_calibrated)."""
     torch = _torch()
     B, Hkv, D = k_new.shape
-    _check(_L.paged_kv_append(
+    fn = _L.paged_kv_append_calibrated if calibrated else _L.paged_kv_append
+    _check(fn(
         _dev(k_new, "k_new"), _dev(v_new, "v_new"), _code(k_new),
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _code(k_cache),
         _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),

@@ -313,6 +313,24 @@ int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
   return PKV_OK;
 }
 
+int paged_kv_append_calibrated(const void *k_new, const void *v_new, int new_dtype, void *k_cache, void *v_cache,
+                               int cache_dtype, float *k_scale, float *v_scale, const int64_t *slot_mapping, int B,
+                               int Hkv, int D, int64_t num_blocks, pkv_stream_t stream) {
+  if (cache_dtype != PKV_FP8_E4M3)
+    return paged_kv_append(k_new, v_new, new_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale, slot_mapping, B,
+                           Hkv, D, num_blocks, stream);
+  if (B < 0 || Hkv <= 0 || num_blocks <= 0) return PKV_EINVAL;
+  if (esize_of(new_dtype) == 0) return PKV_EINVAL;
+  if (new_dtype == PKV_FP8_E4M3) return PKV_EUNSUPPORTED;
+  if (D != 64 && D != 128) return PKV_EUNSUPPORTED;
+  if (B == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale) return PKV_EINVAL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+  return cuda_status(launch_append_calibrated(k_new, v_new, new_dtype, k_cache, v_cache, k_scale, v_scale,
+                                              slot_mapping, B, Hkv, D, num_blocks,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int cache_dtype, int q_dtype, int num_splits,
                                  size_t *bytes_out) {
   return paged_decode_multi_workspace_bytes(B, 1, Hq, Hkv, D, cache_dtype, q_dtype, num_splits, bytes_out);

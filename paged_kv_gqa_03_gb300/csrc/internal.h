@@ -139,6 +139,9 @@ cudaError_t launch_append(const void *k_new, const void *v_new, int new_dtype, v
                           void *v_cache, int cache_dtype, float *k_scale, float *v_scale,
                           const int64_t *slot_mapping, int B, int Hkv, int D, int64_t num_blocks,
                           cudaStream_t stream);
+cudaError_t launch_append_calibrated(const void *k_new, const void *v_new, int new_dtype, void *k_cache,
+                                     void *v_cache, float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                                     int B, int Hkv, int D, int64_t num_blocks, cudaStream_t stream);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int sm_count, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, int cache_dtype, float *k_scale,
                                float *v_scale, const int32_t *pairs, int n_pairs, int Hkv, int D,

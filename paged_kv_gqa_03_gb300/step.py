@@ -48,7 +48,7 @@ class _Staging:
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, Hq, q_dtype, max_blocks, k_scale=None, v_scale=None,
-                 num_splits=0, stream=None, scale=None, q_len=1, window=0):
+                 num_splits=0, stream=None, scale=None, q_len=1, window=0, calibrated=False):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
         self.num_blocks, self.Hkv, _, self.D = k_cache.shape
@@ -57,6 +57,7 @@ class DecodeStep:
         self.num_splits = num_splits
         self.q_len = q_len
         self.window = window
+        self.calibrated = calibrated
         self.scale = 1.0 / float(np.sqrt(self.D)) if scale is None else float(scale)
         self.device = k_cache.device
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -180,7 +181,7 @@ class DecodeStep:
             k_new = k_new.view(-1, self.Hkv, self.D)
             v_new = v_new.view(-1, self.Hkv, self.D)
         paged_kv_append(k_new, v_new, self.k_cache, self.v_cache, self.d_slots, self.k_scale,
-                        self.v_scale, stream=s)
+                        self.v_scale, stream=s, calibrated=self.calibrated)
         self.attend(q, out)
 
     def attend(self, q, out):
