@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import compare, run_gpu_step, run_oracle_step
+from gpu_helpers import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +139,52 @@ def test_calibration_lowers_the_attention_error():
         errs[cal] = float(np.sqrt(np.mean((out.double().cpu().numpy() - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))
     print("relative RMS error, opener-scaled vs calibrated:", errs)
     assert errs[True] < errs[False]
+
+
+def test_mixed_precision_layers_share_one_block_table():
+    """'大模型推理加速核心KV Cache 复用机制与内存布局优化' §四: keep FP16 KV in the
+    key layers and FP8 elsewhere.  Three layers of one model step share the
+    block manager's table, lengths and slot mapping; layers 0 and 2 use f16
+    caches, layer 1 a calibrated fp8 cache; every layer's append and attention
+    match the oracle."""
+    pkv = _pkv()
+    dev = "cuda"
+    B, Hq, Hkv, D = 5, 16, 2, 128
+    start = [33, 100, 7, 64, 250]
+    nb = sum(s // 16 + 2 for s in start) + 4
+    g = torch.Generator().manual_seed(17)
+    bm = pkv.BlockManager(nb)
+    for b, s in enumerate(start):
+        assert bm.allocate(b, s)
+    slots, pairs = bm.append_slots(list(range(B)))
+    assert pairs == []
+    table, lens = bm.export(list(range(B)), max(s // 16 + 2 for s in start))
+    d_slots = torch.tensor(slots, dtype=torch.int64, device=dev)
+    d_table, d_lens = torch.from_numpy(table).to(dev), torch.from_numpy(lens).to(dev)
+    for layer, dtype in enumerate(("f16", "fp8_e4m3", "f16")):
+        q = torch.randn((B, Hq, D), generator=g).to(torch.float16)
+        kn = torch.randn((B, Hkv, D), generator=g).to(torch.float16)
+        vn = torch.randn((B, Hkv, D), generator=g).to(torch.float16)
+        if dtype == "f16":
+            kc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.float16)
+            vc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.float16)
+            ks = vs = None
+        else:
+            kc = torch.randint(0, 0x7e, (nb, Hkv, 16, D), generator=g, dtype=torch.uint8).view(torch.float8_e4m3fn)
+            vc = torch.randint(0, 0x7e, (nb, Hkv, 16, D), generator=g, dtype=torch.uint8).view(torch.float8_e4m3fn)
+            ks = torch.rand((nb, Hkv), generator=g) * 0.01 + 0.001
+            vs = torch.rand((nb, Hkv), generator=g) * 0.01 + 0.001
+        dk, dv = kc.to(dev), vc.to(dev)
+        dks = None if ks is None else ks.to(dev)
+        dvs = None if vs is None else vs.to(dev)
+        pkv.paged_kv_append(kn.to(dev), vn.to(dev), dk, dv, d_slots, dks, dvs, calibrated=True)
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+        pkv.paged_decode_attention(out, q.to(dev), dk, dv, d_table, d_lens, 1 / math.sqrt(D), dks, dvs)
+        torch.cuda.synchronize()
+        rk, rv, rks, rvs = oracle.append(kc, vc, dtype, kn, vn, "f16", slots,
+                                         None if ks is None else ks.numpy(), None if vs is None else vs.numpy(),
+                                         calibrated=True)
+        assert np.array_equal(dk.cpu().view(torch.uint8).numpy().reshape(-1), rk.view(np.uint8).reshape(-1))
+        ref = oracle.decode(q, "f16", rk, rv, dtype, table, lens, scale=1 / math.sqrt(D), k_scale=rks,
+                            v_scale=rvs)
+        compare(out, ref, dtype, f"layer {layer} ({dtype})")
