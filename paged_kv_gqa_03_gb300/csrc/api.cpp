@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "pagedkv.h"
+#include "prefill.h"
 
 namespace pkv {
 
@@ -346,6 +347,25 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
                                       num_splits, workspace, workspace_bytes, stream);
 }
 
+// The two prefill kernels run one tile pipeline and differ in scheduling.
+// One CTA per work item (row tile x kv head x sequence) runs the per-tile
+// loop fastest and suits long items: new tokens after a cached prefix of
+// thousands of positions.  The persistent kernel (one CTA per SM walking its
+// items) saves each item's start-up and balances short items of unequal
+// length: prompts without a long prefix.  The longest context the block
+// table can describe (max_blocks * block size) less the new tokens bounds
+// the prefix; a bound of 2048 positions or more picks one CTA per item.
+// PKV_PREFILL_KERNEL=persistent|tiles in the environment overrides the choice.
+static cudaError_t launch_prefill_auto(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK,
+                                       const CUtensorMap &tmV, cudaStream_t s) {
+  bool tiles = (int64_t)p.max_blocks * kBlock - p.max_q_len >= 2048;
+  if (const char *force = std::getenv("PKV_PREFILL_KERNEL")) {
+    if (!std::strcmp(force, "tiles")) tiles = true;
+    if (!std::strcmp(force, "persistent")) tiles = false;
+  }
+  return tiles ? launch_prefill_tiles(p, cache_dtype, tmK, tmV, s) : launch_prefill(p, cache_dtype, tmK, tmV, s);
+}
+
 int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const void *k_cache, const void *v_cache,
                                  int cache_dtype, const float *k_scale, const float *v_scale,
                                  const int32_t *block_table, int max_blocks_per_seq, const int32_t *context_lens,
@@ -411,7 +431,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
       pp.window = window < (1 << 30) ? window : 0;
       pp.scale_log2 = scale * 1.4426950408889634f;
       pp.timeout_ns = 4000000000ull;
-      return cuda_status(launch_prefill(pp, cache_dtype, tmK, tmV, s));
+      return cuda_status(launch_prefill_auto(pp, cache_dtype, tmK, tmV, s));
     }
   }
   const DecodeKernel &k = registry().k[c.ki];
@@ -534,7 +554,7 @@ int paged_prefill_attention(void *out, const void *q, int q_dtype, const void *k
   p.window = window < (1 << 30) ? window : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = 4000000000ull;
-  return cuda_status(launch_prefill(p, cache_dtype, tmK, tmV, s));
+  return cuda_status(launch_prefill_auto(p, cache_dtype, tmK, tmV, s));
 }
 
 int paged_decode_status(const void *workspace, size_t workspace_bytes, pkv_stream_t stream, int *flags_out) {

@@ -7,90 +7,73 @@
 // flash_attention: Q in row blocks, K / V in blocks of 128 positions, online
 // softmax with running max m and sum l, O rescaled by exp(m_old - m_new)) with
 // the causal mask of "苦猿的大模型日记 Day45" PART 04.  GB300 design:
-//  * one CTA per (sequence, kv head, tile of 128 query rows); a row is (new
+//  * work items of (sequence, kv head, tile of 128 query rows); a row is (new
 //    token i, query head g) of the kv head's group, token-major, so GQA heads
 //    share every K / V tile;
-//  * K / V tiles of 128 positions = 8 paged blocks, fetched by TMA through the
-//    block table (one 2 KiB box per block and 64-element panel) into a 3-deep
-//    K ring and a 2-deep V ring: a K slot frees as soon as S = Q . K^T has
-//    read it, a V slot when P . V has;
-//  * S (128 x 128, f32) and O (128 x D, f32) live in tensor memory; S has three
-//    buffers, and each buffer's P (the 16-bit weights) is written back over
-//    the S columns its thread has read, so P . V takes A from tensor memory
-//    (tcgen05.mma A-in-TMEM) and B = V from shared memory (128-byte swizzle,
-//    MN-major); Q and K are 128-byte-swizzled K-major operands;
-//  * eight softmax warps: thread (row, half) owns half of one query row's
-//    columns (tcgen05.ld / st 32x32b; warps w and w + 4 share a lane
-//    quarter); the halves exchange their partial row max once per tile;
-//  * O is rescaled in tensor memory only when a row's running max grows by
-//    more than 8 (log2 units): the result is exact either way, since P and l
-//    share the stale max, and p <= 2^8 keeps P well inside 16-bit range;
-//  * P must have V's type (kind::f16 takes one type for A and B).  f16 keeps
-//    11 significant bits, enough for the 2e-3 output bound; bf16 keeps 8, so a
-//    bf16 P goes in as a high part plus its bf16 residual, two MMAs on the
-//    same V tile (the weights then carry ~16 bits);
-//  * warp roles: 0-7 softmax + epilogue, 8 TMA producer, 9 MMA issue and
-//    tensor-memory allocation.  Every wait is bounded; a timeout sets
-//    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
-//    memory.
-#include <math.h>
-
-#include "common.cuh"
-#include "internal.h"
-#include "tcgen05.cuh"
+//  * one persistent CTA per SM walks its items round by round, the items
+//    ordered heaviest first and dealt out serpentine so the CTAs' totals stay
+//    near the mean; tensor memory, barriers and the K / V pipeline live
+//    across items, so an item's epilogue overlaps the next item's loads and S
+//    MMAs, and the next item's Q is copied asynchronously during the current
+//    item's last tile (prefill_tiles.cu runs one CTA per item instead);
+//  * the tile pipeline (K / V rings, S / P / O in tensor memory, softmax
+//    warps, warp roles) is the one described in prefill_common.cuh.
+#include "prefill.h"
+#include "prefill_common.cuh"
 
 namespace pkv {
 
-template <class T, int D_>
-struct PrefillCfg {
-  static constexpr int D = D_;
-  static constexpr bool BF = T::kCode == PKV_BF16;
-  static constexpr bool SPLIT = BF;                     // P as bf16 high + residual
-  static constexpr int M = 128;                         // query rows per CTA
-  static constexpr int N = 128;                         // cache positions per K / V tile
-  static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
-  static constexpr int PANELS = D / 64;                 // 128-byte panels per row
-  static constexpr int PANEL_Q = M * 128;               // one Q panel (128 rows)
-  static constexpr int PANEL_KV = N * 128;              // one K or V panel (128 positions)
-  static constexpr int Q_BYTES = PANELS * PANEL_Q;
-  static constexpr int KV_BYTES = PANELS * PANEL_KV;    // one K (or V) tile
-  static constexpr int KSTAGES = 3, VSTAGES = 2;
-  static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
-  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * KV_BYTES;
-  static constexpr int SBUF = 3;                        // S / P buffers in tensor memory
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = SBUF * N;           // O after the S buffers
-  static constexpr int SOFTMAX = 256;                   // threads: 128 rows x 2 halves
-  static constexpr int THREADS = SOFTMAX + 64;          // + producer warp + MMA warp
-  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1;  // warp ids
-  static_assert(D == 64 || D == 128, "head dim");
-  static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
-  static_assert(LOADS <= 32, "one box per producer lane");
-  static_assert(SMEM + 4096 <= 232448, "shared memory");
+// One work item: (row tile, kv head, sequence); every role derives the same
+// description from the item index.
+struct PrefillItem {
+  int b, h, qs, n, R, r0, ctx, nblk, first, j_first, T;
+  bool valid;  // the tile holds rows of the sequence
+  bool bad_q;  // the sequence's new-token count is negative or above max_q_len (flagged once)
+  bool bad_ctx;
 };
 
-// A bounded wait whose outcome is the same for every lane of the warp (the
-// tensor-memory loads and arrivals that follow are warp-collective).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-  return __all_sync(kFull, mbar_wait_bounded(bar, parity, limit_ns));
+template <class Cfg>
+__device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int i) {
+  PrefillItem it;
+  // heaviest (latest) row tiles first: the rank over (sequence, kv head) varies fastest
+  const int per_rank = p.B * p.Hkv;
+  const int tile = p.max_tiles - 1 - i / per_rank;
+  const int rest = i % per_rank;
+  it.b = rest / p.Hkv;
+  it.h = rest % p.Hkv;
+  it.qs = p.q_start ? __ldg(p.q_start + it.b) : it.b * p.uniform_q_len;
+  it.n = p.q_start ? __ldg(p.q_start + it.b + 1) - it.qs : p.uniform_q_len;
+  it.bad_q = tile == 0 && (it.n > p.max_q_len || it.n < 0);
+  it.R = it.n * p.G;
+  it.r0 = tile * Cfg::M;
+  it.valid = it.n > 0 && it.r0 < it.R;
+  const int ctx_raw = __ldg(p.context_lens + it.b);
+  it.ctx = ctx_raw < 0 ? 0 : (ctx_raw > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx_raw);
+  it.bad_ctx = it.valid && ctx_raw != it.ctx;
+  it.nblk = (it.ctx + kBlock - 1) / kBlock;
+  it.first = it.j_first = it.T = 0;
+  if (it.valid) {
+    const int i_lo = it.r0 / p.G, i_hi = min(it.R - 1, it.r0 + Cfg::M - 1) / p.G;
+    const int lim_lo = it.ctx - it.n + i_lo + 1, lim_hi = it.ctx - it.n + i_hi + 1;  // exclusive causal ends
+    it.first = p.window > 0 ? max(0, lim_lo - p.window) : 0;
+    it.j_first = it.first / Cfg::N;
+    it.T = lim_hi > 0 ? (lim_hi - 1) / Cfg::N - it.j_first + 1 : 0;  // K / V tiles to stream
+  }
+  return it;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-template <bool BF>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF)
-    return pack_bf16x2(lo, hi);
-  else
-    return pack_f16x2(lo, hi);
+// The CTA's item of round k: rounds deal the items out serpentine (CTA c
+// takes k * grid + c in even rounds, k * grid + grid - 1 - c in odd ones), so
+// with the items ordered heaviest first the CTAs' totals stay near the mean.
+// May be past the item count in the last round.
+__device__ __forceinline__ int round_item(int k) {
+  const int c = (int)blockIdx.x, G = (int)gridDim.x;
+  return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
+// Persistent: one CTA per SM walks its work items round by round; tensor
+// memory, barriers and the K / V pipeline live across items, so one item's
+// epilogue overlaps the next item's loads and S MMAs.
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmK,
@@ -103,32 +86,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
   __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
   // per S buffer: S written, P written, P . V done.  (One P barrier per buffer:
-  // the softmax may finish tile j + 1 before the MMA warp waits for tile j, but
-  // it cannot finish tile j + SBUF before that.)
-  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
+  // the softmax may finish tile g + 1 before the MMA warp waits for tile g, but
+  // it cannot finish tile g + SBUF before that.)
+  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF];
+  // per item: Q staged, O read out; row-max exchange per tile, row-sum exchange per item
+  __shared__ __align__(8) uint64_t q_full, o_free, xch[2], xl, fin;
   __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
   __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, cta_flags, k_consumed, v_consumed, k_issued, v_issued;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = p.max_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) row tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int qs = p.q_start ? __ldg(p.q_start + b) : b * p.uniform_q_len;
-  const int n = p.q_start ? __ldg(p.q_start + b + 1) - qs : p.uniform_q_len;
-  if (tid == 0 && tile == 0 && (n > p.max_q_len || n < 0) && p.status) atomicOr(p.status, PKV_FLAG_BAD_LEN);
-  const int R = n * p.G;  // query rows of this kv head
-  const int r0 = tile * Cfg::M;
-  if (n <= 0 || r0 >= R) return;  // the whole CTA: no barrier or tensor memory touched yet
-
-  const int ctx_raw = __ldg(p.context_lens + b);
-  const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx_raw);
-  const int nblk = (ctx + kBlock - 1) / kBlock;
-  const int i_lo = r0 / p.G, i_hi = min(R - 1, r0 + Cfg::M - 1) / p.G;
-  const int lim_lo = ctx - n + i_lo + 1, lim_hi = ctx - n + i_hi + 1;  // exclusive causal ends
-  const int first = p.window > 0 ? max(0, lim_lo - p.window) : 0;
-  const int j_first = first / Cfg::N;
-  const int T = lim_hi > 0 ? (lim_hi - 1) / Cfg::N - j_first + 1 : 0;  // K / V tiles to stream
+  const int n_items = p.max_tiles * p.Hkv * p.B;
+  const int n_rounds = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
 
   if (tid == 0) {
 #pragma unroll
@@ -147,13 +117,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(&p_full[s], Cfg::SOFTMAX / 32);
       mbar_init(&pv_done[s], 1);
     }
+    mbar_init(&q_full, Cfg::SOFTMAX / 32);
+    mbar_init(&o_free, Cfg::SOFTMAX / 32);
     mbar_init(&xch[0], Cfg::SOFTMAX / 32);
     mbar_init(&xch[1], Cfg::SOFTMAX / 32);
     mbar_init(&xl, Cfg::SOFTMAX / 32);
     mbar_init(&fin, 1);
     fence_barrier_init();
     abort_flag = 0;
-    cta_flags = ctx_raw != ctx ? PKV_FLAG_BAD_LEN : 0;
+    cta_flags = 0;
     k_consumed = v_consumed = k_issued = v_issued = 0;
   }
   if (warp == Cfg::ISSUER) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
@@ -161,69 +133,81 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (tid < Cfg::SOFTMAX) {  // Q tile: thread (row, half) stages half of its row (zeros past R)
-    const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
-    const int r = r0 + row;
-    const int ii = r / p.G, g = r - ii * p.G;
-    const uint4 *src = r < R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
-                                                             ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D)
-                             : nullptr;
-#pragma unroll
-    for (int k = 0; k < Cfg::D / 16; ++k) {
-      const int c = half * (Cfg::D / 16) + k;
-      const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      sts128(smem_u32(sQ + (c >> 3) * Cfg::PANEL_Q + row * 128 + (((c & 7) ^ (row & 7)) << 4)), v);
-    }
-    fence_proxy_async();
-  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = tmem_base;
 
   if (warp == Cfg::PRODUCER) {
-    // ---------------- TMA producer ----------------
-    // lane l fetches block (l % 8) of a tile, panel l / 8; the ids of the next
-    // tile are read one tile ahead
+    // ---------------- TMA producer: every tile of every item, one global counter ----------------
+    // lane l fetches block (l % 8) of a tile, panel l / 8; a cursor walks the
+    // CTA's tiles across items and the block ids are read one tile ahead
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
-    auto block_row = [&](int jj, int *bad) -> int64_t {
-      const int lb = (j_first + jj) * Cfg::BLOCKS + slot;
-      // past the context, or wholly before every row's window (such blocks may
-      // have been released): nothing to read, the box past the tensor fills zeros
-      if (jj >= T || lb >= nblk || (lb + 1) * kBlock <= first) return p.num_blocks * p.Hkv;
-      const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
-      if (id >= 0 && (int64_t)id < p.num_blocks) return (int64_t)id * p.Hkv + h;
-      *bad = 1;
-      return p.num_blocks * p.Hkv;
+    int ck = -1, cj = 0, cT = 0;  // cursor: tile cj of the cT of round ck's item
+    PrefillItem ct{};
+    auto step = [&]() -> bool {  // to the cursor's next tile; false past the CTA's last
+      if (++cj < cT) return true;
+      for (++ck; ck < n_rounds; ++ck) {
+        const int ci = round_item(ck);
+        if (ci >= n_items) continue;
+        ct = prefill_item<Cfg>(p, ci);
+        if (ct.valid && ct.T > 0) {
+          cj = 0;
+          cT = ct.T;
+          return true;
+        }
+      }
+      return false;
     };
     int bad = 0;
-    int64_t trow = block_row(0, &bad);
-    for (int j = 0; j < T; ++j) {
-      const int64_t next = block_row(j + 1, &bad);
-      const int ks = j % Cfg::KSTAGES, vs = j % Cfg::VSTAGES;
-      if (j >= Cfg::KSTAGES &&
-          !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
+    // box row of this lane's block of the cursor tile: past the context, or
+    // wholly before every row's window (such blocks may have been released),
+    // the box past the tensor, which fills zeros
+    auto block_row = [&]() -> int64_t {
+      const int lb = (ct.j_first + cj) * Cfg::BLOCKS + slot;
+      if (lb >= ct.nblk || (lb + 1) * kBlock <= ct.first) return p.num_blocks * p.Hkv;
+      const int id = __ldg(p.block_table + (size_t)ct.b * p.max_blocks + lb);
+      const bool good = id >= 0 && (int64_t)id < p.num_blocks;
+      bad |= good ? 0 : 1;
+      return good ? (int64_t)id * p.Hkv + ct.h : p.num_blocks * p.Hkv;
+    };
+    bool have = step(), ok = true;
+    int64_t trow = have ? block_row() : 0;
+    for (int g = 0; have; ++g) {
+      const bool have_next = step();
+      const int64_t next = have_next ? block_row() : 0;
+      const int ks = g % Cfg::KSTAGES, vs = g % Cfg::VSTAGES;
+      if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns)) {
+        ok = false;
         break;
-      if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+      }
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
         tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
                     (int)(trow * kBlock), &k_full[ks]);
-      if (lane == 0) k_issued = j + 1;
-      if (j >= Cfg::VSTAGES &&
-          !warp_wait(&v_empty[vs], (uint32_t)((j / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
+      if (lane == 0) k_issued = g + 1;
+      if (g >= Cfg::VSTAGES && !warp_wait(&v_empty[vs], (uint32_t)((g / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns)) {
+        ok = false;
         break;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
         tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
                     (int)(trow * kBlock), &v_full[vs]);
-      if (lane == 0) v_issued = j + 1;
+      if (lane == 0) v_issued = g + 1;
       trow = next;
+      have = have_next;
     }
-    if (bad) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
-    if (__any_sync(kFull, k_issued < T || v_issued < T) && lane == 0 && !*(volatile int *)&abort_flag) {
+    if (__any_sync(kFull, bad)) {
+      if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
+    }
+    if (!ok && lane == 0) {
       atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
       abort_flag = 1;
     }
@@ -233,15 +217,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
     const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
-    // S = Q . K^T of tile jj into S buffer jj % SBUF (free once P . V of tile
-    // jj - SBUF, which read P from it, is done)
-    auto issue_s = [&](int jj) -> bool {
-      const int ks = jj % Cfg::KSTAGES, sb = jj % Cfg::SBUF;
-      if (!warp_wait(&k_full[ks], (uint32_t)(jj / Cfg::KSTAGES) & 1u, p.timeout_ns)) return false;
-      if (jj >= Cfg::SBUF &&
-          !warp_wait(&pv_done[sb], (uint32_t)((jj / Cfg::SBUF) - 1) & 1u, p.timeout_ns))
+    int g = 0;        // global K / V tile
+    int items = 0;    // valid items so far (Q phases)
+    int o_items = 0;  // items with tiles so far (O hand-offs)
+    // S = Q . K^T of global tile gg into S buffer gg % SBUF (free once P . V of
+    // tile gg - SBUF, which read P from it, is done)
+    auto issue_s = [&](int gg) -> bool {
+      const int ks = gg % Cfg::KSTAGES, sb = gg % Cfg::SBUF;
+      if (!warp_wait(&k_full[ks], (uint32_t)(gg / Cfg::KSTAGES) & 1u, p.timeout_ns)) return false;
+      if (gg >= Cfg::SBUF && !warp_wait(&pv_done[sb], (uint32_t)((gg / Cfg::SBUF) - 1) & 1u, p.timeout_ns))
         return false;
-      if (lane == 0) k_consumed = jj + 1;
+      if (lane == 0) k_consumed = gg + 1;
       tc::fence_after();
       if (lane == 0) {
         const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
@@ -259,47 +245,66 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       __syncwarp();
       return true;
     };
-    // S runs one tile ahead of P . V (tensor-pipe order ... S(j+1), P . V(j)).
-    // (Two ahead measured much slower: S(j+2) reuses the buffer of P . V(j-1),
-    // so its issue waits for that P . V to complete and the pipe drains.)
-    if (T > 0) ok = issue_s(0);
-    for (int j = 0; j < T && ok; ++j) {
-      if (j + 1 < T && !(ok = issue_s(j + 1))) break;
-      const int vs = j % Cfg::VSTAGES, sb = j % Cfg::SBUF;
-      ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
-      if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = round_item(k);
+      if (i >= n_items) continue;
+      const PrefillItem it = prefill_item<Cfg>(p, i);
+      if (!it.valid || it.T == 0) continue;
+      // this item's Q is staged (only items with tiles stage one)
+      ok = warp_wait(&q_full, (uint32_t)items & 1u, p.timeout_ns);
+      ++items;
       if (!ok) break;
-      if (lane == 0) v_consumed = j + 1;
-      uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-      // stale cache rows past ctx inside the sequence's last block: zero them in V
-      // (their weights are 0, but 0 * NaN would still poison P . V)
-      const int kv0 = (j_first + j) * Cfg::N;
-      const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
-      if (z0 >= 0 && z0 < z1) {
-        for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
-          const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
-          sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
-        }
-        fence_proxy_async();
-      }
-      __syncwarp();
       tc::fence_after();
-      if (lane == 0) {
-        const uint32_t v0 = smem_u32(vt);
-        const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
-#pragma unroll
-        for (int k = 0; k < Cfg::N / 16; ++k) {
-          // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
-          const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
-          const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
-          tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (j > 0 || k > 0) ? 1u : 0u);
-          if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
+      // S runs one tile ahead of P . V (tensor-pipe order ... S(g+1), P . V(g)).
+      // (Two ahead measured much slower: S(g+2) reuses the buffer of P . V(g-1),
+      // so its issue waits for that P . V to complete and the pipe drains.)
+      ok = issue_s(g);
+      for (int j = 0; j < it.T && ok; ++j) {
+        const int gj = g + j;
+        if (j + 1 < it.T && !(ok = issue_s(gj + 1))) break;
+        const int vs = gj % Cfg::VSTAGES, sb = gj % Cfg::SBUF;
+        // the first P . V of an item overwrites O: the previous item's O must be read out
+        if (j == 0 && o_items > 0 && !(ok = warp_wait(&o_free, (uint32_t)(o_items - 1) & 1u, p.timeout_ns))) break;
+        ok = warp_wait(&v_full[vs], (uint32_t)(gj / Cfg::VSTAGES) & 1u, p.timeout_ns);
+        if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(gj / Cfg::SBUF) & 1u, p.timeout_ns);
+        if (!ok) break;
+        if (lane == 0) v_consumed = gj + 1;
+        uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
+        // stale cache rows past ctx inside the sequence's last block: zero them in V
+        // (their weights are 0, but 0 * NaN would still poison P . V)
+        const int kv0 = (it.j_first + j) * Cfg::N;
+        const int z0 = it.ctx - kv0, z1 = min(it.nblk * kBlock - kv0, Cfg::N);
+        if (z0 >= 0 && z0 < z1) {
+          for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
+            const int r = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
+            sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + r * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
+          }
+          fence_proxy_async();
         }
-        tc::commit(&pv_done[sb]);
-        tc::commit(&v_empty[vs]);
+        __syncwarp();
+        tc::fence_after();
+        if (lane == 0) {
+          const uint32_t v0 = smem_u32(vt);
+          const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
+#pragma unroll
+          for (int k = 0; k < Cfg::N / 16; ++k) {
+            // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+            const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
+            const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
+            tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (j > 0 || k > 0) ? 1u : 0u);
+            if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
+          }
+          tc::commit(&pv_done[sb]);
+          tc::commit(&v_empty[vs]);
+        }
+        __syncwarp();
+        if (__any_sync(kFull, *(volatile int *)&abort_flag)) {
+          ok = false;
+          break;
+        }
       }
-      __syncwarp();
-      if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+      g += it.T;
+      ++o_items;
     }
     if (!ok && lane == 0) {
       atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
@@ -310,133 +315,209 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int SC = Cfg::N / 2;  // S columns of a thread (its half of the row)
     constexpr int OC = Cfg::D / 2;  // O columns of a thread
     const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
-    const int r = r0 + row;
-    const bool valid = r < R;
-    const int lim = valid ? ctx - n + r / p.G + 1 : 0;  // visible positions [lo, lim)
-    const int lo = (valid && p.window > 0) ? max(0, lim - p.window) : 0;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
-    float m_run = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int sb = j % Cfg::SBUF;
-      ok = warp_wait(&s_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
-      if (!ok) break;
-      tc::fence_after();
-      const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
-      uint32_t s[SC / 32][32];
+    // thread (row, half) stages half of row `row` of item i's Q tile (zeros past R)
+    auto stage_q = [&](int i, bool async) {
+      const PrefillItem it = prefill_item<Cfg>(p, i);
+      const int r = it.r0 + row;
+      const int ii = r / p.G, g = r - ii * p.G;
+      const uint4 *src = r < it.R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
+                                                                  ((size_t)(it.qs + ii) * p.Hq + it.h * p.G + g) *
+                                                                      Cfg::D)
+                                  : nullptr;
 #pragma unroll
-      for (int q = 0; q < SC / 32; ++q) tc::ld32(scol + (uint32_t)(q * 32), s[q]);
-      const int kv0 = (j_first + j) * Cfg::N + half * SC;
-      if (!(kv0 >= lo && kv0 + SC <= lim)) {  // a mask edge crosses these columns
+      for (int k = 0; k < Cfg::D / 16; ++k) {
+        const int cc = half * (Cfg::D / 16) + k;
+        const uint32_t dst = smem_u32(sQ + (cc >> 3) * Cfg::PANEL_Q + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
+        if (src && async)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + cc) : "memory");
+        else
+          sts128(dst, src ? __ldg(src + cc) : make_uint4(0, 0, 0, 0));
+      }
+    };
+    auto release_q = [&](bool async) {
+      if (async) asm volatile("cp.async.wait_all;" ::: "memory");
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full);
+    };
+    // Q is staged for the CTA's items with tiles only, one after another: Q of
+    // the next such item is released after this one's last S has landed, so
+    // the MMA warp has waited for every earlier Q (no barrier phase is skipped)
+    auto next_work = [&](int k) {  // the first round from k on whose item has tiles (or n_rounds)
+      for (; k < n_rounds; ++k) {
+        const int i = round_item(k);
+        if (i >= n_items) continue;
+        const PrefillItem t = prefill_item<Cfg>(p, i);
+        if (t.valid && t.T > 0) break;
+      }
+      return k;
+    };
+    {
+      const int first = next_work(0);
+      if (first < n_rounds) {
+        stage_q(round_item(first), false);
+        release_q(false);
+      }
+    }
+    bool ok = true;
+    int g = 0;        // global tile (S buffers, exchange parity)
+    int o_items = 0;  // items with tiles so far
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int cur = round_item(k);
+      if (cur >= n_items) continue;
+      const PrefillItem it = prefill_item<Cfg>(p, cur);
+      if (tid == 0 && (it.bad_q || it.bad_ctx)) atomicOr(&cta_flags, PKV_FLAG_BAD_LEN);
+      if (!it.valid) continue;
+      const int T = it.T, j_first = it.j_first;
+      const int r = it.r0 + row;
+      const bool valid = r < it.R;
+      const int lim = valid ? it.ctx - it.n + r / p.G + 1 : 0;  // visible positions [lo, lim)
+      const int lo = (valid && p.window > 0) ? max(0, lim - p.window) : 0;
+      const int ii = r / p.G, gq = r - ii * p.G;
+      uint4 *dst = valid ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                     ((size_t)(it.qs + ii) * p.Hq + it.h * p.G + gq) * Cfg::D +
+                                                     half * OC)
+                         : nullptr;
+      float m_run = -INFINITY, l = 0.f;
+      bool staged = false;  // the next item's Q copy is in flight
+      for (int j = 0; j < T; ++j) {
+        const int gj = g + j, sb = gj % Cfg::SBUF;
+        ok = warp_wait(&s_full[sb], (uint32_t)(gj / Cfg::SBUF) & 1u, p.timeout_ns);
+        if (!ok) break;
+        tc::fence_after();
+        const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
+        uint32_t s[SC / 32][32];
+#pragma unroll
+        for (int q = 0; q < SC / 32; ++q) tc::ld32(scol + (uint32_t)(q * 32), s[q]);
+        if (j + 1 == T) {
+          // every S MMA of this item has completed (its last S just landed):
+          // the next item's Q can replace this one's while the softmax runs
+          const int nxt = next_work(k + 1);
+          if (nxt < n_rounds) {
+            stage_q(round_item(nxt), true);
+            staged = true;
+          }
+        }
+        const int kv0 = (j_first + j) * Cfg::N + half * SC;
+        if (!(kv0 >= lo && kv0 + SC <= lim)) {  // a mask edge crosses these columns
+#pragma unroll
+          for (int q = 0; q < SC / 32; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int pos = kv0 + q * 32 + e;
+              if (pos < lo || pos >= lim) s[q][e] = 0xff800000u;  // -inf
+            }
+        }
+        float mx = -INFINITY;
 #pragma unroll
         for (int q = 0; q < SC / 32; ++q)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int pos = kv0 + q * 32 + e;
-            if (pos < lo || pos >= lim) s[q][e] = 0xff800000u;  // -inf
-          }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < SC / 32; ++q)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
-      // the row max over both halves (double-buffered exchange, bounded wait)
-      red[j & 1][half][row] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xch[j & 1]);
-      ok = warp_wait(&xch[j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
-      if (!ok) break;
-      mx = fmaxf(mx, red[j & 1][half ^ 1][row]);
-      const float m_new = fmaxf(m_run, mx * c);
-      // warps w and w + 4 hold the same rows and the same m_new: same decision
-      const bool rescale = __any_sync(kFull, m_new > m_run + 8.f);
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
-        m_run = m_new;
-      }
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      float sum = 0.f;
-      uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
-#pragma unroll
-      for (int e = 0; e < SC / 2; ++e) {
-        const int col = 2 * e;
-        const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
-        const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
-        sum += a0 + a1;
-        w[e] = pack2<Cfg::BF>(a0, a1);
-        if constexpr (Cfg::SPLIT) {
-          const float2 hi = unpack2(BF16{}, w[e]);
-          wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
+        // the row max over both halves (double-buffered exchange, bounded wait)
+        red[gj & 1][half][row] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xch[gj & 1]);
+        ok = warp_wait(&xch[gj & 1], (uint32_t)(gj >> 1) & 1u, p.timeout_ns);
+        if (!ok) break;
+        mx = fmaxf(mx, red[gj & 1][half ^ 1][row]);
+        const float m_new = fmaxf(m_run, mx * c);
+        // warps w and w + 4 hold the same rows and the same m_new: same decision
+        const bool rescale = __any_sync(kFull, m_new > m_run + 8.f);
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
+          m_run = m_new;
         }
+        const float mu = m_run == -INFINITY ? 0.f : m_run;
+        float sum = 0.f;
+        uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
+#pragma unroll
+        for (int e = 0; e < SC / 2; ++e) {
+          const int col = 2 * e;
+          const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
+          const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
+          sum += a0 + a1;
+          w[e] = pack2<Cfg::BF>(a0, a1);
+          if constexpr (Cfg::SPLIT) {
+            const float2 hi = unpack2(BF16{}, w[e]);
+            wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
+          }
+        }
+        l = l * alpha + sum;
+        // P over this thread's own (already read) S columns: high part, then residual
+        tc::st32(scol, w);
+        if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
+        // O must hold P . V of the previous tile before it is scaled, and be
+        // scaled before P . V of this tile (issued after the arrival below)
+        if (rescale && j > 0) {
+          ok = warp_wait(&pv_done[(gj - 1) % Cfg::SBUF], (uint32_t)((gj - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+          if (!ok) break;
+          tc::fence_after();
+#pragma unroll
+          for (int q = 0; q < OC / 32; ++q) {
+            uint32_t o[32];
+            const uint32_t ta = tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32);
+            tc::ld32(ta, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::st32(ta, o);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
       }
-      if (rescale && j > 0) {  // O must hold P . V of the previous tile before it is scaled
-        ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+      if (!ok) break;
+      // the next item's Q: its copy overlapped this item's last tile
+      if (staged) release_q(true);
+      // epilogue: O of this item
+      if (T > 0) {
+        const int gl = g + T - 1;
+        ok = warp_wait(&pv_done[gl % Cfg::SBUF], (uint32_t)(gl / Cfg::SBUF) & 1u, p.timeout_ns);
+        if (ok) {  // the row sum over both halves
+          red_l[half][row] = l;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xl);
+          ok = warp_wait(&xl, (uint32_t)o_items & 1u, p.timeout_ns);
+        }
         if (!ok) break;
         tc::fence_after();
+        const float lt = l + red_l[half ^ 1][row];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
+        uint32_t o[OC / 32][32];
 #pragma unroll
-        for (int q = 0; q < OC / 32; ++q) {
-          uint32_t o[32];
-          const uint32_t ta = tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32);
-          tc::ld32(ta, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tc::st32(ta, o);
-        }
-      }
-      l = l * alpha + sum;
-      // P over this thread's own (already read) S columns: high part, then residual
-      tc::st32(scol, w);
-      if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
-    }
-    if (ok && T > 0)
-      ok = warp_wait(&pv_done[(T - 1) % Cfg::SBUF], (uint32_t)((T - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
-    if (ok) {  // the row sum over both halves
-      red_l[half][row] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xl);
-      ok = warp_wait(&xl, 0, p.timeout_ns);
-    }
-    if (!ok) {
-      if (lane == 0) {
-        atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
-        abort_flag = 1;
-      }
-    } else {
-      tc::fence_after();
-      const float lt = l + red_l[half ^ 1][row];
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
-      const int ii = r / p.G, g = r - ii * p.G;
-      uint4 *dst = valid ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
-                                                     ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D + half * OC)
-                         : nullptr;
-#pragma unroll
-      for (int q = 0; q < OC / 32; ++q) {
-        uint32_t o[32];
-        if (T > 0) {
-          tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
+        for (int q = 0; q < OC / 32; ++q) tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o[q]);
+        // O is in registers: the next item's P . V may overwrite it, and the
+        // row sums may be overwritten by the next exchange
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free);
         if (dst) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t wv[4];
+          for (int q = 0; q < OC / 32; ++q)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
-                                     __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
-            dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          }
+            for (int v = 0; v < 4; ++v) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                wv[e] = pack2<Cfg::BF>(__uint_as_float(o[q][v * 8 + 2 * e]) * inv,
+                                       __uint_as_float(o[q][v * 8 + 2 * e + 1]) * inv);
+              dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
         }
+        ++o_items;
+      } else if (dst) {  // no visible position for any row of the tile: zeros
+#pragma unroll
+        for (int q = 0; q < OC / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
       }
+      g += T;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
     }
   }
 
@@ -452,6 +533,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_wait_bounded(&k_full[j % Cfg::KSTAGES], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
     for (int j = v_consumed; j < v_issued; ++j)
       mbar_wait_bounded(&v_full[j % Cfg::VSTAGES], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+  } else if (tid < Cfg::SOFTMAX) {
+    asm volatile("cp.async.wait_all;" ::: "memory");  // a Q copy left in flight by an abort
   }
   tc::fence_before();
   __syncthreads();
@@ -473,7 +556,14 @@ static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, co
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  const dim3 grid((unsigned)p.max_tiles, (unsigned)p.Hkv, (unsigned)p.B);
+  static int sms[64] = {};
+  if (!sms[dev]) {
+    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t items = (int64_t)p.max_tiles * p.Hkv * p.B;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(items < sms[dev] ? items : sms[dev]);  // one persistent CTA per SM
   prefill_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, tmK, tmV);
   return cudaGetLastError();
 }

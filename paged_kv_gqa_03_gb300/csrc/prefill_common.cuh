@@ -1,0 +1,94 @@
+// prefill_common.cuh — pieces shared by the two tcgen05 prefill kernels
+// (prefill.cu: one persistent CTA per SM walking many work items;
+// prefill_tiles.cu: one CTA per work item): the tile configuration, bounded
+// warp-wide barrier waits and the softmax arithmetic helpers.
+//
+// The computation is FlashAttention's tiled form ("LLM推理优化实战" §3.2
+// flash_attention: Q in row blocks, K / V in blocks of 128 positions, online
+// softmax with running max m and sum l, O rescaled by exp(m_old - m_new)) with
+// the causal mask of "苦猿的大模型日记 Day45" PART 04.  The tile pipeline both
+// kernels run:
+//  * K / V tiles of 128 positions = 8 paged blocks, fetched by TMA through the
+//    block table (one 2 KiB box per block and 64-element panel) into a 3-deep
+//    K ring and a 2-deep V ring: a K slot frees as soon as S = Q . K^T has
+//    read it, a V slot when P . V has;
+//  * S (128 x 128, f32) and O (128 x D, f32) live in tensor memory; S has three
+//    buffers, and each buffer's P (the 16-bit weights) is written back over
+//    the S columns its thread has read, so P . V takes A from tensor memory
+//    (tcgen05.mma A-in-TMEM) and B = V from shared memory (128-byte swizzle,
+//    MN-major); Q and K are 128-byte-swizzled K-major operands;
+//  * eight softmax warps: thread (row, half) owns half of one query row's
+//    columns (tcgen05.ld / st 32x32b; warps w and w + 4 share a lane
+//    quarter); the halves exchange their partial row max once per tile;
+//  * O is rescaled in tensor memory only when a row's running max grows by
+//    more than 8 (log2 units): the result is exact either way, since P and l
+//    share the stale max, and p <= 2^8 keeps P well inside 16-bit range;
+//  * P must have V's type (kind::f16 takes one type for A and B).  f16 keeps
+//    11 significant bits, enough for the 2e-3 output bound; bf16 keeps 8, so a
+//    bf16 P goes in as a high part plus its bf16 residual, two MMAs on the
+//    same V tile (the weights then carry ~16 bits);
+//  * warp roles: 0-7 softmax + epilogue, 8 TMA producer, 9 MMA issue and
+//    tensor-memory allocation.  Every wait is bounded; a timeout sets
+//    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
+//    memory.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+template <class T, int D_>
+struct PrefillCfg {
+  static constexpr int D = D_;
+  static constexpr bool BF = T::kCode == PKV_BF16;
+  static constexpr bool SPLIT = BF;                     // P as bf16 high + residual
+  static constexpr int M = 128;                         // query rows per CTA
+  static constexpr int N = 128;                         // cache positions per K / V tile
+  static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
+  static constexpr int PANELS = D / 64;                 // 128-byte panels per row
+  static constexpr int PANEL_Q = M * 128;               // one Q panel (128 rows)
+  static constexpr int PANEL_KV = N * 128;              // one K or V panel (128 positions)
+  static constexpr int Q_BYTES = PANELS * PANEL_Q;
+  static constexpr int KV_BYTES = PANELS * PANEL_KV;    // one K (or V) tile
+  static constexpr int KSTAGES = 3, VSTAGES = 2;
+  static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
+  static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * KV_BYTES;
+  static constexpr int SBUF = 3;                        // S / P buffers in tensor memory
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = SBUF * N;           // O after the S buffers
+  static constexpr int SOFTMAX = 256;                   // threads: 128 rows x 2 halves
+  static constexpr int THREADS = SOFTMAX + 64;          // + producer warp + MMA warp
+  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1;  // warp ids
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
+  static_assert(LOADS <= 32, "one box per producer lane");
+  static_assert(SMEM + 4096 <= 232448, "shared memory");
+};
+
+// A bounded wait whose outcome is the same for every lane of the warp (the
+// tensor-memory loads and arrivals that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(kFull, mbar_wait_bounded(bar, parity, limit_ns));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF)
+    return pack_bf16x2(lo, hi);
+  else
+    return pack_f16x2(lo, hi);
+}
+
+}  // namespace pkv

@@ -1,0 +1,416 @@
+// prefill_tiles.cu — the tcgen05 prefill kernel with one CTA per work item
+// (sequence, kv head, tile of 128 query rows): grid (row tiles, kv heads,
+// sequences), the latest (heaviest) row tiles first, so the CTAs resident
+// at one time share the K / V of few (sequence, kv head) pairs in L2.  Each
+// CTA stages its Q tile, allocates tensor memory, streams its K / V tiles
+// through the pipeline described in prefill_common.cuh and writes its rows.
+// Chosen for long work items (a cached prefix of thousands of positions
+// before the new tokens): there the per-tile loop of this kernel runs about
+// 5-10% faster than the persistent kernel's, and the per-CTA start-up is
+// small against the item.
+#include "prefill.h"
+#include "prefill_common.cuh"
+
+namespace pkv {
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    prefill_tile_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + Cfg::Q_BYTES;
+  uint8_t *sV = sK + (size_t)Cfg::KSTAGES * Cfg::KV_BYTES;
+  __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
+  __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
+  // per S buffer: S written, P written, P . V done.  (One P barrier per buffer:
+  // the softmax may finish tile j + 1 before the MMA warp waits for tile j, but
+  // it cannot finish tile j + SBUF before that.)
+  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
+  __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
+  __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag, cta_flags, k_consumed, v_consumed, k_issued, v_issued;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = p.max_tiles - 1 - (int)blockIdx.x;  // heaviest (latest) row tiles first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int qs = p.q_start ? __ldg(p.q_start + b) : b * p.uniform_q_len;
+  const int n = p.q_start ? __ldg(p.q_start + b + 1) - qs : p.uniform_q_len;
+  if (tid == 0 && tile == 0 && (n > p.max_q_len || n < 0) && p.status) atomicOr(p.status, PKV_FLAG_BAD_LEN);
+  const int R = n * p.G;  // query rows of this kv head
+  const int r0 = tile * Cfg::M;
+  if (n <= 0 || r0 >= R) return;  // the whole CTA: no barrier or tensor memory touched yet
+
+  const int ctx_raw = __ldg(p.context_lens + b);
+  const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > p.max_blocks * kBlock ? p.max_blocks * kBlock : ctx_raw);
+  const int nblk = (ctx + kBlock - 1) / kBlock;
+  const int i_lo = r0 / p.G, i_hi = min(R - 1, r0 + Cfg::M - 1) / p.G;
+  const int lim_lo = ctx - n + i_lo + 1, lim_hi = ctx - n + i_hi + 1;  // exclusive causal ends
+  const int first = p.window > 0 ? max(0, lim_lo - p.window) : 0;
+  const int j_first = first / Cfg::N;
+  const int T = lim_hi > 0 ? (lim_hi - 1) / Cfg::N - j_first + 1 : 0;  // K / V tiles to stream
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < Cfg::KSTAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+#pragma unroll
+    for (int s = 0; s < Cfg::VSTAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+#pragma unroll
+    for (int s = 0; s < Cfg::SBUF; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], Cfg::SOFTMAX / 32);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(&xch[0], Cfg::SOFTMAX / 32);
+    mbar_init(&xch[1], Cfg::SOFTMAX / 32);
+    mbar_init(&xl, Cfg::SOFTMAX / 32);
+    mbar_init(&fin, 1);
+    fence_barrier_init();
+    abort_flag = 0;
+    cta_flags = ctx_raw != ctx ? PKV_FLAG_BAD_LEN : 0;
+    k_consumed = v_consumed = k_issued = v_issued = 0;
+  }
+  if (warp == Cfg::ISSUER) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
+  if (warp == Cfg::PRODUCER && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (tid < Cfg::SOFTMAX) {  // Q tile: thread (row, half) stages half of its row (zeros past R)
+    const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
+    const int r = r0 + row;
+    const int ii = r / p.G, g = r - ii * p.G;
+    const uint4 *src = r < R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
+                                                             ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D)
+                             : nullptr;
+#pragma unroll
+    for (int k = 0; k < Cfg::D / 16; ++k) {
+      const int c = half * (Cfg::D / 16) + k;
+      const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      sts128(smem_u32(sQ + (c >> 3) * Cfg::PANEL_Q + row * 128 + (((c & 7) ^ (row & 7)) << 4)), v);
+    }
+    fence_proxy_async();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = tmem_base;
+
+  if (warp == Cfg::PRODUCER) {
+    // ---------------- TMA producer ----------------
+    // lane l fetches block (l % 8) of a tile, panel l / 8; the ids of the next
+    // tile are read one tile ahead
+    const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
+    auto block_row = [&](int jj, int *bad) -> int64_t {
+      const int lb = (j_first + jj) * Cfg::BLOCKS + slot;
+      // past the context, or wholly before every row's window (such blocks may
+      // have been released): nothing to read, the box past the tensor fills zeros
+      if (jj >= T || lb >= nblk || (lb + 1) * kBlock <= first) return p.num_blocks * p.Hkv;
+      const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
+      if (id >= 0 && (int64_t)id < p.num_blocks) return (int64_t)id * p.Hkv + h;
+      *bad = 1;
+      return p.num_blocks * p.Hkv;
+    };
+    int bad = 0;
+    int64_t trow = block_row(0, &bad);
+    for (int j = 0; j < T; ++j) {
+      const int64_t next = block_row(j + 1, &bad);
+      const int ks = j % Cfg::KSTAGES, vs = j % Cfg::VSTAGES;
+      if (j >= Cfg::KSTAGES &&
+          !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
+        break;
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
+      __syncwarp();
+      if (lane < Cfg::LOADS)
+        tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
+                    (int)(trow * kBlock), &k_full[ks]);
+      if (lane == 0) k_issued = j + 1;
+      if (j >= Cfg::VSTAGES &&
+          !warp_wait(&v_empty[vs], (uint32_t)((j / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
+      __syncwarp();
+      if (lane < Cfg::LOADS)
+        tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
+                    (int)(trow * kBlock), &v_full[vs]);
+      if (lane == 0) v_issued = j + 1;
+      trow = next;
+    }
+    if (bad) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
+    if (__any_sync(kFull, k_issued < T || v_issued < T) && lane == 0 && !*(volatile int *)&abort_flag) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
+    }
+  } else if (warp == Cfg::ISSUER) {
+    // ---------------- MMA issue ----------------
+    constexpr uint32_t idS = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::N, false);
+    constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
+    const uint32_t q0 = smem_u32(sQ);
+    bool ok = true;
+    // S = Q . K^T of tile jj into S buffer jj % SBUF (free once P . V of tile
+    // jj - SBUF, which read P from it, is done)
+    auto issue_s = [&](int jj) -> bool {
+      const int ks = jj % Cfg::KSTAGES, sb = jj % Cfg::SBUF;
+      if (!warp_wait(&k_full[ks], (uint32_t)(jj / Cfg::KSTAGES) & 1u, p.timeout_ns)) return false;
+      if (jj >= Cfg::SBUF &&
+          !warp_wait(&pv_done[sb], (uint32_t)((jj / Cfg::SBUF) - 1) & 1u, p.timeout_ns))
+        return false;
+      if (lane == 0) k_consumed = jj + 1;
+      tc::fence_after();
+      if (lane == 0) {
+        const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
+        const uint32_t dS = tbase + (uint32_t)(sb * Cfg::N);
+#pragma unroll
+        for (int k = 0; k < Cfg::D / 16; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
+          const uint32_t offk = (uint32_t)((k >> 2) * Cfg::PANEL_KV + (k & 3) * 32);
+          tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
+                      k > 0 ? 1u : 0u);
+        }
+        tc::commit(&s_full[sb]);
+        tc::commit(&k_empty[ks]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // S runs one tile ahead of P . V (tensor-pipe order ... S(j+1), P . V(j)).
+    // (Two ahead measured much slower: S(j+2) reuses the buffer of P . V(j-1),
+    // so its issue waits for that P . V to complete and the pipe drains.)
+    if (T > 0) ok = issue_s(0);
+    for (int j = 0; j < T && ok; ++j) {
+      if (j + 1 < T && !(ok = issue_s(j + 1))) break;
+      const int vs = j % Cfg::VSTAGES, sb = j % Cfg::SBUF;
+      ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+      if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
+      if (!ok) break;
+      if (lane == 0) v_consumed = j + 1;
+      uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
+      // stale cache rows past ctx inside the sequence's last block: zero them in V
+      // (their weights are 0, but 0 * NaN would still poison P . V)
+      const int kv0 = (j_first + j) * Cfg::N;
+      const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
+      if (z0 >= 0 && z0 < z1) {
+        for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
+          const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
+          sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
+        }
+        fence_proxy_async();
+      }
+      __syncwarp();
+      tc::fence_after();
+      if (lane == 0) {
+        const uint32_t v0 = smem_u32(vt);
+        const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
+#pragma unroll
+        for (int k = 0; k < Cfg::N / 16; ++k) {
+          // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+          const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
+          const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
+          tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (j > 0 || k > 0) ? 1u : 0u);
+          if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
+        }
+        tc::commit(&pv_done[sb]);
+        tc::commit(&v_empty[vs]);
+      }
+      __syncwarp();
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
+    }
+  } else {
+    // ---------------- softmax + epilogue: thread (row, half) ----------------
+    constexpr int SC = Cfg::N / 2;  // S columns of a thread (its half of the row)
+    constexpr int OC = Cfg::D / 2;  // O columns of a thread
+    const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
+    const int r = r0 + row;
+    const bool valid = r < R;
+    const int lim = valid ? ctx - n + r / p.G + 1 : 0;  // visible positions [lo, lim)
+    const int lo = (valid && p.window > 0) ? max(0, lim - p.window) : 0;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c = p.scale_log2;
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int sb = j % Cfg::SBUF;
+      ok = warp_wait(&s_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
+      if (!ok) break;
+      tc::fence_after();
+      const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
+      uint32_t s[SC / 32][32];
+#pragma unroll
+      for (int q = 0; q < SC / 32; ++q) tc::ld32(scol + (uint32_t)(q * 32), s[q]);
+      const int kv0 = (j_first + j) * Cfg::N + half * SC;
+      if (!(kv0 >= lo && kv0 + SC <= lim)) {  // a mask edge crosses these columns
+#pragma unroll
+        for (int q = 0; q < SC / 32; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int pos = kv0 + q * 32 + e;
+            if (pos < lo || pos >= lim) s[q][e] = 0xff800000u;  // -inf
+          }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < SC / 32; ++q)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
+      // the row max over both halves (double-buffered exchange, bounded wait)
+      red[j & 1][half][row] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xch[j & 1]);
+      ok = warp_wait(&xch[j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
+      if (!ok) break;
+      mx = fmaxf(mx, red[j & 1][half ^ 1][row]);
+      const float m_new = fmaxf(m_run, mx * c);
+      // warps w and w + 4 hold the same rows and the same m_new: same decision
+      const bool rescale = __any_sync(kFull, m_new > m_run + 8.f);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = m_new == -INFINITY ? 1.f : ex2(m_run - m_new);
+        m_run = m_new;
+      }
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      float sum = 0.f;
+      uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
+#pragma unroll
+      for (int e = 0; e < SC / 2; ++e) {
+        const int col = 2 * e;
+        const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
+        const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
+        sum += a0 + a1;
+        w[e] = pack2<Cfg::BF>(a0, a1);
+        if constexpr (Cfg::SPLIT) {
+          const float2 hi = unpack2(BF16{}, w[e]);
+          wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
+        }
+      }
+      if (rescale && j > 0) {  // O must hold P . V of the previous tile before it is scaled
+        ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+        if (!ok) break;
+        tc::fence_after();
+#pragma unroll
+        for (int q = 0; q < OC / 32; ++q) {
+          uint32_t o[32];
+          const uint32_t ta = tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32);
+          tc::ld32(ta, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st32(ta, o);
+        }
+      }
+      l = l * alpha + sum;
+      // P over this thread's own (already read) S columns: high part, then residual
+      tc::st32(scol, w);
+      if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+    }
+    if (ok && T > 0)
+      ok = warp_wait(&pv_done[(T - 1) % Cfg::SBUF], (uint32_t)((T - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
+    if (ok) {  // the row sum over both halves
+      red_l[half][row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xl);
+      ok = warp_wait(&xl, 0, p.timeout_ns);
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+        abort_flag = 1;
+      }
+    } else {
+      tc::fence_after();
+      const float lt = l + red_l[half ^ 1][row];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
+      const int ii = r / p.G, g = r - ii * p.G;
+      uint4 *dst = valid ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
+                                                     ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D + half * OC)
+                         : nullptr;
+#pragma unroll
+      for (int q = 0; q < OC / 32; ++q) {
+        uint32_t o[32];
+        if (T > 0) {
+          tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (dst) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                     __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+            dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- drain, then free tensor memory ----------------
+  tc::fence_before();
+  __syncthreads();
+  if (warp == Cfg::ISSUER) {
+    if (lane == 0) tc::commit(&fin);  // completes once every issued MMA has
+    __syncwarp();
+    if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+  } else if (warp == Cfg::PRODUCER && lane == 0) {  // copies issued but never consumed (abort only)
+    for (int j = k_consumed; j < k_issued; ++j)
+      mbar_wait_bounded(&k_full[j % Cfg::KSTAGES], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
+    for (int j = v_consumed; j < v_issued; ++j)
+      mbar_wait_bounded(&v_full[j % Cfg::VSTAGES], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == Cfg::ISSUER) tc::dealloc(tbase, Cfg::TMEM_COLS);
+  if (tid == 0 && cta_flags && p.status) atomicOr(p.status, cta_flags);
+}
+
+template <class Cfg>
+static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              cudaStream_t stream) {
+  static int configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(prefill_tile_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  const dim3 grid((unsigned)p.max_tiles, (unsigned)p.Hkv, (unsigned)p.B);
+  prefill_tile_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, tmK, tmV);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tiles(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                           cudaStream_t stream) {
+  if (p.max_tiles <= 0 || p.B <= 0) return cudaSuccess;
+  if (cache_dtype == PKV_BF16) {
+    if (p.D == 128) return launch_cfg<PrefillCfg<BF16, 128>>(p, tmK, tmV, stream);
+    if (p.D == 64) return launch_cfg<PrefillCfg<BF16, 64>>(p, tmK, tmV, stream);
+  } else if (cache_dtype == PKV_F16) {
+    if (p.D == 128) return launch_cfg<PrefillCfg<F16, 128>>(p, tmK, tmV, stream);
+    if (p.D == 64) return launch_cfg<PrefillCfg<F16, 64>>(p, tmK, tmV, stream);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

@@ -186,11 +186,14 @@ def test_captured_multi_query_step_matches_eager():
     assert torch.equal(step.k_cache.cpu(), eager_k)
 
 
+@pytest.mark.parametrize("kernel", ["persistent", "tiles"])
 @pytest.mark.parametrize("dtype,D,window", [("bf16", 128, 0), ("f16", 64, 0), ("bf16", 128, 37)])
-def test_multi_query_tensor_core_route(dtype, D, window):
+def test_multi_query_tensor_core_route(dtype, D, window, kernel, monkeypatch):
     """40 sequences x 4 kv heads (160 (sequence, kv head) tiles, one per SM or
-    more): with num_splits = 0 the call takes the tensor-core kernel, with a
-    fixed split count the 8-row-unit decode kernel; both against the oracle."""
+    more): with num_splits = 0 the call takes a tensor-core prefill kernel
+    (each of the two), with a fixed split count the 8-row-unit decode kernel;
+    both against the oracle."""
+    monkeypatch.setenv("PKV_PREFILL_KERNEL", kernel)
     spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=5, ctx_range=(5, 300), free_frac=0.3,
                 min_free=16, window=window)
     for seed, splits in ((61, 0), (62, 7)):

@@ -16,6 +16,15 @@ from workloads import make_prefill
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["persistent", "tiles"])
+def prefill_kernel(request, monkeypatch):
+    """Every test runs on both prefill kernels (one persistent CTA per SM,
+    one CTA per work item), through the library's environment override of
+    its automatic choice."""
+    monkeypatch.setenv("PKV_PREFILL_KERNEL", request.param)
+    return request.param
+
+
 def _pkv():
     import paged_kv_gqa_03_gb300 as pkv
     return pkv
@@ -107,3 +116,20 @@ def test_prefill_flags_and_empty_sequences():
     out, status = run_gpu(c, max_q_len=20)            # sequence 2 has 33 new tokens
     assert status == _pkv().PKV_FLAG_BAD_LEN
     compare(out[:20], ref[:20], "bf16", "rows inside max_q_len")
+
+
+def test_prefill_items_without_context_in_a_persistent_grid():
+    """608 work items (4 sequences x 8 kv heads x 19 row tiles), so each
+    persistent CTA walks several; sequence 0 keeps 300 new tokens but only
+    100 positions, so its first 12 row tiles see no position and stream no
+    K / V tile, interleaved with items that do.  Every output against the
+    oracle, rows without context 0."""
+    c = make_prefill(13, [300, 120, 250, 64], [0, 40, 7, 0], 64, 8, 128, "bf16")
+    c["ctx"] = c["ctx"].copy()
+    c["ctx"][0] = 100
+    out, status = run_gpu(c)
+    assert status == 0
+    assert torch.all(out[:200].float() == 0)
+    ref = oracle.prefill(c["q"], "bf16", c["kc"], c["vc"], "bf16", c["table"], c["ctx"], c["q_start"],
+                         scale=1.0 / math.sqrt(128))
+    compare(out, ref, "bf16", "prefill with rows without context")
