@@ -458,6 +458,18 @@ def peak_bf16():
         return 1900.0, "fallback"
 
 
+def prefill_kernel_name(c):
+    """The kernel the library runs for this workload: one CTA per work item
+    when the block table admits a cached prefix of 2048+ positions before
+    the new tokens, the persistent kernel otherwise (unless overridden)."""
+    force = os.environ.get("PKV_PREFILL_KERNEL", "")
+    tiles = c["table"].shape[1] * 16 - max(c["n"]) >= 2048
+    if force in ("tiles", "persistent"):
+        tiles = force == "tiles"
+    return ("prefill_tile_kernel (tcgen05, one CTA per work item)" if tiles
+            else "prefill_kernel (tcgen05, persistent)")
+
+
 def run_prefill(args, world, rank, local):
     """Paged prefill on the tensor cores: each launch attends every new token
     of the workload causally; value = useful TFLOP/s (4 * D per query head and
@@ -577,7 +589,7 @@ def run_prefill(args, world, rank, local):
         "config": {"workload": f"prefill {args.prefill}", "B": len(c["n"]), "new_tokens": c["n"][0],
                    "cached_prefix": c["prefix"][0], "Hq": c["Hq"], "Hkv": c["Hkv"], "D": c["D"],
                    "window": args.window, "block_size": 16, "l2": "flushed (256 MB write) before every timed launch"},
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (tcgen05)", "achieved": round(tflops, 1),
+        "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(c), "achieved": round(tflops, 1),
                      "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "traffic": None, "algorithmic_flops_per_launch": flops,
                      "note": "bf16 P is split into high + residual parts (1.5x the MMA work of one P)"},
