@@ -13,7 +13,15 @@
 
 namespace pkv {
 
-template <class Cfg>
+// REP > 1 (a work item of at most 128 / REP query rows, e.g. a few new
+// tokens of one GQA group): the tile holds REP replicas of the item's rows,
+// and replica q takes the 16-position k-steps k with k mod REP = q of every
+// K / V tile (its other P columns are written as zeros), so a softmax thread
+// handles 64 / REP columns of a tile instead of 64; each replica keeps its
+// own running max and sum, and the epilogue merges the REP partial rows
+// (weights 2^(m_q - max m), through the then idle K ring).  The tensor work
+// per tile is unchanged.
+template <class Cfg, int REP>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     prefill_tile_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV) {
@@ -28,6 +36,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // the softmax may finish tile j + 1 before the MMA warp waits for tile j, but
   // it cannot finish tile j + SBUF before that.)
   __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
+  __shared__ __align__(8) uint64_t mrg[2];  // replica merge: (max, sum) written, partial O staged
+  static_assert(REP == 1 || REP == 2 || REP == 4, "replicas");
+  constexpr int RW = Cfg::M / REP;  // query rows of one replica
+  constexpr int KL = 4 / REP;       // k-steps of a replica in each half of a tile
+  static_assert((REP - 1) * RW * Cfg::D * 4 <= Cfg::KSTAGES * Cfg::KV_BYTES, "replica staging");
   __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
   __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
   __shared__ uint32_t tmem_base;
@@ -72,6 +85,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&xch[0], Cfg::SOFTMAX / 32);
     mbar_init(&xch[1], Cfg::SOFTMAX / 32);
     mbar_init(&xl, Cfg::SOFTMAX / 32);
+    mbar_init(&mrg[0], Cfg::SOFTMAX / 32);
+    mbar_init(&mrg[1], Cfg::SOFTMAX / 32);
     mbar_init(&fin, 1);
     fence_barrier_init();
     abort_flag = 0;
@@ -85,7 +100,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   }
   if (tid < Cfg::SOFTMAX) {  // Q tile: thread (row, half) stages half of its row (zeros past R)
     const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
-    const int r = r0 + row;
+    const int r = r0 + row % RW;
     const int ii = r / p.G, g = r - ii * p.G;
     const uint4 *src = r < R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
                                                              ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D)
@@ -232,7 +247,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int SC = Cfg::N / 2;  // S columns of a thread (its half of the row)
     constexpr int OC = Cfg::D / 2;  // O columns of a thread
     const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
-    const int r = r0 + row;
+    const int rr = row % RW, rep = row / RW;  // query row of the item, replica
+    const int r = r0 + rr;
     const bool valid = r < R;
     const int lim = valid ? ctx - n + r / p.G + 1 : 0;  // visible positions [lo, lim)
     const int lo = (valid && p.window > 0) ? max(0, lim - p.window) : 0;
@@ -246,24 +262,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (!ok) break;
       tc::fence_after();
       const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
-      uint32_t s[SC / 32][32];
-#pragma unroll
-      for (int q = 0; q < SC / 32; ++q) tc::ld32(scol + (uint32_t)(q * 32), s[q]);
-      const int kv0 = (j_first + j) * Cfg::N + half * SC;
-      if (!(kv0 >= lo && kv0 + SC <= lim)) {  // a mask edge crosses these columns
+      // this thread's S values: all SC columns of its half (REP = 1), or the
+      // KL k-steps rep, rep + REP, ... of its half (16 columns each)
+      constexpr int NV = SC / REP;
+      uint32_t s[NV];
+      const int kvh = (j_first + j) * Cfg::N + half * SC;  // first position of this half
+      if constexpr (REP == 1) {
 #pragma unroll
         for (int q = 0; q < SC / 32; ++q)
+          tc::ld32(scol + (uint32_t)(q * 32), *reinterpret_cast<uint32_t(*)[32]>(&s[q * 32]));
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int pos = kv0 + q * 32 + e;
-            if (pos < lo || pos >= lim) s[q][e] = 0xff800000u;  // -inf
-          }
+        for (int t = 0; t < KL; ++t)
+          tc::ld16(scol + (uint32_t)((rep + t * REP) * 16), *reinterpret_cast<uint32_t(*)[16]>(&s[t * 16]));
+      }
+      // position of value e: kvh + e (REP = 1), kvh + (rep + (e / 16) * REP) * 16 + e % 16
+      auto pos_of = [&](int e) { return REP == 1 ? kvh + e : kvh + (rep + (e / 16) * REP) * 16 + (e & 15); };
+      if (!(pos_of(0) >= lo && pos_of(NV - 1) < lim)) {  // a mask edge crosses these columns
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+          const int pos = pos_of(e);
+          if (pos < lo || pos >= lim) s[e] = 0xff800000u;  // -inf
+        }
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < SC / 32; ++q)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
+      for (int e = 0; e < NV; ++e) mx = fmaxf(mx, __uint_as_float(s[e]));
       // the row max over both halves (double-buffered exchange, bounded wait)
       red[j & 1][half][row] = mx;
       __syncwarp();
@@ -281,12 +305,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       float sum = 0.f;
-      uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
+      uint32_t w[NV / 2], wl[Cfg::SPLIT ? NV / 2 : 1];
 #pragma unroll
-      for (int e = 0; e < SC / 2; ++e) {
-        const int col = 2 * e;
-        const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
-        const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
+      for (int e = 0; e < NV / 2; ++e) {
+        const float a0 = ex2(fmaf(__uint_as_float(s[2 * e]), c, -mu));
+        const float a1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), c, -mu));
         sum += a0 + a1;
         w[e] = pack2<Cfg::BF>(a0, a1);
         if constexpr (Cfg::SPLIT) {
@@ -310,8 +333,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       l = l * alpha + sum;
       // P over this thread's own (already read) S columns: high part, then residual
-      tc::st32(scol, w);
-      if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
+      if constexpr (REP == 1) {
+        tc::st32(scol, w);
+        if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
+      } else {
+        // 8 packed columns per k-step: this replica's k-steps, zeros in the others
+#pragma unroll
+        for (int t = 0; t < KL; ++t) {
+          const uint32_t pc = scol + (uint32_t)((rep + t * REP) * 8);
+          const uint32_t *v = &w[t * 8];
+          tc::st8(pc, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+          if constexpr (Cfg::SPLIT) {
+            const uint32_t *u = &wl[t * 8];
+            tc::st8(pc + (uint32_t)(SC / 2), u[0], u[1], u[2], u[3], u[4], u[5], u[6], u[7]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q % REP != rep) {
+            tc::st8(scol + (uint32_t)(q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
+            if constexpr (Cfg::SPLIT) tc::st8(scol + (uint32_t)(SC / 2 + q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
+          }
+      }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
@@ -333,30 +376,106 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else {
       tc::fence_after();
       const float lt = l + red_l[half ^ 1][row];
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
       const int ii = r / p.G, g = r - ii * p.G;
       uint4 *dst = valid ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) +
                                                      ((size_t)(qs + ii) * p.Hq + h * p.G + g) * Cfg::D + half * OC)
                          : nullptr;
+      if constexpr (REP == 1) {
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
 #pragma unroll
-      for (int q = 0; q < OC / 32; ++q) {
-        uint32_t o[32];
-        if (T > 0) {
-          tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
-        } else {
+        for (int q = 0; q < OC / 32; ++q) {
+          uint32_t o[32];
+          if (T > 0) {
+            tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (dst) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
-                                     __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
-            dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
           }
+          if (dst) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
+                                       __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+              dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+      } else if (T == 0) {  // no tile: every replica saw nothing
+        if (dst && rep == 0) {
+#pragma unroll
+          for (int q = 0; q < OC / 8; ++q) dst[q] = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        // merge the replicas of query row rr: weights 2^(m_q - M) / sum_q l_q 2^(m_q - M)
+        float *mm = red[T & 1][0], *ml = red[T & 1][1];  // unused by the last tile's exchange
+        if (half == 0) {
+          mm[row] = m_run;
+          ml[row] = lt;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mrg[0]);
+        ok = warp_wait(&mrg[0], 0, p.timeout_ns);
+        if (ok) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < REP; ++q) M = fmaxf(M, mm[q * RW + rr]);
+          float L = 0.f;
+#pragma unroll
+          for (int q = 0; q < REP; ++q) {
+            const float mq = mm[q * RW + rr];
+            if (mq != -INFINITY) L += ml[q * RW + rr] * ex2(mq - M);
+          }
+          const float f = (m_run == -INFINITY || !(L > 0.f)) ? 0.f : ex2(m_run - M) / L;
+          // replicas 1.. stage their weighted rows in the K ring (idle: every S
+          // has completed), swizzled by 16-byte column groups
+          float4 *stage = reinterpret_cast<float4 *>(sK);
+          constexpr int C4 = Cfg::D / 4;  // float4 per staged row
+          uint32_t o[OC / 32][32];
+#pragma unroll
+          for (int q = 0; q < OC / 32; ++q)
+            tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o[q]);
+          if (rep > 0) {
+            float4 *srow = stage + (size_t)((rep - 1) * RW + rr) * C4;
+#pragma unroll
+            for (int q = 0; q < OC / 32; ++q)
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const int c4 = half * (OC / 4) + q * 8 + v;
+                srow[c4 ^ (rr & 7)] = make_float4(__uint_as_float(o[q][4 * v]) * f, __uint_as_float(o[q][4 * v + 1]) * f,
+                                                  __uint_as_float(o[q][4 * v + 2]) * f,
+                                                  __uint_as_float(o[q][4 * v + 3]) * f);
+              }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mrg[1]);
+          ok = warp_wait(&mrg[1], 0, p.timeout_ns);
+          if (ok && rep == 0 && dst) {
+#pragma unroll
+            for (int q = 0; q < OC / 32; ++q)
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = __uint_as_float(o[q][v * 8 + e]) * f;
+#pragma unroll
+                for (int k = 1; k < REP; ++k) {
+                  const float4 *srow = stage + (size_t)((k - 1) * RW + rr) * C4;
+                  const int c4 = half * (OC / 4) + q * 8 + 2 * v;
+                  const float4 x0 = srow[c4 ^ (rr & 7)], x1 = srow[(c4 + 1) ^ (rr & 7)];
+                  acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+                  acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+                }
+                dst[q * 4 + v] = make_uint4(pack2<Cfg::BF>(acc[0], acc[1]), pack2<Cfg::BF>(acc[2], acc[3]),
+                                            pack2<Cfg::BF>(acc[4], acc[5]), pack2<Cfg::BF>(acc[6], acc[7]));
+              }
+          }
+        }
+        if (!ok && lane == 0) {
+          atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+          abort_flag = 1;
         }
       }
     }
@@ -382,7 +501,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (tid == 0 && cta_flags && p.status) atomicOr(p.status, cta_flags);
 }
 
-template <class Cfg>
+template <class Cfg, int REP>
 static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               cudaStream_t stream) {
   static int configured[64] = {};
@@ -391,24 +510,35 @@ static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, co
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_tile_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    e = cudaFuncSetAttribute(prefill_tile_kernel<Cfg, REP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   const dim3 grid((unsigned)p.max_tiles, (unsigned)p.Hkv, (unsigned)p.B);
-  prefill_tile_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, tmK, tmV);
+  prefill_tile_kernel<Cfg, REP><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, tmK, tmV);
   return cudaGetLastError();
 }
 
+// Replicas per tile: 4 when every item has at most 32 query rows
+// (max_q_len * G <= 32), 2 when at most 64, else 1.
+template <class Cfg>
+static cudaError_t launch_rep(const PrefillParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.max_q_len * p.G;
+  if (rows <= 32) return launch_cfg<Cfg, 4>(p, tmK, tmV, stream);
+  if (rows <= 64) return launch_cfg<Cfg, 2>(p, tmK, tmV, stream);
+  return launch_cfg<Cfg, 1>(p, tmK, tmV, stream);
+}
+
 cudaError_t launch_prefill_tiles(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                           cudaStream_t stream) {
+                                 cudaStream_t stream) {
   if (p.max_tiles <= 0 || p.B <= 0) return cudaSuccess;
   if (cache_dtype == PKV_BF16) {
-    if (p.D == 128) return launch_cfg<PrefillCfg<BF16, 128>>(p, tmK, tmV, stream);
-    if (p.D == 64) return launch_cfg<PrefillCfg<BF16, 64>>(p, tmK, tmV, stream);
+    if (p.D == 128) return launch_rep<PrefillCfg<BF16, 128>>(p, tmK, tmV, stream);
+    if (p.D == 64) return launch_rep<PrefillCfg<BF16, 64>>(p, tmK, tmV, stream);
   } else if (cache_dtype == PKV_F16) {
-    if (p.D == 128) return launch_cfg<PrefillCfg<F16, 128>>(p, tmK, tmV, stream);
-    if (p.D == 64) return launch_cfg<PrefillCfg<F16, 64>>(p, tmK, tmV, stream);
+    if (p.D == 128) return launch_rep<PrefillCfg<F16, 128>>(p, tmK, tmV, stream);
+    if (p.D == 64) return launch_rep<PrefillCfg<F16, 64>>(p, tmK, tmV, stream);
   }
   return cudaErrorNotSupported;
 }

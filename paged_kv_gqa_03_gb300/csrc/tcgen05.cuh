@@ -111,6 +111,23 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Warp-wide: 16 consecutive columns (load and wait) / 8 consecutive columns
+// (store) of the warp's 32 lanes.
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void st8(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3, uint32_t v4,
+                                    uint32_t v5, uint32_t v6, uint32_t v7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v0),
+               "r"(v1), "r"(v2), "r"(v3), "r"(v4), "r"(v5), "r"(v6), "r"(v7)
+               : "memory");
+}
+
 // Warp-wide: one 32-bit column of the warp's 32 lanes (load and wait).
 __device__ __forceinline__ uint32_t ld1(uint32_t taddr) {
   uint32_t r;

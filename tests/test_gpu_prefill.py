@@ -133,3 +133,42 @@ def test_prefill_items_without_context_in_a_persistent_grid():
     ref = oracle.prefill(c["q"], "bf16", c["kc"], c["vc"], "bf16", c["table"], c["ctx"], c["q_start"],
                          scale=1.0 / math.sqrt(128))
     compare(out, ref, "bf16", "prefill with rows without context")
+
+
+@pytest.mark.parametrize("spec", [
+    dict(n=[3, 1, 4, 2], prefix=[500, 37, 0, 129], Hq=16, Hkv=2, D=128, dtype="bf16"),   # <= 32 rows: 4 replicas
+    dict(n=[8, 5, 1], prefix=[300, 1000, 16], Hq=8, Hkv=1, D=64, dtype="f16"),           # <= 64 rows: 2 replicas
+    dict(n=[2, 1], prefix=[333, 40], Hq=16, Hkv=1, D=64, dtype="bf16"),                  # MQA group 16, 4 replicas
+    dict(n=[6, 3], prefix=[2500, 200], Hq=8, Hkv=2, D=128, dtype="f16"),                 # group 4, 24 rows
+    dict(n=[4, 4], prefix=[700, 50], Hq=16, Hkv=2, D=128, dtype="bf16", window=100),
+    dict(n=[8, 2], prefix=[900, 5], Hq=16, Hkv=2, D=64, dtype="bf16", window=37),        # 2 replicas, window
+], ids=lambda s: f"{s['dtype']}-q{s['Hq']}-kv{s['Hkv']}-d{s['D']}-n{max(s['n'])}-W{s.get('window', 0)}")
+def test_prefill_few_rows_per_item(spec):
+    """Items of at most 64 query rows (a few new tokens of one GQA group, the
+    speculative-verify shape): the one-CTA-per-item kernel runs replicas of
+    the rows over disjoint k-steps and merges them; every output against
+    the oracle."""
+    spec = dict(spec)
+    window = spec.pop("window", 0)
+    c = make_prefill(17, **spec)
+    out, status = run_gpu(c, window=window)
+    assert status == 0
+    ref = oracle.prefill(c["q"], c["dtype"], c["kc"], c["vc"], c["dtype"], c["table"], c["ctx"],
+                         c["q_start"], scale=1.0 / math.sqrt(c["D"]), window=window)
+    compare(out, ref, c["dtype"], "prefill, few rows per item")
+
+
+def test_prefill_few_rows_without_context():
+    """Four-row items where one sequence has no context at all (its item
+    streams no tile) and one sees only its first positions: zeros where
+    nothing is visible, the oracle elsewhere."""
+    c = make_prefill(23, [4, 4, 3], [60, 10, 0], 16, 2, 128, "bf16")
+    c["ctx"] = c["ctx"].copy()
+    c["ctx"][1] = 0
+    c["ctx"][2] = 2
+    out, status = run_gpu(c)
+    assert status == 0
+    assert torch.all(out[4:8].float() == 0) and torch.all(out[8].float() == 0)
+    ref = oracle.prefill(c["q"], "bf16", c["kc"], c["vc"], "bf16", c["table"], c["ctx"], c["q_start"],
+                         scale=1.0 / math.sqrt(128))
+    compare(out, ref, "bf16", "few rows, no context")
