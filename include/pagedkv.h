@@ -218,9 +218,9 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  * paged_decode_attention; the workspace size comes from
  * paged_decode_multi_workspace_bytes.  Kernels: with q_len >= 2, an F16 or
  * BF16 cache, num_splits = 0, scale > 0 and at least one (sequence, kv head,
- * 128-row tile) per SM, the call runs the tensor-core prefill kernel (see
- * paged_prefill_attention), which reads each (sequence, kv head)'s K/V once
- * for all its q_len * G rows; otherwise each kv head's rows are served in
+ * 128-row tile) per SM, the call runs a tensor-core prefill kernel (chosen
+ * as in paged_prefill_attention), which reads each (sequence, kv head)'s
+ * K/V once for all its q_len * G rows; otherwise each kv head's rows are served in
  * 8-row units by the decode kernel (K/V read once per unit, re-reads mostly
  * from L2) with the split-KV merge.  Both meet the same error bound.
  */
@@ -263,6 +263,14 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
  *   D            64 or 128; B <= 65535
  * Other arguments as for paged_decode_attention.  Asynchronous on `stream`;
  * needs no workspace.
+ *
+ * Two kernels run the same tile pipeline: one CTA per (128-row tile, kv
+ * head, sequence), chosen when max_blocks_per_seq * 16 - max_q_len >= 2048
+ * (the table admits a long cached prefix, so the items are long), and one
+ * persistent CTA per SM walking those items otherwise (prompts: many short
+ * items of unequal length).  The environment variable PKV_PREFILL_KERNEL =
+ * "tiles" or "persistent" overrides the choice; results agree within the
+ * tolerance either way.
  */
 int paged_prefill_attention(void *out, const void *q, int q_dtype,
                             const void *k_cache, const void *v_cache, int cache_dtype,
