@@ -91,4 +91,65 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return pack_f16x2(lo, hi);
 }
 
+// S = Q . K^T of one K tile into tensor-memory columns dS: D / 16 MMAs over
+// K-major, 128-byte-swizzled Q (at q0) and K (at k0) panels; issued by one
+// thread.
+template <class Cfg>
+__device__ __forceinline__ void mma_s_tile(uint32_t dS, uint32_t q0, uint32_t k0) {
+  constexpr uint32_t idS = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::N, false);
+#pragma unroll
+  for (int k = 0; k < Cfg::D / 16; ++k) {
+    const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
+    const uint32_t offk = (uint32_t)((k >> 2) * Cfg::PANEL_KV + (k & 3) * 32);
+    tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
+                k > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P . V of one V tile: P (16-bit pairs) from the S buffer's tensor
+// memory at pb, V (MN-major, at v0) from shared memory; a bf16 P is its high
+// part plus its residual, two MMAs per k-step.  `accumulate` false starts O
+// afresh.  Issued by one thread.
+template <class Cfg>
+__device__ __forceinline__ void mma_pv_tile(uint32_t dO, uint32_t pb, uint32_t v0, bool accumulate) {
+  constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
+#pragma unroll
+  for (int k = 0; k < Cfg::N / 16; ++k) {
+    // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+    const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
+    const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
+    tc::mma_f16_tmem_a(dO, pb + pcol, dv, idO, (accumulate || k > 0) ? 1u : 0u);
+    if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(dO, pb + pcol + Cfg::N / 4, dv, idO, 1u);
+  }
+}
+
+// Warp-wide: zeroes rows [z0, z1) of a V tile in shared memory (stale cache
+// rows past a context inside its last block: their weights are 0, but 0 * NaN
+// would still poison P . V), then makes the writes visible to the tensor core.
+template <class Cfg>
+__device__ __forceinline__ void zero_v_rows(uint8_t *vt, int z0, int z1, int lane) {
+  if (z0 >= 0 && z0 < z1) {
+    for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
+      const int r = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
+      sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + r * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
+    }
+    fence_proxy_async();
+  }
+}
+
+// Warp-wide: multiplies this thread's OC columns of O (tensor memory at ta)
+// by alpha.
+template <class Cfg>
+__device__ __forceinline__ void scale_o(uint32_t ta, float alpha) {
+  constexpr int OC = Cfg::D / 2;
+#pragma unroll
+  for (int q = 0; q < OC / 32; ++q) {
+    uint32_t o[32];
+    tc::ld32(ta + (uint32_t)(q * 32), o);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+    tc::st32(ta + (uint32_t)(q * 32), o);
+  }
+}
+
 }  // namespace pkv

@@ -166,8 +166,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   } else if (warp == Cfg::ISSUER) {
     // ---------------- MMA issue ----------------
-    constexpr uint32_t idS = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::N, false);
-    constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
     const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
     // S = Q . K^T of tile jj into S buffer jj % SBUF (free once P . V of tile
@@ -181,15 +179,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (lane == 0) k_consumed = jj + 1;
       tc::fence_after();
       if (lane == 0) {
-        const uint32_t k0 = smem_u32(sK + (size_t)ks * Cfg::KV_BYTES);
-        const uint32_t dS = tbase + (uint32_t)(sb * Cfg::N);
-#pragma unroll
-        for (int k = 0; k < Cfg::D / 16; ++k) {
-          const uint32_t off = (uint32_t)((k >> 2) * Cfg::PANEL_Q + (k & 3) * 32);
-          const uint32_t offk = (uint32_t)((k >> 2) * Cfg::PANEL_KV + (k & 3) * 32);
-          tc::mma_f16(dS, tc::desc_sw128(q0 + off, 16, 1024), tc::desc_sw128(k0 + offk, 16, 1024), idS,
-                      k > 0 ? 1u : 0u);
-        }
+        mma_s_tile<Cfg>(tbase + (uint32_t)(sb * Cfg::N), q0, smem_u32(sK + (size_t)ks * Cfg::KV_BYTES));
         tc::commit(&s_full[sb]);
         tc::commit(&k_empty[ks]);
       }
@@ -208,30 +198,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (!ok) break;
       if (lane == 0) v_consumed = j + 1;
       uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-      // stale cache rows past ctx inside the sequence's last block: zero them in V
-      // (their weights are 0, but 0 * NaN would still poison P . V)
-      const int kv0 = (j_first + j) * Cfg::N;
-      const int z0 = ctx - kv0, z1 = min(nblk * kBlock - kv0, Cfg::N);
-      if (z0 >= 0 && z0 < z1) {
-        for (int idx = lane; idx < (z1 - z0) * 8 * Cfg::PANELS; idx += 32) {
-          const int row = z0 + idx / (8 * Cfg::PANELS), rest = idx % (8 * Cfg::PANELS);
-          sts128(smem_u32(vt + (rest >> 3) * Cfg::PANEL_KV + row * 128 + (rest & 7) * 16), make_uint4(0, 0, 0, 0));
-        }
-        fence_proxy_async();
-      }
+      const int kv0 = (j_first + j) * Cfg::N;  // first position of the tile
+      zero_v_rows<Cfg>(vt, ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
       __syncwarp();
       tc::fence_after();
       if (lane == 0) {
-        const uint32_t v0 = smem_u32(vt);
-        const uint32_t pb = tbase + (uint32_t)(sb * Cfg::N);
-#pragma unroll
-        for (int k = 0; k < Cfg::N / 16; ++k) {
-          // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
-          const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
-          const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
-          tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol, dv, idO, (j > 0 || k > 0) ? 1u : 0u);
-          if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(tbase + Cfg::COL_O, pb + pcol + Cfg::N / 4, dv, idO, 1u);
-        }
+        mma_pv_tile<Cfg>(tbase + Cfg::COL_O, tbase + (uint32_t)(sb * Cfg::N), smem_u32(vt), j > 0);
         tc::commit(&pv_done[sb]);
         tc::commit(&v_empty[vs]);
       }
@@ -321,15 +293,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
         if (!ok) break;
         tc::fence_after();
-#pragma unroll
-        for (int q = 0; q < OC / 32; ++q) {
-          uint32_t o[32];
-          const uint32_t ta = tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32);
-          tc::ld32(ta, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tc::st32(ta, o);
-        }
+        scale_o<Cfg>(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC), alpha);
       }
       l = l * alpha + sum;
       // P over this thread's own (already read) S columns: high part, then residual
