@@ -79,6 +79,7 @@ typedef enum {
 #define PKV_FLAG_TIMEOUT 1   /* a pipeline wait exceeded its time limit */
 #define PKV_FLAG_BAD_LEN 2   /* context_lens[b] < 0 or > 16 * max_blocks_per_seq (clamped) */
 #define PKV_FLAG_BAD_BLOCK 4 /* a block-table entry outside [0, num_blocks) (read as zeros) */
+#define PKV_FLAG_RANGE 8     /* bf16 tensor-core prefill: a V value of magnitude > 65504 (saturated) */
 
 /* ------------------------------------------------------------------------ */
 /* Step a3 — KV append through a slot mapping.                              */
@@ -259,10 +260,16 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
  *   scale        > 0 (PKV_EINVAL otherwise)
  *   window       0 (none) or W >= 1
  *   status       device int32 or NULL: zeroed by the call, then the OR of
- *                PKV_FLAG_* bits (bad block id, bad length, in-kernel timeout)
+ *                PKV_FLAG_* bits (bad block id, bad length, in-kernel timeout;
+ *                PKV_FLAG_RANGE: a bf16 V value beyond the f16 range, see below)
  *   D            64 or 128; B <= 65535
  * Other arguments as for paged_decode_attention.  Asynchronous on `stream`;
  * needs no workspace.
+ *
+ * For a bf16 cache each V tile is converted to f16 in shared memory so the
+ * attention weights can enter P . V as f16 (11 significant bits, one MMA):
+ * exact for |v| in [2^-14, 65504]; smaller magnitudes lose low bits (an error
+ * below 2^-14 absolute), larger ones saturate and set PKV_FLAG_RANGE.
  *
  * Two kernels run the same tile pipeline: one CTA per (128-row tile, kv
  * head, sequence), chosen when max_blocks_per_seq * 16 - max_q_len >= 2048

@@ -70,7 +70,7 @@ _sig("pkv_bm_num_tokens", _i64, _P, _i64)
 
 PKV_OK, PKV_EINVAL, PKV_EUNSUPPORTED, PKV_EWORKSPACE = 0, -1, -2, -3
 PKV_ECUDA, PKV_ETIMEOUT, PKV_EOOM, PKV_ERANGE, PKV_ENOTFOUND = -4, -5, -6, -7, -8
-PKV_FLAG_TIMEOUT, PKV_FLAG_BAD_LEN, PKV_FLAG_BAD_BLOCK = 1, 2, 4
+PKV_FLAG_TIMEOUT, PKV_FLAG_BAD_LEN, PKV_FLAG_BAD_BLOCK, PKV_FLAG_RANGE = 1, 2, 4, 8
 
 
 def lib():

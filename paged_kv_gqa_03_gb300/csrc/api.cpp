@@ -566,7 +566,7 @@ int paged_decode_status(const void *workspace, size_t workspace_bytes, pkv_strea
   if (e != cudaSuccess) return cuda_status(e);
   if (flags_out) *flags_out = status;
   if (status & PKV_FLAG_TIMEOUT) return PKV_ETIMEOUT;
-  if (status & (PKV_FLAG_BAD_LEN | PKV_FLAG_BAD_BLOCK)) return PKV_ERANGE;
+  if (status & (PKV_FLAG_BAD_LEN | PKV_FLAG_BAD_BLOCK | PKV_FLAG_RANGE)) return PKV_ERANGE;
   return PKV_OK;
 }
 

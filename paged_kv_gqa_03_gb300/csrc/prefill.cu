@@ -260,8 +260,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (!ok) break;
         if (lane == 0) v_consumed = gj + 1;
         uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-        const int kv0 = (it.j_first + j) * Cfg::N;  // first position of the tile
-        zero_v_rows<Cfg>(vt, it.ctx - kv0, min(it.nblk * kBlock - kv0, Cfg::N), lane);
+        if constexpr (!Cfg::VCVT) {  // (with the conversion the softmax warps zero them)
+          const int kv0 = (it.j_first + j) * Cfg::N;  // first position of the tile
+          zero_v_rows<Cfg>(vt, it.ctx - kv0, min(it.nblk * kBlock - kv0, Cfg::N), lane);
+        }
         __syncwarp();
         tc::fence_after();
         if (lane == 0) {
@@ -404,23 +406,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
         float sum = 0.f;
-        uint32_t w[SC / 2], wl[Cfg::SPLIT ? SC / 2 : 1];
+        uint32_t w[SC / 2];
 #pragma unroll
         for (int e = 0; e < SC / 2; ++e) {
           const int col = 2 * e;
           const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
           const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
           sum += a0 + a1;
-          w[e] = pack2<Cfg::BF>(a0, a1);
-          if constexpr (Cfg::SPLIT) {
-            const float2 hi = unpack2(BF16{}, w[e]);
-            wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
-          }
+          w[e] = pack_f16x2(a0, a1);
         }
         l = l * alpha + sum;
-        // P over this thread's own (already read) S columns: high part, then residual
+        // P (f16 pairs) over this thread's own (already read) S columns
         tc::st32(scol, w);
-        if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
         // O must hold P . V of the previous tile before it is scaled, and be
         // scaled before P . V of this tile (issued after the arrival below)
         if (rescale && j > 0) {
@@ -428,6 +425,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (!ok) break;
           tc::fence_after();
           scale_o<Cfg>(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC), alpha);
+        }
+        if constexpr (Cfg::VCVT) {  // V of this tile to f16 (its P . V is issued after the arrival below)
+          const int vs = gj % Cfg::VSTAGES;
+          ok = warp_wait(&v_full[vs], (uint32_t)(gj / Cfg::VSTAGES) & 1u, p.timeout_ns);
+          if (!ok) break;
+          const bool big = convert_v_slice<Cfg>(sV + (size_t)vs * Cfg::KV_BYTES, tid,
+                                                it.ctx - (j_first + j) * Cfg::N);
+          if (__any_sync(kFull, big) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_RANGE);
+          fence_proxy_async();
         }
         tc::wait_st();
         tc::fence_before();

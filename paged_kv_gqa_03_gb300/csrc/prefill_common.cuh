@@ -23,10 +23,13 @@
 //  * O is rescaled in tensor memory only when a row's running max grows by
 //    more than 8 (log2 units): the result is exact either way, since P and l
 //    share the stale max, and p <= 2^8 keeps P well inside 16-bit range;
-//  * P must have V's type (kind::f16 takes one type for A and B).  f16 keeps
-//    11 significant bits, enough for the 2e-3 output bound; bf16 keeps 8, so a
-//    bf16 P goes in as a high part plus its bf16 residual, two MMAs on the
-//    same V tile (the weights then carry ~16 bits);
+//  * P must have V's type (kind::f16 takes one type for A and B) and needs
+//    more than bf16's 8 significant bits for the 2e-3 output bound, so P . V
+//    runs in f16: for a bf16 cache the softmax warps convert each V tile to
+//    f16 in shared memory (conflict-free 16-byte chunks, exact for
+//    magnitudes in [2^-14, 65504], larger ones saturate and are flagged)
+//    after its copy lands and before they release the tile's P; stale rows
+//    past a context are zeroed in the same pass;
 //  * warp roles: 0-7 softmax + epilogue, 8 TMA producer, 9 MMA issue and
 //    tensor-memory allocation.  Every wait is bounded; a timeout sets
 //    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
@@ -45,7 +48,11 @@ template <class T, int D_>
 struct PrefillCfg {
   static constexpr int D = D_;
   static constexpr bool BF = T::kCode == PKV_BF16;
-  static constexpr bool SPLIT = BF;                     // P as bf16 high + residual
+  // P . V runs in f16 for both cache types: P (the weights) needs more than
+  // bf16's 8 significant bits for the 2e-3 bound, and kind::f16 takes one
+  // type for A and B, so a bf16 V tile is converted to f16 in shared memory
+  // by the softmax warps (exact for magnitudes in [2^-14, 65504]).
+  static constexpr bool VCVT = BF;
   static constexpr int M = 128;                         // query rows per CTA
   static constexpr int N = 128;                         // cache positions per K / V tile
   static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
@@ -106,20 +113,18 @@ __device__ __forceinline__ void mma_s_tile(uint32_t dS, uint32_t q0, uint32_t k0
   }
 }
 
-// O (+)= P . V of one V tile: P (16-bit pairs) from the S buffer's tensor
-// memory at pb, V (MN-major, at v0) from shared memory; a bf16 P is its high
-// part plus its residual, two MMAs per k-step.  `accumulate` false starts O
-// afresh.  Issued by one thread.
+// O (+)= P . V of one V tile: P (f16 pairs) from the S buffer's tensor
+// memory at pb, V (f16, MN-major, at v0) from shared memory.  `accumulate`
+// false starts O afresh.  Issued by one thread.
 template <class Cfg>
 __device__ __forceinline__ void mma_pv_tile(uint32_t dO, uint32_t pb, uint32_t v0, bool accumulate) {
-  constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);
+  constexpr uint32_t idO = tc::idesc_f16(false, Cfg::M, Cfg::D, true);  // f16 P and V
 #pragma unroll
   for (int k = 0; k < Cfg::N / 16; ++k) {
     // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
     const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
     const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
     tc::mma_f16_tmem_a(dO, pb + pcol, dv, idO, (accumulate || k > 0) ? 1u : 0u);
-    if constexpr (Cfg::SPLIT) tc::mma_f16_tmem_a(dO, pb + pcol + Cfg::N / 4, dv, idO, 1u);
   }
 }
 
@@ -150,6 +155,40 @@ __device__ __forceinline__ void scale_o(uint32_t ta, float alpha) {
     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
     tc::st32(ta + (uint32_t)(q * 32), o);
   }
+}
+
+// The SOFTMAX softmax threads convert a bf16 V tile to f16 in place, thread
+// tid taking the 16-byte chunks tid, tid + SOFTMAX, ... (a warp's accesses
+// are contiguous: no bank conflicts); chunks of rows at or past zero_from
+// (stale positions past the context) become 0 instead.  Elementwise, so the
+// 128-byte swizzle is unaffected.  Returns true if a value's magnitude
+// exceeds 65504 (converted with saturation).
+template <class Cfg>
+__device__ __forceinline__ bool convert_v_slice(uint8_t *vt, int tid, int zero_from) {
+  constexpr int CHUNKS = Cfg::KV_BYTES / 16 / Cfg::SOFTMAX;
+  static_assert(Cfg::KV_BYTES % (16 * Cfg::SOFTMAX) == 0, "whole chunks per thread");
+  const uint32_t base = smem_u32(vt);
+  bool big = false;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const int i = c * Cfg::SOFTMAX + tid;                // 16-byte chunk of the tile
+    const int row = (i * 16 % Cfg::PANEL_KV) / 128;      // its cache position in the tile
+    uint4 y = make_uint4(0, 0, 0, 0);
+    if (row < zero_from) {
+      const uint4 x = lds128(base + 16 * i);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+        big |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
+        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[e]) : "f"(hi), "f"(lo));
+      }
+      y = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    sts128(base + 16 * i, y);
+  }
+  return big;
 }
 
 }  // namespace pkv

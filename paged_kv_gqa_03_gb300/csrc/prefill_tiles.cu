@@ -198,8 +198,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (!ok) break;
       if (lane == 0) v_consumed = j + 1;
       uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-      const int kv0 = (j_first + j) * Cfg::N;  // first position of the tile
-      zero_v_rows<Cfg>(vt, ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
+      if constexpr (!Cfg::VCVT) {  // (with the conversion the softmax warps zero them)
+        const int kv0 = (j_first + j) * Cfg::N;  // first position of the tile
+        zero_v_rows<Cfg>(vt, ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
+      }
       __syncwarp();
       tc::fence_after();
       if (lane == 0) {
@@ -277,17 +279,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       float sum = 0.f;
-      uint32_t w[NV / 2], wl[Cfg::SPLIT ? NV / 2 : 1];
+      uint32_t w[NV / 2];
 #pragma unroll
       for (int e = 0; e < NV / 2; ++e) {
         const float a0 = ex2(fmaf(__uint_as_float(s[2 * e]), c, -mu));
         const float a1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), c, -mu));
         sum += a0 + a1;
-        w[e] = pack2<Cfg::BF>(a0, a1);
-        if constexpr (Cfg::SPLIT) {
-          const float2 hi = unpack2(BF16{}, w[e]);
-          wl[e] = pack_bf16x2(a0 - hi.x, a1 - hi.y);
-        }
+        w[e] = pack_f16x2(a0, a1);
       }
       if (rescale && j > 0) {  // O must hold P . V of the previous tile before it is scaled
         ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
@@ -296,10 +294,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         scale_o<Cfg>(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC), alpha);
       }
       l = l * alpha + sum;
-      // P over this thread's own (already read) S columns: high part, then residual
+      // P (f16 pairs) over this thread's own (already read) S columns
       if constexpr (REP == 1) {
         tc::st32(scol, w);
-        if constexpr (Cfg::SPLIT) tc::st32(scol + (uint32_t)(SC / 2), wl);
       } else {
         // 8 packed columns per k-step: this replica's k-steps, zeros in the others
 #pragma unroll
@@ -307,17 +304,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const uint32_t pc = scol + (uint32_t)((rep + t * REP) * 8);
           const uint32_t *v = &w[t * 8];
           tc::st8(pc, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
-          if constexpr (Cfg::SPLIT) {
-            const uint32_t *u = &wl[t * 8];
-            tc::st8(pc + (uint32_t)(SC / 2), u[0], u[1], u[2], u[3], u[4], u[5], u[6], u[7]);
-          }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (q % REP != rep) {
             tc::st8(scol + (uint32_t)(q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
-            if constexpr (Cfg::SPLIT) tc::st8(scol + (uint32_t)(SC / 2 + q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
           }
+      }
+      if constexpr (Cfg::VCVT) {  // V of this tile to f16 (its P . V is issued after the arrival below)
+        const int vs = j % Cfg::VSTAGES;
+        ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+        if (!ok) break;
+        const bool big = convert_v_slice<Cfg>(sV + (size_t)vs * Cfg::KV_BYTES, tid,
+                                              ctx - (j_first + j) * Cfg::N);
+        if (__any_sync(kFull, big) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_RANGE);
+        fence_proxy_async();
       }
       tc::wait_st();
       tc::fence_before();

@@ -172,3 +172,18 @@ def test_prefill_few_rows_without_context():
     ref = oracle.prefill(c["q"], "bf16", c["kc"], c["vc"], "bf16", c["table"], c["ctx"], c["q_start"],
                          scale=1.0 / math.sqrt(128))
     compare(out, ref, "bf16", "few rows, no context")
+
+
+def test_prefill_bf16_v_beyond_f16_range_is_flagged():
+    """A bf16 V value above 65504 in magnitude cannot enter the f16 P . V:
+    it saturates and PKV_FLAG_RANGE is set; the outputs stay finite and a
+    sequence whose V stays in range is still exact."""
+    c = make_prefill(29, [40, 30], [100, 20], 8, 2, 128, "bf16")
+    vc = c["vc"].clone()
+    vc[int(c["table"][0, 2]), 1, 5, 7] = 1.0e5          # sequence 0, position 37, kv head 1
+    out, status = run_gpu(dict(c, vc=vc))
+    assert status == _pkv().PKV_FLAG_RANGE
+    assert torch.isfinite(out.float()).all()
+    ref = oracle.prefill(c["q"], "bf16", c["kc"], vc, "bf16", c["table"], c["ctx"], c["q_start"],
+                         scale=1.0 / math.sqrt(128))
+    compare(out[40:], ref[40:], "bf16", "sequence without the large value")
