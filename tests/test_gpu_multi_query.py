@@ -198,3 +198,16 @@ def test_multi_query_tensor_core_route(dtype, D, window, kernel, monkeypatch):
                 min_free=16, window=window)
     for seed, splits in ((61, 0), (62, 7)):
         _check_step(workloads.make(spec, seed=seed), num_splits=splits)
+
+
+@pytest.mark.parametrize("dtype,D,q_len,window", [("bf16", 128, 5, 0), ("bf16", 128, 3, 37), ("f16", 64, 4, 0)])
+def test_multi_query_ragged_contexts_wide_table(dtype, D, q_len, window):
+    """160 (sequence, kv head) items under a block table admitting 8000
+    positions (one long sequence, so the one-CTA-per-item kernel with row
+    replicas serves them) and ragged contexts (q_len .. 3000, many items of
+    a single tile); every output against the oracle."""
+    rng = np.random.default_rng(5)
+    ctx = [8000] + [int(x) for x in rng.integers(q_len, 3000, 39)]
+    spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=q_len, ctx=ctx, free_frac=0.2, min_free=16,
+                window=window)
+    _check_step(workloads.make(spec, seed=71))
