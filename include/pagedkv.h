@@ -156,7 +156,12 @@ int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
 /*
  * Decode attention for one query token per sequence.
  *
- *   out        [B][Hq][D], dtype = q_dtype (fp32 results rounded to nearest even)
+ *   out        [B][Hq][D], dtype = q_dtype (fp32 results rounded to nearest even);
+ *              device memory, or pinned host memory (cudaHostAlloc / torch
+ *              pin_memory, addressed by the GPU under unified addressing):
+ *              the kernels then write the rows over the host link, which
+ *              spares a device-to-host copy of the output (any entry point
+ *              that writes `out`: the multi-query and prefill calls too)
  *   q          [B][Hq][D]; q_dtype: F32 with an F32 cache, else F16/BF16;
  *              must equal cache_dtype for F16/BF16 caches.
  *   k_cache, v_cache  [num_blocks][Hkv][16][D] of cache_dtype

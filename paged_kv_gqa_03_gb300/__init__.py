@@ -135,6 +135,18 @@ def _dev(t, name, dtype=None):
     return t.data_ptr()
 
 
+def _out(t):
+    """The output pointer of a decode call: a CUDA tensor, or pinned host
+    memory that the kernels write directly (see include/pagedkv.h)."""
+    if t.is_cuda:
+        return _dev(t, "out")
+    if not t.is_pinned():
+        raise ValueError("out must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError("out must be contiguous")
+    return t.data_ptr()
+
+
 def _stream(stream):
     if stream is None:
         return _torch().cuda.current_stream().cuda_stream
@@ -204,11 +216,11 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
     tail = (num_blocks, float(scale), num_splits, _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _stream(stream))
     if q.dim() == 4 or window:
-        _check(_L.paged_decode_attention_multi(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
+        _check(_L.paged_decode_attention_multi(_out(out), _dev(q, "q"), _code(q), *args,
                                                B, q_len, int(window), Hq, Hkv, D, *tail),
                "paged_decode_attention_multi")
     else:
-        _check(_L.paged_decode_attention(_dev(out, "out"), _dev(q, "q"), _code(q), *args,
+        _check(_L.paged_decode_attention(_out(out), _dev(q, "q"), _code(q), *args,
                                          B, Hq, Hkv, D, *tail), "paged_decode_attention")
     return workspace
 
@@ -226,7 +238,7 @@ def paged_prefill_attention(out, q, k_cache, v_cache, block_table, context_lens,
     B = q_start.shape[0] - 1
     num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
     _check(_L.paged_prefill_attention(
-        _dev(out, "out"), _dev(q, "q"), _code(q), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _out(out), _dev(q, "q"), _code(q), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _code(k_cache), _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _dev(context_lens, "context_lens", torch.int32), _dev(q_start, "q_start", torch.int32),
         B, int(max_q_len), Hq, Hkv, D, num_blocks, float(scale), int(window),

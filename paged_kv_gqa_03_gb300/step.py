@@ -198,11 +198,14 @@ class DecodeStep:
     def capture(self, h_out):
         """Captures one full step from the current staging buffer — one
         host->device copy of q, k_new, v_new (written into h_q / h_k_new /
-        h_v_new) and the bookkeeping, the append, the attention, and one
-        device->host copy of the output into the pinned tensor h_out — as a
-        CUDA graph; replay() runs it.  Re-capture after a prepare() that
-        switches staging buffers or changes the copy pairs."""
-        self.g_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=self.device)
+        h_v_new) and the bookkeeping, the append, and the attention writing
+        its output straight into the pinned tensor h_out over the host link
+        (no separate device->host copy) — as a CUDA graph; replay() runs it.
+        Re-capture after a prepare() that switches staging buffers or changes
+        the copy pairs."""
+        if not h_out.is_pinned():
+            raise ValueError("h_out must be pinned host memory")
+        self.g_out = h_out
         self._graph_body(h_out)          # eager once: kernels configured, tensor maps encoded
         self.stream.synchronize()
         graph = torch.cuda.CUDAGraph()
@@ -213,8 +216,7 @@ class DecodeStep:
 
     def _graph_body(self, h_out):
         self._copy_in(with_inputs=True)
-        self.launch(self.d_q, self.d_k_new, self.d_v_new, self.g_out)
-        pkv_copy(h_out, self.g_out, stream=self.stream)
+        self.launch(self.d_q, self.d_k_new, self.d_v_new, h_out)
 
     def replay(self):
         with torch.cuda.stream(self.stream):

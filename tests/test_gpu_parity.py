@@ -325,3 +325,33 @@ def test_sm_copy_between_pinned_host_and_device_is_exact():
     assert torch.equal(back, src_host)
     with pytest.raises(pkv.PagedKVError):
         pkv.pkv_copy(dev, src_host, nbytes=7)   # not a multiple of 16 bytes
+
+
+@pytest.mark.parametrize("spec", [
+    dict(B=64, Hq=64, Hkv=8, D=128, dtype="bf16", ctx_range=(1, 3000)),                 # splits + merge
+    dict(B=6, Hq=32, Hkv=32, D=128, dtype="f16", ctx_range=(1, 500)),                   # MHA (CUDA cores)
+    dict(B=48, Hq=64, Hkv=8, D=128, dtype="bf16", q_len=4, ctx_range=(4, 9000)),        # tensor-core route
+    dict(B=8, Hq=32, Hkv=8, D=128, dtype="fp8_e4m3", q_dtype="bf16", ctx_range=(1, 2000)),
+], ids=lambda s: f"{s['dtype']}-q{s['Hq']}-kv{s['Hkv']}-L{s.get('q_len', 1)}")
+def test_output_into_pinned_host_memory_is_identical(spec):
+    """out may be pinned host memory: the kernels write the rows over the
+    host link.  The bytes equal those of the same call into device memory."""
+    pkv = _pkv()
+    dev = "cuda"
+    spec = dict(spec)
+    spec.setdefault("q_dtype", spec["dtype"])
+    spec.update(free_frac=0.2, min_free=4)
+    w = workloads.make(spec, seed=83)
+    table = np.full((w.B, w.max_blocks), -1, dtype=np.int32)
+    for b in range(w.B):
+        table[b, :len(w.tables[b])] = w.tables[b]
+    args = (w.k_cache.to(dev), w.v_cache.to(dev), torch.from_numpy(table).to(dev),
+            torch.tensor(w.context_lens, dtype=torch.int32, device=dev), w.scale,
+            None if w.k_scale is None else w.k_scale.to(dev), None if w.v_scale is None else w.v_scale.to(dev))
+    q = w.q.to(dev)
+    d_out = torch.empty_like(q)
+    h_out = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
+    pkv.paged_decode_attention(d_out, q, *args)
+    pkv.paged_decode_attention(h_out, q, *args)
+    torch.cuda.synchronize()
+    assert torch.equal(d_out.cpu().view(torch.int16), h_out.view(torch.int16))
