@@ -463,7 +463,8 @@ def prefill_kernel_name(c):
     when the block table admits a cached prefix of 2048+ positions before
     the new tokens, the persistent kernel otherwise (unless overridden)."""
     force = os.environ.get("PKV_PREFILL_KERNEL", "")
-    tiles = c["table"].shape[1] * 16 - max(c["n"]) >= 2048
+    G = c["Hq"] // c["Hkv"]
+    tiles = c["table"].shape[1] * 16 - max(c["n"]) >= (1024 if max(c["n"]) * G <= 64 else 2048)
     if force in ("tiles", "persistent"):
         tiles = force == "tiles"
     return ("prefill_tile_kernel (tcgen05, one CTA per work item)" if tiles

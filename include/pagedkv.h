@@ -278,7 +278,8 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
  *
  * Two kernels run the same tile pipeline: one CTA per (128-row tile, kv
  * head, sequence), chosen when max_blocks_per_seq * 16 - max_q_len >= 2048
- * (the table admits a long cached prefix, so the items are long), and one
+ * (the table admits a long cached prefix, so the items are long; 1024 when
+ * max_q_len * Hq / Hkv <= 64, where it runs row replicas), and one
  * persistent CTA per SM walking those items otherwise (prompts: many short
  * items of unequal length).  The environment variable PKV_PREFILL_KERNEL =
  * "tiles" or "persistent" overrides the choice; results agree within the

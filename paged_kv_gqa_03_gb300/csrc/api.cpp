@@ -354,11 +354,16 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
 // items) saves each item's start-up and balances short items of unequal
 // length: prompts without a long prefix.  The longest context the block
 // table can describe (max_blocks * block size) less the new tokens bounds
-// the prefix; a bound of 2048 positions or more picks one CTA per item.
+// the prefix; a bound of 2048 positions or more picks one CTA per item, or
+// 1024 for items of at most 64 rows (a few new tokens of one group), which
+// that kernel serves with row replicas (measured on 70B-layer shapes: at
+// 1024 positions the two kernels tie, at 1500 one CTA per item is 11 %
+// faster, at 300-512 the persistent kernel is 14-15 % faster).
 // PKV_PREFILL_KERNEL=persistent|tiles in the environment overrides the choice.
 static cudaError_t launch_prefill_auto(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK,
                                        const CUtensorMap &tmV, cudaStream_t s) {
-  bool tiles = (int64_t)p.max_blocks * kBlock - p.max_q_len >= 2048;
+  const int64_t bound = (int64_t)p.max_q_len * p.G <= 64 ? 1024 : 2048;
+  bool tiles = (int64_t)p.max_blocks * kBlock - p.max_q_len >= bound;
   if (const char *force = std::getenv("PKV_PREFILL_KERNEL")) {
     if (!std::strcmp(force, "tiles")) tiles = true;
     if (!std::strcmp(force, "persistent")) tiles = false;
