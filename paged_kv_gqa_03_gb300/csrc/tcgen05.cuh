@@ -128,19 +128,5 @@ __device__ __forceinline__ void st8(uint32_t taddr, uint32_t v0, uint32_t v1, ui
                : "memory");
 }
 
-// Warp-wide: one 32-bit column of the warp's 32 lanes (load and wait).
-__device__ __forceinline__ uint32_t ld1(uint32_t taddr) {
-  uint32_t r;
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r)
-      : "r"(taddr));
-  return r;
-}
-__device__ __forceinline__ void st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 }  // namespace tc
 }  // namespace pkv
