@@ -171,38 +171,49 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       bad |= good ? 0 : 1;
       return good ? (int64_t)id * p.Hkv + ct.h : p.num_blocks * p.Hkv;
     };
-    bool have = step(), ok = true;
-    int64_t trow = have ? block_row() : 0;
-    for (int g = 0; have; ++g) {
-      const bool have_next = step();
-      const int64_t next = have_next ? block_row() : 0;
-      const int ks = g % Cfg::KSTAGES, vs = g % Cfg::VSTAGES;
-      if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
-      if (__any_sync(kFull, *(volatile int *)&abort_flag)) {
-        ok = false;
-        break;
-      }
+    // K runs one tile ahead of V: K(g+1) goes out before V(g), so it waits
+    // only for its own slot (S(g-2) done) and not behind V(g)'s (P . V(g-2)
+    // done); the cursor reads block ids two tiles ahead
+    auto issue_k = [&](int g, int64_t trow) -> bool {
+      const int ks = g % Cfg::KSTAGES;
+      if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
+        return false;
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
         tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
                     (int)(trow * kBlock), &k_full[ks]);
       if (lane == 0) k_issued = g + 1;
-      if (g >= Cfg::VSTAGES && !warp_wait(&v_empty[vs], (uint32_t)((g / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
+      return true;
+    };
+    auto issue_v = [&](int g, int64_t trow) -> bool {
+      const int vs = g % Cfg::VSTAGES;
+      if (g >= Cfg::VSTAGES && !warp_wait(&v_empty[vs], (uint32_t)((g / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
+        return false;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
         tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
                     (int)(trow * kBlock), &v_full[vs]);
       if (lane == 0) v_issued = g + 1;
-      trow = next;
-      have = have_next;
+      return true;
+    };
+    bool ok = true;
+    bool h0 = step();  // tiles g and g + 1 exist (cursor one tile further on)
+    int64_t r0 = h0 ? block_row() : 0;
+    bool h1 = h0 && step();
+    int64_t r1 = h1 ? block_row() : 0;
+    if (h0) ok = issue_k(0, r0);
+    for (int g = 0; h0 && ok; ++g) {
+      const bool h2 = h1 && step();
+      const int64_t r2 = h2 ? block_row() : 0;
+      if (h1 && !(ok = issue_k(g + 1, r1))) break;
+      if (!(ok = issue_v(g, r0))) break;
+      h0 = h1;
+      r0 = r1;
+      h1 = h2;
+      r1 = r2;
     }
     if (__any_sync(kFull, bad)) {
       if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
