@@ -162,31 +162,40 @@ __device__ __forceinline__ void scale_o(uint32_t ta, float alpha) {
 // are contiguous: no bank conflicts); chunks of rows at or past zero_from
 // (stale positions past the context) become 0 instead.  Elementwise, so the
 // 128-byte swizzle is unaffected.  Returns true if a value's magnitude
-// exceeds 65504 (converted with saturation).
+// exceeds 65504 (converted with saturation).  The shared-memory accessors
+// are volatile asm, which keeps their order, so the chunks go in batches of
+// four loads ahead of their stores: one load latency per batch, not per chunk.
 template <class Cfg>
 __device__ __forceinline__ bool convert_v_slice(uint8_t *vt, int tid, int zero_from) {
   constexpr int CHUNKS = Cfg::KV_BYTES / 16 / Cfg::SOFTMAX;
+  constexpr int BATCH = 4;
   static_assert(Cfg::KV_BYTES % (16 * Cfg::SOFTMAX) == 0, "whole chunks per thread");
+  static_assert(CHUNKS % BATCH == 0, "whole batches per thread");
   const uint32_t base = smem_u32(vt);
   bool big = false;
 #pragma unroll
-  for (int c = 0; c < CHUNKS; ++c) {
-    const int i = c * Cfg::SOFTMAX + tid;                // 16-byte chunk of the tile
-    const int row = (i * 16 % Cfg::PANEL_KV) / 128;      // its cache position in the tile
-    uint4 y = make_uint4(0, 0, 0, 0);
-    if (row < zero_from) {
-      const uint4 x = lds128(base + 16 * i);
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-      uint32_t h[4];
+  for (int c0 = 0; c0 < CHUNKS; c0 += BATCH) {
+    uint4 x[BATCH];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-        big |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
-        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[e]) : "f"(hi), "f"(lo));
+    for (int k = 0; k < BATCH; ++k) x[k] = lds128(base + 16 * ((c0 + k) * Cfg::SOFTMAX + tid));
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
+      const int i = (c0 + k) * Cfg::SOFTMAX + tid;       // 16-byte chunk of the tile
+      const int row = (i * 16 % Cfg::PANEL_KV) / 128;    // its cache position in the tile
+      uint4 y = make_uint4(0, 0, 0, 0);
+      if (row < zero_from) {
+        const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+          big |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
+          asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[e]) : "f"(hi), "f"(lo));
+        }
+        y = make_uint4(h[0], h[1], h[2], h[3]);
       }
-      y = make_uint4(h[0], h[1], h[2], h[3]);
+      sts128(base + 16 * i, y);
     }
-    sts128(base + 16 * i, y);
   }
   return big;
 }
