@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "pagedkv.h"
+#include "mq_decode.h"
 #include "prefill.h"
 
 namespace pkv {
@@ -105,6 +106,22 @@ int kernel_occupancy(int ki, int *ctas_per_sm, int *sm_count) {
   }
   *ctas_per_sm = f.ctas_per_sm[ki];
   *sm_count = f.sm_count;
+  return PKV_OK;
+}
+
+// The current device's SM count (cached).
+int sm_count(int *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return PKV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceFacts &f = g_dev[dev];
+  if (f.sm_count == 0) {
+    e = cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  *out = f.sm_count;
   return PKV_OK;
 }
 
@@ -310,7 +327,16 @@ int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
   int P = 0;
   rc = plan_call(cache_dtype, q_dtype, B, q_len, Hq, Hkv, D, num_splits, &c, &P);
   if (rc != PKV_OK) return rc;
-  *bytes_out = ws_layout(B, P, D).total;
+  size_t total = ws_layout(B, P, D).total;
+  if (q_len >= 2 && num_splits == 0 && D == kMqHeadDim && q_len * (Hq / Hkv) <= kMqRows && B <= kMqMaxBatch &&
+      (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16)) {
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    const size_t mq = mq_ws_layout(B, sms).total;  // the transposed kernel's partials
+    if (mq > total) total = mq;
+  }
+  *bytes_out = total;
   return PKV_OK;
 }
 
@@ -393,27 +419,75 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
     return PKV_EWORKSPACE;
   if (q_len >= 2 && num_splits == 0) {
-    // Several new tokens per sequence on a 16-bit cache: the tensor-core
-    // prefill kernel streams each (sequence, kv head)'s K/V once for all of
-    // its q_len * G rows (the 8-row units below stream it once per unit).
-    // Used when its grid of (sequence, kv head, 128-row tile) CTAs fills the
-    // GPU; it has no split over the context.
-    int sms = 0, dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_status(e);
+    // Several new tokens per sequence on a 16-bit cache: a tensor-core
+    // kernel streams each (sequence, kv head)'s K/V once for all of its
+    // q_len * G rows (the 8-row units below stream it once per unit).
+    //  * up to 32 rows and head dim 128: the transposed kernel (positions on
+    //    the tensor core's M side, stream-K over every item's tiles, so any
+    //    batch fills the GPU);
+    //  * otherwise the prefill kernel with 128-row tiles, when its grid of
+    //    (sequence, kv head, row tile) items fills the GPU (no context split;
+    //    on the 70B layer at 64 rows it is faster than the transposed kernel,
+    //    whose softmax work grows with the rows);
+    //  * the transposed kernel for 33-64 rows on grids the prefill kernel
+    //    cannot fill.
+    // PKV_MULTI_KERNEL=transposed|prefill|units in the environment forces one
+    // route where it applies (for measurement and tests).
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    const char *force = std::getenv("PKV_MULTI_KERNEL");
+    const bool units = force && !std::strcmp(force, "units");
+    const bool no_mq = units || (force && !std::strcmp(force, "prefill"));
+    const bool want_mq = force && !std::strcmp(force, "transposed");
     const int G = Hq / Hkv;
+    const int R = q_len * G;
     const int64_t tiles = ((int64_t)q_len * G + 127) / 128;
-    if ((cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && B <= 65535 &&
-        (int64_t)B * Hkv * tiles >= sms) {
+    const bool prefill_fills = (int64_t)B * Hkv * tiles >= sms && B <= 65535;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!no_mq && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && D == kMqHeadDim &&
+        R <= kMqRows && B <= kMqMaxBatch && (R <= 32 || !prefill_fills || want_mq)) {
+      const MqWsLayout M = mq_ws_layout(B, sms);
+      if (workspace_bytes >= M.total) {
+        CUtensorMap tmK, tmV;
+        rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+        if (rc != PKV_OK) return rc;
+        rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+        if (rc != PKV_OK) return rc;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        MqParams mp;
+        std::memset(&mp, 0, sizeof(mp));
+        mp.out = out;
+        mp.q = q;
+        mp.block_table = block_table;
+        mp.context_lens = context_lens;
+        mp.status = &reinterpret_cast<WsHeader *>(ws)->status;
+        mp.cta_flags = reinterpret_cast<int32_t *>(ws + M.cta_flags);
+        mp.prefix = reinterpret_cast<int32_t *>(ws + M.prefix);
+        mp.part_o = reinterpret_cast<float *>(ws + M.part_o);
+        mp.part_lse = reinterpret_cast<float *>(ws + M.part_lse);
+        mp.num_blocks = num_blocks;
+        mp.B = B;
+        mp.q_len = q_len;
+        mp.Hq = Hq;
+        mp.Hkv = Hkv;
+        mp.G = G;
+        mp.R = R;
+        mp.max_blocks = max_blocks_per_seq;
+        mp.window = window < (1 << 30) ? window : 0;
+        mp.scale_log2 = scale * 1.4426950408889634f;
+        mp.timeout_ns = 4000000000ull;
+        return cuda_status(launch_mq_decode(mp, cache_dtype, tmK, tmV, sms, s));
+      }
+    }
+    if (!units && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && prefill_fills) {
       CUtensorMap tmK, tmV;
       rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
       if (rc != PKV_OK) return rc;
       rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
       if (rc != PKV_OK) return rc;
-      cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
       WsHeader *hdr = reinterpret_cast<WsHeader *>(static_cast<uint8_t *>(workspace) + L.hdr);
-      e = cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s);
+      cudaError_t e = cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s);
       if (e != cudaSuccess) return cuda_status(e);
       PrefillParams pp;
       std::memset(&pp, 0, sizeof(pp));

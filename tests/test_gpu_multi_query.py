@@ -194,20 +194,92 @@ def test_multi_query_tensor_core_route(dtype, D, window, kernel, monkeypatch):
     (each of the two), with a fixed split count the 8-row-unit decode kernel;
     both against the oracle."""
     monkeypatch.setenv("PKV_PREFILL_KERNEL", kernel)
+    monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
     spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=5, ctx_range=(5, 300), free_frac=0.3,
                 min_free=16, window=window)
     for seed, splits in ((61, 0), (62, 7)):
         _check_step(workloads.make(spec, seed=seed), num_splits=splits)
 
 
+@pytest.mark.parametrize("route", ["transposed", "prefill"])
 @pytest.mark.parametrize("dtype,D,q_len,window", [("bf16", 128, 5, 0), ("bf16", 128, 3, 37), ("f16", 64, 4, 0)])
-def test_multi_query_ragged_contexts_wide_table(dtype, D, q_len, window):
+def test_multi_query_ragged_contexts_wide_table(dtype, D, q_len, window, route, monkeypatch):
     """160 (sequence, kv head) items under a block table admitting 8000
     positions (one long sequence, so the one-CTA-per-item kernel with row
     replicas serves them) and ragged contexts (q_len .. 3000, many items of
     a single tile); every output against the oracle."""
     rng = np.random.default_rng(5)
     ctx = [8000] + [int(x) for x in rng.integers(q_len, 3000, 39)]
+    if route == "prefill":
+        monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
     spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=q_len, ctx=ctx, free_frac=0.2, min_free=16,
                 window=window)
     _check_step(workloads.make(spec, seed=71))
+
+
+# The transposed tensor-core kernel (positions on the M side, stream-K over
+# every (sequence, kv head) item's K / V tiles, the merge of items cut between
+# CTAs) serves 16-bit caches with head dim 128: up to 32 query rows per kv head
+# by default, up to 64 where the 128-row prefill route cannot fill the GPU.
+@pytest.mark.parametrize("dtype,Hq,Hkv,q_len,ctx,window", [
+    ("bf16", 2, 2, 2, [2, 130, 1000], 0),                   # MHA, R = 2 (16-row S^T, mostly padding)
+    ("bf16", 16, 2, 2, [2, 129, 4000, 77], 0),              # R = 16
+    ("f16", 16, 2, 2, [2, 129, 4000, 77], 0),
+    ("bf16", 32, 4, 4, [4, 500, 2048, 3333, 7], 0),         # R = 32
+    ("f16", 32, 4, 4, [4, 500, 2048, 3333, 7], 37),
+    ("bf16", 40, 8, 7, [7, 300, 1500], 0),                  # R = 35: 64-row S^T
+    ("bf16", 48, 3, 3, [3, 900, 260], 100),                 # R = 48, window
+    ("bf16", 64, 8, 8, [8, 1200, 5000, 64], 0),             # R = 64
+    ("f16", 64, 8, 8, [8, 1200, 5000, 64], 1),              # window 1: token i sees only itself
+], ids=lambda v: str(v))
+def test_transposed_kernel_rows_windows_dtypes(dtype, Hq, Hkv, q_len, ctx, window):
+    """Every output against the oracle for 2 to 64 query rows per kv head
+    (non-power-of-two counts padded), windows, bf16 (P as high part +
+    residual) and f16; few items, so most CTAs' ranges are empty or cut an
+    item."""
+    spec = dict(B=len(ctx), Hq=Hq, Hkv=Hkv, D=128, dtype=dtype, q_len=q_len, ctx=ctx, free_frac=0.3,
+                min_free=16, window=window)
+    _check_step(workloads.make(spec, seed=81))
+
+
+@pytest.mark.parametrize("ctx", [[100000], [60000, 4, 45000]])
+def test_transposed_kernel_item_cut_across_every_cta(ctx):
+    """One kv head of one long sequence holds most of the tiles, so its
+    item is cut across (nearly) every CTA and the merge combines up to 152
+    partials per row."""
+    spec = dict(B=len(ctx), Hq=8, Hkv=1, D=128, dtype="bf16", q_len=4, ctx=ctx, free_frac=0.05, min_free=16)
+    _check_step(workloads.make(spec, seed=83))
+
+
+def test_transposed_kernel_flags_a_bad_block_id():
+    """A block id past the pool reads as zeros and raises PKV_FLAG_BAD_BLOCK
+    in the call's status; the other sequence is exact."""
+    pkv = _pkv()
+    dev = "cuda"
+    g = torch.Generator().manual_seed(13)
+    B, L, Hq, Hkv, D, nb = 2, 3, 8, 2, 128, 8
+    q = torch.randn((B, L, Hq, D), generator=g).to(torch.bfloat16)
+    kc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((nb, Hkv, 16, D), generator=g).to(torch.bfloat16)
+    table = torch.tensor([[0, 1, 2], [3, nb + 5, 4]], dtype=torch.int32)
+    lens = torch.tensor([40, 40], dtype=torch.int32)
+    out = torch.empty_like(q, device=dev)
+    ws = pkv.paged_decode_attention(out, q.to(dev), kc.to(dev), vc.to(dev), table.to(dev), lens.to(dev), 0.1)
+    rc, flags = pkv.paged_decode_status(ws)
+    assert flags & pkv.PKV_FLAG_BAD_BLOCK
+    ref = oracle.decode(q[:1], "bf16", kc, vc, "bf16", table[:1].numpy(), lens[:1].numpy(), scale=0.1)
+    compare(out[:1], ref, "bf16", "the good sequence")
+
+
+@pytest.mark.parametrize("q_len,B", [(4, 16), (8, 20)])
+def test_transposed_kernel_equals_the_prefill_route(q_len, B, monkeypatch):
+    """The same 70B-shaped call (B sequences of 8192) through the transposed
+    kernel and the 128-row prefill route, each forced: both within the bound
+    of the oracle.  (At 64 rows with 160 items the prefill route is the
+    default.)"""
+    w = workloads.config(3, B=B, q_len=q_len)
+    monkeypatch.setenv("PKV_MULTI_KERNEL", "transposed")
+    a = _check_step(w)
+    monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
+    b = _check_step(w)
+    print(a, b)
