@@ -21,8 +21,9 @@
 //    between the four warps of a half; the row sum stays per thread until an
 //    item ends;
 //  * O^T += V^T . P^T: A = the V tile read MN-major (the head dim contiguous),
-//    B = P^T written by the softmax threads as one 128-byte row per position
-//    (MN-major, the query rows contiguous, padded to 64).  For a bf16 cache P
+//    B = P^T written by the softmax threads as one row of NR 16-bit values per
+//    position (MN-major, the query rows contiguous; 32 / 64 / 128-byte
+//    swizzle for NR = 16 / 32 / 64).  For a bf16 cache P
 //    goes in as a bf16 high part plus its bf16 residual (two MMAs per k-step,
 //    ~16 significant bits; bf16 alone gives 8, too few for the 2e-3 bound), so
 //    V needs no conversion; an f16 cache takes f16 P directly;
@@ -31,9 +32,10 @@
 //    item cut by a range end is finished by the merge kernel from the CTAs'
 //    normalised partial outputs and log-sum-exps;
 //  * warp roles: 0-7 softmax / epilogue / Q staging, 8 TMA producer (K one
-//    tile ahead of V, block ids read two tiles ahead), 9 MMA issue and tensor-memory allocation.  Every
-//    wait is bounded; a timeout sets PKV_FLAG_TIMEOUT, and the CTA drains its
-//    copies and MMAs and frees its tensor memory.
+//    tile ahead of V; block ids loaded three tiles ahead and first used when
+//    the copies are issued), 9 S^T issue and tensor-memory allocation, 10
+//    P . V issue.  Every wait is bounded; a timeout sets PKV_FLAG_TIMEOUT, and
+//    the CTA drains its copies and MMAs and frees its tensor memory.
 #include <math.h>
 
 #include "mq_decode.h"
@@ -47,7 +49,9 @@ struct MqCfg {
   static constexpr bool BF = T::kCode == PKV_BF16;
   static constexpr int NRH = NRH_;                      // query rows of one softmax half
   static constexpr int NR = 2 * NRH;                    // S^T columns (rows padded)
-  static constexpr int NPV = 64;                        // P^T columns (rows padded to one 128-byte row)
+  static constexpr int NPV = NR;                        // P^T columns (the padded rows)
+  static constexpr int P_ROW = 2 * NR;                  // bytes of one position's P^T row: 32 / 64 / 128
+  static constexpr uint32_t P_LAYOUT = NR == 16 ? 6u : (NR == 32 ? 4u : 2u);  // 32 / 64 / 128-byte swizzle
   static constexpr int N = 128;                         // positions per K / V tile
   static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
   static constexpr int PANELS = D / 64;                 // 128-byte panels per K / V row
@@ -56,14 +60,19 @@ struct MqCfg {
   static constexpr int PANEL_Q = NR * 128;
   static constexpr int Q_BYTES = PANELS * PANEL_Q;
   static constexpr int PARTS = BF ? 2 : 1;              // P: bf16 high part + residual, or f16
-  static constexpr int P_PART = N * 128;                // 128 positions x 64 rows x 2 bytes
+  static constexpr int P_PART = N * P_ROW;
   static constexpr int P_BYTES = PARTS * P_PART;
-  static constexpr int KSTAGES = 2, VSTAGES = 3, PBUF = 1, SBUF = 2;
-  static constexpr int QBUF = NR <= 32 ? 2 : 1;
+  // rings as deep as shared memory allows: a V slot is held from its copy to
+  // the end of its P . V, so V gets the depth
+  static constexpr int KSTAGES = NR <= 32 ? 3 : 2, VSTAGES = 3, PBUF = NR <= 16 ? 2 : 1, SBUF = 2;
+  static constexpr int QBUF = NR <= 16 ? 2 : 1;
   static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
-  static constexpr size_t PREFIX_BYTES = 4 * (kMqMaxBatch + 1);
   static constexpr size_t SMEM = 1024 + (size_t)(KSTAGES + VSTAGES) * KV_BYTES + (size_t)PBUF * P_BYTES +
-                                 (size_t)QBUF * Q_BYTES + PREFIX_BYTES;
+                                 (size_t)QBUF * Q_BYTES;
+  // 16-byte chunk c of position kt's P^T row, swizzled as the P . V operand reads it
+  __device__ static __forceinline__ int p_chunk(int kt, int c) {
+    return c ^ (NR == 16 ? (kt >> 2) & 1 : (NR == 32 ? (kt >> 1) & 3 : kt & 7));
+  }
   static constexpr uint32_t COL_O = 128;                // two O^T buffers of NPV columns after the S^T buffers
   static constexpr uint32_t TMEM_COLS = 256;
   static constexpr int SOFTMAX = 256;                   // 128 positions x 2 halves of the rows
@@ -134,25 +143,20 @@ struct MqSeg {
   bool whole;  // the segment is the whole item (the CTA writes the output itself)
 };
 struct MqWalk {
-  const int32_t *prefix;  // shared memory, B + 1 entries
-  int t, t0, t1, b;
-  __device__ __forceinline__ void start(const int32_t *s_prefix, int B, int tile0, int tile1) {
-    prefix = s_prefix;
+  int t, t0, t1, b, base;  // next tile; the range; the sequence holding tile t and its first tile
+  __device__ __forceinline__ void start(int b0, int base0, int tile0, int tile1) {
+    b = b0;
+    base = base0;
     t = t0 = tile0;
     t1 = tile1;
-    int lo = 0, hi = B;  // the last sequence whose prefix is <= t0 (one with tiles, when t0 < total)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= t0) lo = mid;
-      else hi = mid - 1;
-    }
-    b = lo;
   }
   __device__ __forceinline__ bool next(const MqParams &p, MqSeg &sg) {
     if (t >= t1) return false;
-    while (prefix[b + 1] <= t) ++b;
-    const int base = prefix[b];
-    const MqSeq s = mq_seq(p, b);
+    MqSeq s = mq_seq(p, b);
+    while (t >= base + s.T * p.Hkv) {  // on to the sequence holding tile t (skipping empty ones)
+      base += s.T * p.Hkv;
+      s = mq_seq(p, ++b);
+    }
     const int off = t - base;
     sg.b = b;
     sg.T = s.T;
@@ -185,7 +189,7 @@ __device__ __forceinline__ void mma_st_tile(uint32_t dS, uint32_t k0, uint32_t q
 
 // O^T (+)= V^T . P^T of one tile into dO (128 lanes = head dim, NPV columns
 // = query rows): A = the V tile read MN-major (the head dim contiguous, two
-// 64-element panels), B = each P part (MN-major, one 128-byte row per
+// 64-element panels), B = each P part (MN-major, one P_ROW-byte row per
 // position); 16 positions per MMA.  `accumulate` false starts O^T afresh.
 template <class Cfg>
 __device__ __forceinline__ void mma_pvt_tile(uint32_t dO, uint32_t v0, uint32_t p0, bool accumulate) {
@@ -195,7 +199,9 @@ __device__ __forceinline__ void mma_pvt_tile(uint32_t dO, uint32_t v0, uint32_t 
     const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
 #pragma unroll
     for (int part = 0; part < Cfg::PARTS; ++part) {
-      const uint64_t dp = tc::desc_sw128(p0 + (uint32_t)(part * Cfg::P_PART + k * 2048), Cfg::P_PART, 1024);
+      // 16 positions = 16 P^T rows; 8-row swizzle atoms P_ROW * 8 bytes apart
+      const uint64_t dp = tc::desc_sw(p0 + (uint32_t)(part * Cfg::P_PART + k * 16 * Cfg::P_ROW), Cfg::P_PART,
+                                      8 * Cfg::P_ROW, Cfg::P_LAYOUT);
       tc::mma_f16(dO, dv, dp, id, (accumulate || k > 0 || part > 0) ? 1u : 0u);
     }
   }
@@ -224,7 +230,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint8_t *sV = sK + (size_t)Cfg::KSTAGES * Cfg::KV_BYTES;
   uint8_t *sP = sV + (size_t)Cfg::VSTAGES * Cfg::KV_BYTES;
   uint8_t *sQ = sP + (size_t)Cfg::PBUF * Cfg::P_BYTES;
-  int32_t *s_prefix = reinterpret_cast<int32_t *>(sQ + (size_t)Cfg::QBUF * Cfg::Q_BYTES);
   __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
   __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
   // S^T landed / read out of tensor memory; P written / P . V done (P buffer free)
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __shared__ __align__(8) uint64_t q_full[Cfg::QBUF], o_free[2], xch[2][2], xl[2], fin;
   __shared__ float red[2][2][4][32];  // partial row maxima [tile parity][half][warp quarter][row]
   __shared__ float red_l[2][4][32];   // partial row sums [half][warp quarter][row]
-  __shared__ int32_t s_wsum[8];
+  __shared__ int32_t s_wsum[8], s_b0, s_base0;  // per-warp tile sums; where the CTA's range starts
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag, cta_flags, k_consumed, v_consumed, k_issued, v_issued;
 
@@ -288,7 +293,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc::fence_after();
   const uint32_t tbase = tmem_base;
 
-  // ---- tile prefix over the sequences (256 threads, up to 8 sequences each) ----
+  // ---- tile prefix over the sequences (256 threads, up to 8 sequences each):
+  // the total, where this CTA's range starts, and (CTA 0) the prefix for the
+  // merge kernel ----
   const int B = p.B;
   const int per = (B + Cfg::SOFTMAX - 1) / Cfg::SOFTMAX;
   int tk[kMqMaxBatch / Cfg::SOFTMAX];
@@ -316,6 +323,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (blockIdx.x == 0 && __any_sync(kFull, bad) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_LEN);
   }
   __syncthreads();
+  int W = 0;
+#pragma unroll
+  for (int w = 0; w < Cfg::SOFTMAX / 32; ++w) W += s_wsum[w];
+  const int t0 = (int)((int64_t)W * blockIdx.x / gridDim.x);
+  const int t1 = (int)((int64_t)W * (blockIdx.x + 1) / gridDim.x);
+  if (tid == 0) {  // an empty range (t0 == W): nothing to walk
+    s_b0 = B;
+    s_base0 = W;
+    if (blockIdx.x == 0) p.prefix[B] = W;
+  }
+  __syncthreads();
   if (tid < Cfg::SOFTMAX) {
     int run = incl - own;
     for (int w = 0; w < warp; ++w) run += s_wsum[w];
@@ -323,30 +341,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     for (int k = 0; k < kMqMaxBatch / Cfg::SOFTMAX; ++k) {
       const int b = tid * per + k;
       if (k < per && b < B) {
-        s_prefix[b] = run;
+        if (blockIdx.x == 0) p.prefix[b] = run;
+        if (run <= t0 && t0 < run + tk[k]) {  // the sequence holding the range's first tile
+          s_b0 = b;
+          s_base0 = run;
+        }
         run += tk[k];
       }
     }
-    if (tid == 0) {
-      int total = 0;
-      for (int w = 0; w < Cfg::SOFTMAX / 32; ++w) total += s_wsum[w];
-      s_prefix[B] = total;
-    }
   }
   __syncthreads();
-  if (blockIdx.x == 0 && tid < Cfg::SOFTMAX)  // the merge kernel reads the prefix too
-    for (int b = tid; b <= B; b += Cfg::SOFTMAX) p.prefix[b] = s_prefix[b];
-  const int W = s_prefix[B];
-  const int t0 = (int)((int64_t)W * blockIdx.x / gridDim.x);
-  const int t1 = (int)((int64_t)W * (blockIdx.x + 1) / gridDim.x);
+  const int b0 = s_b0, base0 = s_base0;
 
   if (warp == Cfg::PRODUCER) {
     // ---------------- TMA producer ----------------
     // lane l fetches block (l % 8) of a tile, panel l / 8; a cursor walks the
-    // CTA's tiles and the block ids are read two tiles ahead
+    // CTA's tiles, fetching block ids three tiles ahead
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
     MqWalk wk;
-    wk.start(s_prefix, B, t0, t1);
+    wk.start(b0, base0, t0, t1);
     MqSeg cs{};
     int cj = 0;
     bool have = false;
@@ -357,17 +370,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       return have;
     };
     int bad = 0;
-    // box row of this lane's block of the cursor tile: past the context, or
-    // wholly before every new token's window (such blocks may have been
-    // released), the box past the tensor, which fills zeros
-    auto block_row = [&]() -> int64_t {
+    // this lane's block of the cursor tile: its raw id, loaded here and first
+    // used when the tile's copies are issued (three tiles on), so the load's
+    // latency is hidden; none = past the context, or wholly before every new
+    // token's window (such blocks may have been released)
+    struct Pend {
+      int id, h;
+      bool none;
+    };
+    auto fetch = [&]() -> Pend {
+      Pend f;
       const int lb = (cs.j_first + cj) * Cfg::BLOCKS + slot;
       const int nblk = (cs.ctx + kBlock - 1) / kBlock;
-      if (lb >= nblk || (lb + 1) * kBlock <= cs.first) return p.num_blocks * p.Hkv;
-      const int id = __ldg(p.block_table + (size_t)cs.b * p.max_blocks + lb);
-      const bool good = id >= 0 && (int64_t)id < p.num_blocks;
+      f.h = cs.h;
+      f.none = lb >= nblk || (lb + 1) * kBlock <= cs.first;
+      f.id = f.none ? 0 : __ldg(p.block_table + (size_t)cs.b * p.max_blocks + lb);
+      return f;
+    };
+    // the box row of a fetched block: the box past the tensor (zeros) for none
+    // or a bad id
+    auto row_of = [&](const Pend &f) -> int64_t {
+      if (f.none) return p.num_blocks * p.Hkv;
+      const bool good = f.id >= 0 && (int64_t)f.id < p.num_blocks;
       bad |= good ? 0 : 1;
-      return good ? (int64_t)id * p.Hkv + cs.h : p.num_blocks * p.Hkv;
+      return good ? (int64_t)f.id * p.Hkv + f.h : p.num_blocks * p.Hkv;
     };
     auto issue_k = [&](int g, int64_t trow) -> bool {
       const int ks = g % Cfg::KSTAGES;
@@ -397,20 +423,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // K runs one tile ahead of V: K(g + 1) goes out before V(g), so it waits
     // only for its own slot (S^T(g - 1) done), not behind V(g)'s (P . V(g - 2))
     bool ok = true;
+    const Pend nil{0, 0, true};
     bool h0 = step();
-    int64_t r0 = h0 ? block_row() : 0;
+    const Pend f0 = h0 ? fetch() : nil;
     bool h1 = h0 && step();
-    int64_t r1 = h1 ? block_row() : 0;
+    Pend f1 = h1 ? fetch() : nil;
+    bool h2 = h1 && step();
+    Pend f2 = h2 ? fetch() : nil;
+    int64_t r0 = h0 ? row_of(f0) : 0;
     if (h0) ok = issue_k(0, r0);
     for (int g = 0; h0 && ok; ++g) {
-      const bool h2 = h1 && step();
-      const int64_t r2 = h2 ? block_row() : 0;
-      if (h1 && !(ok = issue_k(g + 1, r1))) break;
+      const bool h3 = h2 && step();
+      const Pend f3 = h3 ? fetch() : nil;
+      int64_t r1 = 0;
+      if (h1) {
+        r1 = row_of(f1);
+        if (!(ok = issue_k(g + 1, r1))) break;
+      }
       if (!(ok = issue_v(g, r0))) break;
       h0 = h1;
       r0 = r1;
       h1 = h2;
-      r1 = r2;
+      f1 = f2;
+      h2 = h3;
+      f2 = f3;
     }
     if (__any_sync(kFull, bad) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
     if (!ok && lane == 0) {
@@ -425,7 +461,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // inputs; each warp's commits track its own MMAs.)
     bool ok = true;
     MqWalk wk;
-    wk.start(s_prefix, B, t0, t1);
+    wk.start(b0, base0, t0, t1);
     MqSeg sg{};
     int g = 0;
     for (int si = 0; ok && wk.next(p, sg); ++si) {
@@ -458,7 +494,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // P . V waits for the O^T buffer it reuses (read out two segments ago)
     bool ok = true;
     MqWalk wk;
-    wk.start(s_prefix, B, t0, t1);
+    wk.start(b0, base0, t0, t1);
     MqSeg sg{};
     int g = 0;
     for (int si = 0; ok && wk.next(p, sg); ++si) {
@@ -525,7 +561,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (lane == 0) mbar_arrive(&q_full[qb]);
     };
     MqWalk wk;
-    wk.start(s_prefix, B, t0, t1);
+    wk.start(b0, base0, t0, t1);
     MqSeg sg{}, nx{};
     bool have = wk.next(p, sg);
     bool nhave = have && wk.next(p, nx);
@@ -663,10 +699,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           ok = warp_wait(&pv_done[pb], (uint32_t)((gj / Cfg::PBUF) - 1) & 1u, p.timeout_ns);
           if (!ok) break;
         }
-        const uint32_t prow = smem_u32(sP + (size_t)pb * Cfg::P_BYTES) + (uint32_t)(kt * 128);
+        const uint32_t prow = smem_u32(sP + (size_t)pb * Cfg::P_BYTES) + (uint32_t)(kt * Cfg::P_ROW);
 #pragma unroll
         for (int k = 0; k < NRH / 8; ++k) {
-          const uint32_t a = prow + ((uint32_t)(((row0 >> 3) + k) ^ (kt & 7)) << 4);
+          const uint32_t a = prow + ((uint32_t)Cfg::p_chunk(kt, (row0 >> 3) + k) << 4);
           uint32_t w[4], wl[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -746,7 +782,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // sequence b by CTA b mod grid
       const size_t per_seq = (size_t)p.q_len * p.Hq * Cfg::D / 8;
       for (int b = blockIdx.x; b < B; b += gridDim.x)
-        if (s_prefix[b + 1] == s_prefix[b]) {
+        if (mq_seq(p, b).T == 0) {
           uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + (size_t)b * per_seq * 8);
           for (size_t i = tid; i < per_seq; i += Cfg::SOFTMAX) dst[i] = make_uint4(0, 0, 0, 0);
         }

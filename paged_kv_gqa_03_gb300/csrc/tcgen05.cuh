@@ -32,6 +32,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The same for the narrower swizzles of an operand whose rows are 64 or 32
+// bytes (layout type 4 = 64-byte swizzle, 6 = 32-byte swizzle; 2 = 128-byte).
+__device__ __forceinline__ uint64_t desc_sw(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
+  return (desc_sw128(saddr, lbo_bytes, sbo_bytes) & ~((uint64_t)7 << 61)) | ((uint64_t)layout << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator:
 // A/B type (0 = f16, 1 = bf16) in bits 7-9 / 10-12, B major-ness (1 = MN)
 // in bit 16, N / 8 in bits 17-22, M / 16 in bits 24-28.
