@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp == Cfg::PRODUCER) {
     // ---------------- TMA producer: every tile of every item, one global counter ----------------
     // lane l fetches block (l % 8) of a tile, panel l / 8; a cursor walks the
-    // CTA's tiles across items and the block ids are read one tile ahead
+    // CTA's tiles across items, fetching block ids three tiles ahead
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
     int ck = -1, cj = 0, cT = 0;  // cursor: tile cj of the cT of round ck's item
     PrefillItem ct{};
@@ -160,20 +160,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       return false;
     };
     int bad = 0;
-    // box row of this lane's block of the cursor tile: past the context, or
-    // wholly before every row's window (such blocks may have been released),
-    // the box past the tensor, which fills zeros
-    auto block_row = [&]() -> int64_t {
+    // this lane's block of the cursor tile: its raw id, loaded here and first
+    // used when the tile's copies are issued (three tiles on), so the load's
+    // latency is hidden; none = past the context, or wholly before every
+    // row's window (such blocks may have been released)
+    struct Pend {
+      int id, h;
+      bool none;
+    };
+    auto fetch = [&]() -> Pend {
+      Pend f;
       const int lb = (ct.j_first + cj) * Cfg::BLOCKS + slot;
-      if (lb >= ct.nblk || (lb + 1) * kBlock <= ct.first) return p.num_blocks * p.Hkv;
-      const int id = __ldg(p.block_table + (size_t)ct.b * p.max_blocks + lb);
-      const bool good = id >= 0 && (int64_t)id < p.num_blocks;
+      f.h = ct.h;
+      f.none = lb >= ct.nblk || (lb + 1) * kBlock <= ct.first;
+      f.id = f.none ? 0 : __ldg(p.block_table + (size_t)ct.b * p.max_blocks + lb);
+      return f;
+    };
+    // the box row of a fetched block: the box past the tensor (zeros) for none
+    // or a bad id
+    auto row_of = [&](const Pend &f) -> int64_t {
+      if (f.none) return p.num_blocks * p.Hkv;
+      const bool good = f.id >= 0 && (int64_t)f.id < p.num_blocks;
       bad |= good ? 0 : 1;
-      return good ? (int64_t)id * p.Hkv + ct.h : p.num_blocks * p.Hkv;
+      return good ? (int64_t)f.id * p.Hkv + f.h : p.num_blocks * p.Hkv;
     };
     // K runs one tile ahead of V: K(g+1) goes out before V(g), so it waits
     // only for its own slot (S(g-2) done) and not behind V(g)'s (P . V(g-2)
-    // done); the cursor reads block ids two tiles ahead
+    // done)
     auto issue_k = [&](int g, int64_t trow) -> bool {
       const int ks = g % Cfg::KSTAGES;
       if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
@@ -200,20 +213,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       return true;
     };
     bool ok = true;
-    bool h0 = step();  // tiles g and g + 1 exist (cursor one tile further on)
-    int64_t r0 = h0 ? block_row() : 0;
+    const Pend nil{0, 0, true};
+    bool h0 = step();  // tiles g, g + 1, g + 2 exist (the cursor one further on)
+    const Pend f0 = h0 ? fetch() : nil;
     bool h1 = h0 && step();
-    int64_t r1 = h1 ? block_row() : 0;
+    Pend f1 = h1 ? fetch() : nil;
+    bool h2 = h1 && step();
+    Pend f2 = h2 ? fetch() : nil;
+    int64_t r0 = h0 ? row_of(f0) : 0;
     if (h0) ok = issue_k(0, r0);
     for (int g = 0; h0 && ok; ++g) {
-      const bool h2 = h1 && step();
-      const int64_t r2 = h2 ? block_row() : 0;
-      if (h1 && !(ok = issue_k(g + 1, r1))) break;
+      const bool h3 = h2 && step();
+      const Pend f3 = h3 ? fetch() : nil;
+      int64_t r1 = 0;
+      if (h1) {
+        r1 = row_of(f1);
+        if (!(ok = issue_k(g + 1, r1))) break;
+      }
       if (!(ok = issue_v(g, r0))) break;
       h0 = h1;
       r0 = r1;
       h1 = h2;
-      r1 = r2;
+      f1 = f2;
+      h2 = h3;
+      f2 = f3;
     }
     if (__any_sync(kFull, bad)) {
       if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);

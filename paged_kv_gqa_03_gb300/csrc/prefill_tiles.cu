@@ -120,23 +120,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (warp == Cfg::PRODUCER) {
     // ---------------- TMA producer ----------------
-    // lane l fetches block (l % 8) of a tile, panel l / 8; the ids of the next
-    // tile are read one tile ahead
+    // lane l fetches block (l % 8) of a tile, panel l / 8; block ids are
+    // loaded three tiles ahead and first used when the tile's copies are
+    // issued, so the loads' latency is hidden
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
-    auto block_row = [&](int jj, int *bad) -> int64_t {
+    struct Pend {
+      int id;
+      bool none;  // past the context, or wholly before every row's window (such
+                  // blocks may have been released): nothing to read
+    };
+    auto fetch = [&](int jj) -> Pend {
       const int lb = (j_first + jj) * Cfg::BLOCKS + slot;
-      // past the context, or wholly before every row's window (such blocks may
-      // have been released): nothing to read, the box past the tensor fills zeros
-      if (jj >= T || lb >= nblk || (lb + 1) * kBlock <= first) return p.num_blocks * p.Hkv;
-      const int id = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
-      if (id >= 0 && (int64_t)id < p.num_blocks) return (int64_t)id * p.Hkv + h;
-      *bad = 1;
-      return p.num_blocks * p.Hkv;
+      Pend f;
+      f.none = jj >= T || lb >= nblk || (lb + 1) * kBlock <= first;
+      f.id = f.none ? 0 : __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
+      return f;
     };
     int bad = 0;
-    int64_t trow = block_row(0, &bad);
+    // the box row of a fetched block; the box past the tensor fills zeros
+    auto row_of = [&](const Pend &f) -> int64_t {
+      if (f.none) return p.num_blocks * p.Hkv;
+      if (f.id >= 0 && (int64_t)f.id < p.num_blocks) return (int64_t)f.id * p.Hkv + h;
+      bad = 1;
+      return p.num_blocks * p.Hkv;
+    };
+    Pend f0 = fetch(0), f1 = fetch(1), f2 = fetch(2);
     for (int j = 0; j < T; ++j) {
-      const int64_t next = block_row(j + 1, &bad);
+      const Pend f3 = fetch(j + 3);
+      const int64_t trow = row_of(f0);
       const int ks = j % Cfg::KSTAGES, vs = j % Cfg::VSTAGES;
       if (j >= Cfg::KSTAGES &&
           !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
@@ -157,7 +168,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
                     (int)(trow * kBlock), &v_full[vs]);
       if (lane == 0) v_issued = j + 1;
-      trow = next;
+      f0 = f1;
+      f1 = f2;
+      f2 = f3;
     }
     if (bad) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
     if (__any_sync(kFull, k_issued < T || v_issued < T) && lane == 0 && !*(volatile int *)&abort_flag) {
