@@ -150,16 +150,18 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_traffic(q_len=1):
-    """DRAM bytes per decode launch from the committed ncu capture, if the
-    kernel sources are unchanged since it was taken and it covers q_len."""
+def kernel_traffic(q_len=1, kernel=""):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    capture (the decode kernel's, or the transposed multi-query kernel's), if
+    the kernel sources are unchanged since it was taken and it covers q_len."""
+    mq = kernel.startswith("mq_decode_kernel")
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "mq_traffic.json" if mq else "decode_traffic.json")) as f:
             rec = json.load(f)
     except Exception:
         return None
     h = hashlib.sha256()
-    for name in ("common.cuh", "decode.cuh", "internal.h"):
+    for name in rec.get("sources", ("common.cuh", "decode.cuh", "internal.h")):
         with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     if rec.get("source_sha256") != h.hexdigest() or rec.get("q_len", 1) != q_len:
@@ -412,6 +414,7 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group() if world > 1 else None
         return
     peak, peak_src = peak_hbm()
+    kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
     value = job_gbs(kv, world, ms_step)
     attn_gbs = kv / (ms_attn * 1e-3) / 1e9
     cpu = None
@@ -429,10 +432,10 @@ def run_ours(args, world, rank, local):
             min(max(0, c - w.q_len + 1 + i), w.window or 1 << 30)
             for c in w.context_lens for i in range(w.q_len)) / (ms_attn * 1e-3) / 1e12, 2),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + decode + merge)",
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": None if w.window else kernel_traffic(w.q_len),
+                     "traffic": None if w.window else kernel_traffic(w.q_len, kname),
                      "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
         "cpu_baseline": cpu,
@@ -456,6 +459,24 @@ def peak_bf16():
             return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except Exception:
         return 1900.0, "fallback"
+
+
+def attention_kernel_name(w, num_splits, sms):
+    """The kernels the library's attention call runs for this decode
+    workload (the C ABI's routing rule, PKV_MULTI_KERNEL honoured)."""
+    if w.q_len == 1:
+        return "paged_decode_attention (plan + decode + merge)"
+    G = w.Hq // w.Hkv
+    R = w.q_len * G
+    force = os.environ.get("PKV_MULTI_KERNEL", "")
+    sixteen = w.dtype in ("bf16", "f16")
+    fills = w.B * w.Hkv * ((R + 127) // 128) >= sms and w.B <= 65535
+    if num_splits == 0 and sixteen and force not in ("units", "prefill") and w.D == 128 and R <= 64 \
+            and w.B <= 2048 and (R <= 32 or not fills or force == "transposed"):
+        return "mq_decode_kernel (transposed tcgen05, stream-K) + mq_merge_kernel"
+    if num_splits == 0 and sixteen and force != "units" and fills:
+        return "prefill tcgen05 kernel (128-row tiles, uniform q_len)"
+    return "paged_decode_attention (plan + decode in 8-row units + merge)"
 
 
 def prefill_kernel_name(c):
