@@ -31,10 +31,10 @@
 //    sequence that is cut into equal ranges, one per CTA (one CTA per SM); an
 //    item cut by a range end is finished by the merge kernel from the CTAs'
 //    normalised partial outputs and log-sum-exps;
-//  * warp roles: 0-7 softmax / epilogue / Q staging, 8 TMA producer (K one
-//    tile ahead of V; block ids loaded three tiles ahead and first used when
-//    the copies are issued), 9 S^T issue and tensor-memory allocation, 10
-//    P . V issue.  Every wait is bounded; a timeout sets PKV_FLAG_TIMEOUT, and
+//  * warp roles: 0-7 softmax / epilogue / Q staging, 8 and 11 TMA producers of
+//    the K and the V tiles (block ids loaded three tiles ahead and first used
+//    when the copies are issued), 9 S^T issue and tensor-memory allocation,
+//    10 P . V issue.  Every wait is bounded; a timeout sets PKV_FLAG_TIMEOUT, and
 //    the CTA drains its copies and MMAs and frees its tensor memory.
 #include <math.h>
 
@@ -76,8 +76,9 @@ struct MqCfg {
   static constexpr uint32_t COL_O = 128;                // two O^T buffers of NPV columns after the S^T buffers
   static constexpr uint32_t TMEM_COLS = 256;
   static constexpr int SOFTMAX = 256;                   // 128 positions x 2 halves of the rows
-  static constexpr int THREADS = SOFTMAX + 96;         // + producer, S^T issuer, P . V issuer
-  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, PV_ISSUER = PRODUCER + 2;
+  static constexpr int THREADS = SOFTMAX + 128;        // + K producer, S^T issuer, P . V issuer, V producer
+  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, PV_ISSUER = PRODUCER + 2,
+                       V_PRODUCER = PRODUCER + 3;
   static_assert(NRH == 8 || NRH == 16 || NRH == 32, "rows per half");
   static_assert(SBUF * NR <= (int)COL_O && COL_O + 2 * NPV <= TMEM_COLS, "tensor memory");
   static_assert(LOADS <= 32, "one box per producer lane");
@@ -353,8 +354,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __syncthreads();
   const int b0 = s_b0, base0 = s_base0;
 
-  if (warp == Cfg::PRODUCER) {
-    // ---------------- TMA producer ----------------
+  if (warp == Cfg::PRODUCER || warp == Cfg::V_PRODUCER) {
+    // ---------------- TMA producers: K tiles (warp 8), V tiles (warp 11) ----------------
+    // two warps, so neither tensor's copies wait behind the other's issue;
     // lane l fetches block (l % 8) of a tile, panel l / 8; a cursor walks the
     // CTA's tiles, fetching block ids three tiles ahead
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int ks = g % Cfg::KSTAGES;
       if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
         return false;
-      if (__any_sync(kFull, *(volatile int *)&abort_flag)) return false;
+        if (__any_sync(kFull, *(volatile int *)&abort_flag)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
@@ -412,6 +414,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int vs = g % Cfg::VSTAGES;
       if (g >= Cfg::VSTAGES && !warp_wait(&v_empty[vs], (uint32_t)((g / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
         return false;
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
@@ -420,29 +423,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (lane == 0) v_issued = g + 1;
       return true;
     };
-    // K runs one tile ahead of V: K(g + 1) goes out before V(g), so it waits
-    // only for its own slot (S^T(g - 1) done), not behind V(g)'s (P . V(g - 2))
+    const bool vw = warp == Cfg::V_PRODUCER;
     bool ok = true;
     const Pend nil{0, 0, true};
     bool h0 = step();
-    const Pend f0 = h0 ? fetch() : nil;
+    Pend f0 = h0 ? fetch() : nil;
     bool h1 = h0 && step();
     Pend f1 = h1 ? fetch() : nil;
     bool h2 = h1 && step();
     Pend f2 = h2 ? fetch() : nil;
-    int64_t r0 = h0 ? row_of(f0) : 0;
-    if (h0) ok = issue_k(0, r0);
     for (int g = 0; h0 && ok; ++g) {
       const bool h3 = h2 && step();
       const Pend f3 = h3 ? fetch() : nil;
-      int64_t r1 = 0;
-      if (h1) {
-        r1 = row_of(f1);
-        if (!(ok = issue_k(g + 1, r1))) break;
-      }
-      if (!(ok = issue_v(g, r0))) break;
+      const int64_t r = row_of(f0);
+      ok = vw ? issue_v(g, r) : issue_k(g, r);
       h0 = h1;
-      r0 = r1;
+      f0 = f1;
       h1 = h2;
       f1 = f2;
       h2 = h3;
@@ -800,7 +796,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (lane == 0) tc::commit(&fin);  // completes once every MMA either warp issued has
     __syncwarp();
     if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
-  } else if (warp == Cfg::PRODUCER && lane == 0) {  // copies issued but never consumed (abort only)
+  } else if ((warp == Cfg::PRODUCER || warp == Cfg::V_PRODUCER) && lane == 0) {  // copies issued, never consumed
     for (int j = k_consumed; j < k_issued; ++j)
       mbar_wait_bounded(&k_full[j % Cfg::KSTAGES], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
     for (int j = v_consumed; j < v_issued; ++j)
