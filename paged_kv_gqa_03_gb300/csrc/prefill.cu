@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc::fence_after();
   const uint32_t tbase = tmem_base;
 
-  if (warp == Cfg::PRODUCER) {
-    // ---------------- TMA producer: every tile of every item, one global counter ----------------
+  if (warp == Cfg::PRODUCER || warp == Cfg::V_PRODUCER) {
+    // ---------------- TMA producers: every K tile (warp 8) / V tile (warp 10) of every item ----------------
     // lane l fetches block (l % 8) of a tile, panel l / 8; a cursor walks the
     // CTA's tiles across items, fetching block ids three tiles ahead
     const int slot = lane & (Cfg::BLOCKS - 1), panel = lane / Cfg::BLOCKS;
@@ -184,9 +184,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       bad |= good ? 0 : 1;
       return good ? (int64_t)f.id * p.Hkv + f.h : p.num_blocks * p.Hkv;
     };
-    // K runs one tile ahead of V: K(g+1) goes out before V(g), so it waits
-    // only for its own slot (S(g-2) done) and not behind V(g)'s (P . V(g-2)
-    // done)
     auto issue_k = [&](int g, int64_t trow) -> bool {
       const int ks = g % Cfg::KSTAGES;
       if (g >= Cfg::KSTAGES && !warp_wait(&k_empty[ks], (uint32_t)((g / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
@@ -204,6 +201,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int vs = g % Cfg::VSTAGES;
       if (g >= Cfg::VSTAGES && !warp_wait(&v_empty[vs], (uint32_t)((g / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
         return false;
+      if (__any_sync(kFull, *(volatile int *)&abort_flag)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
       __syncwarp();
       if (lane < Cfg::LOADS)
@@ -212,27 +210,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (lane == 0) v_issued = g + 1;
       return true;
     };
+    const bool vw = warp == Cfg::V_PRODUCER;
     bool ok = true;
     const Pend nil{0, 0, true};
     bool h0 = step();  // tiles g, g + 1, g + 2 exist (the cursor one further on)
-    const Pend f0 = h0 ? fetch() : nil;
+    Pend f0 = h0 ? fetch() : nil;
     bool h1 = h0 && step();
     Pend f1 = h1 ? fetch() : nil;
     bool h2 = h1 && step();
     Pend f2 = h2 ? fetch() : nil;
-    int64_t r0 = h0 ? row_of(f0) : 0;
-    if (h0) ok = issue_k(0, r0);
     for (int g = 0; h0 && ok; ++g) {
       const bool h3 = h2 && step();
       const Pend f3 = h3 ? fetch() : nil;
-      int64_t r1 = 0;
-      if (h1) {
-        r1 = row_of(f1);
-        if (!(ok = issue_k(g + 1, r1))) break;
-      }
-      if (!(ok = issue_v(g, r0))) break;
+      const int64_t r = row_of(f0);
+      ok = vw ? issue_v(g, r) : issue_k(g, r);
       h0 = h1;
-      r0 = r1;
+      f0 = f1;
       h1 = h2;
       f1 = f2;
       h2 = h3;

@@ -30,8 +30,10 @@
 //    magnitudes in [2^-14, 65504], larger ones saturate and are flagged)
 //    after its copy lands and before they release the tile's P; stale rows
 //    past a context are zeroed in the same pass;
-//  * warp roles: 0-7 softmax + epilogue, 8 TMA producer, 9 MMA issue and
-//    tensor-memory allocation.  Every wait is bounded; a timeout sets
+//  * warp roles: 0-7 softmax + epilogue, 8 and 10 TMA producers of the K and
+//    the V tiles (one warp issuing both tensors' copies spent much of each
+//    tile period inside its issues), 9 MMA issue and tensor-memory
+//    allocation.  Every wait is bounded; a timeout sets
 //    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
 //    memory.
 #pragma once
@@ -68,8 +70,8 @@ struct PrefillCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = SBUF * N;           // O after the S buffers
   static constexpr int SOFTMAX = 256;                   // threads: 128 rows x 2 halves
-  static constexpr int THREADS = SOFTMAX + 64;          // + producer warp + MMA warp
-  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1;  // warp ids
+  static constexpr int THREADS = SOFTMAX + 96;          // + K producer, MMA, V producer warps
+  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, V_PRODUCER = PRODUCER + 2;  // warp ids
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
   static_assert(LOADS <= 32, "one box per producer lane");

@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc::fence_after();
   const uint32_t tbase = tmem_base;
 
-  if (warp == Cfg::PRODUCER) {
-    // ---------------- TMA producer ----------------
+  if (warp == Cfg::PRODUCER || warp == Cfg::V_PRODUCER) {
+    // ---------------- TMA producers: K tiles (warp 8), V tiles (warp 10) ----------------
     // lane l fetches block (l % 8) of a tile, panel l / 8; block ids are
     // loaded three tiles ahead and first used when the tile's copies are
     // issued, so the loads' latency is hidden
@@ -144,36 +144,43 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       bad = 1;
       return p.num_blocks * p.Hkv;
     };
+    const bool vw = warp == Cfg::V_PRODUCER;
     Pend f0 = fetch(0), f1 = fetch(1), f2 = fetch(2);
     for (int j = 0; j < T; ++j) {
       const Pend f3 = fetch(j + 3);
       const int64_t trow = row_of(f0);
-      const int ks = j % Cfg::KSTAGES, vs = j % Cfg::VSTAGES;
-      if (j >= Cfg::KSTAGES &&
-          !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
-        break;
-      if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
-      __syncwarp();
-      if (lane < Cfg::LOADS)
-        tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
-                    (int)(trow * kBlock), &k_full[ks]);
-      if (lane == 0) k_issued = j + 1;
-      if (j >= Cfg::VSTAGES &&
-          !warp_wait(&v_empty[vs], (uint32_t)((j / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
-      __syncwarp();
-      if (lane < Cfg::LOADS)
-        tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
-                    (int)(trow * kBlock), &v_full[vs]);
-      if (lane == 0) v_issued = j + 1;
+      if (!vw) {
+        const int ks = j % Cfg::KSTAGES;
+        if (j >= Cfg::KSTAGES &&
+            !warp_wait(&k_empty[ks], (uint32_t)((j / Cfg::KSTAGES) - 1) & 1u, p.timeout_ns))
+          break;
+        if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&k_full[ks], Cfg::KV_BYTES);
+        __syncwarp();
+        if (lane < Cfg::LOADS)
+          tma_load_2d(sK + (size_t)ks * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmK, panel * 64,
+                      (int)(trow * kBlock), &k_full[ks]);
+        if (lane == 0) k_issued = j + 1;
+      } else {
+        const int vs = j % Cfg::VSTAGES;
+        if (j >= Cfg::VSTAGES &&
+            !warp_wait(&v_empty[vs], (uint32_t)((j / Cfg::VSTAGES) - 1) & 1u, p.timeout_ns))
+          break;
+        if (__any_sync(kFull, *(volatile int *)&abort_flag)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&v_full[vs], Cfg::KV_BYTES);
+        __syncwarp();
+        if (lane < Cfg::LOADS)
+          tma_load_2d(sV + (size_t)vs * Cfg::KV_BYTES + panel * Cfg::PANEL_KV + slot * 2048, &tmV, panel * 64,
+                      (int)(trow * kBlock), &v_full[vs]);
+        if (lane == 0) v_issued = j + 1;
+      }
       f0 = f1;
       f1 = f2;
       f2 = f3;
     }
     if (bad) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
-    if (__any_sync(kFull, k_issued < T || v_issued < T) && lane == 0 && !*(volatile int *)&abort_flag) {
+    if (__any_sync(kFull, (vw ? *(volatile int *)&v_issued : *(volatile int *)&k_issued) < T) && lane == 0 &&
+        !*(volatile int *)&abort_flag) {
       atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
       abort_flag = 1;
     }
