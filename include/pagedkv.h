@@ -222,13 +222,26 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  *              decode entry point
  * Everything else, including the workspace rule, is as for
  * paged_decode_attention; the workspace size comes from
- * paged_decode_multi_workspace_bytes.  Kernels: with q_len >= 2, an F16 or
- * BF16 cache, num_splits = 0, scale > 0 and at least one (sequence, kv head,
- * 128-row tile) per SM, the call runs a tensor-core prefill kernel (chosen
- * as in paged_prefill_attention), which reads each (sequence, kv head)'s
- * K/V once for all its q_len * G rows; otherwise each kv head's rows are served in
- * 8-row units by the decode kernel (K/V read once per unit, re-reads mostly
- * from L2) with the split-KV merge.  Both meet the same error bound.
+ * paged_decode_multi_workspace_bytes (which covers every kernel below).
+ * Kernels, all meeting the same error bound; with q_len >= 2, an F16 or BF16
+ * cache, num_splits = 0 and scale > 0:
+ *  - R = q_len * G <= 32 query rows per kv head, D = 128, B <= 2048: a
+ *    tensor-core kernel with the cache positions on the MMA's M side (S^T =
+ *    K . Q^T, O^T = V^T . P^T), one CTA per SM over equal shares of all
+ *    (sequence, kv head) K/V tiles (any batch shape fills the GPU) and a
+ *    merge of the (sequence, kv head) items cut between CTAs; each K/V byte is
+ *    read once for all R rows;
+ *  - R <= 64 the same, unless the tensor-core prefill kernel's grid (below)
+ *    fills the SMs;
+ *  - otherwise, with at least one (sequence, kv head, 128-row tile) per SM,
+ *    a tensor-core prefill kernel (chosen as in paged_prefill_attention),
+ *    which also reads each (sequence, kv head)'s K/V once for all its rows;
+ *  - otherwise (FP8 or F32 caches, a fixed split count, small grids) each kv
+ *    head's rows are served in 8-row units by the decode kernel (K/V read once
+ *    per unit, re-reads mostly from L2) with the split-KV merge.
+ * The environment variable PKV_MULTI_KERNEL = transposed | prefill | units
+ * forces the first, second or last route where it applies (measurement and
+ * tests).
  */
 #define PKV_MAX_Q_LEN 64
 int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
