@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&xch[0], Cfg::SOFTMAX / 32);
     mbar_init(&xch[1], Cfg::SOFTMAX / 32);
     mbar_init(&xl, Cfg::SOFTMAX / 32);
-    mbar_init(&fin, 1);
+    mbar_init(&fin, 2);  // one commit from each issuing warp
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = 0;
@@ -239,12 +239,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       abort_flag = 1;
     }
   } else if (warp == Cfg::ISSUER) {
-    // ---------------- MMA issue ----------------
+    // ---------------- S issue (P . V has a warp of its own) ----------------
     const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
-    int g = 0;        // global K / V tile
-    int items = 0;    // valid items so far (Q phases)
-    int o_items = 0;  // items with tiles so far (O hand-offs)
+    int g = 0;      // global K / V tile
+    int items = 0;  // valid items so far (Q phases)
     // S = Q . K^T of global tile gg into S buffer gg % SBUF (free once P . V of
     // tile gg - SBUF, which read P from it, is done)
     auto issue_s = [&](int gg) -> bool {
@@ -272,13 +271,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       ++items;
       if (!ok) break;
       tc::fence_after();
-      // S runs one tile ahead of P . V (tensor-pipe order ... S(g+1), P . V(g)).
-      // (Two ahead measured much slower: S(g+2) reuses the buffer of P . V(g-1),
-      // so its issue waits for that P . V to complete and the pipe drains.)
-      ok = issue_s(g);
+      for (int j = 0; j < it.T && ok; ++j) {
+        ok = issue_s(g + j);
+        if (ok && __any_sync(kFull, *(volatile int *)&abort_flag)) ok = false;
+      }
+      g += it.T;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
+    }
+  } else if (warp == Cfg::PV_ISSUER) {
+    // ---------------- P . V issue ----------------
+    bool ok = true;
+    int g = 0;        // global K / V tile
+    int o_items = 0;  // items with tiles so far (O hand-offs)
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int i = round_item(k);
+      if (i >= n_items) continue;
+      const PrefillItem it = prefill_item<Cfg>(p, i);
+      if (!it.valid || it.T == 0) continue;
       for (int j = 0; j < it.T && ok; ++j) {
         const int gj = g + j;
-        if (j + 1 < it.T && !(ok = issue_s(gj + 1))) break;
         const int vs = gj % Cfg::VSTAGES, sb = gj % Cfg::SBUF;
         // the first P . V of an item overwrites O: the previous item's O must be read out
         if (j == 0 && o_items > 0 && !(ok = warp_wait(&o_free, (uint32_t)(o_items - 1) & 1u, p.timeout_ns))) break;
@@ -299,10 +313,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           tc::commit(&v_empty[vs]);
         }
         __syncwarp();
-        if (__any_sync(kFull, *(volatile int *)&abort_flag)) {
-          ok = false;
-          break;
-        }
+        if (__any_sync(kFull, *(volatile int *)&abort_flag)) ok = false;
       }
       g += it.T;
       ++o_items;
@@ -521,8 +532,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // ---------------- drain, then free tensor memory ----------------
   tc::fence_before();
   __syncthreads();
-  if (warp == Cfg::ISSUER) {
-    if (lane == 0) tc::commit(&fin);  // completes once every issued MMA has
+  if (warp == Cfg::ISSUER || warp == Cfg::PV_ISSUER) {
+    if (lane == 0) tc::commit(&fin);  // completes once every MMA either warp issued has
     __syncwarp();
     if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
   } else if (warp == Cfg::PRODUCER && lane == 0) {  // copies issued but never consumed (abort only)

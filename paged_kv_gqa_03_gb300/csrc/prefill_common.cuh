@@ -32,8 +32,9 @@
 //    past a context are zeroed in the same pass;
 //  * warp roles: 0-7 softmax + epilogue, 8 and 10 TMA producers of the K and
 //    the V tiles (one warp issuing both tensors' copies spent much of each
-//    tile period inside its issues), 9 MMA issue and tensor-memory
-//    allocation.  Every wait is bounded; a timeout sets
+//    tile period inside its issues), 9 S issue and tensor-memory allocation,
+//    11 P . V issue (S waits only for K and for its buffer's last P . V,
+//    P . V only for V and P: neither stream waits behind the other's inputs).  Every wait is bounded; a timeout sets
 //    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
 //    memory.
 #pragma once
@@ -70,8 +71,9 @@ struct PrefillCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = SBUF * N;           // O after the S buffers
   static constexpr int SOFTMAX = 256;                   // threads: 128 rows x 2 halves
-  static constexpr int THREADS = SOFTMAX + 96;          // + K producer, MMA, V producer warps
-  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, V_PRODUCER = PRODUCER + 2;  // warp ids
+  static constexpr int THREADS = SOFTMAX + 128;         // + K producer, S issue, V producer, P . V issue warps
+  static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, V_PRODUCER = PRODUCER + 2,
+                       PV_ISSUER = PRODUCER + 3;  // warp ids
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
   static_assert(LOADS <= 32, "one box per producer lane");

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&xl, Cfg::SOFTMAX / 32);
     mbar_init(&mrg[0], Cfg::SOFTMAX / 32);
     mbar_init(&mrg[1], Cfg::SOFTMAX / 32);
-    mbar_init(&fin, 1);
+    mbar_init(&fin, 2);  // one commit from each issuing warp
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = ctx_raw != ctx ? PKV_FLAG_BAD_LEN : 0;
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       abort_flag = 1;
     }
   } else if (warp == Cfg::ISSUER) {
-    // ---------------- MMA issue ----------------
+    // ---------------- S issue (P . V has a warp of its own) ----------------
     const uint32_t q0 = smem_u32(sQ);
     bool ok = true;
     // S = Q . K^T of tile jj into S buffer jj % SBUF (free once P . V of tile
@@ -206,12 +206,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       __syncwarp();
       return true;
     };
-    // S runs one tile ahead of P . V (tensor-pipe order ... S(j+1), P . V(j)).
-    // (Two ahead measured much slower: S(j+2) reuses the buffer of P . V(j-1),
-    // so its issue waits for that P . V to complete and the pipe drains.)
-    if (T > 0) ok = issue_s(0);
     for (int j = 0; j < T && ok; ++j) {
-      if (j + 1 < T && !(ok = issue_s(j + 1))) break;
+      ok = issue_s(j);
+      if (ok && __any_sync(kFull, *(volatile int *)&abort_flag)) ok = false;
+    }
+    if (!ok && lane == 0) {
+      atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+      abort_flag = 1;
+    }
+  } else if (warp == Cfg::PV_ISSUER) {
+    // ---------------- P . V issue ----------------
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
       const int vs = j % Cfg::VSTAGES, sb = j % Cfg::SBUF;
       ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
       if (ok) ok = warp_wait(&p_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
@@ -469,8 +475,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // ---------------- drain, then free tensor memory ----------------
   tc::fence_before();
   __syncthreads();
-  if (warp == Cfg::ISSUER) {
-    if (lane == 0) tc::commit(&fin);  // completes once every issued MMA has
+  if (warp == Cfg::ISSUER || warp == Cfg::PV_ISSUER) {
+    if (lane == 0) tc::commit(&fin);  // completes once every MMA either warp issued has
     __syncwarp();
     if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
   } else if (warp == Cfg::PRODUCER && lane == 0) {  // copies issued but never consumed (abort only)
