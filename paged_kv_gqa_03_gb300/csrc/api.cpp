@@ -110,7 +110,7 @@ int kernel_occupancy(int ki, int *ctas_per_sm, int *sm_count) {
 }
 
 // The current device's SM count (cached).
-int sm_count(int *out) {
+int device_sm_count(int *out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e);
@@ -331,7 +331,7 @@ int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
   if (q_len >= 2 && num_splits == 0 && D == kMqHeadDim && q_len * (Hq / Hkv) <= kMqRows && B <= kMqMaxBatch &&
       (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16)) {
     int sms = 0;
-    rc = sm_count(&sms);
+    rc = device_sm_count(&sms);
     if (rc != PKV_OK) return rc;
     const size_t mq = mq_ws_layout(B, sms).total;  // the transposed kernel's partials
     if (mq > total) total = mq;
@@ -434,7 +434,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
     // PKV_MULTI_KERNEL=transposed|prefill|units in the environment forces one
     // route where it applies (for measurement and tests).
     int sms = 0;
-    rc = sm_count(&sms);
+    rc = device_sm_count(&sms);
     if (rc != PKV_OK) return rc;
     const char *force = std::getenv("PKV_MULTI_KERNEL");
     const bool units = force && !std::strcmp(force, "units");
