@@ -1,0 +1,60 @@
+"""The kernel name bench.py writes into a decode line's roofline mirrors the C
+ABI's routing of paged_decode_attention_multi: q_len 1 -> the decode kernel;
+16-bit caches with head dim 128 and up to 32 query rows per kv head -> the
+transposed tensor-core kernel; 33-64 rows -> the 128-row prefill kernel when
+its grid fills the SMs, else the transposed kernel; fp8 / f32 caches, a fixed
+split count or small grids of wider rows -> the 8-row decode units;
+PKV_MULTI_KERNEL forces a route where it applies.  Host logic only."""
+from types import SimpleNamespace
+
+import pytest
+
+import bench
+
+SMS = 152
+
+
+def _w(q_len, B=64, Hq=64, Hkv=8, D=128, dtype="bf16"):
+    return SimpleNamespace(q_len=q_len, B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype)
+
+
+def _route(name):
+    if name.startswith("mq_decode_kernel"):
+        return "transposed"
+    if name.startswith("prefill"):
+        return "prefill"
+    if "8-row units" in name:
+        return "units"
+    return "decode"
+
+
+@pytest.mark.parametrize("w,splits,want", [
+    (_w(1), 0, "decode"),
+    (_w(2), 0, "transposed"),                       # 16 rows
+    (_w(4), 0, "transposed"),                       # 32 rows
+    (_w(8), 0, "prefill"),                          # 64 rows, 512 items fill 152 SMs
+    (_w(8, B=4), 0, "transposed"),                  # 64 rows, 32 items: the prefill grid would not fill
+    (_w(16, Hq=64, Hkv=8), 0, "prefill"),           # 128 rows: past the transposed kernel
+    (_w(16, B=4), 0, "units"),                      # 128 rows, small grid
+    (_w(4, dtype="fp8_e4m3"), 0, "units"),
+    (_w(4, dtype="f32"), 0, "units"),
+    (_w(4), 7, "units"),                            # a fixed split count
+    (_w(4, D=64), 0, "prefill"),                    # head dim 64: the prefill kernel
+    (_w(4, D=64, B=2), 0, "units"),
+    (_w(4, dtype="f16"), 0, "transposed"),
+    (_w(4, B=4096), 0, "prefill"),                  # past the transposed kernel's batch bound
+], ids=lambda v: str(v) if not isinstance(v, SimpleNamespace) else f"L{v.q_len}-B{v.B}-D{v.D}-{v.dtype}")
+def test_roofline_kernel_follows_the_routing(w, splits, want, monkeypatch):
+    monkeypatch.delenv("PKV_MULTI_KERNEL", raising=False)
+    assert _route(bench.attention_kernel_name(w, splits, SMS)) == want
+
+
+@pytest.mark.parametrize("force,w,want", [
+    ("prefill", _w(4), "prefill"),
+    ("units", _w(4), "units"),
+    ("transposed", _w(8), "transposed"),            # forced on 64 rows with a full prefill grid
+    ("transposed", _w(16), "prefill"),              # cannot apply past 64 rows
+])
+def test_roofline_kernel_honours_the_override(force, w, want, monkeypatch):
+    monkeypatch.setenv("PKV_MULTI_KERNEL", force)
+    assert _route(bench.attention_kernel_name(w, 0, SMS)) == want
