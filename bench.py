@@ -444,7 +444,7 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": round(ms_e2e, 4)},
         "host_a1_us": round(host_a1_us, 1),
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step(w, kname, step.ncow) * args.steps,
         "num_splits": args.num_splits,
         "check": check,
     }
@@ -459,6 +459,21 @@ def peak_bf16():
             return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except Exception:
         return 1900.0, "fallback"
+
+
+def launches_per_step(w, kernel_name, ncow):
+    """Our kernels launched by one timed step (DecodeStep.launch): the
+    copy-on-write block copy when the step has pairs, the append, and the
+    attention call's kernels for its route (decode + merge, plus the plan
+    kernel from 2048 sequences on; the transposed kernel + its merge; one
+    prefill kernel)."""
+    if kernel_name.startswith("mq_decode_kernel"):
+        attn = 2
+    elif kernel_name.startswith("prefill"):
+        attn = 1
+    else:
+        attn = 2 + (1 if w.B >= 2048 else 0)
+    return (1 if ncow else 0) + 1 + attn
 
 
 def attention_kernel_name(w, num_splits, sms):
