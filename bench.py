@@ -326,6 +326,8 @@ def run_ours(args, world, rank, local):
     kv = w.kv_bytes()
 
 
+    kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
+
     # warm-up
     for _ in range(args.warmup):
         step.launch(q, kn, vn, out)
@@ -344,8 +346,10 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
+    timed_launches = 0
     for _ in range(args.steps):
         step.launch(q, kn, vn, out)
+        timed_launches += launches_per_step(w, kname, step.ncow)
     e1.record(stream)
     e1.synchronize()
     barrier(world)
@@ -414,7 +418,6 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group() if world > 1 else None
         return
     peak, peak_src = peak_hbm()
-    kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
     value = job_gbs(kv, world, ms_step)
     attn_gbs = kv / (ms_attn * 1e-3) / 1e9
     cpu = None
@@ -438,19 +441,34 @@ def run_ours(args, world, rank, local):
                      "traffic": None if w.window else kernel_traffic(w.q_len, kname),
                      "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
+        "unique_kv": unique_kv_line(w, ms_step, ms_attn, peak),
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_gbs(kv, world, ms_e2e), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
         "host_a1_us": round(host_a1_us, 1),
         "clocks": clocks,
-        "gpu_launches": launches_per_step(w, kname, step.ncow) * args.steps,
+        "gpu_launches": timed_launches,
         "num_splits": args.num_splits,
         "check": check,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def unique_kv_line(w, ms_step, ms_attn, peak):
+    """For a workload whose sequences share prefix blocks: the distinct K/V
+    bytes a step reads (each shared block once, whole blocks), per step and
+    per attention call, against the HBM peak.  The logical figure counts
+    every sequence's read of the shared blocks, most of which L2 serves."""
+    if not w.prefix_blocks:
+        return None
+    u = w.unique_kv_bytes()
+    return {"bytes": u, "logical_bytes": w.kv_bytes(),
+            "step_gbs": round(u / (ms_step * 1e-3) / 1e9, 2),
+            "attn_gbs": round(u / (ms_attn * 1e-3) / 1e9, 2),
+            "attn_frac": round(u / (ms_attn * 1e-3) / 1e9 / peak, 4)}
 
 
 def peak_bf16():
