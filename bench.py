@@ -54,6 +54,10 @@ def parse():
                     help="fp8 caches: append with calibrated (running-max, power-of-two) block scales")
     ap.add_argument("--prefill", default="",
                     help="time paged prefill (tensor cores) on a prefill workload: page, llama70b, chunked")
+    ap.add_argument("--mq-route", default="auto", choices=["auto", "transposed", "prefill", "units"],
+                    help="force the library's kernel route for q_len >= 2 (pkv_set_route)")
+    ap.add_argument("--prefill-route", default="auto", choices=["auto", "persistent", "tiles"],
+                    help="force the prefill kernel's schedule (pkv_set_route)")
     return ap.parse_args()
 
 
@@ -311,6 +315,8 @@ def run_ours(args, world, rank, local):
            "fp8_e4m3": torch.float8_e4m3fn}
     w = _workload(args)
     w.calibrated = args.calibrated
+    pkv.pkv_set_route("multi_query", args.mq_route)
+    pkv.pkv_set_route("prefill", args.prefill_route)
     stream = torch.cuda.Stream(dev)
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
@@ -326,7 +332,8 @@ def run_ours(args, world, rank, local):
     kv = w.kv_bytes()
 
 
-    kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count)
+    kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                  args.mq_route)
 
     # warm-up
     for _ in range(args.warmup):
@@ -494,14 +501,14 @@ def launches_per_step(w, kernel_name, ncow):
     return (1 if ncow else 0) + 1 + attn
 
 
-def attention_kernel_name(w, num_splits, sms):
+def attention_kernel_name(w, num_splits, sms, force="auto"):
     """The kernels the library's attention call runs for this decode
-    workload (the C ABI's routing rule, PKV_MULTI_KERNEL honoured)."""
+    workload (the C ABI's routing rule, with the route forced by
+    pkv_set_route("multi_query", force) honoured)."""
     if w.q_len == 1:
         return "paged_decode_attention (plan + decode + merge)"
     G = w.Hq // w.Hkv
     R = w.q_len * G
-    force = os.environ.get("PKV_MULTI_KERNEL", "")
     sixteen = w.dtype in ("bf16", "f16")
     fills = w.B * w.Hkv * ((R + 127) // 128) >= sms and w.B <= 65535
     if num_splits == 0 and sixteen and force not in ("units", "prefill") and w.D == 128 and R <= 64 \
@@ -512,11 +519,10 @@ def attention_kernel_name(w, num_splits, sms):
     return "paged_decode_attention (plan + decode in 8-row units + merge)"
 
 
-def prefill_kernel_name(c):
+def prefill_kernel_name(c, force="auto"):
     """The kernel the library runs for this workload: one CTA per work item
     when the block table admits a cached prefix of 2048+ positions before
-    the new tokens, the persistent kernel otherwise (unless overridden)."""
-    force = os.environ.get("PKV_PREFILL_KERNEL", "")
+    the new tokens, the persistent kernel otherwise (unless forced)."""
     G = c["Hq"] // c["Hkv"]
     tiles = c["table"].shape[1] * 16 - max(c["n"]) >= (1024 if max(c["n"]) * G <= 64 else 2048)
     if force in ("tiles", "persistent"):
@@ -537,6 +543,7 @@ def run_prefill(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    pkv.pkv_set_route("prefill", args.prefill_route)
     spec = dict(workloads.PREFILL_SPECS[args.prefill])
     c = workloads.make_prefill(2000 + list(workloads.PREFILL_SPECS).index(args.prefill), **spec,
                                free=8, window=args.window)
@@ -644,7 +651,7 @@ def run_prefill(args, world, rank, local):
         "config": {"workload": f"prefill {args.prefill}", "B": len(c["n"]), "new_tokens": c["n"][0],
                    "cached_prefix": c["prefix"][0], "Hq": c["Hq"], "Hkv": c["Hkv"], "D": c["D"],
                    "window": args.window, "block_size": 16, "l2": "flushed (256 MB write) before every timed launch"},
-        "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(c), "achieved": round(tflops, 1),
+        "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(c, args.prefill_route), "achieved": round(tflops, 1),
                      "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "traffic": None, "algorithmic_flops_per_launch": flops,
                      "note": "P . V runs in f16 (a bf16 V tile is converted to f16 in shared memory)"},

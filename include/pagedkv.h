@@ -323,14 +323,20 @@ int paged_prefill_attention(void *out, const void *q, int q_dtype,
  *    runs (16 MiB holds D = 128 with ~2000 partitions, more than one per
  *    resident warp of a GB300).
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *  - Set-up: the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *    first call before any stream capture.
+ *  - Set-up: every call looks up the array's device address in the current
+ *    device's context (cudaGetSymbolAddress, a host-side lookup that
+ *    allocates nothing), so the address stays right after a cudaDeviceReset.
+ *    The first call on a device also loads the library's device code there;
+ *    make that first call before any stream capture.
  *  - Sharing: every call on a device uses the same array, which keeps the last
  *    call's contents.  Nothing in it has to start at zero (each call writes
  *    what it later reads), so it is never cleared.  Calls that overlap on the
  *    GPU (several streams or host threads) race on the array: serialise them.
- *  - paged_decode_status() does not apply (there is no workspace to pass).
+ *  - Status: paged_decode_static_status() reads the status bits the last
+ *    call on the current device recorded in the array (timeouts, bad block
+ *    ids, clamped lengths).  After a call whose status is not PKV_OK the
+ *    output may hold partial results of an earlier call: check it before
+ *    using the output when the inputs are not trusted.
  */
 #define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 int paged_decode_attention_static(void *out, const void *q, int q_dtype,
@@ -341,6 +347,14 @@ int paged_decode_attention_static(void *out, const void *q, int q_dtype,
                                   int B, int Hq, int Hkv, int D, int64_t num_blocks,
                                   float scale, int num_splits,
                                   pkv_stream_t stream);
+
+/*
+ * paged_decode_status() for paged_decode_attention_static: synchronises
+ * `stream` and reads the status bits of the last static call on the current
+ * device (the array every such call shares).  Same returns as
+ * paged_decode_status.  No counterpart on the pages.
+ */
+int paged_decode_static_status(pkv_stream_t stream, int *flags_out);
 
 /*
  * Synchronises `stream` and reads the status bits (PKV_FLAG_*) that the last
@@ -385,6 +399,38 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype,
                          const int32_t *src_dst_pairs, int n_pairs,
                          int Hkv, int D, int64_t num_blocks,
                          pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Route overrides (measurement and tests).                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * The library picks its kernels by a fixed rule of each call's shapes (see
+ * paged_decode_attention_multi and paged_prefill_attention); nothing in it
+ * reads the environment.  pkv_set_route replaces that rule for one decision,
+ * process-wide, until the decision is set back to PKV_ROUTE_AUTO, so that
+ * tests can run each kernel on the same inputs and measurements can compare
+ * them.  A forced route applies only where the chosen kernel supports the
+ * call (otherwise the automatic rule decides).  Each call reads the setting
+ * once; change it only while no call is being issued on another host thread.
+ *   which = PKV_ROUTE_MULTI_QUERY (q_len >= 2 decode on 16-bit caches):
+ *           PKV_ROUTE_AUTO, PKV_MQ_TRANSPOSED (the transposed tensor-core
+ *           kernel), PKV_MQ_PREFILL (the 128-row prefill kernel), PKV_MQ_UNITS
+ *           (the decode kernel's 8-row units with the split-KV merge)
+ *   which = PKV_ROUTE_PREFILL (the prefill kernel's schedule):
+ *           PKV_ROUTE_AUTO, PKV_PREFILL_PERSISTENT, PKV_PREFILL_PER_ITEM
+ * Returns PKV_EINVAL for an unknown `which` or `choice`; pkv_get_route
+ * returns the current setting (or PKV_EINVAL).
+ */
+#define PKV_ROUTE_MULTI_QUERY 0
+#define PKV_ROUTE_PREFILL 1
+#define PKV_ROUTE_AUTO 0
+#define PKV_MQ_TRANSPOSED 1
+#define PKV_MQ_PREFILL 2
+#define PKV_MQ_UNITS 3
+#define PKV_PREFILL_PERSISTENT 1
+#define PKV_PREFILL_PER_ITEM 2
+int pkv_set_route(int which, int choice);
+int pkv_get_route(int which);
 
 /* ------------------------------------------------------------------------ */
 /* Staging copy.                                                            */

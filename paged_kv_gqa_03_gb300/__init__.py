@@ -14,7 +14,9 @@ import os
 __all__ = [
     "PagedKVError", "paged_kv_append", "paged_decode_workspace_bytes",
     "paged_decode_attention", "paged_prefill_attention", "paged_decode_status", "paged_decode_merge",
-    "paged_kv_copy_blocks", "pkv_copy", "pkv_status_string", "pkv_version", "BlockManager",
+    "paged_decode_attention_static", "paged_decode_static_status",
+    "paged_kv_copy_blocks", "pkv_copy", "pkv_status_string", "pkv_version", "pkv_set_route",
+    "pkv_get_route", "BlockManager",
     "DTYPE_CODES", "LIB_PATH", "lib",
 ]
 
@@ -49,12 +51,17 @@ _sig("paged_decode_attention_multi", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _
 _sig("paged_prefill_attention", _i32, _P, _P, _i32, _P, _P, _i32, _P, _i32, _P, _P,
      _i32, _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P, _P)
 _sig("paged_decode_status", _i32, _P, _sz, _P, ctypes.POINTER(_i32))
+_sig("paged_decode_attention_static", _i32, _P, _P, _i32, _P, _P, _i32, _P, _P, _P, _i32, _P,
+     _i32, _i32, _i32, _i32, _i64, ctypes.c_float, _i32, _P)
+_sig("paged_decode_static_status", _i32, _P, ctypes.POINTER(_i32))
 _sig("paged_decode_merge", _i32, _P, _i32, _P, _P, _i32, _i32, _i32, _i32, _P)
 _sig("paged_kv_copy_blocks", _i32, _P, _P, _i32, _P, _P, _P, _i32, _i32, _i32, _i64, _P)
 _sig("pkv_copy", _i32, _P, _P, _sz, _P)
 _sig("pkv_status_string", ctypes.c_char_p, _i32)
 _sig("pkv_last_cuda_error", _i32)
 _sig("pkv_version", _i32)
+_sig("pkv_set_route", _i32, _i32, _i32)
+_sig("pkv_get_route", _i32, _i32)
 _sig("pkv_bm_create", _P, _i64)
 _sig("pkv_bm_destroy", None, _P)
 _sig("pkv_bm_allocate", _i32, _P, _i64, _i64)
@@ -71,6 +78,7 @@ _sig("pkv_bm_num_tokens", _i64, _P, _i64)
 PKV_OK, PKV_EINVAL, PKV_EUNSUPPORTED, PKV_EWORKSPACE = 0, -1, -2, -3
 PKV_ECUDA, PKV_ETIMEOUT, PKV_EOOM, PKV_ERANGE, PKV_ENOTFOUND = -4, -5, -6, -7, -8
 PKV_FLAG_TIMEOUT, PKV_FLAG_BAD_LEN, PKV_FLAG_BAD_BLOCK, PKV_FLAG_RANGE = 1, 2, 4, 8
+PKV_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def lib():
@@ -98,6 +106,26 @@ def pkv_status_string(status):
 
 def pkv_version():
     return _L.pkv_version()
+
+
+# Kernel-route decisions that pkv_set_route can force (include/pagedkv.h).
+ROUTES = {"multi_query": (0, ("auto", "transposed", "prefill", "units")),
+          "prefill": (1, ("auto", "persistent", "tiles"))}
+
+
+def pkv_set_route(which, choice):
+    """Forces one kernel-route decision process-wide ("multi_query":
+    auto / transposed / prefill / units; "prefill": auto / persistent /
+    tiles); returns the previous choice.  "auto" restores the library's rule."""
+    idx, names = ROUTES[which]
+    prev = names[_L.pkv_get_route(idx)]
+    _check(_L.pkv_set_route(idx, names.index(choice)), "pkv_set_route")
+    return prev
+
+
+def pkv_get_route(which):
+    idx, names = ROUTES[which]
+    return names[_L.pkv_get_route(idx)]
 
 
 def _torch():
@@ -254,6 +282,35 @@ def paged_decode_status(workspace, stream=None):
                                 ctypes.byref(flags))
     if rc not in (PKV_OK, PKV_ETIMEOUT, PKV_ERANGE):
         _check(rc, "paged_decode_status")
+    return rc, flags.value
+
+
+def paged_decode_attention_static(out, q, k_cache, v_cache, block_table, context_lens, scale,
+                                  k_scale=None, v_scale=None, num_splits=0, stream=None):
+    """paged_decode_attention (one new token per sequence, q, out [B, Hq, D])
+    on the scratch array the library keeps on each GPU instead of a caller's
+    workspace, for callers that cannot allocate device memory.  Calls on one
+    GPU share that array: they must not overlap on the GPU."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out shape {tuple(out.shape)} != q shape {tuple(q.shape)}")
+    num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
+    _check(_L.paged_decode_attention_static(
+        _out(out), _dev(q, "q"), _code(q), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _code(k_cache), _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, num_blocks, float(scale),
+        num_splits, _stream(stream)), "paged_decode_attention_static")
+
+
+def paged_decode_static_status(stream=None):
+    """paged_decode_status for the static scratch of the current device:
+    (status, PKV_FLAG_* bits) of the last paged_decode_attention_static."""
+    flags = _i32(0)
+    rc = _L.paged_decode_static_status(_stream(stream), ctypes.byref(flags))
+    if rc not in (PKV_OK, PKV_ETIMEOUT, PKV_ERANGE):
+        _check(rc, "paged_decode_static_status")
     return rc, flags.value
 
 

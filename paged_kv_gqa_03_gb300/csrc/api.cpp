@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -73,6 +74,9 @@ Registry &registry() {
   });
   return r;
 }
+
+// Route overrides set by pkv_set_route (PKV_ROUTE_AUTO = the rule of shapes).
+std::atomic<int> g_route[2];
 
 struct DeviceFacts {
   int sm_count = 0;
@@ -194,18 +198,19 @@ struct Choice {
 // Picks the kernel for a shape: tensor cores (8-head chunks, unused head
 // columns padded) for every group size on 16-bit and fp8 caches — even for
 // MHA the mma.sync block step measured faster on GB300 than the CUDA-core one
-// (5.83 vs 5.56 TB/s, fp16 MHA layer) — and CUDA cores for fp32 caches.
-// PKV_PATH=mma or =simt forces one path wherever it is compiled (comparison
-// runs); PKV_DECODE_WARPS / PKV_DECODE_STAGES pick an alternative pipeline
-// shape where one is compiled.
+// (5.83 vs 5.56 TB/s, fp16 MHA layer) — and CUDA cores for fp32 caches.  The
+// first compiled match is the default pipeline shape.  A build with
+// PKV_SWEEP_SHAPES defined (pipeline-shape sweeps, not the product build)
+// also compiles alternative shapes and lets PKV_PATH=mma|simt,
+// PKV_DECODE_WARPS and PKV_DECODE_STAGES in the environment pick among them.
 int choose_kernel(int cache_dtype, int q_dtype, int D, int R, Choice *c) {
+#ifdef PKV_SWEEP_SHAPES
   static const int force = [] {
     const char *v = std::getenv("PKV_PATH");
     if (v && std::strcmp(v, "simt") == 0) return 1;
     if (v && std::strcmp(v, "mma") == 0) return 2;
     return 0;
   }();
-  // otherwise the first compiled match is the default shape
   static const int want_warps = [] {
     const char *v = std::getenv("PKV_DECODE_WARPS");
     return v ? std::atoi(v) : 0;
@@ -214,6 +219,9 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int R, Choice *c) {
     const char *v = std::getenv("PKV_DECODE_STAGES");
     return v ? std::atoi(v) : 0;
   }();
+#else
+  constexpr int force = 0, want_warps = 0, want_stages = 0;
+#endif
   const bool mma = cache_dtype != PKV_F32 && force != 1;
   const int GC = mma ? 8 : (R >= 2 ? 2 : 1);
   Registry &r = registry();
@@ -279,7 +287,24 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_version(void) { return 10000; }
+int pkv_version(void) { return 10100; }
+
+int pkv_set_route(int which, int choice) {
+  if (which == PKV_ROUTE_MULTI_QUERY) {
+    if (choice < PKV_ROUTE_AUTO || choice > PKV_MQ_UNITS) return PKV_EINVAL;
+  } else if (which == PKV_ROUTE_PREFILL) {
+    if (choice < PKV_ROUTE_AUTO || choice > PKV_PREFILL_PER_ITEM) return PKV_EINVAL;
+  } else {
+    return PKV_EINVAL;
+  }
+  g_route[which].store(choice, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+int pkv_get_route(int which) {
+  if (which != PKV_ROUTE_MULTI_QUERY && which != PKV_ROUTE_PREFILL) return PKV_EINVAL;
+  return g_route[which].load(std::memory_order_relaxed);
+}
 
 int pkv_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -385,15 +410,14 @@ int paged_decode_attention(void *out, const void *q, int q_dtype, const void *k_
 // that kernel serves with row replicas (measured on 70B-layer shapes: at
 // 1024 positions the two kernels tie, at 1500 one CTA per item is 11 %
 // faster, at 300-512 the persistent kernel is 14-15 % faster).
-// PKV_PREFILL_KERNEL=persistent|tiles in the environment overrides the choice.
+// pkv_set_route(PKV_ROUTE_PREFILL, ...) overrides the choice.
 static cudaError_t launch_prefill_auto(const PrefillParams &p, int cache_dtype, const CUtensorMap &tmK,
                                        const CUtensorMap &tmV, cudaStream_t s) {
   const int64_t bound = (int64_t)p.max_q_len * p.G <= 64 ? 1024 : 2048;
   bool tiles = (int64_t)p.max_blocks * kBlock - p.max_q_len >= bound;
-  if (const char *force = std::getenv("PKV_PREFILL_KERNEL")) {
-    if (!std::strcmp(force, "tiles")) tiles = true;
-    if (!std::strcmp(force, "persistent")) tiles = false;
-  }
+  const int force = g_route[PKV_ROUTE_PREFILL].load(std::memory_order_relaxed);
+  if (force == PKV_PREFILL_PER_ITEM) tiles = true;
+  if (force == PKV_PREFILL_PERSISTENT) tiles = false;
   return tiles ? launch_prefill_tiles(p, cache_dtype, tmK, tmV, s) : launch_prefill(p, cache_dtype, tmK, tmV, s);
 }
 
@@ -431,15 +455,15 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
     //    whose softmax work grows with the rows);
     //  * the transposed kernel for 33-64 rows on grids the prefill kernel
     //    cannot fill.
-    // PKV_MULTI_KERNEL=transposed|prefill|units in the environment forces one
-    // route where it applies (for measurement and tests).
+    // pkv_set_route(PKV_ROUTE_MULTI_QUERY, ...) forces one route where it
+    // applies (for measurement and tests).
     int sms = 0;
     rc = device_sm_count(&sms);
     if (rc != PKV_OK) return rc;
-    const char *force = std::getenv("PKV_MULTI_KERNEL");
-    const bool units = force && !std::strcmp(force, "units");
-    const bool no_mq = units || (force && !std::strcmp(force, "prefill"));
-    const bool want_mq = force && !std::strcmp(force, "transposed");
+    const int force = g_route[PKV_ROUTE_MULTI_QUERY].load(std::memory_order_relaxed);
+    const bool units = force == PKV_MQ_UNITS;
+    const bool no_mq = units || force == PKV_MQ_PREFILL;
+    const bool want_mq = force == PKV_MQ_TRANSPOSED;
     const int G = Hq / Hkv;
     const int R = q_len * G;
     const int64_t tiles = ((int64_t)q_len * G + 127) / 128;

@@ -7,14 +7,19 @@ int register_decode_f16(DecodeKernel *out) {
   int n = 0;
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 64, 8, true, kWarps, kBudget>>();
+#ifdef PKV_SWEEP_SHAPES
+  // for comparison runs and sweeps only, not in the product build: the
+  // CUDA-core path on this cache type (PKV_PATH=simt) and alternative
+  // pipeline shapes (warps per CTA, pipeline bytes per warp;
+  // PKV_DECODE_WARPS / PKV_DECODE_STAGES)
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 64, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 64, 1, false, kWarps, kBudget>>();
-  // alternative pipeline shapes (PKV_DECODE_WARPS / PKV_DECODE_STAGES)
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 4, 16 * 1024>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 6, 16 * 1024>>();
   out[n++] = decode_entry<DecodeCfg<F16, F16, 128, 8, true, 4, 24 * 1024>>();
+#endif
   return n;
 }
 

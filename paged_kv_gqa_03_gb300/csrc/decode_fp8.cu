@@ -15,6 +15,11 @@ int register_decode_fp8(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 8, true, kFp8Warps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, kFp8Warps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 8, true, kFp8Warps, kBudget>>();
+#ifdef PKV_SWEEP_SHAPES
+  // for comparison runs and sweeps only, not in the product build: the
+  // CUDA-core path on this cache type (PKV_PATH=simt) and alternative
+  // pipeline shapes (warps per CTA, pipeline bytes per warp;
+  // PKV_DECODE_WARPS / PKV_DECODE_STAGES)
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 2, false, kWarps, kBudget>>();
@@ -23,11 +28,11 @@ int register_decode_fp8(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 1, false, kWarps, kBudget>>();
-  // alternative pipeline shapes (PKV_DECODE_WARPS / PKV_DECODE_STAGES)
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 5, 16 * 1024>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 6, 16 * 1024>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 8, 12 * 1024>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 4, 20 * 1024>>();
+#endif
   return n;
 }
 

@@ -12,8 +12,6 @@
 // ordinary entry point on it.  Nothing here allocates.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "internal.h"
 #include "pagedkv.h"
 
@@ -23,32 +21,22 @@ namespace {
 // holds it until the process exits.
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_static_scratch on the current device.  In host code the
-// array's name only stands in for the symbol; the address a kernel may use
-// comes from cudaGetSymbolAddress, looked up once per device.
+// Device address of g_static_scratch in the current device's context.  In
+// host code the array's name only stands in for the symbol; the address a
+// kernel may use comes from cudaGetSymbolAddress with the device current.  It
+// is looked up on every call rather than kept: a host-side lookup that
+// allocates nothing, and one that stays right after cudaDeviceReset rebuilds
+// the context (and with it the array) at a possibly different address.  The
+// first lookup on a device loads the library's device code there, which is
+// why that first call must come before any stream capture.
 int scratch_on_current_device(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    pkv::record_cuda_error(e);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    pkv::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     return PKV_ECUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) return PKV_EUNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      pkv::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-      return PKV_ECUDA;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return PKV_OK;
 }
 
@@ -72,4 +60,11 @@ extern "C" int paged_decode_attention_static(void *out, const void *q, int q_dty
   return paged_decode_attention(out, q, q_dtype, k_cache, v_cache, cache_dtype, k_scale, v_scale, block_table,
                                 max_blocks_per_seq, context_lens, B, Hq, Hkv, D, num_blocks, scale, num_splits,
                                 scratch, (size_t)PKV_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int paged_decode_static_status(pkv_stream_t stream, int *flags_out) {
+  void *scratch = nullptr;
+  const int rc = scratch_on_current_device(&scratch);
+  if (rc != PKV_OK) return rc;
+  return paged_decode_status(scratch, (size_t)PKV_STATIC_SCRATCH_BYTES, stream, flags_out);
 }

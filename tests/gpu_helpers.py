@@ -1,5 +1,7 @@
 """Runs one decode step of a workload through the C ABI on the GPU and the
 same step through the oracle on the CPU, and compares them."""
+from contextlib import contextmanager
+
 import numpy as np
 import torch
 
@@ -87,3 +89,17 @@ def run_oracle_step(w):
     out = oracle.decode(w.q, w.q_dtype, kc, vc, w.dtype, table, lens, scale=w.scale,
                         k_scale=ks, v_scale=vs, window=w.window)
     return slots, table, lens, (kc, vc, ks, vs), out
+
+
+@contextmanager
+def routes(**choices):
+    """Forces kernel-route decisions of the library (pkv_set_route) inside
+    the block, e.g. routes(multi_query="transposed", prefill="tiles"), and
+    restores the previous settings after it."""
+    import paged_kv_gqa_03_gb300 as pkv
+    prev = {k: pkv.pkv_set_route(k, v) for k, v in choices.items()}
+    try:
+        yield
+    finally:
+        for k, v in prev.items():
+            pkv.pkv_set_route(k, v)

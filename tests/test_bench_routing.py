@@ -4,7 +4,7 @@ ABI's routing of paged_decode_attention_multi: q_len 1 -> the decode kernel;
 transposed tensor-core kernel; 33-64 rows -> the 128-row prefill kernel when
 its grid fills the SMs, else the transposed kernel; fp8 / f32 caches, a fixed
 split count or small grids of wider rows -> the 8-row decode units;
-PKV_MULTI_KERNEL forces a route where it applies.  Host logic only."""
+a route forced through pkv_set_route applies where it can.  Host logic only."""
 from types import SimpleNamespace
 
 import pytest
@@ -44,8 +44,7 @@ def _route(name):
     (_w(4, dtype="f16"), 0, "transposed"),
     (_w(4, B=4096), 0, "prefill"),                  # past the transposed kernel's batch bound
 ], ids=lambda v: str(v) if not isinstance(v, SimpleNamespace) else f"L{v.q_len}-B{v.B}-D{v.D}-{v.dtype}")
-def test_roofline_kernel_follows_the_routing(w, splits, want, monkeypatch):
-    monkeypatch.delenv("PKV_MULTI_KERNEL", raising=False)
+def test_roofline_kernel_follows_the_routing(w, splits, want):
     assert _route(bench.attention_kernel_name(w, splits, SMS)) == want
 
 
@@ -55,6 +54,5 @@ def test_roofline_kernel_follows_the_routing(w, splits, want, monkeypatch):
     ("transposed", _w(8), "transposed"),            # forced on 64 rows with a full prefill grid
     ("transposed", _w(16), "prefill"),              # cannot apply past 64 rows
 ])
-def test_roofline_kernel_honours_the_override(force, w, want, monkeypatch):
-    monkeypatch.setenv("PKV_MULTI_KERNEL", force)
-    assert _route(bench.attention_kernel_name(w, 0, SMS)) == want
+def test_roofline_kernel_honours_the_override(force, w, want):
+    assert _route(bench.attention_kernel_name(w, 0, SMS, force)) == want

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import compare, run_gpu_step, run_oracle_step
+from gpu_helpers import compare, routes, run_gpu_step, run_oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -188,33 +188,31 @@ def test_captured_multi_query_step_matches_eager():
 
 @pytest.mark.parametrize("kernel", ["persistent", "tiles"])
 @pytest.mark.parametrize("dtype,D,window", [("bf16", 128, 0), ("f16", 64, 0), ("bf16", 128, 37)])
-def test_multi_query_tensor_core_route(dtype, D, window, kernel, monkeypatch):
+def test_multi_query_tensor_core_route(dtype, D, window, kernel):
     """40 sequences x 4 kv heads (160 (sequence, kv head) tiles, one per SM or
     more): with num_splits = 0 the call takes a tensor-core prefill kernel
     (each of the two), with a fixed split count the 8-row-unit decode kernel;
     both against the oracle."""
-    monkeypatch.setenv("PKV_PREFILL_KERNEL", kernel)
-    monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
     spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=5, ctx_range=(5, 300), free_frac=0.3,
                 min_free=16, window=window)
-    for seed, splits in ((61, 0), (62, 7)):
-        _check_step(workloads.make(spec, seed=seed), num_splits=splits)
+    with routes(multi_query="prefill", prefill=kernel):
+        for seed, splits in ((61, 0), (62, 7)):
+            _check_step(workloads.make(spec, seed=seed), num_splits=splits)
 
 
 @pytest.mark.parametrize("route", ["transposed", "prefill"])
 @pytest.mark.parametrize("dtype,D,q_len,window", [("bf16", 128, 5, 0), ("bf16", 128, 3, 37), ("f16", 64, 4, 0)])
-def test_multi_query_ragged_contexts_wide_table(dtype, D, q_len, window, route, monkeypatch):
+def test_multi_query_ragged_contexts_wide_table(dtype, D, q_len, window, route):
     """160 (sequence, kv head) items under a block table admitting 8000
     positions (one long sequence, so the one-CTA-per-item kernel with row
     replicas serves them) and ragged contexts (q_len .. 3000, many items of
     a single tile); every output against the oracle."""
     rng = np.random.default_rng(5)
     ctx = [8000] + [int(x) for x in rng.integers(q_len, 3000, 39)]
-    if route == "prefill":
-        monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
     spec = dict(B=40, Hq=32, Hkv=4, D=D, dtype=dtype, q_len=q_len, ctx=ctx, free_frac=0.2, min_free=16,
                 window=window)
-    _check_step(workloads.make(spec, seed=71))
+    with routes(multi_query="prefill" if route == "prefill" else "auto"):
+        _check_step(workloads.make(spec, seed=71))
 
 
 # The transposed tensor-core kernel (positions on the M side, stream-K over
@@ -272,14 +270,14 @@ def test_transposed_kernel_flags_a_bad_block_id():
 
 
 @pytest.mark.parametrize("q_len,B", [(4, 16), (8, 20)])
-def test_transposed_kernel_equals_the_prefill_route(q_len, B, monkeypatch):
+def test_transposed_kernel_equals_the_prefill_route(q_len, B):
     """The same 70B-shaped call (B sequences of 8192) through the transposed
     kernel and the 128-row prefill route, each forced: both within the bound
     of the oracle.  (At 64 rows with 160 items the prefill route is the
     default.)"""
     w = workloads.config(3, B=B, q_len=q_len)
-    monkeypatch.setenv("PKV_MULTI_KERNEL", "transposed")
-    a = _check_step(w)
-    monkeypatch.setenv("PKV_MULTI_KERNEL", "prefill")
-    b = _check_step(w)
+    with routes(multi_query="transposed"):
+        a = _check_step(w)
+    with routes(multi_query="prefill"):
+        b = _check_step(w)
     print(a, b)

@@ -17,12 +17,14 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(autouse=True, params=["persistent", "tiles"])
-def prefill_kernel(request, monkeypatch):
+def prefill_kernel(request):
     """Every test runs on both prefill kernels (one persistent CTA per SM,
-    one CTA per work item), through the library's environment override of
-    its automatic choice."""
-    monkeypatch.setenv("PKV_PREFILL_KERNEL", request.param)
-    return request.param
+    one CTA per work item), through the library's route override of its
+    automatic choice."""
+    pkv = _pkv()
+    prev = pkv.pkv_set_route("prefill", request.param)
+    yield request.param
+    pkv.pkv_set_route("prefill", prev)
 
 
 def _pkv():
