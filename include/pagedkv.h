@@ -79,7 +79,7 @@ typedef enum {
 #define PKV_FLAG_TIMEOUT 1   /* a pipeline wait exceeded its time limit */
 #define PKV_FLAG_BAD_LEN 2   /* context_lens[b] < 0 or > 16 * max_blocks_per_seq (clamped) */
 #define PKV_FLAG_BAD_BLOCK 4 /* a block-table entry outside [0, num_blocks) (read as zeros) */
-#define PKV_FLAG_RANGE 8     /* bf16 tensor-core prefill: a V value of magnitude > 65504 (saturated) */
+#define PKV_FLAG_RANGE 8     /* reserved: a value outside the range a kernel can represent (no kernel raises it) */
 
 /* ------------------------------------------------------------------------ */
 /* Step a3 — KV append through a slot mapping.                              */
@@ -239,9 +239,9 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  *  - otherwise (FP8 or F32 caches, a fixed split count, small grids) each kv
  *    head's rows are served in 8-row units by the decode kernel (K/V read once
  *    per unit, re-reads mostly from L2) with the split-KV merge.
- * The environment variable PKV_MULTI_KERNEL = transposed | prefill | units
- * forces the first, second or last route where it applies (measurement and
- * tests).
+ * pkv_set_route(PKV_ROUTE_MULTI_QUERY, PKV_MQ_TRANSPOSED | PKV_MQ_PREFILL |
+ * PKV_MQ_UNITS) forces the first, second or last route where it applies
+ * (measurement and tests).
  */
 #define PKV_MAX_Q_LEN 64
 int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
@@ -278,25 +278,25 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype,
  *   scale        > 0 (PKV_EINVAL otherwise)
  *   window       0 (none) or W >= 1
  *   status       device int32 or NULL: zeroed by the call, then the OR of
- *                PKV_FLAG_* bits (bad block id, bad length, in-kernel timeout;
- *                PKV_FLAG_RANGE: a bf16 V value beyond the f16 range, see below)
+ *                PKV_FLAG_* bits (bad block id, bad length, in-kernel timeout)
  *   D            64 or 128; B <= 65535
  * Other arguments as for paged_decode_attention.  Asynchronous on `stream`;
  * needs no workspace.
  *
- * For a bf16 cache each V tile is converted to f16 in shared memory so the
- * attention weights can enter P . V as f16 (11 significant bits, one MMA):
- * exact for |v| in [2^-14, 65504]; smaller magnitudes lose low bits (an error
- * below 2^-14 absolute), larger ones saturate and set PKV_FLAG_RANGE.
+ * P . V takes V exactly as stored.  For a bf16 cache the attention weights
+ * enter it as a bf16 high part plus its bf16 residual (two MMAs per 16
+ * positions, ~16 significant bits; bf16 alone would give 8), for an f16 cache
+ * as f16: every V value of either type is used as it is, over its type's
+ * whole range.
  *
  * Two kernels run the same tile pipeline: one CTA per (128-row tile, kv
  * head, sequence), chosen when max_blocks_per_seq * 16 - max_q_len >= 2048
  * (the table admits a long cached prefix, so the items are long; 1024 when
  * max_q_len * Hq / Hkv <= 64, where it runs row replicas), and one
  * persistent CTA per SM walking those items otherwise (prompts: many short
- * items of unequal length).  The environment variable PKV_PREFILL_KERNEL =
- * "tiles" or "persistent" overrides the choice; results agree within the
- * tolerance either way.
+ * items of unequal length).  pkv_set_route(PKV_ROUTE_PREFILL,
+ * PKV_PREFILL_PER_ITEM | PKV_PREFILL_PERSISTENT) overrides the choice;
+ * results agree within the tolerance either way.
  */
 int paged_prefill_attention(void *out, const void *q, int q_dtype,
                             const void *k_cache, const void *v_cache, int cache_dtype,
@@ -431,6 +431,33 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype,
 #define PKV_PREFILL_PER_ITEM 2
 int pkv_set_route(int which, int choice);
 int pkv_get_route(int which);
+
+/* ------------------------------------------------------------------------ */
+/* Failure-path test hook.                                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * Makes the next call that launches the given kernel family take its timeout
+ * path, so that tests can check that path without a fault or a hang.  In that
+ * call every bounded in-kernel wait is limited to limit_ns (normally 4 s), and
+ *  - PKV_STALL_DECODE (the decode kernel: paged_decode_attention, and the
+ *    8-row-unit route of paged_decode_attention_multi): the worker holding the
+ *    first work item replaces its first pipeline wait by a wait on a barrier
+ *    that nothing completes;
+ *  - PKV_STALL_PREFILL (either prefill kernel, from paged_prefill_attention or
+ *    the multi-query route): the softmax warps of every CTA with work replace
+ *    their first wait for S by such a wait.
+ * That wait gives up after limit_ns; the CTA records PKV_FLAG_TIMEOUT, lets
+ * the copies and tensor-core operations it has in flight complete (waiting
+ * within the same limit), frees its tensor memory and exits; its outputs are
+ * left incomplete.  The call's status (paged_decode_status, or the prefill
+ * status word) reports the timeout, and the workspace is fit for the next
+ * call.  One-shot: the next call that launches the family consumes the
+ * request; limit_ns = 0 cancels it.  limit_ns must lie in [1e6, 1e10]
+ * (1 ms .. 10 s), else PKV_EINVAL.  For tests of the failure path only.
+ */
+#define PKV_STALL_DECODE 0
+#define PKV_STALL_PREFILL 1
+int pkv_test_stall_next(int which, uint64_t limit_ns);
 
 /* ------------------------------------------------------------------------ */
 /* Staging copy.                                                            */

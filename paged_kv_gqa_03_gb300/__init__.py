@@ -16,7 +16,7 @@ __all__ = [
     "paged_decode_attention", "paged_prefill_attention", "paged_decode_status", "paged_decode_merge",
     "paged_decode_attention_static", "paged_decode_static_status",
     "paged_kv_copy_blocks", "pkv_copy", "pkv_status_string", "pkv_version", "pkv_set_route",
-    "pkv_get_route", "BlockManager",
+    "pkv_get_route", "pkv_test_stall_next", "BlockManager", "Prepared",
     "DTYPE_CODES", "LIB_PATH", "lib",
 ]
 
@@ -62,6 +62,7 @@ _sig("pkv_last_cuda_error", _i32)
 _sig("pkv_version", _i32)
 _sig("pkv_set_route", _i32, _i32, _i32)
 _sig("pkv_get_route", _i32, _i32)
+_sig("pkv_test_stall_next", _i32, _i32, ctypes.c_uint64)
 _sig("pkv_bm_create", _P, _i64)
 _sig("pkv_bm_destroy", None, _P)
 _sig("pkv_bm_allocate", _i32, _P, _i64, _i64)
@@ -121,6 +122,15 @@ def pkv_set_route(which, choice):
     prev = names[_L.pkv_get_route(idx)]
     _check(_L.pkv_set_route(idx, names.index(choice)), "pkv_set_route")
     return prev
+
+
+def pkv_test_stall_next(which, limit_ns):
+    """Failure-path test hook: the next call that launches the "decode" or
+    "prefill" kernel family runs out a wait on a barrier nothing completes
+    (every wait of that call limited to limit_ns) and reports
+    PKV_FLAG_TIMEOUT; see include/pagedkv.h."""
+    _check(_L.pkv_test_stall_next({"decode": 0, "prefill": 1}[which], int(limit_ns)),
+           "pkv_test_stall_next")
 
 
 def pkv_get_route(which):
@@ -183,20 +193,39 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+class Prepared:
+    """One C call with its arguments marshalled once (returned by the calls
+    below when given prepare=True): calling it issues the call again on the
+    same buffers and stream, for a decode loop that runs the same step every
+    iteration.  The buffers must stay alive and keep their addresses."""
+
+    __slots__ = ("fn", "args", "name")
+
+    def __init__(self, fn, args, name):
+        self.fn, self.args, self.name = fn, args, name
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != PKV_OK:
+            raise PagedKVError(rc, self.name)
+
+
 def paged_kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None,
-                    stream=None, calibrated=False):
+                    stream=None, calibrated=False, prepare=False):
     """Writes k_new/v_new [B, Hkv, D] into the caches [num_blocks, Hkv, 16, D]
     at slot_mapping[b] (int64; < 0 skips).  calibrated=True: FP8 block scales
     follow the block's running max (paged_kv_append_calibrated)."""
     torch = _torch()
     B, Hkv, D = k_new.shape
     fn = _L.paged_kv_append_calibrated if calibrated else _L.paged_kv_append
-    _check(fn(
-        _dev(k_new, "k_new"), _dev(v_new, "v_new"), _code(k_new),
-        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _code(k_cache),
-        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
-        _dev(slot_mapping, "slot_mapping", torch.int64), B, Hkv, D, k_cache.shape[0],
-        _stream(stream)), "paged_kv_append")
+    args = (_dev(k_new, "k_new"), _dev(v_new, "v_new"), _code(k_new),
+            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _code(k_cache),
+            _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+            _dev(slot_mapping, "slot_mapping", torch.int64), B, Hkv, D, k_cache.shape[0],
+            _stream(stream))
+    if prepare:
+        return Prepared(fn, args, "paged_kv_append")
+    _check(fn(*args), "paged_kv_append")
 
 
 def paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits=0, q_len=1):
@@ -216,7 +245,7 @@ def paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits
 
 def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, scale,
                            k_scale=None, v_scale=None, num_splits=0, workspace=None, stream=None,
-                           window=0):
+                           window=0, prepare=False):
     """out[b, hq] = softmax(scale * q[b, hq] . K_b^T) V_b over the paged cache.
 
     q, out [B, Hq, D]: one new token per sequence (paged_decode_attention).
@@ -224,7 +253,8 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
     the cache up to its own position (paged_decode_attention_multi).
     window > 0: each row sees only its `window` most recent positions.
     workspace: a uint8 CUDA tensor of paged_decode_workspace_bytes(...) bytes;
-    allocated here (by torch) when None."""
+    allocated here (by torch) when None.  prepare=True returns the call as a
+    Prepared object instead of issuing it."""
     torch = _torch()
     if q.dim() == 4:
         B, q_len, Hq, D = q.shape
@@ -244,12 +274,14 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, context_lens, 
     tail = (num_blocks, float(scale), num_splits, _dev(workspace, "workspace"),
             workspace.numel() * workspace.element_size(), _stream(stream))
     if q.dim() == 4 or window:
-        _check(_L.paged_decode_attention_multi(_out(out), _dev(q, "q"), _code(q), *args,
-                                               B, q_len, int(window), Hq, Hkv, D, *tail),
-               "paged_decode_attention_multi")
+        fn, name = _L.paged_decode_attention_multi, "paged_decode_attention_multi"
+        full = (_out(out), _dev(q, "q"), _code(q), *args, B, q_len, int(window), Hq, Hkv, D, *tail)
     else:
-        _check(_L.paged_decode_attention(_out(out), _dev(q, "q"), _code(q), *args,
-                                         B, Hq, Hkv, D, *tail), "paged_decode_attention")
+        fn, name = _L.paged_decode_attention, "paged_decode_attention"
+        full = (_out(out), _dev(q, "q"), _code(q), *args, B, Hq, Hkv, D, *tail)
+    if prepare:
+        return Prepared(fn, full, name)
+    _check(fn(*full), name)
     return workspace
 
 

@@ -78,6 +78,23 @@ Registry &registry() {
 // Route overrides set by pkv_set_route (PKV_ROUTE_AUTO = the rule of shapes).
 std::atomic<int> g_route[2];
 
+// Limit of every bounded in-kernel wait (a wait that runs out sets
+// PKV_FLAG_TIMEOUT instead of hanging).
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Pending failure-path test requests (pkv_test_stall_next), one per kernel
+// family, consumed by the next call that launches that family: the wait
+// limit of that call, or 0.
+std::atomic<uint64_t> g_stall[2];
+
+// Sets the wait limit and the test hook of a launch from a pending request.
+template <class Params>
+void take_stall(Params &p, int which) {
+  const uint64_t st = g_stall[which].exchange(0, std::memory_order_relaxed);
+  p.stall_ns = st;
+  p.timeout_ns = st ? st : kWaitLimitNs;
+}
+
 struct DeviceFacts {
   int sm_count = 0;
   int ctas_per_sm[kMaxKernels] = {};  // 0 = not yet configured
@@ -186,6 +203,48 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int64_t num_
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+  return PKV_OK;
+}
+
+// Encoded tensor maps of recently used caches.  A map depends only on the
+// cache's base address, element type and dimensions, which make up the key,
+// so a hit is always the map the encoder would produce; decode calls on the
+// same cache (every layer step of a serving loop) skip the encoder.  Small
+// and fixed in size, replaced round-robin; no allocation.
+struct MapKey {
+  const void *base;
+  int64_t num_blocks;
+  int dtype, Hkv, D;
+  bool operator==(const MapKey &o) const {
+    return base == o.base && num_blocks == o.num_blocks && dtype == o.dtype && Hkv == o.Hkv && D == o.D;
+  }
+};
+struct MapCache {
+  static constexpr int kEntries = 64;
+  MapKey key[kEntries] = {};
+  CUtensorMap map[kEntries];
+  int used = 0, next = 0;
+  std::mutex mu;
+};
+MapCache g_maps;
+
+int cache_map(CUtensorMap *map, const void *base, int dtype, int64_t num_blocks, int Hkv, int D) {
+  const MapKey k{base, num_blocks, dtype, Hkv, D};
+  {
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    for (int i = 0; i < g_maps.used; ++i)
+      if (g_maps.key[i] == k) {
+        *map = g_maps.map[i];
+        return PKV_OK;
+      }
+  }
+  const int rc = encode_cache_map(map, base, dtype, num_blocks, Hkv, D);
+  if (rc != PKV_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_maps.mu);
+  const int slot = g_maps.used < MapCache::kEntries ? g_maps.used++ : g_maps.next;
+  if (g_maps.used == MapCache::kEntries) g_maps.next = (slot + 1) % MapCache::kEntries;
+  g_maps.key[slot] = k;
+  g_maps.map[slot] = *map;
   return PKV_OK;
 }
 
@@ -298,6 +357,13 @@ int pkv_set_route(int which, int choice) {
     return PKV_EINVAL;
   }
   g_route[which].store(choice, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+int pkv_test_stall_next(int which, uint64_t limit_ns) {
+  if (which != PKV_STALL_DECODE && which != PKV_STALL_PREFILL) return PKV_EINVAL;
+  if (limit_ns != 0 && (limit_ns < 1000000ull || limit_ns > 10000000000ull)) return PKV_EINVAL;
+  g_stall[which].store(limit_ns, std::memory_order_relaxed);
   return PKV_OK;
 }
 
@@ -474,9 +540,9 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
       const MqWsLayout M = mq_ws_layout(B, sms);
       if (workspace_bytes >= M.total) {
         CUtensorMap tmK, tmV;
-        rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+        rc = cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
         if (rc != PKV_OK) return rc;
-        rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+        rc = cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
         if (rc != PKV_OK) return rc;
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         MqParams mp;
@@ -500,15 +566,15 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
         mp.max_blocks = max_blocks_per_seq;
         mp.window = window < (1 << 30) ? window : 0;
         mp.scale_log2 = scale * 1.4426950408889634f;
-        mp.timeout_ns = 4000000000ull;
+        mp.timeout_ns = kWaitLimitNs;
         return cuda_status(launch_mq_decode(mp, cache_dtype, tmK, tmV, sms, s));
       }
     }
     if (!units && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && prefill_fills) {
       CUtensorMap tmK, tmV;
-      rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+      rc = cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
       if (rc != PKV_OK) return rc;
-      rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+      rc = cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
       if (rc != PKV_OK) return rc;
       WsHeader *hdr = reinterpret_cast<WsHeader *>(static_cast<uint8_t *>(workspace) + L.hdr);
       cudaError_t e = cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s);
@@ -533,7 +599,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
       pp.max_tiles = (int)tiles;
       pp.window = window < (1 << 30) ? window : 0;
       pp.scale_log2 = scale * 1.4426950408889634f;
-      pp.timeout_ns = 4000000000ull;
+      take_stall(pp, PKV_STALL_PREFILL);
       return cuda_status(launch_prefill_auto(pp, cache_dtype, tmK, tmV, s));
     }
   }
@@ -543,9 +609,9 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   if (rc != PKV_OK) return rc;
 
   CUtensorMap tmK, tmV;
-  rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+  rc = cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
   if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+  rc = cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
   if (rc != PKV_OK) return rc;
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -581,7 +647,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   p.max_blocks = max_blocks_per_seq;
   p.out_dtype = q_dtype;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = 4000000000ull;
+  take_stall(p, PKV_STALL_DECODE);
 
   p.inline_plan = B + 1 <= kInlinePrefix ? 1 : 0;
   p.n_ctas = (P + k.warps - 1) / k.warps;
@@ -628,9 +694,9 @@ int paged_prefill_attention(void *out, const void *q, int q_dtype, const void *k
   if (!out || !q || !k_cache || !v_cache || !block_table || !context_lens || !q_start) return PKV_EINVAL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
   CUtensorMap tmK, tmV;
-  rc = encode_cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
+  rc = cache_map(&tmK, k_cache, cache_dtype, num_blocks, Hkv, D);
   if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
+  rc = cache_map(&tmV, v_cache, cache_dtype, num_blocks, Hkv, D);
   if (rc != PKV_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (status) {
@@ -656,7 +722,7 @@ int paged_prefill_attention(void *out, const void *q, int q_dtype, const void *k
   p.max_tiles = (int)tiles;
   p.window = window < (1 << 30) ? window : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = 4000000000ull;
+  take_stall(p, PKV_STALL_PREFILL);
   return cuda_status(launch_prefill_auto(p, cache_dtype, tmK, tmV, s));
 }
 

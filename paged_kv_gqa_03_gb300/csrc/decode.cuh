@@ -45,21 +45,28 @@
 
 namespace pkv {
 
-template <class CacheT, class QT, int D_, int GC_, bool MMA_, int WARPS_, int BUDGET_>
+// BPS_ = blocks per pipeline stage.  2 (fp8 tensor-core path only): a stage
+// holds two consecutive blocks of one unit, which share one barrier, one
+// stage record, one online-softmax update (one max exchange, one accumulator
+// rescale per 32 tokens) and one producer step — an fp8 block carries half a
+// 16-bit block's bytes for the same per-block instructions, which made the
+// one-block fp8 kernel issue-bound.
+template <class CacheT, class QT, int D_, int GC_, bool MMA_, int WARPS_, int BUDGET_, int BPS_ = 1>
 struct DecodeCfg {
   using Cache = CacheT;
   using Q = QT;
-  static constexpr int D = D_, GC = GC_, WARPS = WARPS_;
+  static constexpr int D = D_, GC = GC_, WARPS = WARPS_, BPS = BPS_;
   static constexpr bool MMA = MMA_;
   static constexpr bool FP8 = CacheT::kBytes == 1;
   static constexpr int ROWB = D * CacheT::kBytes;           // bytes per token row
   static constexpr int TILE = kBlock * ROWB;                // bytes per (block, head) tile
-  static constexpr int STAGES_RAW = BUDGET_ / (2 * TILE);
+  static constexpr int STAGE_BYTES = BPS * 2 * TILE;        // K and V tiles of a stage's blocks
+  static constexpr int STAGES_RAW = BUDGET_ / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr int NBOX = ROWB >= 128 ? ROWB / 128 : 1;  // TMA boxes per tile
   static constexpr int BOX_ROWS = ROWB >= 128 ? kBlock : kBlock * ROWB / 128;
   static constexpr int BOX_ELEMS = 128 / CacheT::kBytes;
-  static constexpr size_t TILES_BYTES = (size_t)WARPS * STAGES * 2 * TILE;
+  static constexpr size_t TILES_BYTES = (size_t)WARPS * STAGES * STAGE_BYTES;
   static constexpr size_t META_BYTES = (size_t)WARPS * STAGES * sizeof(StageMeta);
   static constexpr size_t BAR_BYTES = (size_t)WARPS * STAGES * 8;
   static constexpr size_t QBUF_BYTES = MMA ? 0 : (size_t)WARPS * GC * D * 4;
@@ -72,6 +79,7 @@ struct DecodeCfg {
   static_assert(TILE % 1024 == 0, "tiles must keep 1024-byte alignment for the swizzle");
   static_assert(!MMA || GC == 8, "the MMA path serves 8-head chunks");
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BPS == 1 || (BPS == 2 && MMA && FP8), "two blocks per stage: the fp8 tensor-core path");
 };
 
 // ---------------------------------------------------------------------------
@@ -94,42 +102,81 @@ __device__ __forceinline__ void load_seq(Producer &pr, const DecodeParams &p) {
   pr.j0 = first_block(p, ctx);
 }
 
+// Block-table entry (and, for fp8, the block's K / V scales) of block jj of
+// the producer's current unit, from the lane-parallel window of 32 entries;
+// the window moves to start at jj when jj leaves it (the following window
+// is loaded one window ahead).
 template <class Cfg>
-__device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, const CUtensorMap *tmK,
-                                        const CUtensorMap *tmV, uint8_t *tiles, StageMeta *meta,
-                                        uint64_t *bars, int stage, int lane, int *cta_flags) {
-  __syncwarp();
-  const int h = pr.hu / p.NC;
-  if (!(pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j >= pr.win_j0 && pr.j < pr.win_j0 + 32)) {
+__device__ __forceinline__ int window_block(Producer &pr, const DecodeParams &p, int jj, int h, int lane,
+                                            float &ks, float &vs) {
+  if (!(pr.b == pr.win_b && pr.hu == pr.win_hu && jj >= pr.win_j0 && jj < pr.win_j0 + 32)) {
     const int32_t *row = p.block_table + (size_t)pr.b * p.max_blocks;
-    if (pr.b == pr.win_b && pr.hu == pr.win_hu && pr.j == pr.win_j0 + 32) {
+    if (pr.b == pr.win_b && pr.hu == pr.win_hu && jj == pr.win_j0 + 32) {
       pr.win_id = pr.nxt_id;  // the window loaded ahead
     } else {
-      const int jj = pr.j + lane;
-      pr.win_id = jj < pr.n ? __ldg(row + jj) : 0;
+      const int jw = jj + lane;
+      pr.win_id = jw < pr.n ? __ldg(row + jw) : 0;
     }
     pr.win_b = pr.b;
     pr.win_hu = pr.hu;
-    pr.win_j0 = pr.j;
+    pr.win_j0 = jj;
     // load the following window now; it is first needed 32 blocks later
-    const int jn = pr.j + 32 + lane;
+    const int jn = jj + 32 + lane;
     pr.nxt_id = jn < pr.n ? __ldg(row + jn) : 0;
     if constexpr (Cfg::FP8) {
-      const int jj = pr.j + lane, id = pr.win_id;
-      float ks = 0.f, vs = 0.f;
-      if (jj < pr.n && id >= 0 && (int64_t)id < p.num_blocks) {
-        ks = __ldg(p.k_scale + (size_t)id * p.Hkv + h);
-        vs = __ldg(p.v_scale + (size_t)id * p.Hkv + h);
+      const int jw = jj + lane, id = pr.win_id;
+      float a = 0.f, c = 0.f;
+      if (jw < pr.n && id >= 0 && (int64_t)id < p.num_blocks) {
+        a = __ldg(p.k_scale + (size_t)id * p.Hkv + h);
+        c = __ldg(p.v_scale + (size_t)id * p.Hkv + h);
       }
-      pr.win_ks = ks;
-      pr.win_vs = vs;
+      pr.win_ks = a;
+      pr.win_vs = c;
     }
   }
-  const int blk = __shfl_sync(kFull, pr.win_id, pr.j - pr.win_j0);
-  float ks = 1.f, vs = 1.f;
+  const int blk = __shfl_sync(kFull, pr.win_id, jj - pr.win_j0);
+  ks = vs = 1.f;
   if constexpr (Cfg::FP8) {
-    ks = __shfl_sync(kFull, pr.win_ks, pr.j - pr.win_j0);
-    vs = __shfl_sync(kFull, pr.win_vs, pr.j - pr.win_j0);
+    ks = __shfl_sync(kFull, pr.win_ks, jj - pr.win_j0);
+    vs = __shfl_sync(kFull, pr.win_vs, jj - pr.win_j0);
+  }
+  return blk;
+}
+
+// Lane 0: the TMA copies of one block's K and V tiles to dk / dv, onto bar.
+// A bad id reads the tile just past the end of the tensor: TMA fills zeros.
+template <class Cfg>
+__device__ __forceinline__ void issue_block(const DecodeParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                            uint8_t *dk, uint8_t *dv, int blk, int h, uint64_t *bar,
+                                            int *cta_flags) {
+  const bool bad = blk < 0 || (int64_t)blk >= p.num_blocks;
+  const int64_t tile_row = bad ? p.num_blocks * p.Hkv : (int64_t)blk * p.Hkv + h;
+  if (bad) atomicOr(cta_flags, PKV_FLAG_BAD_BLOCK);
+  const int y = (int)(tile_row * Cfg::BOX_ROWS);
+#pragma unroll
+  for (int bx = 0; bx < Cfg::NBOX; ++bx) {
+    tma_load_2d(dk + bx * 2048, tmK, bx * Cfg::BOX_ELEMS, y, bar);
+    tma_load_2d(dv + bx * 2048, tmV, bx * Cfg::BOX_ELEMS, y, bar);
+  }
+}
+
+// Fills pipeline stage `stage` with the worker's next item (with BPS = 2 also
+// the one after it, when it is the next block of the same unit and inside the
+// worker's range) and advances the producer; returns the blocks issued.
+template <class Cfg>
+__device__ __forceinline__ int produce(Producer &pr, const DecodeParams &p, const CUtensorMap *tmK,
+                                       const CUtensorMap *tmV, uint8_t *tiles, StageMeta *meta,
+                                       uint64_t *bars, int stage, int lane, int *cta_flags) {
+  __syncwarp();
+  const int h = pr.hu / p.NC;
+  float ks, vs, ks1 = 1.f, vs1 = 1.f;
+  const int blk = window_block<Cfg>(pr, p, pr.j, h, lane, ks, vs);
+  int nb = 1, blk1 = 0;
+  if constexpr (Cfg::BPS == 2) {
+    if (pr.pi + 1 < pr.e && pr.j + 1 < pr.n) {
+      nb = 2;
+      blk1 = window_block<Cfg>(pr, p, pr.j + 1, h, lane, ks1, vs1);
+    }
   }
   int flags = 0;
   if (pr.pi == pr.s || pr.j == pr.j0) {
@@ -137,18 +184,15 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     pr.seg_j0 = pr.j;
     pr.seg_wfirst = (pr.pi == pr.s);
   }
-  if (pr.pi + 1 == pr.e || pr.j + 1 == pr.n) {
+  const int jl = pr.j + nb - 1;  // the stage's last block
+  if (pr.pi + nb == pr.e || jl + 1 == pr.n) {
     flags |= kLast;
-    if (pr.seg_j0 == pr.j0 && pr.j + 1 == pr.n) flags |= kComplete;
+    if (pr.seg_j0 == pr.j0 && jl + 1 == pr.n) flags |= kComplete;
   }
   if (pr.seg_wfirst) flags |= kWFirst;
   const int rem = pr.ctx - pr.j * kBlock;
   const int nvalid = min(kBlock, rem);
   if (lane == 0) {
-    const bool bad = blk < 0 || (int64_t)blk >= p.num_blocks;
-    // a bad id reads the tile just past the end of the tensor: TMA fills zeros
-    const int64_t tile_row = bad ? p.num_blocks * p.Hkv : (int64_t)blk * p.Hkv + h;
-    if (bad) atomicOr(cta_flags, PKV_FLAG_BAD_BLOCK);
     StageMeta m;
     m.b = pr.b;
     m.hu = pr.hu;
@@ -158,22 +202,21 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     m.vs = vs;
     m.flags = flags;
     m.rem = rem;
+    m.ks1 = ks1;
+    m.vs1 = vs1;
+    m.nb = nb;
+    m.pad = 0;
     meta[stage] = m;
     // the warp's reads of this stage have completed (their results were
     // consumed), so the TMA overwrite needs no proxy fence here
-    mbar_arrive_expect_tx(&bars[stage], 2 * Cfg::TILE);
-    uint8_t *dk = tiles + (size_t)stage * 2 * Cfg::TILE;
-    uint8_t *dv = dk + Cfg::TILE;
-    const int y = (int)(tile_row * Cfg::BOX_ROWS);
-#pragma unroll
-    for (int bx = 0; bx < Cfg::NBOX; ++bx) {
-      tma_load_2d(dk + bx * 2048, tmK, bx * Cfg::BOX_ELEMS, y, &bars[stage]);
-      tma_load_2d(dv + bx * 2048, tmV, bx * Cfg::BOX_ELEMS, y, &bars[stage]);
-    }
+    mbar_arrive_expect_tx(&bars[stage], nb * 2 * Cfg::TILE);
+    uint8_t *dk = tiles + (size_t)stage * Cfg::STAGE_BYTES;
+    issue_block<Cfg>(p, tmK, tmV, dk, dk + Cfg::TILE, blk, h, &bars[stage], cta_flags);
+    if (nb == 2) issue_block<Cfg>(p, tmK, tmV, dk + 2 * Cfg::TILE, dk + 3 * Cfg::TILE, blk1, h, &bars[stage], cta_flags);
   }
-  // advance to the next item
-  ++pr.pi;
-  ++pr.j;
+  // advance past the stage's items
+  pr.pi += nb;
+  pr.j += nb;
   if (pr.j == pr.n && pr.pi < pr.e) {
     if (++pr.hu == p.HU) {
       pr.hu = 0;
@@ -184,6 +227,7 @@ __device__ __forceinline__ void produce(Producer &pr, const DecodeParams &p, con
     }
     pr.j = pr.j0;
   }
+  return nb;
 }
 
 // Zeroes token rows [nvalid, 16) of a tile so stale (possibly non-finite)
@@ -420,6 +464,139 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
 #pragma unroll
     for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) mma16816<false>(st.acc[mt], f.v[mt], pb0, pb1);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Two-block stages (fp8 caches): the same arithmetic as mma_load /
+// mma_compute, over the 32 tokens of two consecutive blocks of one unit with
+// one online-softmax update.  K fragments are loaded and consumed before the
+// V fragments, which keeps the register footprint of two blocks in bounds.
+// ---------------------------------------------------------------------------
+// S^T = K . Q^T of one fp8 block (two independent MMA chains, summed).
+template <class Cfg>
+__device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_t *tk, int lane, float (&s)[4]) {
+  constexpr int ROWB = Cfg::ROWB;
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t kb = smem_u32(tk);
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
+    // k-slots 2t,2t+1 | 2t+8,2t+9 of row gid (+8) hold d = 16ks + 4t + {0,1} | {2,3}
+    const uint32_t k0 = lds32(kb + tile_off<ROWB>(gid, 16 * ks + 4 * tig));
+    const uint32_t k1 = lds32(kb + tile_off<ROWB>(gid + 8, 16 * ks + 4 * tig));
+    uint32_t a[4];
+    a[0] = e4m3x2_to_f16x2((uint16_t)(k0 & 0xffff));
+    a[1] = e4m3x2_to_f16x2((uint16_t)(k1 & 0xffff));
+    a[2] = e4m3x2_to_f16x2((uint16_t)(k0 >> 16));
+    a[3] = e4m3x2_to_f16x2((uint16_t)(k1 >> 16));
+    if (ks & 1)
+      mma16816<false>(s1, a, st.qb[ks][0], st.qb[ks][1]);
+    else
+      mma16816<false>(s0, a, st.qb[ks][0], st.qb[ks][1]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] = s0[i] + s1[i];
+}
+
+// O^T += V^T . P^T of one fp8 block, P (with the block's V scale folded in)
+// already in B-operand form.
+template <class Cfg>
+__device__ __forceinline__ void fp8_pv(MmaState<Cfg> &st, const uint8_t *tv, int lane, uint32_t pb0, uint32_t pb1) {
+  constexpr int ROWB = Cfg::ROWB;
+  constexpr int DPT = Cfg::D / 8;  // head-dim bytes owned by one row group
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t vb = smem_u32(tv);
+  const int trow[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+  uint32_t v[4][DPT / 4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DPT == 16) {
+      const uint4 r = lds128(vb + tile_off<ROWB>(trow[i], 16 * gid));
+      v[i][0] = r.x; v[i][1] = r.y; v[i][2] = r.z; v[i][3] = r.w;
+    } else {
+      const uint2 r = lds64(vb + tile_off<ROWB>(trow[i], 8 * gid));
+      v[i][0] = r.x; v[i][1] = r.y;
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+    // bytes 2mt, 2mt+1 of the thread's head-dim run, from token rows
+    // (2t, 2t+1) and (2t+8, 2t+9), paired for the f16x2 conversion
+    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+    const uint32_t x = __byte_perm(v[0][mt >> 1], v[1][mt >> 1], sel);
+    const uint32_t y = __byte_perm(v[2][mt >> 1], v[3][mt >> 1], sel);
+    uint32_t a[4];
+    a[0] = e4m3x2_to_f16x2((uint16_t)(x & 0xffff));
+    a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
+    a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
+    a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
+    mma16816<false>(st.acc[mt], a, pb0, pb1);
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_pair(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
+                                         uint8_t *tk0, int lane) {
+  static_assert(Cfg::FP8, "two-block stages are the fp8 path");
+  constexpr int ROWB = Cfg::ROWB;
+  const int gid = lane >> 2;
+  const bool two = m.nb == 2;
+  uint8_t *tv0 = tk0 + Cfg::TILE, *tk1 = tk0 + 2 * Cfg::TILE, *tv1 = tk0 + 3 * Cfg::TILE;
+  const int rem0 = m.rem, rem1 = m.rem - kBlock;
+  if (rem0 < kBlock) zero_tail_rows<ROWB>(tv0, rem0, lane);
+  if (two && rem1 < kBlock) zero_tail_rows<ROWB>(tv1, rem1, lane);
+
+  float s[4], t[4];
+  fp8_scores<Cfg>(st, tk0, lane, s);
+  if (two) fp8_scores<Cfg>(st, tk1, lane, t);
+
+  // token rows r of a block visible to score column c: base_c <= r < base_c + W
+  // (see mma_compute); the second block's base is 16 lower
+  const uint32_t wl = (uint32_t)p.wlen;
+  const int base0 = rem0 - st.back0 - p.wlen, base1 = rem0 - st.back1 - p.wlen;
+  const float sc0 = p.scale_log2 * m.ks, sc1 = p.scale_log2 * m.ks1;
+  float x0 = s[0] * sc0, x1 = s[1] * sc0, x2 = s[2] * sc0, x3 = s[3] * sc0;
+  if ((uint32_t)(gid - base0) >= wl) x0 = -INFINITY;
+  if ((uint32_t)(gid - base1) >= wl) x1 = -INFINITY;
+  if ((uint32_t)(gid + 8 - base0) >= wl) x2 = -INFINITY;
+  if ((uint32_t)(gid + 8 - base1) >= wl) x3 = -INFINITY;
+  float y0 = -INFINITY, y1 = -INFINITY, y2 = -INFINITY, y3 = -INFINITY;
+  if (two) {
+    y0 = t[0] * sc1; y1 = t[1] * sc1; y2 = t[2] * sc1; y3 = t[3] * sc1;
+    if ((uint32_t)(gid + 16 - base0) >= wl) y0 = -INFINITY;
+    if ((uint32_t)(gid + 16 - base1) >= wl) y1 = -INFINITY;
+    if ((uint32_t)(gid + 24 - base0) >= wl) y2 = -INFINITY;
+    if ((uint32_t)(gid + 24 - base1) >= wl) y3 = -INFINITY;
+  }
+  float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  // a column that has seen no visible position yet keeps weight 0 (not NaN)
+  const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = exp2f(st.m0 - mb0), al1 = exp2f(st.m1 - mb1);
+  const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1), p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
+  const float q0 = exp2f(y0 - mb0), q1 = exp2f(y1 - mb1), q2 = exp2f(y2 - mb0), q3 = exp2f(y3 - mb1);
+  st.l0 = st.l0 * al0 + ((p0 + p2) + (q0 + q2));
+  st.l1 = st.l1 * al1 + ((p1 + p3) + (q1 + q3));
+  st.m0 = mn0;
+  st.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+    st.acc[mt][0] *= al0;
+    st.acc[mt][1] *= al1;
+    st.acc[mt][2] *= al0;
+    st.acc[mt][3] *= al1;
+  }
+  // the V scales folded into the weights
+  fp8_pv<Cfg>(st, tv0, lane, movmatrix_trans(pack_f16x2(p0 * m.vs, p1 * m.vs)),
+              movmatrix_trans(pack_f16x2(p2 * m.vs, p3 * m.vs)));
+  if (two)
+    fp8_pv<Cfg>(st, tv1, lane, movmatrix_trans(pack_f16x2(q0 * m.vs1, q1 * m.vs1)),
+                movmatrix_trans(pack_f16x2(q2 * m.vs1, q3 * m.vs1)));
 }
 
 // Head-dim index held by accumulator row group `r` (0: gid, 1: gid + 8) of m-tile mt.
@@ -730,8 +907,9 @@ __device__ __forceinline__ void inline_plan(const DecodeParams &p, int32_t *s_pr
 // Partition w's first item {s, b, hu, j} and its end, from the prefix.
 __device__ __forceinline__ int4 locate(const DecodeParams &p, const int32_t *pre, int w, int *end) {
   const int64_t W = (int64_t)p.HU * pre[p.B];
-  const int64_t s = W * w / p.P;
-  *end = (int)(W * (w + 1) / p.P);
+  const int64_t Pe = active_partitions(p, W);
+  const int64_t s = w < Pe ? W * w / Pe : W;
+  *end = w < Pe ? (int)(W * (w + 1) / Pe) : (int)W;
   if (s >= W) return make_int4((int)W, p.B, 0, 0);
   int lo = 0, hi = p.B - 1;  // largest b with HU * prefix[b] <= s
   while (lo < hi) {
@@ -759,7 +937,7 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
   // shared array so every access stays a shared-memory access
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  uint8_t *tiles = smem + (size_t)wib * Cfg::STAGES * 2 * Cfg::TILE;
+  uint8_t *tiles = smem + (size_t)wib * Cfg::STAGES * Cfg::STAGE_BYTES;
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + Cfg::TILES_BYTES) + wib * Cfg::STAGES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES) + wib * Cfg::STAGES;
   float *qbuf = reinterpret_cast<float *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES + Cfg::BAR_BYTES) +
@@ -768,6 +946,7 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       reinterpret_cast<int32_t *>(smem + Cfg::TILES_BYTES + Cfg::META_BYTES + Cfg::BAR_BYTES + Cfg::QBUF_BYTES);
   __shared__ int32_t s_scan[32];
   __shared__ int cta_flags;
+  __shared__ __align__(8) uint64_t dead_bar;  // failure-path test hook: nothing ever arrives on it
   if (threadIdx.x == 0) cta_flags = 0;
   if (lane == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) mbar_init(&bars[s], 1);
@@ -792,6 +971,17 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       e = p.starts[w + 1].x;
     }
     const int total = e - st0.x;
+    // Failure-path test hook: the worker holding the first work item replaces
+    // its first pipeline wait by a wait on dead_bar, which runs out and takes
+    // the timeout path below.
+    const bool stall = p.stall_ns != 0 && st0.x == 0 && total > 0;
+    if (stall) {
+      if (lane == 0) {
+        mbar_init(&dead_bar, 1);
+        fence_barrier_init();
+      }
+      __syncwarp();
+    }
     if (total > 0) {
       Producer pr;
       pr.pi = st0.x;
@@ -808,6 +998,35 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       pr.win_id = 0;
       pr.win_ks = pr.win_vs = 0.f;
       load_seq(pr, p);
+      if constexpr (Cfg::BPS == 2) {
+        // two-block stages: items issued / consumed are counted apart from
+        // the stages that carry them
+        int issued = 0, nst = 0;
+        for (; nst < Cfg::STAGES && issued < total; ++nst)
+          issued += produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, nst, lane, &cta_flags);
+        MmaState<Cfg> state;
+        for (int done = 0, i = 0; done < total; ++i) {
+          const int stage = i % Cfg::STAGES;
+          const uint32_t parity = (uint32_t)(i / Cfg::STAGES) & 1u;
+          if ((stall && i == 0) ? !mbar_wait_bounded(&dead_bar, 0, p.timeout_ns)
+                                : !mbar_wait_bounded(&bars[stage], parity, p.timeout_ns)) {
+            if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
+            // let the copies still in flight land before the CTA's memory goes away
+            for (int k = i; k < nst; ++k)
+              mbar_wait_bounded(&bars[k % Cfg::STAGES], (uint32_t)(k / Cfg::STAGES) & 1u, p.timeout_ns);
+            break;
+          }
+          const StageMeta m = meta[stage];
+          if (m.flags & kFirst) mma_begin<Cfg>(state, p, m, lane);
+          mma_pair<Cfg>(state, p, m, tiles + (size_t)stage * Cfg::STAGE_BYTES, lane);
+          if (issued < total) {  // refilled once its fragments are consumed (as below)
+            issued += produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, stage, lane, &cta_flags);
+            ++nst;
+          }
+          if (m.flags & kLast) mma_finish<Cfg>(state, p, m, w, lane);
+          done += m.nb;
+        }
+      } else {
       int issued = 0;
       for (; issued < Cfg::STAGES && issued < total; ++issued)
         produce<Cfg>(pr, p, &tmK, &tmV, tiles, meta, bars, issued, lane, &cta_flags);
@@ -816,7 +1035,8 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
       for (int i = 0; i < total; ++i) {
         const int stage = i % Cfg::STAGES;
         const uint32_t parity = (uint32_t)(i / Cfg::STAGES) & 1u;
-        if (!mbar_wait_bounded(&bars[stage], parity, p.timeout_ns)) {
+        if ((stall && i == 0) ? !mbar_wait_bounded(&dead_bar, 0, p.timeout_ns)
+                              : !mbar_wait_bounded(&bars[stage], parity, p.timeout_ns)) {
           if (lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
           // let the copies still in flight land before the CTA's memory goes away
           for (int k = i; k < issued; ++k)
@@ -824,7 +1044,7 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
           break;
         }
         const StageMeta m = meta[stage];
-        uint8_t *tk = tiles + (size_t)stage * 2 * Cfg::TILE;
+        uint8_t *tk = tiles + (size_t)stage * Cfg::STAGE_BYTES;
         uint8_t *tv = tk + Cfg::TILE;
         if constexpr (Cfg::MMA) {
           // The stage is refilled after the block is computed: every fragment
@@ -853,6 +1073,7 @@ __global__ void __launch_bounds__(Cfg::WARPS * 32, Cfg::MIN_CTAS)
           else
             simt_finish<Cfg>(state, p, m, w, lane);
         }
+      }
       }
     }
   }

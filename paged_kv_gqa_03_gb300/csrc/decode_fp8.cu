@@ -5,21 +5,24 @@
 namespace pkv {
 
 // fp8 blocks carry half the bytes of bf16 ones for the same per-block work, so
-// they want more warps in flight: 4 warps x 16 KiB (4 stages), 3 CTAs per SM
-// measured 5.91 TB/s on the long-context fp8 layer against 5.11 for 5 x 16 KiB.
+// they want more warps in flight: 4 warps x 16 KiB, 3 CTAs per SM.  With one
+// block per stage (4 stages) that shape measured 5.91 TB/s on the long-context
+// fp8 layer against 5.11 for 5 x 16 KiB, and it was issue-bound (half the
+// bytes per instruction of the bf16 kernel); stages of two blocks (2 stages of
+// 8 KiB) share the per-stage and per-softmax-update work between 32 tokens.
 constexpr int kFp8Warps = 4;
 
 int register_decode_fp8(DecodeKernel *out) {
   int n = 0;
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, kFp8Warps, kBudget>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 8, true, kFp8Warps, kBudget>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, kFp8Warps, kBudget>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 8, true, kFp8Warps, kBudget>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, kFp8Warps, kBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 8, true, kFp8Warps, kBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, kFp8Warps, kBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 8, true, kFp8Warps, kBudget, 2>>();
 #ifdef PKV_SWEEP_SHAPES
   // for comparison runs and sweeps only, not in the product build: the
-  // CUDA-core path on this cache type (PKV_PATH=simt) and alternative
-  // pipeline shapes (warps per CTA, pipeline bytes per warp;
-  // PKV_DECODE_WARPS / PKV_DECODE_STAGES)
+  // CUDA-core path on this cache type (PKV_PATH=simt), one block per stage
+  // (PKV_DECODE_STAGES=4) and alternative pipeline shapes (warps per CTA,
+  // pipeline bytes per warp; PKV_DECODE_WARPS / PKV_DECODE_STAGES)
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 2, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 2, false, kWarps, kBudget>>();
@@ -28,10 +31,11 @@ int register_decode_fp8(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 1, false, kWarps, kBudget>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 1, false, kWarps, kBudget>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 5, 16 * 1024>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 6, 16 * 1024>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 8, 12 * 1024>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 4, 20 * 1024>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, kFp8Warps, kBudget, 1>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, kFp8Warps, 24 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 5, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 6, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 3, 24 * 1024, 2>>();
 #endif
   return n;
 }

@@ -30,12 +30,16 @@ struct WsHeader {
 // scans context_lens into shared memory); larger ones use the plan kernel.
 constexpr int kInlinePrefix = 2048;
 
-// Per stage of a warp's pipeline: what the producer issued into it.
+// Per stage of a warp's pipeline: what the producer issued into it (one
+// block, or two consecutive blocks of one unit on the two-block fp8 path).
 struct StageMeta {
   int32_t b, hu, j, nvalid;  // nvalid = min(16, rem): cache rows of the block inside ctx
-  float ks, vs;
+  float ks, vs;              // fp8 scales of the (first) block
   int32_t flags;
   int32_t rem;               // ctx - 16 j: positions of the sequence from this block on
+  float ks1, vs1;            // fp8 scales of the second block
+  int32_t nb;                // blocks in the stage (1 or 2)
+  int32_t pad;
 };
 enum : int32_t {
   kFirst = 1,     // first block of a segment: reset state, load q
@@ -67,6 +71,7 @@ struct DecodeParams {
   int out_dtype;
   float scale_log2;     // softmax scale * log2(e)
   uint64_t timeout_ns;
+  uint64_t stall_ns;    // failure-path test hook (pkv_test_stall_next): 0 = off
   int inline_plan;      // 1: the decode kernel computes prefix and partition starts itself
   int n_ctas;           // decode grid size
 };
@@ -85,6 +90,14 @@ __device__ __forceinline__ int first_block(const DecodeParams &p, int ctx) {
 // Work items (blocks streamed per unit) of a sequence of (clamped) length ctx.
 __device__ __forceinline__ int seq_items(const DecodeParams &p, int ctx) {
   return (ctx + kBlock - 1) / kBlock - first_block(p, ctx);
+}
+// Partitions that receive work: P, or one per work item when the call has
+// fewer items than partitions (a small step: more partitions would only add
+// empty ranges for the merge to walk).  Partition w < Pe covers items
+// [W w / Pe, W (w + 1) / Pe); the decode kernel, the plan and the merge
+// compute it alike from W.
+__device__ __forceinline__ int64_t active_partitions(const DecodeParams &p, int64_t W) {
+  return W < p.P ? (W > 0 ? W : 1) : p.P;
 }
 #endif
 
@@ -125,6 +138,7 @@ struct PrefillParams {
   int window;               // 0 = none
   float scale_log2;         // softmax scale * log2(e), > 0
   uint64_t timeout_ns;
+  uint64_t stall_ns;        // failure-path test hook (pkv_test_stall_next): 0 = off
 };
 // Launches the prefill kernel for (cache dtype, D); cudaErrorNotSupported for
 // a combination that is not compiled.

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   }
   __syncthreads();  // prefix[B] is read below by other threads
   const int64_t W = (int64_t)p.HU * total_blocks;
+  const int64_t Pe = active_partitions(p, W);
   if (tid == 0) {
     p.hdr->P = p.P;
     p.hdr->W = (int32_t)W;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   }
   const int32_t *pre = in_smem ? s_prefix : p.prefix;
   for (int w = tid; w <= p.P; w += blockDim.x) {
-    const int64_t s = W * w / p.P;
+    const int64_t s = w < Pe ? W * w / Pe : W;
     int4 r;
     if (s >= W) {
       r = make_int4((int)W, p.B, 0, 0);
@@ -127,7 +128,10 @@ cudaError_t launch_plan(const DecodeParams &p, cudaStream_t stream) {
 // items [floor(w W / P), floor((w+1) W / P)) — the plan kernel's rule,
 // recomputed.  Segments are taken in chunks whose LSEs are staged in shared
 // memory; each thread keeps an online max / sum for its head and accumulates
-// 4 head-dim elements of every partial with one 16-byte load.
+// 4 head-dim elements of every partial with one 16-byte load, eight
+// partials' loads in flight at a time (a long context cut over many warps —
+// the 32K fp8 layer has ~14 partials per unit — would otherwise pay one L2
+// latency per partial in sequence).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 v) {
   if (dtype == PKV_F32) {
@@ -141,9 +145,9 @@ __device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 
   }
 }
 
-__global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) splitk_merge_kernel(const DecodeParams p) {
   constexpr int kSegChunk = 32;
-  constexpr int kVecPerThread = kChunkMax * 128 / 4 / 128;  // float4s per thread (D <= 128)
+  constexpr int kBatch = 8;  // partials whose loads are in flight together
   __shared__ float s_lse[kSegChunk][kChunkMax];
   __shared__ int32_t s_base[kSegChunk];
   grid_dep_wait();
@@ -167,78 +171,76 @@ __global__ void __launch_bounds__(128) splitk_merge_kernel(const DecodeParams p)
   const int D = p.D;
   const int pb = p.prefix[b];
   const int n = p.prefix[b + 1] - pb;
-  const int nvec = gc * D / 4;
+  const int nvec = gc * D / 4;  // float4s of the unit's rows: <= blockDim.x
   // output offset of row r0 + g of this unit ([B][q_len][Hq][D])
   auto out_row = [&](int g) {
     const int r = r0 + g, i = r / p.G;
     return (((size_t)b * p.q_len + i) * p.Hq + h * p.G + (r - i * p.G)) * (size_t)D;
   };
+  const int v = threadIdx.x;
+  const int g = (4 * v) / D, d = (4 * v) % D;
   if (n == 0) {  // nothing to attend: the output is zero
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x)
-      store4_out(p.out_dtype, p.out, out_row(4 * v / D) + (4 * v) % D, make_float4(0.f, 0.f, 0.f, 0.f));
+    if (v < nvec) store4_out(p.out_dtype, p.out, out_row(g) + d, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
   const int64_t W = (int64_t)p.HU * p.prefix[p.B];
+  const int64_t Pe = active_partitions(p, W);
   const int64_t a = (int64_t)p.HU * pb + (int64_t)hu * n, e = a + n;
-  const int wf = (int)(((a + 1) * p.P - 1) / W);
-  const int wl = (int)((e * p.P - 1) / W);
+  const int wf = (int)(((a + 1) * Pe - 1) / W);
+  const int wl = (int)((e * Pe - 1) / W);
   if (wf == wl) return;
 
-  float4 acc[kVecPerThread];
-  float M[kVecPerThread], den[kVecPerThread];
-#pragma unroll
-  for (int k = 0; k < kVecPerThread; ++k) {
-    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    M[k] = -INFINITY;
-    den[k] = 0.f;
-  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = -INFINITY, den = 0.f;
   for (int cs = wf; cs <= wl; cs += kSegChunk) {
     const int ns = min(kSegChunk, wl - cs + 1);
     __syncthreads();  // the previous chunk's staging has been consumed
     for (int i = threadIdx.x; i < ns * kChunkMax; i += blockDim.x) {
-      const int sgi = i / kChunkMax, g = i % kChunkMax;
+      const int sgi = i / kChunkMax, gg = i % kChunkMax;
       const int w = cs + sgi;
-      const int64_t sw = W * w / p.P, ew = W * (w + 1) / p.P;
+      const int64_t sw = W * w / Pe, ew = W * (w + 1) / Pe;
       const bool valid = (a > sw ? a : sw) < (e < ew ? e : ew);
       const int slot = sw >= a ? 0 : 1;
       const int32_t base = (int32_t)(((int64_t)w * 2 + slot) * kChunkMax);
-      if (g == 0) s_base[sgi] = base;
-      s_lse[sgi][g] = (valid && g < gc) ? p.part_lse[base + g] : -INFINITY;
+      if (gg == 0) s_base[sgi] = base;
+      s_lse[sgi][gg] = (valid && gg < gc) ? p.part_lse[base + gg] : -INFINITY;
     }
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kVecPerThread; ++k) {
-      const int v = threadIdx.x + k * blockDim.x;
-      if (v >= nvec) continue;
-      const int g = (4 * v) / D, d = (4 * v) % D;
-      float cm = -INFINITY;
-      for (int sgi = 0; sgi < ns; ++sgi) cm = fmaxf(cm, s_lse[sgi][g]);
-      if (cm == -INFINITY) continue;
-      const float mn = fmaxf(M[k], cm);
-      const float rescale = exp2f(M[k] - mn);
-      acc[k].x *= rescale; acc[k].y *= rescale; acc[k].z *= rescale; acc[k].w *= rescale;
-      den[k] *= rescale;
-      for (int sgi = 0; sgi < ns; ++sgi) {
-        const float l = s_lse[sgi][g];
-        if (l == -INFINITY) continue;
-        const float wt = exp2f(l - mn);
-        const float4 o = *reinterpret_cast<const float4 *>(p.part_o + ((size_t)s_base[sgi] + g) * D + d);
-        acc[k].x = fmaf(wt, o.x, acc[k].x);
-        acc[k].y = fmaf(wt, o.y, acc[k].y);
-        acc[k].z = fmaf(wt, o.z, acc[k].z);
-        acc[k].w = fmaf(wt, o.w, acc[k].w);
-        den[k] += wt;
-      }
-      M[k] = mn;
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kVecPerThread; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
     if (v >= nvec) continue;
-    const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;  // no visible position: 0
-    store4_out(p.out_dtype, p.out, out_row(4 * v / D) + (4 * v) % D,
-               make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv));
+    float cm = -INFINITY;
+    for (int sgi = 0; sgi < ns; ++sgi) cm = fmaxf(cm, s_lse[sgi][g]);
+    if (cm == -INFINITY) continue;
+    const float mn = fmaxf(M, cm);
+    const float rescale = exp2f(M - mn);
+    acc.x *= rescale; acc.y *= rescale; acc.z *= rescale; acc.w *= rescale;
+    den *= rescale;
+    // a batch of partials is loaded before any is used, so their L2
+    // latencies overlap (empty partials load nothing and weigh 0)
+    for (int s0 = 0; s0 < ns; s0 += kBatch) {
+      float4 o[kBatch];
+      float wt[kBatch];
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        const int sgi = s0 + t < ns ? s0 + t : 0;
+        const float l = s0 + t < ns ? s_lse[sgi][g] : -INFINITY;
+        wt[t] = l == -INFINITY ? 0.f : exp2f(l - mn);
+        o[t] = l == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f)
+                              : *reinterpret_cast<const float4 *>(p.part_o + ((size_t)s_base[sgi] + g) * D + d);
+      }
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        acc.x = fmaf(wt[t], o[t].x, acc.x);
+        acc.y = fmaf(wt[t], o[t].y, acc.y);
+        acc.z = fmaf(wt[t], o[t].z, acc.z);
+        acc.w = fmaf(wt[t], o[t].w, acc.w);
+        den += wt[t];
+      }
+    }
+    M = mn;
+  }
+  if (v < nvec) {
+    const float inv = den > 0.f ? 1.f / den : 0.f;  // no visible position: 0
+    store4_out(p.out_dtype, p.out, out_row(g) + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
 }
 
@@ -246,8 +248,12 @@ cudaError_t launch_splitk_merge(const DecodeParams &p, cudaStream_t stream, bool
   const int units = p.B * p.HU;
   if (units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
+  // one float4 of a unit's rows per thread (D <= 128): as many threads as the
+  // widest unit has float4s (an MHA unit has one row, 32 float4s at D = 128)
+  const int rows = p.GC < p.R ? p.GC : p.R;
+  const int threads = (rows * p.D / 4 + 31) / 32 * 32;
   cfg.gridDim = dim3(units);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(threads < 32 ? 32 : threads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

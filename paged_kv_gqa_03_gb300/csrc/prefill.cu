@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF];
   // per item: Q staged, O read out; row-max exchange per tile, row-sum exchange per item
   __shared__ __align__(8) uint64_t q_full, o_free, xch[2], xl, fin;
+  __shared__ __align__(8) uint64_t dead;
   __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
   __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
   __shared__ uint32_t tmem_base;
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&xch[1], Cfg::SOFTMAX / 32);
     mbar_init(&xl, Cfg::SOFTMAX / 32);
     mbar_init(&fin, 2);  // one commit from each issuing warp
+    mbar_init(&dead, 1);  // failure-path test hook: nothing ever arrives on it
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = 0;
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (!ok) break;
         if (lane == 0) v_consumed = gj + 1;
         uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-        if constexpr (!Cfg::VCVT) {  // (with the conversion the softmax warps zero them)
+        {  // stale cache rows past the context: weight 0, but 0 * NaN is NaN
           const int kv0 = (it.j_first + j) * Cfg::N;  // first position of the tile
           zero_v_rows<Cfg>(vt, it.ctx - kv0, min(it.nblk * kBlock - kv0, Cfg::N), lane);
         }
@@ -396,7 +398,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       bool staged = false;  // the next item's Q copy is in flight
       for (int j = 0; j < T; ++j) {
         const int gj = g + j, sb = gj % Cfg::SBUF;
-        ok = warp_wait(&s_full[sb], (uint32_t)(gj / Cfg::SBUF) & 1u, p.timeout_ns);
+        // failure-path test hook: the first tile's wait is on a barrier
+        // nothing completes, so it runs out and the CTA takes its abort path
+        ok = (p.stall_ns != 0 && gj == 0)
+                 ? warp_wait(&dead, 0, p.timeout_ns)
+                 : warp_wait(&s_full[sb], (uint32_t)(gj / Cfg::SBUF) & 1u, p.timeout_ns);
         if (!ok) break;
         tc::fence_after();
         const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
@@ -444,18 +450,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
         float sum = 0.f;
-        uint32_t w[SC / 2];
+        uint32_t w[SC / 2], wl[Cfg::BF ? SC / 2 : 1];
 #pragma unroll
         for (int e = 0; e < SC / 2; ++e) {
           const int col = 2 * e;
           const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
           const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
           sum += a0 + a1;
-          w[e] = pack_f16x2(a0, a1);
+          if constexpr (Cfg::BF) {  // bf16 high part and residual: ~16 significant bits
+            const __nv_bfloat162 hp = __floats2bfloat162_rn(a0, a1);
+            const float2 hf = __bfloat1622float2(hp);
+            w[e] = *reinterpret_cast<const uint32_t *>(&hp);
+            wl[e] = pack_bf16x2(a0 - hf.x, a1 - hf.y);
+          } else {
+            w[e] = pack_f16x2(a0, a1);
+          }
         }
         l = l * alpha + sum;
-        // P (f16 pairs) over this thread's own (already read) S columns
+        // P over this thread's own (already read) S columns
         tc::st32(scol, w);
+        if constexpr (Cfg::BF) tc::st32(scol + 32, wl);
         // O must hold P . V of the previous tile before it is scaled, and be
         // scaled before P . V of this tile (issued after the arrival below)
         if (rescale && j > 0) {
@@ -463,15 +477,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if (!ok) break;
           tc::fence_after();
           scale_o<Cfg>(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC), alpha);
-        }
-        if constexpr (Cfg::VCVT) {  // V of this tile to f16 (its P . V is issued after the arrival below)
-          const int vs = gj % Cfg::VSTAGES;
-          ok = warp_wait(&v_full[vs], (uint32_t)(gj / Cfg::VSTAGES) & 1u, p.timeout_ns);
-          if (!ok) break;
-          const bool big = convert_v_slice<Cfg>(sV + (size_t)vs * Cfg::KV_BYTES, tid,
-                                                it.ctx - (j_first + j) * Cfg::N);
-          if (__any_sync(kFull, big) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_RANGE);
-          fence_proxy_async();
         }
         tc::wait_st();
         tc::fence_before();

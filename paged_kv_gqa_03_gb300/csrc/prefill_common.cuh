@@ -23,13 +23,14 @@
 //  * O is rescaled in tensor memory only when a row's running max grows by
 //    more than 8 (log2 units): the result is exact either way, since P and l
 //    share the stale max, and p <= 2^8 keeps P well inside 16-bit range;
-//  * P must have V's type (kind::f16 takes one type for A and B) and needs
-//    more than bf16's 8 significant bits for the 2e-3 output bound, so P . V
-//    runs in f16: for a bf16 cache the softmax warps convert each V tile to
-//    f16 in shared memory (conflict-free 16-byte chunks, exact for
-//    magnitudes in [2^-14, 65504], larger ones saturate and are flagged)
-//    after its copy lands and before they release the tile's P; stale rows
-//    past a context are zeroed in the same pass;
+//  * P . V takes P in the cache's 16-bit type (kind::f16 takes one type for
+//    A and B, and V is read as the TMA lands it).  P needs more than bf16's 8
+//    significant bits for the 2e-3 output bound, so for a bf16 cache P goes
+//    in as a bf16 high part plus its bf16 residual (two MMAs per k-step, ~16
+//    significant bits), written over the thread's S columns (high parts in
+//    the first 32 of a half's 64 columns, residuals in the other 32); an f16
+//    cache takes f16 P.  V is used exactly as stored, over bf16's whole range;
+//    stale rows past a context are zeroed in shared memory before P . V;
 //  * warp roles: 0-7 softmax + epilogue, 8 and 10 TMA producers of the K and
 //    the V tiles (one warp issuing both tensors' copies spent much of each
 //    tile period inside its issues), 9 S issue and tensor-memory allocation,
@@ -51,11 +52,8 @@ template <class T, int D_>
 struct PrefillCfg {
   static constexpr int D = D_;
   static constexpr bool BF = T::kCode == PKV_BF16;
-  // P . V runs in f16 for both cache types: P (the weights) needs more than
-  // bf16's 8 significant bits for the 2e-3 bound, and kind::f16 takes one
-  // type for A and B, so a bf16 V tile is converted to f16 in shared memory
-  // by the softmax warps (exact for magnitudes in [2^-14, 65504]).
-  static constexpr bool VCVT = BF;
+  // P . V in the cache's type: for bf16, P as a high part plus its residual
+  static constexpr int PARTS = BF ? 2 : 1;
   static constexpr int M = 128;                         // query rows per CTA
   static constexpr int N = 128;                         // cache positions per K / V tile
   static constexpr int BLOCKS = N / kBlock;             // paged blocks per tile
@@ -122,13 +120,16 @@ __device__ __forceinline__ void mma_s_tile(uint32_t dS, uint32_t q0, uint32_t k0
 // false starts O afresh.  Issued by one thread.
 template <class Cfg>
 __device__ __forceinline__ void mma_pv_tile(uint32_t dO, uint32_t pb, uint32_t v0, bool accumulate) {
-  constexpr uint32_t idO = tc::idesc_f16(false, Cfg::M, Cfg::D, true);  // f16 P and V
+  constexpr uint32_t idO = tc::idesc_f16(Cfg::BF, Cfg::M, Cfg::D, true);  // P and V of the cache's type
 #pragma unroll
   for (int k = 0; k < Cfg::N / 16; ++k) {
-    // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs
+    // positions 16k .. 16k + 15: half k / 4 of the row, packed pairs (bf16:
+    // the high parts, the residuals 32 columns further)
     const uint32_t pcol = (uint32_t)((k >> 2) * (Cfg::N / 2) + (k & 3) * 8);
     const uint64_t dv = tc::desc_sw128(v0 + (uint32_t)k * 2048, Cfg::PANEL_KV, 1024);
-    tc::mma_f16_tmem_a(dO, pb + pcol, dv, idO, (accumulate || k > 0) ? 1u : 0u);
+#pragma unroll
+    for (int part = 0; part < Cfg::PARTS; ++part)
+      tc::mma_f16_tmem_a(dO, pb + pcol + (uint32_t)(part * 32), dv, idO, (accumulate || k > 0 || part > 0) ? 1u : 0u);
   }
 }
 
@@ -159,49 +160,6 @@ __device__ __forceinline__ void scale_o(uint32_t ta, float alpha) {
     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
     tc::st32(ta + (uint32_t)(q * 32), o);
   }
-}
-
-// The SOFTMAX softmax threads convert a bf16 V tile to f16 in place, thread
-// tid taking the 16-byte chunks tid, tid + SOFTMAX, ... (a warp's accesses
-// are contiguous: no bank conflicts); chunks of rows at or past zero_from
-// (stale positions past the context) become 0 instead.  Elementwise, so the
-// 128-byte swizzle is unaffected.  Returns true if a value's magnitude
-// exceeds 65504 (converted with saturation).  The shared-memory accessors
-// are volatile asm, which keeps their order, so the chunks go in batches of
-// four loads ahead of their stores: one load latency per batch, not per chunk.
-template <class Cfg>
-__device__ __forceinline__ bool convert_v_slice(uint8_t *vt, int tid, int zero_from) {
-  constexpr int CHUNKS = Cfg::KV_BYTES / 16 / Cfg::SOFTMAX;
-  constexpr int BATCH = 4;
-  static_assert(Cfg::KV_BYTES % (16 * Cfg::SOFTMAX) == 0, "whole chunks per thread");
-  static_assert(CHUNKS % BATCH == 0, "whole batches per thread");
-  const uint32_t base = smem_u32(vt);
-  bool big = false;
-#pragma unroll
-  for (int c0 = 0; c0 < CHUNKS; c0 += BATCH) {
-    uint4 x[BATCH];
-#pragma unroll
-    for (int k = 0; k < BATCH; ++k) x[k] = lds128(base + 16 * ((c0 + k) * Cfg::SOFTMAX + tid));
-#pragma unroll
-    for (int k = 0; k < BATCH; ++k) {
-      const int i = (c0 + k) * Cfg::SOFTMAX + tid;       // 16-byte chunk of the tile
-      const int row = (i * 16 % Cfg::PANEL_KV) / 128;    // its cache position in the tile
-      uint4 y = make_uint4(0, 0, 0, 0);
-      if (row < zero_from) {
-        const uint32_t w[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
-        uint32_t h[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-          big |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
-          asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[e]) : "f"(hi), "f"(lo));
-        }
-        y = make_uint4(h[0], h[1], h[2], h[3]);
-      }
-      sts128(base + 16 * i, y);
-    }
-  }
-  return big;
 }
 
 }  // namespace pkv

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // it cannot finish tile j + SBUF before that.)
   __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
   __shared__ __align__(8) uint64_t mrg[2];  // replica merge: (max, sum) written, partial O staged
+  __shared__ __align__(8) uint64_t dead;
   static_assert(REP == 1 || REP == 2 || REP == 4, "replicas");
   constexpr int RW = Cfg::M / REP;  // query rows of one replica
   constexpr int KL = 4 / REP;       // k-steps of a replica in each half of a tile
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&mrg[0], Cfg::SOFTMAX / 32);
     mbar_init(&mrg[1], Cfg::SOFTMAX / 32);
     mbar_init(&fin, 2);  // one commit from each issuing warp
+    mbar_init(&dead, 1);  // failure-path test hook: nothing ever arrives on it
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = ctx_raw != ctx ? PKV_FLAG_BAD_LEN : 0;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (!ok) break;
       if (lane == 0) v_consumed = j + 1;
       uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
-      if constexpr (!Cfg::VCVT) {  // (with the conversion the softmax warps zero them)
+      {  // stale cache rows past the context: weight 0, but 0 * NaN is NaN
         const int kv0 = (j_first + j) * Cfg::N;  // first position of the tile
         zero_v_rows<Cfg>(vt, ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
       }
@@ -258,7 +260,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int sb = j % Cfg::SBUF;
-      ok = warp_wait(&s_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
+      // failure-path test hook: the first tile's wait is on a barrier
+      // nothing completes, so it runs out and the CTA takes its abort path
+      ok = (p.stall_ns != 0 && j == 0)
+               ? warp_wait(&dead, 0, p.timeout_ns)
+               : warp_wait(&s_full[sb], (uint32_t)(j / Cfg::SBUF) & 1u, p.timeout_ns);
       if (!ok) break;
       tc::fence_after();
       const uint32_t scol = tbase + lane_base + (uint32_t)(sb * Cfg::N + half * SC);
@@ -305,13 +311,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       const float mu = m_run == -INFINITY ? 0.f : m_run;
       float sum = 0.f;
-      uint32_t w[NV / 2];
+      uint32_t w[NV / 2], wl[Cfg::BF ? NV / 2 : 1];
 #pragma unroll
       for (int e = 0; e < NV / 2; ++e) {
         const float a0 = ex2(fmaf(__uint_as_float(s[2 * e]), c, -mu));
         const float a1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), c, -mu));
         sum += a0 + a1;
-        w[e] = pack_f16x2(a0, a1);
+        if constexpr (Cfg::BF) {  // bf16 high part and residual: ~16 significant bits
+          const __nv_bfloat162 hp = __floats2bfloat162_rn(a0, a1);
+          const float2 hf = __bfloat1622float2(hp);
+          w[e] = *reinterpret_cast<const uint32_t *>(&hp);
+          wl[e] = pack_bf16x2(a0 - hf.x, a1 - hf.y);
+        } else {
+          w[e] = pack_f16x2(a0, a1);
+        }
       }
       if (rescale && j > 0) {  // O must hold P . V of the previous tile before it is scaled
         ok = warp_wait(&pv_done[(j - 1) % Cfg::SBUF], (uint32_t)((j - 1) / Cfg::SBUF) & 1u, p.timeout_ns);
@@ -320,9 +333,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         scale_o<Cfg>(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC), alpha);
       }
       l = l * alpha + sum;
-      // P (f16 pairs) over this thread's own (already read) S columns
+      // P (bf16: high parts and residuals; f16: f16 pairs) over this thread's own (already read) S columns
       if constexpr (REP == 1) {
         tc::st32(scol, w);
+        if constexpr (Cfg::BF) tc::st32(scol + 32, wl);
       } else {
         // 8 packed columns per k-step: this replica's k-steps, zeros in the others
 #pragma unroll
@@ -330,21 +344,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const uint32_t pc = scol + (uint32_t)((rep + t * REP) * 8);
           const uint32_t *v = &w[t * 8];
           tc::st8(pc, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+          if constexpr (Cfg::BF) {
+            const uint32_t *u = &wl[t * 8];
+            tc::st8(pc + 32, u[0], u[1], u[2], u[3], u[4], u[5], u[6], u[7]);
+          }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (q % REP != rep) {
             tc::st8(scol + (uint32_t)(q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
+            if constexpr (Cfg::BF) tc::st8(scol + (uint32_t)(32 + q * 8), 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
           }
-      }
-      if constexpr (Cfg::VCVT) {  // V of this tile to f16 (its P . V is issued after the arrival below)
-        const int vs = j % Cfg::VSTAGES;
-        ok = warp_wait(&v_full[vs], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
-        if (!ok) break;
-        const bool big = convert_v_slice<Cfg>(sV + (size_t)vs * Cfg::KV_BYTES, tid,
-                                              ctx - (j_first + j) * Cfg::N);
-        if (__any_sync(kFull, big) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_RANGE);
-        fence_proxy_async();
       }
       tc::wait_st();
       tc::fence_before();
