@@ -154,23 +154,38 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_traffic(q_len=1, kernel=""):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    capture (the decode kernel's, or the transposed multi-query kernel's), if
-    the kernel sources are unchanged since it was taken and it covers q_len."""
+TRAFFIC_RECORDS = {"bf16": "decode_traffic.json", "f16": "decode_traffic_f16.json",
+                   "fp8_e4m3": "decode_traffic_fp8.json"}
+
+
+def kernel_traffic(w, kernel=""):
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu
+    capture of that kernel (the decode kernel for the cache's dtype, or the
+    transposed multi-query kernel) on a smaller case of the same kernel:
+    reads scale with the K/V bytes a launch attends, writes (partials and
+    outputs) are kept as captured.  None when the kernel's sources changed
+    since the capture, the record covers another q_len, or the workload's
+    sequences share blocks (L2 then serves most of the logical bytes)."""
+    if w.window or w.prefix_blocks:
+        return None
     mq = kernel.startswith("mq_decode_kernel")
+    name = "mq_traffic.json" if mq else TRAFFIC_RECORDS.get(w.dtype)
+    if name is None:
+        return None
     try:
-        with open(os.path.join(ROOT, "profiles", "mq_traffic.json" if mq else "decode_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             rec = json.load(f)
     except Exception:
         return None
     h = hashlib.sha256()
-    for name in rec.get("sources", ("common.cuh", "decode.cuh", "internal.h")):
-        with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", name), "rb") as f:
+    for src in rec.get("sources", ("common.cuh", "decode.cuh", "internal.h")):
+        with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", src), "rb") as f:
             h.update(f.read())
-    if rec.get("source_sha256") != h.hexdigest() or rec.get("q_len", 1) != q_len:
+    if rec.get("source_sha256") != h.hexdigest() or rec.get("q_len", 1) != w.q_len:
         return None
-    return rec.get("dram_bytes_per_launch_scaled")
+    if "kv_bytes" not in rec:
+        return None
+    return int(rec["dram_bytes_read"] / rec["kv_bytes"] * w.kv_bytes() + rec["dram_bytes_write"])
 
 
 def oracle_sample_rate(w, seconds, threads=0):
@@ -295,7 +310,30 @@ def _config(w):
             "context_lens": (w.context_lens[0] if len(set(w.context_lens)) == 1
                              else f"{min(w.context_lens)}..{max(w.context_lens)}"),
             "num_blocks": w.num_blocks,
-            "l2": f"KV read per step {w.kv_bytes() / 1e9:.2f} GB > 129 MB L2; no flush needed"}
+            "pool_extra_blocks": getattr(w, "extra_blocks", 0),
+            "l2": (f"KV read per step {w.kv_bytes() / 1e9:.2f} GB > 129 MB L2; no flush needed"
+                   if w.kv_bytes() > 129e6 else
+                   f"KV read per step {w.kv_bytes() / 1e6:.2f} MB < 129 MB L2: L2-resident across steps, "
+                   "not flushed (a small case: launch latency, not HBM, bounds it)")}
+
+
+def grow_pool(w, extra):
+    """Appends `extra` free physical blocks (zeros; fp8 scales 1) to the
+    workload's pool, so that the end-to-end loop can advance every context
+    by one token per step; the block tables and every value already in the
+    pool stay as drawn."""
+    import torch
+    if extra <= 0:
+        return
+    def grow(t, fill):
+        pad = torch.full((extra,) + tuple(t.shape[1:]), fill, dtype=torch.uint8 if t.element_size() == 1 else t.dtype)
+        base = t.view(torch.uint8) if t.element_size() == 1 else t
+        out = torch.cat([base, pad])
+        return out.view(t.dtype) if t.element_size() == 1 else out
+    w.k_cache, w.v_cache = grow(w.k_cache, 0), grow(w.v_cache, 0)
+    if w.k_scale is not None:
+        w.k_scale, w.v_scale = grow(w.k_scale, 1.0), grow(w.v_scale, 1.0)
+    w.num_blocks += extra
 
 
 def run_ours(args, world, rank, local):
@@ -315,12 +353,19 @@ def run_ours(args, world, rank, local):
            "fp8_e4m3": torch.float8_e4m3fn}
     w = _workload(args)
     w.calibrated = args.calibrated
+    # room for the end-to-end loop's advancing contexts
+    e2e_steps = args.steps + 4
+    grow_blocks = -(-(e2e_steps + 1) * w.q_len // 16) + 1      # per sequence
+    extra = w.B * grow_blocks
+    grow_pool(w, extra)
+    w.extra_blocks = extra
     pkv.pkv_set_route("multi_query", args.mq_route)
     pkv.pkv_set_route("prefill", args.prefill_route)
     stream = torch.cuda.Stream(dev)
     ks = None if w.k_scale is None else w.k_scale.to(dev)
     vs = None if w.v_scale is None else w.v_scale.to(dev)
-    step = DecodeStep(w.k_cache.to(dev), w.v_cache.to(dev), w.Hq, tdt[w.q_dtype], w.max_blocks,
+    # block tables with room for the end-to-end loop's growth
+    step = DecodeStep(w.k_cache.to(dev), w.v_cache.to(dev), w.Hq, tdt[w.q_dtype], w.max_blocks + grow_blocks,
                       ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
                       q_len=w.q_len, window=w.window, calibrated=args.calibrated)
     for b in range(w.B):
@@ -330,7 +375,6 @@ def run_ours(args, world, rank, local):
     q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
     out = torch.empty_like(q)
     kv = w.kv_bytes()
-
 
     kname = attention_kernel_name(w, args.num_splits, torch.cuda.get_device_properties(dev).multi_processor_count,
                                   args.mq_route)
@@ -373,53 +417,65 @@ def run_ours(args, world, rank, local):
     ms_attn = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
     clocks = sampler.stop()
 
-    # (3) end to end through the public API from pinned host buffers: each step
-    # copies q, k_new, v_new and the bookkeeping to the device, runs append +
-    # attention and copies the output back (one captured CUDA graph per step),
-    # then the host reads the result
-    step.h_q.copy_(w.q)           # the step's inputs sit in the pinned staging buffer
-    step.h_k_new.copy_(w.k_new)
-    step.h_v_new.copy_(w.v_new)
+    # host cost of one attention call (argument marshalling, the C ABI's
+    # checks and launches), issued back to back without waiting
+    torch.cuda.synchronize()
+    nh = 100
+    th0 = time.perf_counter()
+    for _ in range(nh):
+        step.attend(q, out)
+    host_us = (time.perf_counter() - th0) / nh * 1e6
+    stream.synchronize()
+
+    # a spot check of the device-timed step's outputs against the oracle on
+    # two sequences, before the serving loop below advances the bookkeeping
+    # (the calibrated append re-quantises blocks, so its cache is the
+    # oracle's only after the same sequence of appends: no spot check there)
+    check = spot_check(w, out, step) if rank == 0 and not args.calibrated else None
+
+    # (3) end to end through the public API from pinned host memory, as a
+    # serving loop runs it: every step appends q_len new tokens to every
+    # sequence (contexts advance; blocks open every 16 tokens), the host's a1
+    # of step n + 1 (slot mapping, copy-on-write pairs, tables) runs while step
+    # n runs on the GPU, a captured graph per staging buffer copies the inputs
+    # and the bookkeeping in, appends, attends and writes the output into
+    # pinned host memory, and the host reads the output
     hout = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
-    step.capture(hout)
-    for _ in range(3):
-        step.replay()
+    step.stage_inputs(w.q, w.k_new, w.v_new, both=True)
+    step.prepare()
+    for _ in range(4):                  # the first step eager, then both graphs captured
+        step.run(hout)
+        step.prepare()
         stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    a1_us, wait_us, step_lens = [], [], []
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(stream)
-    for _ in range(args.steps):
-        step.replay()
-        stream.synchronize()             # the host reads the step's result
-        _ = float(hout.view(-1)[0])
+    for n in range(args.steps):
+        gev[n][0].record(stream)
+        step.run(hout)
+        gev[n][1].record(stream)         # the step's own GPU time (copies in and out included)
+        step_lens.append(step.h_lens.numpy().copy())   # this step's context lengths
+        t0 = time.perf_counter()
+        step.prepare()                  # a1 of the next step, overlapping this one
+        t1 = time.perf_counter()
+        stream.synchronize()
+        t2 = time.perf_counter()
+        _ = float(hout.view(-1)[0])     # the host reads the step's result
+        a1_us.append((t1 - t0) * 1e6)
+        wait_us.append((t2 - t1) * 1e6)
     x1.record(stream)
     x1.synchronize()
     barrier(world)
     ms_e2e = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, dev)
+    kv_e2e = sum(w.kv_bytes(lens) for lens in step_lens) / args.steps
     h2d = step.h2d_bytes(with_inputs=True)
     d2h = hout.numel() * hout.element_size()
-    out = step.g_out
-
-    # host side of a1 (slot mapping, copy-on-write pairs, table export) on a
-    # fresh block manager holding the same sequences, median over steps
-    host_a1 = []
-    for _ in range(max(5, min(args.steps, 20))):
-        probe = DecodeStep(step.k_cache, step.v_cache, w.Hq, tdt[w.q_dtype], w.max_blocks,
-                           ks, vs, num_splits=args.num_splits, stream=stream, scale=w.scale,
-                           q_len=w.q_len, window=w.window)
-        for b in range(w.B):
-            probe.adopt(b, w.tables[b], w.cached[b])
-        probe._buffers(w.B)
-        t0 = time.perf_counter()
-        probe.prepare()
-        host_a1.append((time.perf_counter() - t0) * 1e6)
-    host_a1_us = statistics.median(host_a1)
-
-    # a spot check of the timed outputs against the oracle on two sequences
-    # (the calibrated append re-quantises blocks, so its cache is the oracle's
-    # only after the same sequence of appends: no spot check there)
-    check = spot_check(w, out, step) if rank == 0 and not args.calibrated else None
+    host_a1_us = statistics.median(a1_us)
+    graph_ms = statistics.median(a.elapsed_time(b) for a, b in gev)
 
     if rank != 0:
         torch.distributed.destroy_process_group() if world > 1 else None
@@ -445,15 +501,26 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": round(attn_gbs, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(attn_gbs / peak, 4),
-                     "traffic": None if w.window else kernel_traffic(w.q_len, kname),
+                     "traffic": kernel_traffic(w, kname),
                      "algorithmic_bytes_per_launch": kv,
                      "ms_per_launch": round(ms_attn, 4)},
         "unique_kv": unique_kv_line(w, ms_step, ms_attn, peak),
         "cpu_baseline": cpu,
-        "e2e": {"value": round(job_gbs(kv, world, ms_e2e), 2), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(kv_e2e, world, ms_e2e), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(ms_e2e, 4)},
+                "ms_per_step": round(ms_e2e, 4),
+                "loop": "serving loop: contexts advance one token per sequence per step; a1 of step n+1 "
+                        "on the host while step n runs; graph per staging buffer; output read by the host",
+                "a1_us_median": round(host_a1_us, 1),
+                "host_wait_after_a1_us_median": round(statistics.median(wait_us), 1),
+                "a1_overlapped_steps": sum(1 for x in wait_us if x > 5.0),
+                "gap_vs_device_step_ms": round(ms_e2e - ms_step, 4),
+                "graph_gpu_ms_median": round(graph_ms, 4),
+                "gap_split": "graph_gpu_ms - ms_per_step of the device loop: the step's copies in and out; "
+                             "e2e ms_per_step - graph_gpu_ms: graph launch, host wake-up after the GPU "
+                             "finishes and the host's read of the output"},
         "host_a1_us": round(host_a1_us, 1),
+        "host_us_per_attention_call": round(host_us, 1),
         "clocks": clocks,
         "gpu_launches": timed_launches,
         "num_splits": args.num_splits,
@@ -654,7 +721,7 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": prefill_kernel_name(c, args.prefill_route), "achieved": round(tflops, 1),
                      "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "traffic": None, "algorithmic_flops_per_launch": flops,
-                     "note": "P . V runs in f16 (a bf16 V tile is converted to f16 in shared memory)"},
+                     "note": "bf16 caches: P . V takes P as a bf16 high part plus residual (two MMAs per k-step)"},
         "e2e": {"value": round(flops / (ms_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": q.numel() * q.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": round(ms_e2e, 4)},

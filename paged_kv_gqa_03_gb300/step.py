@@ -68,6 +68,9 @@ class DecodeStep:
         self._turn = 0
         self.ncow = 0
         self.graph = None
+        self._calls = {}    # marshalled C calls (Prepared), keyed by their buffers
+        self._graphs = {}   # run(): one captured step per (staging buffer, output)
+        self._ran = False
 
     # -- buffers ---------------------------------------------------------------
     def _layout(self, B):
@@ -94,6 +97,8 @@ class DecodeStep:
         if self._B == B:
             return
         self._B = B
+        self._calls.clear()     # their buffers are about to be replaced
+        self._graphs.clear()
         layout, total = self._layout(B)
         pin = torch.cuda.is_available()
         self._host = [_Staging(layout, total, torch.device("cpu"), pin) for _ in range(2)]
@@ -177,18 +182,35 @@ class DecodeStep:
         if self.ncow:
             paged_kv_copy_blocks(self.k_cache, self.v_cache, self.d_pairs[:2 * self.ncow].view(-1, 2),
                                  self.k_scale, self.v_scale, stream=s)
-        if self.q_len > 1:
-            k_new = k_new.view(-1, self.Hkv, self.D)
-            v_new = v_new.view(-1, self.Hkv, self.D)
-        paged_kv_append(k_new, v_new, self.k_cache, self.v_cache, self.d_slots, self.k_scale,
-                        self.v_scale, stream=s, calibrated=self.calibrated)
+        key = ("append", k_new.data_ptr(), v_new.data_ptr(), self.d_slots.data_ptr())
+        call = self._calls.get(key)
+        if call is None:
+            if self.q_len > 1:
+                k_new = k_new.view(-1, self.Hkv, self.D)
+                v_new = v_new.view(-1, self.Hkv, self.D)
+            call = self._remember(key, paged_kv_append(
+                k_new, v_new, self.k_cache, self.v_cache, self.d_slots, self.k_scale, self.v_scale,
+                stream=s, calibrated=self.calibrated, prepare=True))
+        call()
         self.attend(q, out)
 
     def attend(self, q, out):
-        paged_decode_attention(out, q, self.k_cache, self.v_cache, self.d_table, self.d_lens,
-                               self.scale, self.k_scale, self.v_scale,
-                               num_splits=self.num_splits, workspace=self._ws, stream=self.stream,
-                               window=self.window)
+        """a4-a8 on the current bookkeeping.  The C call's arguments are
+        marshalled once per (q, out) pair and reused."""
+        key = ("attend", q.data_ptr(), out.data_ptr(), self.d_table.data_ptr())
+        call = self._calls.get(key)
+        if call is None:
+            call = self._remember(key, paged_decode_attention(
+                out, q, self.k_cache, self.v_cache, self.d_table, self.d_lens, self.scale,
+                self.k_scale, self.v_scale, num_splits=self.num_splits, workspace=self._ws,
+                stream=self.stream, window=self.window, prepare=True))
+        call()
+
+    def _remember(self, key, call):
+        if len(self._calls) >= 8:
+            self._calls.clear()
+        self._calls[key] = call
+        return call
 
     @property
     def workspace(self):
@@ -217,6 +239,52 @@ class DecodeStep:
     def _graph_body(self, h_out):
         self._copy_in(with_inputs=True)
         self.launch(self.d_q, self.d_k_new, self.d_v_new, h_out)
+
+    # -- a serving loop from host memory ----------------------------------------
+    def stage_inputs(self, q, k_new, v_new, both=False):
+        """Writes a step's q, k_new, v_new (host tensors) into the current
+        staging buffer (both=True: into both buffers)."""
+        for t in ((0, 1) if both else (self._turn,)):
+            hs = self._host[t]
+            hs["q"].copy_(q)
+            hs["k_new"].copy_(k_new)
+            hs["v_new"].copy_(v_new)
+
+    def run(self, h_out):
+        """Issues one whole step from host memory, asynchronously: the copy of
+        the current staging buffer (inputs and the bookkeeping of the last
+        prepare()), the append and the attention writing into the pinned
+        tensor h_out.  Each staging buffer has a CUDA graph of its own,
+        captured on first use, so a loop can run step n from one buffer
+        while prepare() writes step n + 1 into the other:
+
+            step.prepare(); step.run(h_out)
+            while serving:
+                step.prepare()            # a1 of the next step, on the host
+                stream.synchronize()      # this step's output is in h_out
+                ...read h_out, stage the next inputs...
+                step.run(h_out)
+
+        The first step runs eagerly (it configures the kernels and encodes
+        their tensor maps outside any capture), and so does a step with
+        copy-on-write pairs (rare): the graphs hold no block copy."""
+        if not h_out.is_pinned():
+            raise ValueError("h_out must be pinned host memory")
+        if self.stream.cuda_stream == 0:
+            raise ValueError("run() captures CUDA graphs: give the DecodeStep a non-default stream")
+        if self.ncow or not self._ran:
+            self._graph_body(h_out)
+            self._ran = True
+            return
+        key = (self._turn, h_out.data_ptr())
+        graph = self._graphs.get(key)
+        if graph is None:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=self.stream):
+                self._graph_body(h_out)
+            self._graphs[key] = graph
+        with torch.cuda.stream(self.stream):
+            graph.replay()
 
     def replay(self):
         with torch.cuda.stream(self.stream):

@@ -110,14 +110,17 @@ class Workload:
             return min(ctx, self.window + self.q_len - 1)
         return ctx
 
-    def kv_bytes(self):
+    def kv_bytes(self, context_lens=None):
         """Logical bytes of K and V attention reads (+ fp8 scales): the
-        positions attended (inside the window, if any)."""
+        positions attended (inside the window, if any), for the workload's
+        context lengths or the ones given (a later step of the same
+        sequences)."""
+        lens = self.context_lens if context_lens is None else [int(c) for c in context_lens]
         per_tok = 2 * self.Hkv * self.D * ITEMSIZE[self.dtype]
-        total = sum(self.attended(c) for c in self.context_lens) * per_tok
+        total = sum(self.attended(c) for c in lens) * per_tok
         if self.dtype == "fp8_e4m3":
             total += sum((c + BLOCK - 1) // BLOCK - (c - self.attended(c)) // BLOCK
-                         for c in self.context_lens) * self.Hkv * 2 * 4
+                         for c in lens) * self.Hkv * 2 * 4
         return total
 
     def unique_kv_bytes(self):
