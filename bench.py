@@ -577,8 +577,9 @@ def attention_kernel_name(w, num_splits, sms, force="auto"):
     G = w.Hq // w.Hkv
     R = w.q_len * G
     sixteen = w.dtype in ("bf16", "f16")
+    fp8_ok = w.dtype == "fp8_e4m3" and R <= 32 and (R > 16 or force == "transposed")  # widened to f16 there
     fills = w.B * w.Hkv * ((R + 127) // 128) >= sms and w.B <= 65535
-    if num_splits == 0 and sixteen and force not in ("units", "prefill") and w.D == 128 and R <= 64 \
+    if num_splits == 0 and (sixteen or fp8_ok) and force not in ("units", "prefill") and w.D == 128 and R <= 64 \
             and w.B <= 2048 and (R <= 32 or not fills or force == "transposed"):
         return "mq_decode_kernel (transposed tcgen05, stream-K) + mq_merge_kernel"
     if num_splits == 0 and sixteen and force != "units" and fills:

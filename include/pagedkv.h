@@ -236,9 +236,15 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  *  - otherwise, with at least one (sequence, kv head, 128-row tile) per SM,
  *    a tensor-core prefill kernel (chosen as in paged_prefill_attention),
  *    which also reads each (sequence, kv head)'s K/V once for all its rows;
- *  - otherwise (FP8 or F32 caches, a fixed split count, small grids) each kv
- *    head's rows are served in 8-row units by the decode kernel (K/V read once
- *    per unit, re-reads mostly from L2) with the split-KV merge.
+ *  - an FP8 cache with 17-32 rows, D = 128, B <= 2048: the first kernel,
+ *    whose producer warps copy the E4M3 tiles and whose softmax warps widen
+ *    each to f16 in shared memory (exact) while the previous tile's softmax
+ *    runs; the block scales multiply the scores and are folded into the
+ *    weights;
+ *  - otherwise (FP8 caches up to 16 rows, F32 caches, a fixed split count,
+ *    small grids) each kv head's rows are served in 8-row units by the
+ *    decode kernel (K/V read once per unit, re-reads mostly from L2) with the
+ *    split-KV merge.
  * pkv_set_route(PKV_ROUTE_MULTI_QUERY, PKV_MQ_TRANSPOSED | PKV_MQ_PREFILL |
  * PKV_MQ_UNITS) forces the first, second or last route where it applies
  * (measurement and tests).

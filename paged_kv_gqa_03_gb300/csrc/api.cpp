@@ -420,7 +420,8 @@ int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
   if (rc != PKV_OK) return rc;
   size_t total = ws_layout(B, P, D).total;
   if (q_len >= 2 && num_splits == 0 && D == kMqHeadDim && q_len * (Hq / Hkv) <= kMqRows && B <= kMqMaxBatch &&
-      (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16)) {
+      (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16 ||
+       (cache_dtype == PKV_FP8_E4M3 && q_len * (Hq / Hkv) <= kMqRowsFp8))) {
     int sms = 0;
     rc = device_sm_count(&sms);
     if (rc != PKV_OK) return rc;
@@ -535,8 +536,15 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
     const int64_t tiles = ((int64_t)q_len * G + 127) / 128;
     const bool prefill_fills = (int64_t)B * Hkv * tiles >= sms && B <= 65535;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (!no_mq && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && D == kMqHeadDim &&
-        R <= kMqRows && B <= kMqMaxBatch && (R <= 32 || !prefill_fills || want_mq)) {
+    // FP8 caches take the transposed kernel for 17-32 rows (it widens each
+    // tile to f16 in shared memory, which on 32 KiB fp8 tiles costs more than
+    // the tile's HBM time: ~2.1-2.4 TB/s whatever the rows, against the 8-row
+    // units' 6.0 / 3.2 / 1.7 TB/s at 8 / 16 / 32 rows on the 32K fp8 layer);
+    // they have no prefill route
+    const bool fp8 = cache_dtype == PKV_FP8_E4M3;
+    const bool fp8_mq = fp8 && R <= kMqRowsFp8 && (R > 16 || want_mq);
+    if (!no_mq && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16 || fp8_mq) && scale > 0.f &&
+        D == kMqHeadDim && R <= kMqRows && B <= kMqMaxBatch && (R <= 32 || !prefill_fills || want_mq)) {
       const MqWsLayout M = mq_ws_layout(B, sms);
       if (workspace_bytes >= M.total) {
         CUtensorMap tmK, tmV;
@@ -549,6 +557,8 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
         std::memset(&mp, 0, sizeof(mp));
         mp.out = out;
         mp.q = q;
+        mp.k_scale = k_scale;
+        mp.v_scale = v_scale;
         mp.block_table = block_table;
         mp.context_lens = context_lens;
         mp.status = &reinterpret_cast<WsHeader *>(ws)->status;
@@ -567,7 +577,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
         mp.window = window < (1 << 30) ? window : 0;
         mp.scale_log2 = scale * 1.4426950408889634f;
         mp.timeout_ns = kWaitLimitNs;
-        return cuda_status(launch_mq_decode(mp, cache_dtype, tmK, tmV, sms, s));
+        return cuda_status(launch_mq_decode(mp, cache_dtype, q_dtype, tmK, tmV, sms, s));
       }
     }
     if (!units && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16) && scale > 0.f && prefill_fills) {

@@ -43,10 +43,16 @@
 
 namespace pkv {
 
-template <class T, int NRH_>
+// T: the cache type; QT: the query / output type (= T for 16-bit caches).
+// An fp8 cache is widened to f16 in shared memory (exact: every E4M3 value
+// is an f16 value) and the MMAs run on f16 (Q converted when staged), so
+// BF (the MMA operand type) is false for it while OUT_BF follows the query.
+template <class T, int NRH_, class QT = T>
 struct MqCfg {
   static constexpr int D = kMqHeadDim;
-  static constexpr bool BF = T::kCode == PKV_BF16;
+  static constexpr bool FP8 = T::kBytes == 1;
+  static constexpr bool BF = !FP8 && T::kCode == PKV_BF16;
+  static constexpr bool OUT_BF = QT::kCode == PKV_BF16;
   static constexpr int NRH = NRH_;                      // query rows of one softmax half
   static constexpr int NR = 2 * NRH;                    // S^T columns (rows padded)
   static constexpr int NPV = NR;                        // P^T columns (the padded rows)
@@ -63,12 +69,20 @@ struct MqCfg {
   static constexpr int P_PART = N * P_ROW;
   static constexpr int P_BYTES = PARTS * P_PART;
   // rings as deep as shared memory allows: a V slot is held from its copy to
-  // the end of its P . V, so V gets the depth
-  static constexpr int KSTAGES = NR <= 32 ? 3 : 2, VSTAGES = 3, PBUF = NR <= 16 ? 2 : 1, SBUF = 2;
+  // the end of its P . V, so V gets the depth.  fp8: the copies land in raw
+  // rings of RAW_BYTES tiles (one 128-byte panel per position), the producers
+  // widen each tile into the f16 operand rings below.
+  // fp8: two raw slots per tensor; the softmax warps widen tile g + 1 while
+  // they process tile g, into two-deep f16 rings
+  static constexpr int KSTAGES = FP8 ? 2 : (NR <= 32 ? 3 : 2), VSTAGES = FP8 ? 2 : 3;
+  static constexpr int PBUF = NR <= 16 ? 2 : 1, SBUF = 2;
   static constexpr int QBUF = NR <= 16 ? 2 : 1;
-  static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
+  static constexpr int RAW_BYTES = N * D;               // one fp8 K (or V) tile
+  static constexpr int KRAW = FP8 ? 2 : 0, VRAW = FP8 ? 2 : 0;
+  static constexpr int SC_RING = 8;                     // fp8 block scales of the tiles in flight
+  static constexpr int LOADS = FP8 ? BLOCKS : BLOCKS * PANELS;  // TMA boxes per K (or V) tile
   static constexpr size_t SMEM = 1024 + (size_t)(KSTAGES + VSTAGES) * KV_BYTES + (size_t)PBUF * P_BYTES +
-                                 (size_t)QBUF * Q_BYTES;
+                                 (size_t)QBUF * Q_BYTES + (size_t)(KRAW + VRAW) * RAW_BYTES;
   // 16-byte chunk c of position kt's P^T row, swizzled as the P . V operand reads it
   __device__ static __forceinline__ int p_chunk(int kt, int c) {
     return c ^ (NR == 16 ? (kt >> 2) & 1 : (NR == 32 ? (kt >> 1) & 3 : kt & 7));
@@ -80,6 +94,7 @@ struct MqCfg {
   static constexpr int PRODUCER = SOFTMAX / 32, ISSUER = PRODUCER + 1, PV_ISSUER = PRODUCER + 2,
                        V_PRODUCER = PRODUCER + 3;
   static_assert(NRH == 8 || NRH == 16 || NRH == 32, "rows per half");
+  static_assert(!FP8 || NRH <= 16, "fp8: up to 32 rows (shared memory)");
   static_assert(SBUF * NR <= (int)COL_O && COL_O + 2 * NPV <= TMEM_COLS, "tensor memory");
   static_assert(LOADS <= 32, "one box per producer lane");
   static_assert(SMEM + 4096 <= 232448, "shared memory");
@@ -220,6 +235,62 @@ __device__ __forceinline__ void ld_cols(uint32_t ta, uint32_t (&r)[NRH]) {
     tc::ld32(ta, r);
 }
 
+// fp8 caches: the softmax threads' widening of one landed E4M3 tile (TMA
+// layout: 128 rows of 128 bytes, 128-byte swizzle) into the f16 operand
+// layout of a 16-bit tile (two 64-element panels of 128-byte rows, 128-byte
+// swizzle), the layout the MMAs read K (K-major) and V (MN-major) from.  Each
+// E4M3 value is an f16 value, so the widening is exact; rows at or past
+// zero_from (stale positions past the context) become zeros.  Thread t takes
+// the 16-byte chunks t, t + 256, t + 512, t + 768 (eight threads per row:
+// conflict-free loads), its four loads in flight together.
+template <class Cfg>
+__device__ __forceinline__ void widen_share(const uint8_t *raw, uint8_t *op, int zero_from, int tid) {
+  constexpr int PER = Cfg::N * 8 / Cfg::SOFTMAX;  // chunks of a thread
+  const uint32_t rb = smem_u32(raw), ob = smem_u32(op);
+  uint4 x[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + k * Cfg::SOFTMAX, r = i >> 3, c = i & 7;
+    x[k] = lds128(rb + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)));
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = tid + k * Cfg::SOFTMAX, r = i >> 3, c = i & 7;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (r < zero_from) {
+      lo = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[k].x & 0xffff)), e4m3x2_to_f16x2((uint16_t)(x[k].x >> 16)),
+                      e4m3x2_to_f16x2((uint16_t)(x[k].y & 0xffff)), e4m3x2_to_f16x2((uint16_t)(x[k].y >> 16)));
+      hi = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[k].z & 0xffff)), e4m3x2_to_f16x2((uint16_t)(x[k].z >> 16)),
+                      e4m3x2_to_f16x2((uint16_t)(x[k].w & 0xffff)), e4m3x2_to_f16x2((uint16_t)(x[k].w >> 16)));
+    }
+    // elements 16c .. 16c + 15: panel c / 4, 16-byte chunks 2 (c % 4) and
+    // 2 (c % 4) + 1.  The two panels share banks, so threads of panel 1 store
+    // their odd chunk first: each store's eight threads of a row then cover
+    // all 32 banks (no conflict)
+    const uint32_t row = ob + (uint32_t)((c >> 2) * Cfg::PANEL_KV + r * 128);
+    const int ch = (c & 3) * 2;
+    const bool odd_first = c >= 4;
+    sts128(row + (uint32_t)(((ch + (odd_first ? 1 : 0)) ^ (r & 7)) << 4), odd_first ? hi : lo);
+    sts128(row + (uint32_t)(((ch + (odd_first ? 0 : 1)) ^ (r & 7)) << 4), odd_first ? lo : hi);
+  }
+}
+
+// A query row (16-byte chunk of 8 values) as the MMA operand type: f16 for
+// fp8 caches (a bf16 query converted, exact for normal f16 magnitudes),
+// unchanged otherwise.
+template <class Cfg>
+__device__ __forceinline__ uint4 q_chunk(uint4 v) {
+  if constexpr (Cfg::FP8 && Cfg::OUT_BF) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+    return make_uint4(h[0], h[1], h[2], h[3]);
+  } else {
+    return v;
+  }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mq_decode_kernel(const __grid_constant__ MqParams p, const __grid_constant__ CUtensorMap tmK,
@@ -231,7 +302,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint8_t *sV = sK + (size_t)Cfg::KSTAGES * Cfg::KV_BYTES;
   uint8_t *sP = sV + (size_t)Cfg::VSTAGES * Cfg::KV_BYTES;
   uint8_t *sQ = sP + (size_t)Cfg::PBUF * Cfg::P_BYTES;
+  uint8_t *sKr = sQ + (size_t)Cfg::QBUF * Cfg::Q_BYTES;     // fp8: raw K / V rings
+  uint8_t *sVr = sKr + (size_t)Cfg::KRAW * Cfg::RAW_BYTES;
   __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
+  // fp8: raw K / V tiles landed / widened (the widened tiles are announced on k_full / v_full)
+  __shared__ __align__(8) uint64_t kr_full[Cfg::FP8 ? Cfg::KRAW : 1], vr_full[Cfg::FP8 ? Cfg::VRAW : 1];
+  __shared__ __align__(8) uint64_t kr_empty[Cfg::FP8 ? Cfg::KRAW : 1], vr_empty[Cfg::FP8 ? Cfg::VRAW : 1];
+  __shared__ int raw_zero[Cfg::FP8 ? Cfg::VRAW : 1];        // fp8 V: first stale row of each raw tile
+  __shared__ int kr_issued, vr_issued;                      // fp8: raw copies issued
   __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
   // S^T landed / read out of tensor memory; P written / P . V done (P buffer free)
   __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], s_free[Cfg::SBUF], p_full[Cfg::PBUF], pv_done[Cfg::PBUF];
@@ -247,12 +325,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < Cfg::KSTAGES; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], Cfg::FP8 ? Cfg::SOFTMAX / 32 : 1);  // fp8: every softmax warp's share widened
       mbar_init(&k_empty[s], 1);
     }
 #pragma unroll
     for (int s = 0; s < Cfg::VSTAGES; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], Cfg::FP8 ? Cfg::SOFTMAX / 32 : 1);
       mbar_init(&v_empty[s], 1);
     }
 #pragma unroll
@@ -276,10 +354,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     mbar_init(&xl[0], 4);
     mbar_init(&xl[1], 4);
     mbar_init(&fin, 2);  // one commit from each issuing warp
+    if constexpr (Cfg::FP8) {
+#pragma unroll
+      for (int s = 0; s < Cfg::KRAW; ++s) {
+        mbar_init(&kr_full[s], 1);
+        mbar_init(&kr_empty[s], Cfg::SOFTMAX / 32);
+      }
+#pragma unroll
+      for (int s = 0; s < Cfg::VRAW; ++s) {
+        mbar_init(&vr_full[s], 1);
+        mbar_init(&vr_empty[s], Cfg::SOFTMAX / 32);
+      }
+    }
     fence_barrier_init();
     abort_flag = 0;
     cta_flags = 0;
     k_consumed = v_consumed = k_issued = v_issued = 0;
+    kr_issued = vr_issued = 0;
   }
   if (warp == Cfg::ISSUER) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
   if (warp == Cfg::PRODUCER && lane == 0) {
@@ -379,6 +470,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     struct Pend {
       int id, h;
       bool none;
+      int zf;  // fp8 V: the tile's first row past the context (zeroed when widened)
     };
     auto fetch = [&]() -> Pend {
       Pend f;
@@ -387,6 +479,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       f.h = cs.h;
       f.none = lb >= nblk || (lb + 1) * kBlock <= cs.first;
       f.id = f.none ? 0 : __ldg(p.block_table + (size_t)cs.b * p.max_blocks + lb);
+      f.zf = cs.ctx - (cs.j_first + cj) * Cfg::N;
       return f;
     };
     // the box row of a fetched block: the box past the tensor (zeros) for none
@@ -425,13 +518,48 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     };
     const bool vw = warp == Cfg::V_PRODUCER;
     bool ok = true;
-    const Pend nil{0, 0, true};
+    const Pend nil{0, 0, true, 0};
     bool h0 = step();
     Pend f0 = h0 ? fetch() : nil;
     bool h1 = h0 && step();
     Pend f1 = h1 ? fetch() : nil;
     bool h2 = h1 && step();
     Pend f2 = h2 ? fetch() : nil;
+    if constexpr (Cfg::FP8) {
+      // fp8: the tiles land raw (RAW ring); the softmax warps widen tile g + 1
+      // into the f16 operand ring while they process tile g and then release
+      // its raw slot (kr_empty / vr_empty), which this warp reissues
+      static_assert(Cfg::KRAW == Cfg::VRAW, "same raw ring depths for K and V");
+      constexpr int RAWN = Cfg::KRAW;
+      uint8_t *raw = vw ? sVr : sKr;
+      uint64_t *rbar = vw ? vr_full : kr_full;
+      uint64_t *rfree = vw ? vr_empty : kr_empty;
+      const CUtensorMap *tm = vw ? &tmV : &tmK;
+      int *r_issued = vw ? &vr_issued : &kr_issued;
+      for (int g = 0; h0 && ok; ++g) {
+        const bool h3 = h2 && step();
+        const Pend f3 = h3 ? fetch() : nil;
+        const int rs = g % RAWN;
+        if (g >= RAWN) ok = warp_wait(&rfree[rs], (uint32_t)((g / RAWN) - 1) & 1u, p.timeout_ns);
+        if (ok && __any_sync(kFull, *(volatile int *)&abort_flag)) ok = false;
+        if (!ok) break;
+        const int64_t trow = row_of(f0);
+        if (lane == 0) {
+          if (vw) raw_zero[rs] = f0.zf;
+          mbar_arrive_expect_tx(&rbar[rs], Cfg::RAW_BYTES);
+        }
+        __syncwarp();
+        if (lane < Cfg::LOADS)
+          tma_load_2d(raw + (size_t)rs * Cfg::RAW_BYTES + slot * 2048, tm, 0, (int)(trow * kBlock), &rbar[rs]);
+        if (lane == 0) *r_issued = g + 1;
+        h0 = h1;
+        f0 = f1;
+        h1 = h2;
+        f1 = f2;
+        h2 = h3;
+        f2 = f3;
+      }
+    } else {
     for (int g = 0; h0 && ok; ++g) {
       const bool h3 = h2 && step();
       const Pend f3 = h3 ? fetch() : nil;
@@ -443,6 +571,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       f1 = f2;
       h2 = h3;
       f2 = f3;
+    }
     }
     if (__any_sync(kFull, bad) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_BAD_BLOCK);
     if (!ok && lane == 0) {
@@ -505,7 +634,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0) v_consumed = g + 1;
         uint8_t *vt = sV + (size_t)vs * Cfg::KV_BYTES;
         const int kv0 = (sg.j_first + j) * Cfg::N;  // first position of the tile
-        zero_v_rows<Cfg>(vt, sg.ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
+        if constexpr (!Cfg::FP8)  // (fp8: the widening wrote zeros there)
+          zero_v_rows<Cfg>(vt, sg.ctx - kv0, min(nblk * kBlock - kv0, Cfg::N), lane);
         __syncwarp();
         tc::fence_after();
         if (lane == 0) {
@@ -541,10 +671,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const int ii = r / p.G, gq = r - ii * p.G;
           const uint4 *src = reinterpret_cast<const uint4 *>(
               static_cast<const uint16_t *>(p.q) + (((size_t)s.b * p.q_len + ii) * p.Hq + s.h * p.G + gq) * Cfg::D) + cc;
-          if (async)
+          if (async && !Cfg::FP8)  // (fp8: Q is converted to f16 on the way, synchronously)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
           else
-            sts128(dst, __ldg(src));
+            sts128(dst, q_chunk<Cfg>(__ldg(src)));
         } else {
           sts128(dst, make_uint4(0, 0, 0, 0));
         }
@@ -556,6 +686,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[qb]);
     };
+    // fp8: widen K (or V) of the CTA's tile gt (its global index in the
+    // walk) from its raw slot into the f16 ring, then announce it and free
+    // the raw slot.  The ring slot is free: K(gt - 2)'s S has completed and
+    // V(gt - 2)'s P . V has been waited for by the caller.
+    const int ntiles = t1 - t0;
+    auto widen = [&](int gt, bool v) -> bool {
+      constexpr int RAWN = Cfg::KRAW > 0 ? Cfg::KRAW : 1;  // (16-bit caches never call this)
+      const int rs = gt % RAWN, os = gt % Cfg::KSTAGES;
+      if (!warp_wait(v ? &vr_full[rs] : &kr_full[rs], (uint32_t)(gt / RAWN) & 1u, p.timeout_ns)) return false;
+      widen_share<Cfg>((v ? sVr : sKr) + (size_t)rs * Cfg::RAW_BYTES, (v ? sV : sK) + (size_t)os * Cfg::KV_BYTES,
+                       v ? raw_zero[rs] : Cfg::N, tid);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(v ? &v_full[os] : &k_full[os]);
+        mbar_arrive(v ? &vr_empty[rs] : &kr_empty[rs]);
+      }
+      return true;
+    };
     MqWalk wk;
     wk.start(b0, base0, t0, t1);
     MqSeg sg{}, nx{};
@@ -566,6 +715,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       release_q(0, false);
     }
     bool ok = true;
+    if constexpr (Cfg::FP8) {  // the first tile's K and V
+      if (ntiles > 0) ok = widen(0, false) && widen(0, true);
+    }
     int g = 0, si = 0;
     float m_run[NRH], l_part[NRH];
     while (have && ok) {
@@ -583,15 +735,46 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         m_run[e] = -INFINITY;
         l_part[e] = 0.f;
       }
+      // fp8: the K and V scales of this position's block, software-pipelined
+      // within the segment: the block id two tiles ahead and the scales one
+      // tile ahead are loaded while this tile is processed (0 for positions
+      // no block holds: masked anyway)
+      const int nblk_s = (sg.ctx + kBlock - 1) / kBlock;
+      auto block_id = [&](int jj) -> int {  // -1: no block / none to read
+        const int lb = ((sg.j_first + sg.j0 + jj) * Cfg::N + kt) / kBlock;
+        if (jj >= n || lb >= nblk_s || (lb + 1) * kBlock <= sg.first) return -1;
+        return __ldg(p.block_table + (size_t)sg.b * p.max_blocks + lb);
+      };
+      auto scale_of = [&](int id, const float *tab) -> float {
+        return id >= 0 && (int64_t)id < p.num_blocks ? __ldg(tab + (size_t)id * p.Hkv + sg.h) : 0.f;
+      };
+      [[maybe_unused]] float ksc_n = 0.f, vsc_n = 0.f;
+      [[maybe_unused]] int id_nn = -1;
+      if constexpr (Cfg::FP8) {
+        const int id0 = block_id(0);
+        ksc_n = scale_of(id0, p.k_scale);
+        vsc_n = scale_of(id0, p.v_scale);
+        id_nn = block_id(1);
+      }
       for (int j = 0; j < n; ++j) {
         const int gj = g + j, sb = gj % Cfg::SBUF, par = gj & 1;
+        const int pos = (sg.j_first + sg.j0 + j) * Cfg::N + kt;
+        float ksc = 1.f, vsc = 1.f;
+        if constexpr (Cfg::FP8) {
+          ksc = ksc_n;
+          vsc = vsc_n;
+          ksc_n = scale_of(id_nn, p.k_scale);  // tile j + 1
+          vsc_n = scale_of(id_nn, p.v_scale);
+          id_nn = block_id(j + 2);
+          // K of the next tile, so its S can run while this tile's softmax does
+          if (gj + 1 < ntiles && !(ok = widen(gj + 1, false))) break;
+        }
         ok = warp_wait(&s_full[sb], (uint32_t)(gj / Cfg::SBUF) & 1u, p.timeout_ns);
         if (!ok) break;
         tc::fence_after();
         // S^T of this thread's position and rows, masked: new token i sees the
         // position iff imin <= i < imin + window (imin = pos - ctx + q_len)
         const uint32_t scol = tbase + lane_base + (uint32_t)(sb * NR + row0);
-        const int pos = (sg.j_first + sg.j0 + j) * Cfg::N + kt;
         const int imin = pos - sg.ctx + p.q_len;
         const int rlo = imin > 0 ? (imin < p.q_len ? imin * p.G : p.R) : 0;
         const int rhi = p.window > 0 ? (imin + p.window >= p.q_len ? p.R : max(0, imin + p.window) * p.G) : p.R;
@@ -600,7 +783,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           uint32_t sr[NRH];
           ld_cols<NRH>(scol, sr);
 #pragma unroll
-          for (int e = 0; e < NRH; ++e) s[e] = __uint_as_float(sr[e]);
+          for (int e = 0; e < NRH; ++e) s[e] = __uint_as_float(sr[e]) * ksc;  // (fp8: the block's K scale)
           if (!(rlo <= row0 && rhi >= row0 + NRH)) {
 #pragma unroll
             for (int e = 0; e < NRH; ++e)
@@ -702,7 +885,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           uint32_t w[4], wl[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float a0 = s[8 * k + 2 * q], a1 = s[8 * k + 2 * q + 1];
+            // (fp8: the block's V scale folded into the weights)
+            const float a0 = s[8 * k + 2 * q] * vsc, a1 = s[8 * k + 2 * q + 1] * vsc;
             if constexpr (Cfg::BF) {
               w[q] = pack_bf16x2(a0, a1);
               wl[q] = pack_bf16x2(a0 - __uint_as_float(w[q] << 16), a1 - __uint_as_float(w[q] & 0xffff0000u));
@@ -717,6 +901,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[pb]);
+        if constexpr (Cfg::FP8) {
+          // V of the next tile into the ring slot P . V(gj - 1) read
+          if (gj + 1 < ntiles) {
+            if (gj >= 1) {
+              ok = warp_wait(&pv_done[(gj - 1) % Cfg::PBUF], (uint32_t)((gj - 1) / Cfg::PBUF) & 1u, p.timeout_ns);
+              if (!ok) break;
+            }
+            if (!(ok = widen(gj + 1, true))) break;
+          }
+        }
       }
       if (!ok) break;
       if (staged) release_q((si + 1) % Cfg::QBUF, true);
@@ -749,7 +943,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int ii = r / p.G, gq = r - ii * p.G;
             const size_t idx = (((size_t)sg.b * p.q_len + ii) * p.Hq + sg.h * p.G + gq) * Cfg::D + d;
             const float v = L > 0.f ? __uint_as_float(o[e]) / L : 0.f;  // a row that sees nothing gives 0
-            if constexpr (Cfg::BF)
+            if constexpr (Cfg::OUT_BF)
               store_scalar(BF16{}, p.out, idx, v);
             else
               store_scalar(F16{}, p.out, idx, v);
@@ -797,10 +991,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __syncwarp();
     if (!mbar_wait_bounded(&fin, 0, p.timeout_ns) && lane == 0) atomicOr(&cta_flags, PKV_FLAG_TIMEOUT);
   } else if ((warp == Cfg::PRODUCER || warp == Cfg::V_PRODUCER) && lane == 0) {  // copies issued, never consumed
+    if constexpr (Cfg::FP8) {  // the raw copies last issued into each slot (the f16 rings are written by this CTA)
+      for (int j = kr_issued > Cfg::KRAW ? kr_issued - Cfg::KRAW : 0; j < kr_issued; ++j)
+        mbar_wait_bounded(&kr_full[j % Cfg::KRAW], (uint32_t)(j / Cfg::KRAW) & 1u, p.timeout_ns);
+      for (int j = vr_issued > Cfg::VRAW ? vr_issued - Cfg::VRAW : 0; j < vr_issued; ++j)
+        mbar_wait_bounded(&vr_full[j % Cfg::VRAW], (uint32_t)(j / Cfg::VRAW) & 1u, p.timeout_ns);
+    } else {
     for (int j = k_consumed; j < k_issued; ++j)
       mbar_wait_bounded(&k_full[j % Cfg::KSTAGES], (uint32_t)(j / Cfg::KSTAGES) & 1u, p.timeout_ns);
     for (int j = v_consumed; j < v_issued; ++j)
       mbar_wait_bounded(&v_full[j % Cfg::VSTAGES], (uint32_t)(j / Cfg::VSTAGES) & 1u, p.timeout_ns);
+    }
   } else if (tid < Cfg::SOFTMAX) {
     asm volatile("cp.async.wait_all;" ::: "memory");  // a Q copy left in flight by an abort
   }
@@ -930,22 +1131,29 @@ static cudaError_t launch_mq_cfg(const MqParams &p, const CUtensorMap &tmK, cons
   mc.stream = stream;
   mc.attrs = attr;
   mc.numAttrs = 1;
-  return cudaLaunchKernelEx(&mc, mq_merge_kernel, p, grid, Cfg::BF ? 1 : 0);
+  return cudaLaunchKernelEx(&mc, mq_merge_kernel, p, grid, Cfg::OUT_BF ? 1 : 0);
 }
 
-template <class T>
+template <class T, class QT = T>
 static cudaError_t launch_mq_rows(const MqParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, int grid,
                                   cudaStream_t stream) {
-  if (p.R <= 16) return launch_mq_cfg<MqCfg<T, 8>>(p, tmK, tmV, grid, stream);
-  if (p.R <= 32) return launch_mq_cfg<MqCfg<T, 16>>(p, tmK, tmV, grid, stream);
-  return launch_mq_cfg<MqCfg<T, 32>>(p, tmK, tmV, grid, stream);
+  if (p.R <= 16) return launch_mq_cfg<MqCfg<T, 8, QT>>(p, tmK, tmV, grid, stream);
+  if (p.R <= 32) return launch_mq_cfg<MqCfg<T, 16, QT>>(p, tmK, tmV, grid, stream);
+  if constexpr (T::kBytes == 1)
+    return cudaErrorNotSupported;  // fp8: up to 32 rows
+  else
+    return launch_mq_cfg<MqCfg<T, 32, QT>>(p, tmK, tmV, grid, stream);
 }
 
-cudaError_t launch_mq_decode(const MqParams &p, int cache_dtype, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                             int grid, cudaStream_t stream) {
+cudaError_t launch_mq_decode(const MqParams &p, int cache_dtype, int q_dtype, const CUtensorMap &tmK,
+                             const CUtensorMap &tmV, int grid, cudaStream_t stream) {
   if (p.R < 1 || p.R > kMqRows || p.B < 1 || p.B > kMqMaxBatch || grid < 1) return cudaErrorNotSupported;
   if (cache_dtype == PKV_BF16) return launch_mq_rows<BF16>(p, tmK, tmV, grid, stream);
   if (cache_dtype == PKV_F16) return launch_mq_rows<F16>(p, tmK, tmV, grid, stream);
+  if (cache_dtype == PKV_FP8_E4M3 && p.R <= kMqRowsFp8) {
+    if (q_dtype == PKV_BF16) return launch_mq_rows<E4M3, BF16>(p, tmK, tmV, grid, stream);
+    if (q_dtype == PKV_F16) return launch_mq_rows<E4M3, F16>(p, tmK, tmV, grid, stream);
+  }
   return cudaErrorNotSupported;
 }
 

@@ -1,6 +1,6 @@
 // mq_decode.h — host side of the transposed tensor-core multi-query decode
 // (mq_decode.cu): q_len new tokens per sequence, q_len * G <= 64 query rows
-// per kv head, head dim 128, 16-bit caches.
+// per kv head (32 for fp8 caches), head dim 128, 16-bit or fp8 caches.
 #pragma once
 
 #include "internal.h"
@@ -10,10 +10,13 @@ namespace pkv {
 constexpr int kMqRows = 64;         // most query rows (q_len * G) per kv head
 constexpr int kMqMaxBatch = 2048;   // sequences: each CTA keeps their tile prefix in shared memory
 constexpr int kMqHeadDim = 128;
+constexpr int kMqRowsFp8 = 32;      // fp8 caches: most query rows (shared memory also holds the raw tiles)
 
 struct MqParams {
-  void *out;                    // [B][q_len][Hq][D], the cache's 16-bit type
+  void *out;                    // [B][q_len][Hq][D], the query's 16-bit type
   const void *q;                // [B][q_len][Hq][D]
+  const float *k_scale;         // fp8 caches: [num_blocks][Hkv] block scales (else null)
+  const float *v_scale;
   const int32_t *block_table;   // [B][max_blocks]
   const int32_t *context_lens;  // [B], the appended tokens included
   int32_t *status;              // PKV_FLAG_* bits of the call (written by the merge kernel)
@@ -37,7 +40,7 @@ MqWsLayout mq_ws_layout(int B, int grid);
 // Launches the decode kernel (grid CTAs, one per SM) and, for grid > 1, the
 // merge of items split between CTAs.  cudaErrorNotSupported for a shape the
 // kernel is not built for.
-cudaError_t launch_mq_decode(const MqParams &p, int cache_dtype, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                             int grid, cudaStream_t stream);
+cudaError_t launch_mq_decode(const MqParams &p, int cache_dtype, int q_dtype, const CUtensorMap &tmK,
+                             const CUtensorMap &tmV, int grid, cudaStream_t stream);
 
 }  // namespace pkv

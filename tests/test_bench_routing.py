@@ -3,7 +3,8 @@ ABI's routing of paged_decode_attention_multi: q_len 1 -> the decode kernel;
 16-bit caches with head dim 128 and up to 32 query rows per kv head -> the
 transposed tensor-core kernel; 33-64 rows -> the 128-row prefill kernel when
 its grid fills the SMs, else the transposed kernel; fp8 / f32 caches, a fixed
-split count or small grids of wider rows -> the 8-row decode units;
+split count or small grids of wider rows -> the 8-row decode units; fp8
+caches with 17-32 rows -> the transposed kernel (tiles widened to f16);
 a route forced through pkv_set_route applies where it can.  Host logic only."""
 from types import SimpleNamespace
 
@@ -36,7 +37,10 @@ def _route(name):
     (_w(8, B=4), 0, "transposed"),                  # 64 rows, 32 items: the prefill grid would not fill
     (_w(16, Hq=64, Hkv=8), 0, "prefill"),           # 128 rows: past the transposed kernel
     (_w(16, B=4), 0, "units"),                      # 128 rows, small grid
-    (_w(4, dtype="fp8_e4m3"), 0, "units"),
+    (_w(4, dtype="fp8_e4m3"), 0, "transposed"),      # fp8, 32 rows: widened to f16 in the transposed kernel
+    (_w(4, dtype="fp8_e4m3", Hq=32), 0, "units"),     # the 32K fp8 layer's group 4 at q_len 4: 16 rows, units faster
+    (_w(8, dtype="fp8_e4m3", Hq=32), 0, "transposed"),  # 32 rows
+    (_w(8, dtype="fp8_e4m3"), 0, "units"),            # fp8, 64 rows: no fp8 prefill route
     (_w(4, dtype="f32"), 0, "units"),
     (_w(4), 7, "units"),                            # a fixed split count
     (_w(4, D=64), 0, "prefill"),                    # head dim 64: the prefill kernel
@@ -53,6 +57,7 @@ def test_roofline_kernel_follows_the_routing(w, splits, want):
     ("units", _w(4), "units"),
     ("transposed", _w(8), "transposed"),            # forced on 64 rows with a full prefill grid
     ("transposed", _w(16), "prefill"),              # cannot apply past 64 rows
+    ("transposed", _w(4, dtype="fp8_e4m3", Hq=32), "transposed"),  # fp8 at 16 rows, forced
 ])
 def test_roofline_kernel_honours_the_override(force, w, want):
     assert _route(bench.attention_kernel_name(w, 0, SMS, force)) == want

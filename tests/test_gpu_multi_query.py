@@ -281,3 +281,58 @@ def test_transposed_kernel_equals_the_prefill_route(q_len, B):
     with routes(multi_query="prefill"):
         b = _check_step(w)
     print(a, b)
+
+
+# FP8 caches on the transposed kernel: each E4M3 tile is widened to f16 in
+# shared memory by the producer warps (exact), the MMAs run on f16 (the query
+# converted when staged), the block's K scale multiplies the scores and its V
+# scale is folded into the weights; up to 32 query rows per kv head.
+@pytest.mark.parametrize("q_dtype,Hq,Hkv,q_len,ctx,window", [
+    ("bf16", 2, 2, 2, [2, 130, 1000], 0),                   # MHA, R = 2
+    ("bf16", 16, 2, 2, [2, 129, 4000, 77], 0),              # R = 16
+    ("f16", 16, 2, 2, [2, 129, 4000, 77], 0),
+    ("bf16", 32, 4, 4, [4, 500, 2048, 3333, 7], 0),         # R = 32
+    ("f16", 32, 4, 4, [4, 500, 2048, 3333, 7], 37),
+    ("bf16", 24, 8, 7, [7, 300, 1500], 100),                # R = 21, window
+    ("bf16", 32, 8, 8, [8, 1200, 5000, 64], 1),             # window 1: token i sees only itself
+], ids=lambda v: str(v))
+def test_transposed_kernel_fp8(q_dtype, Hq, Hkv, q_len, ctx, window):
+    spec = dict(B=len(ctx), Hq=Hq, Hkv=Hkv, D=128, dtype="fp8_e4m3", q_dtype=q_dtype, q_len=q_len, ctx=ctx,
+                free_frac=0.3, min_free=16, window=window)
+    with routes(multi_query="transposed"):
+        _check_step(workloads.make(spec, seed=91))
+
+
+@pytest.mark.parametrize("route", ["transposed", "auto"])
+def test_fp8_long_context_layer_multi_query(route):
+    """The long-context fp8 layer (16 sequences of 32768 positions, Hq 32,
+    Hkv 8) verifying 4 draft tokens per sequence (16 rows per kv head), on
+    the transposed kernel (forced) and on the default route (the 8-row
+    units); every output compared."""
+    w = workloads.config(5, q_len=4)
+    with routes(multi_query=route):
+        print(_check_step(w))
+
+
+def test_transposed_kernel_fp8_flags_a_bad_block_id():
+    """A block id past the pool reads as zeros with scale 0 and raises
+    PKV_FLAG_BAD_BLOCK; the other sequence is exact."""
+    pkv = _pkv()
+    dev = "cuda"
+    w = workloads.make(dict(B=2, Hq=8, Hkv=2, D=128, dtype="fp8_e4m3", q_dtype="bf16", q_len=3, ctx=[40, 40],
+                            free_frac=0.5, min_free=8), seed=93)
+    table = np.full((2, 3), 0, dtype=np.int32)
+    for b in range(2):
+        table[b, :len(w.tables[b])] = w.tables[b]
+    table[1, 1] = w.num_blocks + 5
+    lens = np.array(w.cached, dtype=np.int32)
+    q = w.q.to(dev)
+    out = torch.empty_like(q)
+    with routes(multi_query="transposed"):
+        ws = pkv.paged_decode_attention(out, q, w.k_cache.to(dev), w.v_cache.to(dev), torch.from_numpy(table).to(dev),
+                                        torch.from_numpy(lens).to(dev), w.scale, w.k_scale.to(dev), w.v_scale.to(dev))
+    rc, flags = pkv.paged_decode_status(ws)
+    assert flags & pkv.PKV_FLAG_BAD_BLOCK
+    ref = oracle.decode(w.q[:1], "bf16", w.k_cache, w.v_cache, "fp8_e4m3", table[:1], lens[:1], scale=w.scale,
+                        k_scale=w.k_scale.numpy(), v_scale=w.v_scale.numpy())
+    compare(out[:1], ref, "fp8_e4m3", "the good sequence")
