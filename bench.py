@@ -577,14 +577,15 @@ def attention_kernel_name(w, num_splits, sms, force="auto"):
     G = w.Hq // w.Hkv
     R = w.q_len * G
     sixteen = w.dtype in ("bf16", "f16")
-    fp8_ok = w.dtype == "fp8_e4m3" and R <= 32 and (R > 16 or force == "transposed")  # widened to f16 there
+    fp8_ok = w.dtype == "fp8_e4m3" and R <= 32 and force == "transposed"  # widened to f16 there: forced only
     fills = w.B * w.Hkv * ((R + 127) // 128) >= sms and w.B <= 65535
     if num_splits == 0 and (sixteen or fp8_ok) and force not in ("units", "prefill") and w.D == 128 and R <= 64 \
             and w.B <= 2048 and (R <= 32 or not fills or force == "transposed"):
         return "mq_decode_kernel (transposed tcgen05, stream-K) + mq_merge_kernel"
     if num_splits == 0 and sixteen and force != "units" and fills:
         return "prefill tcgen05 kernel (128-row tiles, uniform q_len)"
-    return "paged_decode_attention (plan + decode in 8-row units + merge)"
+    rows = 16 if w.dtype == "fp8_e4m3" and R > 8 else 8  # fp8 kv heads past 8 rows: 16-row units
+    return f"paged_decode_attention (plan + decode in {rows}-row units + merge)"
 
 
 def prefill_kernel_name(c, force="auto"):

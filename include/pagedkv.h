@@ -236,18 +236,18 @@ int paged_decode_attention(void *out, const void *q, int q_dtype,
  *  - otherwise, with at least one (sequence, kv head, 128-row tile) per SM,
  *    a tensor-core prefill kernel (chosen as in paged_prefill_attention),
  *    which also reads each (sequence, kv head)'s K/V once for all its rows;
- *  - an FP8 cache with 17-32 rows, D = 128, B <= 2048: the first kernel,
- *    whose producer warps copy the E4M3 tiles and whose softmax warps widen
- *    each to f16 in shared memory (exact) while the previous tile's softmax
- *    runs; the block scales multiply the scores and are folded into the
- *    weights;
- *  - otherwise (FP8 caches up to 16 rows, F32 caches, a fixed split count,
- *    small grids) each kv head's rows are served in 8-row units by the
- *    decode kernel (K/V read once per unit, re-reads mostly from L2) with the
- *    split-KV merge.
+ *  - otherwise (FP8 and F32 caches, a fixed split count, small grids) each
+ *    kv head's rows are served in units by the decode kernel (K/V read once
+ *    per unit, re-reads mostly from L2) with the split-KV merge: units of 8
+ *    rows, or of 16 rows on an FP8 cache with more than 8 rows per kv head
+ *    (each E4M3 element widened to f16 once per 16 rows).
  * pkv_set_route(PKV_ROUTE_MULTI_QUERY, PKV_MQ_TRANSPOSED | PKV_MQ_PREFILL |
  * PKV_MQ_UNITS) forces the first, second or last route where it applies
- * (measurement and tests).
+ * (measurement and tests).  Forced, the first route also takes an FP8 cache
+ * with up to 32 rows and D = 128: its producer warps copy the E4M3 tiles
+ * and its softmax warps widen each to f16 in shared memory (exact), the
+ * block scales multiplying the scores and folded into the weights (slower
+ * than the 16-row units on GB300, hence not automatic).
  */
 #define PKV_MAX_Q_LEN 64
 int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
@@ -418,10 +418,10 @@ int paged_kv_copy_blocks(void *k_cache, void *v_cache, int cache_dtype,
  * them.  A forced route applies only where the chosen kernel supports the
  * call (otherwise the automatic rule decides).  Each call reads the setting
  * once; change it only while no call is being issued on another host thread.
- *   which = PKV_ROUTE_MULTI_QUERY (q_len >= 2 decode on 16-bit caches):
+ *   which = PKV_ROUTE_MULTI_QUERY (q_len >= 2 decode):
  *           PKV_ROUTE_AUTO, PKV_MQ_TRANSPOSED (the transposed tensor-core
  *           kernel), PKV_MQ_PREFILL (the 128-row prefill kernel), PKV_MQ_UNITS
- *           (the decode kernel's 8-row units with the split-KV merge)
+ *           (the decode kernel's 8- or 16-row units with the split-KV merge)
  *   which = PKV_ROUTE_PREFILL (the prefill kernel's schedule):
  *           PKV_ROUTE_AUTO, PKV_PREFILL_PERSISTENT, PKV_PREFILL_PER_ITEM
  * Returns PKV_EINVAL for an unknown `which` or `choice`; pkv_get_route
@@ -446,7 +446,7 @@ int pkv_get_route(int which);
  * path, so that tests can check that path without a fault or a hang.  In that
  * call every bounded in-kernel wait is limited to limit_ns (normally 4 s), and
  *  - PKV_STALL_DECODE (the decode kernel: paged_decode_attention, and the
- *    8-row-unit route of paged_decode_attention_multi): the worker holding the
+ *    unit route of paged_decode_attention_multi): the worker holding the
  *    first work item replaces its first pipeline wait by a wait on a barrier
  *    that nothing completes;
  *  - PKV_STALL_PREFILL (either prefill kernel, from paged_prefill_attention or

@@ -31,7 +31,7 @@ void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e);
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout ws_layout(int B, int P, int D) {
+WsLayout ws_layout(int B, int P, int D, int GC) {
   WsLayout L;
   size_t o = 0;
   L.hdr = o;
@@ -41,9 +41,9 @@ WsLayout ws_layout(int B, int P, int D) {
   L.starts = o;
   o = align_up(o + sizeof(int4) * (size_t)(P + 1), 256);
   L.part_o = o;
-  o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax * D, 256);
+  o = align_up(o + sizeof(float) * (size_t)P * 2 * GC * D, 256);
   L.part_lse = o;
-  o = align_up(o + sizeof(float) * (size_t)P * 2 * kChunkMax, 256);
+  o = align_up(o + sizeof(float) * (size_t)P * 2 * GC, 256);
   L.cta_flags = o;
   o = align_up(o + sizeof(int32_t) * (size_t)P, 256);
   L.total = o;
@@ -261,7 +261,8 @@ struct Choice {
 // first compiled match is the default pipeline shape.  A build with
 // PKV_SWEEP_SHAPES defined (pipeline-shape sweeps, not the product build)
 // also compiles alternative shapes and lets PKV_PATH=mma|simt,
-// PKV_DECODE_WARPS and PKV_DECODE_STAGES in the environment pick among them.
+// PKV_DECODE_WARPS, PKV_DECODE_STAGES and PKV_DECODE_GC=8 in the environment
+// pick among them.
 int choose_kernel(int cache_dtype, int q_dtype, int D, int R, Choice *c) {
 #ifdef PKV_SWEEP_SHAPES
   static const int force = [] {
@@ -278,20 +279,35 @@ int choose_kernel(int cache_dtype, int q_dtype, int D, int R, Choice *c) {
     const char *v = std::getenv("PKV_DECODE_STAGES");
     return v ? std::atoi(v) : 0;
   }();
+  static const int want_gc = [] {
+    const char *v = std::getenv("PKV_DECODE_GC");
+    return v ? std::atoi(v) : 0;
+  }();
 #else
-  constexpr int force = 0, want_warps = 0, want_stages = 0;
+  constexpr int force = 0, want_warps = 0, want_stages = 0, want_gc = 0;
 #endif
   const bool mma = cache_dtype != PKV_F32 && force != 1;
-  const int GC = mma ? 8 : (R >= 2 ? 2 : 1);
+  // fp8 caches serve a kv head with more than 8 rows in 16-row units: each
+  // E4M3 element is widened once per 16 rows instead of once per 8 (on the
+  // 32K fp8 layer at 16 rows, one 16-row unit per kv head against two 8-row
+  // units streaming the same blocks)
+  int GC = mma ? 8 : (R >= 2 ? 2 : 1);
+  if (mma && cache_dtype == PKV_FP8_E4M3 && R > 8 && want_gc != 8) GC = 16;
   Registry &r = registry();
   int first = -1;
-  for (int i = 0; i < r.n; ++i) {
-    const DecodeKernel &k = r.k[i];
-    if (k.mma == (mma ? 1 : 0) && k.cache_dtype == cache_dtype && k.q_dtype == q_dtype && k.D == D && k.GC == GC) {
-      if (first < 0) first = i;
-      if ((want_warps == 0 || k.warps == want_warps) && (want_stages == 0 || k.stages == want_stages)) {
-        first = i;
-        break;
+  for (int pass = 0; pass < 2 && first < 0; ++pass) {
+    if (pass == 1) {
+      if (GC != 16) break;
+      GC = 8;  // no 16-row kernel for this (q dtype, D): 8-row units
+    }
+    for (int i = 0; i < r.n; ++i) {
+      const DecodeKernel &k = r.k[i];
+      if (k.mma == (mma ? 1 : 0) && k.cache_dtype == cache_dtype && k.q_dtype == q_dtype && k.D == D && k.GC == GC) {
+        if (first < 0) first = i;
+        if ((want_warps == 0 || k.warps == want_warps) && (want_stages == 0 || k.stages == want_stages)) {
+          first = i;
+          break;
+        }
       }
     }
   }
@@ -418,7 +434,7 @@ int paged_decode_multi_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
   int P = 0;
   rc = plan_call(cache_dtype, q_dtype, B, q_len, Hq, Hkv, D, num_splits, &c, &P);
   if (rc != PKV_OK) return rc;
-  size_t total = ws_layout(B, P, D).total;
+  size_t total = ws_layout(B, P, D, c.GC).total;
   if (q_len >= 2 && num_splits == 0 && D == kMqHeadDim && q_len * (Hq / Hkv) <= kMqRows && B <= kMqMaxBatch &&
       (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16 ||
        (cache_dtype == PKV_FP8_E4M3 && q_len * (Hq / Hkv) <= kMqRowsFp8))) {
@@ -506,7 +522,7 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   int P = 0;
   rc = plan_call(cache_dtype, q_dtype, B, q_len, Hq, Hkv, D, num_splits, &c, &P);
   if (rc != PKV_OK) return rc;
-  const WsLayout L = ws_layout(B, P, D);
+  const WsLayout L = ws_layout(B, P, D, c.GC);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total)
     return PKV_EWORKSPACE;
   if (q_len >= 2 && num_splits == 0) {
@@ -536,13 +552,14 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
     const int64_t tiles = ((int64_t)q_len * G + 127) / 128;
     const bool prefill_fills = (int64_t)B * Hkv * tiles >= sms && B <= 65535;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // FP8 caches take the transposed kernel for 17-32 rows (it widens each
-    // tile to f16 in shared memory, which on 32 KiB fp8 tiles costs more than
-    // the tile's HBM time: ~2.1-2.4 TB/s whatever the rows, against the 8-row
-    // units' 6.0 / 3.2 / 1.7 TB/s at 8 / 16 / 32 rows on the 32K fp8 layer);
-    // they have no prefill route
+    // FP8 caches take the decode kernel's units (16 rows each past 8 rows):
+    // the transposed kernel widens each tile to f16 in shared memory, which
+    // on 32 KiB fp8 tiles costs more than the tile's HBM time (~2.1 TB/s
+    // whatever the rows, against the units' 6.1 / 4.6 / 2.4 TB/s at 8 / 16 /
+    // 32 rows on the 32K fp8 layer); it runs only when forced.  FP8 caches
+    // have no prefill route.
     const bool fp8 = cache_dtype == PKV_FP8_E4M3;
-    const bool fp8_mq = fp8 && R <= kMqRowsFp8 && (R > 16 || want_mq);
+    const bool fp8_mq = fp8 && R <= kMqRowsFp8 && want_mq;
     if (!no_mq && (cache_dtype == PKV_BF16 || cache_dtype == PKV_F16 || fp8_mq) && scale > 0.f &&
         D == kMqHeadDim && R <= kMqRows && B <= kMqMaxBatch && (R <= 32 || !prefill_fills || want_mq)) {
       const MqWsLayout M = mq_ws_layout(B, sms);

@@ -29,10 +29,13 @@
 // reached through the block table ("LLM推理优化实战" §2.2 block table) — onto
 // the slot's mbarrier, STAGES blocks ahead of the consumer.
 //
-// Compute.  MMA path (f16/bf16/fp8 caches, group >= 3): per 16-token block,
-// S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8] and O^T[D x 8] += V^T[D x 16] .
+// Compute.  MMA path (f16/bf16/fp8 caches): per 16-token block,
+// S^T[16 tok x 8 rows] = K[16 x D] . Q^T[D x 8] and O^T[D x 8] += V^T[D x 16] .
 // P^T[16 x 8] with mma.sync m16n8k16 (fp32 accumulate); P moves from the
-// score fragment to the B operand with movmatrix.  CUDA-core path (fp32
+// score fragment to the B operand with movmatrix.  Units serve 8 rows; on
+// fp8 caches a kv head with more than 8 rows (several new tokens per
+// sequence) is served in 16-row units, two 8-row column groups per MMA A
+// operand, so each E4M3 K / V element is widened to f16 once per 16 rows.  CUDA-core path (fp32
 // caches, groups of 1-2): lanes split tokens for q.K and head-dim slices for
 // p.V.  Scores use the scale of "苦猿的大模型日记 Day45" PART 02
 // (softmax(QK^T / sqrt(d))), applied in fp32 in the log2 domain.
@@ -77,7 +80,8 @@ struct DecodeCfg {
   static constexpr int CTAS_RAW = (int)(233472 / (SMEM + 1024));
   static constexpr int MIN_CTAS = CTAS_RAW < 1 ? 1 : (CTAS_RAW > 8 ? 8 : CTAS_RAW);
   static_assert(TILE % 1024 == 0, "tiles must keep 1024-byte alignment for the swizzle");
-  static_assert(!MMA || GC == 8, "the MMA path serves 8-head chunks");
+  static_assert(!MMA || GC == 8 || (GC == 16 && FP8 && BPS == 2),
+                "the MMA path serves 8-row units (16-row units: the two-block fp8 path)");
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BPS == 1 || (BPS == 2 && MMA && FP8), "two blocks per stage: the fp8 tensor-core path");
 };
@@ -264,10 +268,11 @@ template <class Cfg>
 struct MmaState {
   static constexpr int KS = Cfg::D / 16;  // k-steps of q.K
   static constexpr int MT = Cfg::D / 16;  // m-tiles of V^T
-  uint32_t qb[KS][2];
-  float acc[MT][4];
-  float m0, m1, l0, l1;
-  int back0, back1;  // row_back of the score columns 2 tig, 2 tig + 1
+  static constexpr int NH = Cfg::GC >= 8 ? Cfg::GC / 8 : 1;  // 8-row column groups of a unit
+  uint32_t qb[NH][KS][2];
+  float acc[NH][MT][4];
+  float m[NH][2], l[NH][2];  // per score column 8 nh + 2 tig, 8 nh + 2 tig + 1
+  int back[NH][2];           // row_back of those columns
 };
 
 template <class Cfg>
@@ -276,42 +281,46 @@ __device__ __forceinline__ void mma_begin(MmaState<Cfg> &st, const DecodeParams 
   const int gid = lane >> 2, tig = lane & 3;
   const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
   const int gc = min(Cfg::GC, p.R - r0);
-  const size_t row = gid < gc ? query_row(p, m.b, h, r0 + gid) : 0;
-  st.back0 = row_back(p, r0 + 2 * tig);
-  st.back1 = row_back(p, r0 + 2 * tig + 1);
 #pragma unroll
-  for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
-    uint32_t b0 = 0, b1 = 0;
-    if (gid < gc) {
-      if constexpr (Cfg::FP8) {
-        // k-slots 2t,2t+1 | 2t+8,2t+9 hold d = 16ks + 4t + {0,1} | {2,3}
-        const uint2 raw = *reinterpret_cast<const uint2 *>(
-            reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 4 * tig);
-        float2 x0, x1;
-        if constexpr (Cfg::Q::kCode == PKV_BF16) {
-          x0 = unpack2(BF16{}, raw.x);
-          x1 = unpack2(BF16{}, raw.y);
+  for (int nh = 0; nh < MmaState<Cfg>::NH; ++nh) {
+    const int rq = 8 * nh + gid;  // the q row (B-operand column) this lane loads
+    const size_t row = rq < gc ? query_row(p, m.b, h, r0 + rq) : 0;
+    st.back[nh][0] = row_back(p, r0 + 8 * nh + 2 * tig);
+    st.back[nh][1] = row_back(p, r0 + 8 * nh + 2 * tig + 1);
+#pragma unroll
+    for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
+      uint32_t b0 = 0, b1 = 0;
+      if (rq < gc) {
+        if constexpr (Cfg::FP8) {
+          // k-slots 2t,2t+1 | 2t+8,2t+9 hold d = 16ks + 4t + {0,1} | {2,3}
+          const uint2 raw = *reinterpret_cast<const uint2 *>(
+              reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 4 * tig);
+          float2 x0, x1;
+          if constexpr (Cfg::Q::kCode == PKV_BF16) {
+            x0 = unpack2(BF16{}, raw.x);
+            x1 = unpack2(BF16{}, raw.y);
+          } else {
+            x0 = unpack2(F16{}, raw.x);
+            x1 = unpack2(F16{}, raw.y);
+          }
+          b0 = pack_f16x2(x0.x, x0.y);
+          b1 = pack_f16x2(x1.x, x1.y);
         } else {
-          x0 = unpack2(F16{}, raw.x);
-          x1 = unpack2(F16{}, raw.y);
+          const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 2 * tig;
+          b0 = *reinterpret_cast<const uint32_t *>(qr);
+          b1 = *reinterpret_cast<const uint32_t *>(qr + 8);
         }
-        b0 = pack_f16x2(x0.x, x0.y);
-        b1 = pack_f16x2(x1.x, x1.y);
-      } else {
-        const uint16_t *qr = reinterpret_cast<const uint16_t *>(p.q) + row + 16 * ks + 2 * tig;
-        b0 = *reinterpret_cast<const uint32_t *>(qr);
-        b1 = *reinterpret_cast<const uint32_t *>(qr + 8);
       }
+      st.qb[nh][ks][0] = b0;
+      st.qb[nh][ks][1] = b1;
     }
-    st.qb[ks][0] = b0;
-    st.qb[ks][1] = b1;
+#pragma unroll
+    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) st.acc[nh][mt][r] = 0.f;
+    st.m[nh][0] = st.m[nh][1] = -INFINITY;
+    st.l[nh][0] = st.l[nh][1] = 0.f;
   }
-#pragma unroll
-  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) st.acc[mt][r] = 0.f;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
 }
 
 // A block's K and V operands in registers (MMA fragments, or raw fp8 words).
@@ -364,11 +373,12 @@ __device__ __forceinline__ void mma_load(MmaFrags<Cfg> &f, uint8_t *tk, uint8_t 
 template <class Cfg>
 __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cfg> &f, const DecodeParams &p,
                                             const StageMeta &m, int lane) {
+  static_assert(MmaState<Cfg>::NH == 1, "one-block steps serve 8-row units");
   constexpr bool kBF = (Cfg::Cache::kCode == PKV_BF16);
   const int gid = lane >> 2;
   // token rows r of the block visible to score column c: base_c <= r < base_c + W,
   // base_c = rem - back_c - W (one unsigned compare; W = 2^30 without a window)
-  const int base0 = m.rem - st.back0 - p.wlen, base1 = m.rem - st.back1 - p.wlen;
+  const int base0 = m.rem - st.back[0][0] - p.wlen, base1 = m.rem - st.back[0][1] - p.wlen;
   const uint32_t wl = (uint32_t)p.wlen;
 
   // ---- scores S^T = K . Q^T (16 tokens x 8 heads), two independent chains ----
@@ -386,9 +396,9 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
       a[0] = f.k[ks][0]; a[1] = f.k[ks][1]; a[2] = f.k[ks][2]; a[3] = f.k[ks][3];
     }
     if (ks & 1)
-      mma16816<kBF>(s1, a, st.qb[ks][0], st.qb[ks][1]);
+      mma16816<kBF>(s1, a, st.qb[0][ks][0], st.qb[0][ks][1]);
     else
-      mma16816<kBF>(s, a, st.qb[ks][0], st.qb[ks][1]);
+      mma16816<kBF>(s, a, st.qb[0][ks][0], st.qb[0][ks][1]);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) s[i] += s1[i];
@@ -406,22 +416,22 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
     mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
     mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
   }
-  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  const float mn0 = fmaxf(st.m[0][0], mx0), mn1 = fmaxf(st.m[0][1], mx1);
   // a column that has seen no visible position yet keeps weight 0 (not NaN)
   const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(st.m0 - mb0), al1 = exp2f(st.m1 - mb1);
+  const float al0 = exp2f(st.m[0][0] - mb0), al1 = exp2f(st.m[0][1] - mb1);
   const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1);
   const float p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
-  st.l0 = st.l0 * al0 + (p0 + p2);
-  st.l1 = st.l1 * al1 + (p1 + p3);
-  st.m0 = mn0;
-  st.m1 = mn1;
+  st.l[0][0] = st.l[0][0] * al0 + (p0 + p2);
+  st.l[0][1] = st.l[0][1] * al1 + (p1 + p3);
+  st.m[0][0] = mn0;
+  st.m[0][1] = mn1;
 #pragma unroll
   for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
-    st.acc[mt][0] *= al0;
-    st.acc[mt][1] *= al1;
-    st.acc[mt][2] *= al0;
-    st.acc[mt][3] *= al1;
+    st.acc[0][mt][0] *= al0;
+    st.acc[0][mt][1] *= al1;
+    st.acc[0][mt][2] *= al0;
+    st.acc[0][mt][3] *= al1;
   }
 
   // ---- O^T += V^T . P^T ----
@@ -441,7 +451,7 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
       a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
       a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
       a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
-      mma16816<false>(st.acc[mt], a, pb0, pb1);
+      mma16816<false>(st.acc[0][mt], a, pb0, pb1);
     }
   } else if constexpr (kBF) {
     // bf16 keeps 8 significant bits; short contexts give weights near 1
@@ -455,14 +465,14 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
     const uint32_t lb1 = movmatrix_trans(pack_bf16x2(p2 - f23.x, p3 - f23.y));
 #pragma unroll
     for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
-      mma16816<true>(st.acc[mt], f.v[mt], pb0, pb1);
-      mma16816<true>(st.acc[mt], f.v[mt], lb0, lb1);
+      mma16816<true>(st.acc[0][mt], f.v[mt], pb0, pb1);
+      mma16816<true>(st.acc[0][mt], f.v[mt], lb0, lb1);
     }
   } else {
     const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
     const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
 #pragma unroll
-    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) mma16816<false>(st.acc[mt], f.v[mt], pb0, pb1);
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) mma16816<false>(st.acc[0][mt], f.v[mt], pb0, pb1);
   }
 }
 
@@ -472,13 +482,20 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
 // one online-softmax update.  K fragments are loaded and consumed before the
 // V fragments, which keeps the register footprint of two blocks in bounds.
 // ---------------------------------------------------------------------------
-// S^T = K . Q^T of one fp8 block (two independent MMA chains, summed).
+// S^T = K . Q^T of one fp8 block for every 8-row group of the unit (two
+// independent MMA chains per group, summed); each K fragment is widened once
+// for all groups.
 template <class Cfg>
-__device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_t *tk, int lane, float (&s)[4]) {
-  constexpr int ROWB = Cfg::ROWB;
+__device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_t *tk, int lane,
+                                           float (&s)[MmaState<Cfg>::NH][4]) {
+  constexpr int ROWB = Cfg::ROWB, NH = MmaState<Cfg>::NH;
   const int gid = lane >> 2, tig = lane & 3;
   const uint32_t kb = smem_u32(tk);
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  float s0[NH][4], s1[NH][4];
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s0[nh][i] = s1[nh][i] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < MmaState<Cfg>::KS; ++ks) {
     // k-slots 2t,2t+1 | 2t+8,2t+9 of row gid (+8) hold d = 16ks + 4t + {0,1} | {2,3}
@@ -489,20 +506,27 @@ __device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_
     a[1] = e4m3x2_to_f16x2((uint16_t)(k1 & 0xffff));
     a[2] = e4m3x2_to_f16x2((uint16_t)(k0 >> 16));
     a[3] = e4m3x2_to_f16x2((uint16_t)(k1 >> 16));
-    if (ks & 1)
-      mma16816<false>(s1, a, st.qb[ks][0], st.qb[ks][1]);
-    else
-      mma16816<false>(s0, a, st.qb[ks][0], st.qb[ks][1]);
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+      if (ks & 1)
+        mma16816<false>(s1[nh], a, st.qb[nh][ks][0], st.qb[nh][ks][1]);
+      else
+        mma16816<false>(s0[nh], a, st.qb[nh][ks][0], st.qb[nh][ks][1]);
+    }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) s[i] = s0[i] + s1[i];
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[nh][i] = s0[nh][i] + s1[nh][i];
 }
 
-// O^T += V^T . P^T of one fp8 block, P (with the block's V scale folded in)
-// already in B-operand form.
+// O^T += V^T . P^T of one fp8 block for every 8-row group, P (with the
+// block's V scale folded in) already in B-operand form; each V fragment is
+// widened once for all groups.
 template <class Cfg>
-__device__ __forceinline__ void fp8_pv(MmaState<Cfg> &st, const uint8_t *tv, int lane, uint32_t pb0, uint32_t pb1) {
-  constexpr int ROWB = Cfg::ROWB;
+__device__ __forceinline__ void fp8_pv(MmaState<Cfg> &st, const uint8_t *tv, int lane,
+                                       const uint32_t (&pb)[MmaState<Cfg>::NH][2]) {
+  constexpr int ROWB = Cfg::ROWB, NH = MmaState<Cfg>::NH;
   constexpr int DPT = Cfg::D / 8;  // head-dim bytes owned by one row group
   const int gid = lane >> 2, tig = lane & 3;
   const uint32_t vb = smem_u32(tv);
@@ -530,7 +554,8 @@ __device__ __forceinline__ void fp8_pv(MmaState<Cfg> &st, const uint8_t *tv, int
     a[1] = e4m3x2_to_f16x2((uint16_t)(x >> 16));
     a[2] = e4m3x2_to_f16x2((uint16_t)(y & 0xffff));
     a[3] = e4m3x2_to_f16x2((uint16_t)(y >> 16));
-    mma16816<false>(st.acc[mt], a, pb0, pb1);
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) mma16816<false>(st.acc[nh][mt], a, pb[nh][0], pb[nh][1]);
   }
 }
 
@@ -538,7 +563,7 @@ template <class Cfg>
 __device__ __forceinline__ void mma_pair(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
                                          uint8_t *tk0, int lane) {
   static_assert(Cfg::FP8, "two-block stages are the fp8 path");
-  constexpr int ROWB = Cfg::ROWB;
+  constexpr int ROWB = Cfg::ROWB, NH = MmaState<Cfg>::NH;
   const int gid = lane >> 2;
   const bool two = m.nb == 2;
   uint8_t *tv0 = tk0 + Cfg::TILE, *tk1 = tk0 + 2 * Cfg::TILE, *tv1 = tk0 + 3 * Cfg::TILE;
@@ -546,57 +571,62 @@ __device__ __forceinline__ void mma_pair(MmaState<Cfg> &st, const DecodeParams &
   if (rem0 < kBlock) zero_tail_rows<ROWB>(tv0, rem0, lane);
   if (two && rem1 < kBlock) zero_tail_rows<ROWB>(tv1, rem1, lane);
 
-  float s[4], t[4];
+  float s[NH][4], t[NH][4];
   fp8_scores<Cfg>(st, tk0, lane, s);
   if (two) fp8_scores<Cfg>(st, tk1, lane, t);
 
-  // token rows r of a block visible to score column c: base_c <= r < base_c + W
-  // (see mma_compute); the second block's base is 16 lower
   const uint32_t wl = (uint32_t)p.wlen;
-  const int base0 = rem0 - st.back0 - p.wlen, base1 = rem0 - st.back1 - p.wlen;
   const float sc0 = p.scale_log2 * m.ks, sc1 = p.scale_log2 * m.ks1;
-  float x0 = s[0] * sc0, x1 = s[1] * sc0, x2 = s[2] * sc0, x3 = s[3] * sc0;
-  if ((uint32_t)(gid - base0) >= wl) x0 = -INFINITY;
-  if ((uint32_t)(gid - base1) >= wl) x1 = -INFINITY;
-  if ((uint32_t)(gid + 8 - base0) >= wl) x2 = -INFINITY;
-  if ((uint32_t)(gid + 8 - base1) >= wl) x3 = -INFINITY;
-  float y0 = -INFINITY, y1 = -INFINITY, y2 = -INFINITY, y3 = -INFINITY;
-  if (two) {
-    y0 = t[0] * sc1; y1 = t[1] * sc1; y2 = t[2] * sc1; y3 = t[3] * sc1;
-    if ((uint32_t)(gid + 16 - base0) >= wl) y0 = -INFINITY;
-    if ((uint32_t)(gid + 16 - base1) >= wl) y1 = -INFINITY;
-    if ((uint32_t)(gid + 24 - base0) >= wl) y2 = -INFINITY;
-    if ((uint32_t)(gid + 24 - base1) >= wl) y3 = -INFINITY;
-  }
-  float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
+  uint32_t pa[NH][2], pc[NH][2];  // B operands of the first and second block
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-  }
-  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-  // a column that has seen no visible position yet keeps weight 0 (not NaN)
-  const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(st.m0 - mb0), al1 = exp2f(st.m1 - mb1);
-  const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1), p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
-  const float q0 = exp2f(y0 - mb0), q1 = exp2f(y1 - mb1), q2 = exp2f(y2 - mb0), q3 = exp2f(y3 - mb1);
-  st.l0 = st.l0 * al0 + ((p0 + p2) + (q0 + q2));
-  st.l1 = st.l1 * al1 + ((p1 + p3) + (q1 + q3));
-  st.m0 = mn0;
-  st.m1 = mn1;
+  for (int nh = 0; nh < NH; ++nh) {
+    // token rows r of a block visible to score column c: base_c <= r < base_c + W
+    // (see mma_compute); the second block's base is 16 lower
+    const int base0 = rem0 - st.back[nh][0] - p.wlen, base1 = rem0 - st.back[nh][1] - p.wlen;
+    float x0 = s[nh][0] * sc0, x1 = s[nh][1] * sc0, x2 = s[nh][2] * sc0, x3 = s[nh][3] * sc0;
+    if ((uint32_t)(gid - base0) >= wl) x0 = -INFINITY;
+    if ((uint32_t)(gid - base1) >= wl) x1 = -INFINITY;
+    if ((uint32_t)(gid + 8 - base0) >= wl) x2 = -INFINITY;
+    if ((uint32_t)(gid + 8 - base1) >= wl) x3 = -INFINITY;
+    float y0 = -INFINITY, y1 = -INFINITY, y2 = -INFINITY, y3 = -INFINITY;
+    if (two) {
+      y0 = t[nh][0] * sc1; y1 = t[nh][1] * sc1; y2 = t[nh][2] * sc1; y3 = t[nh][3] * sc1;
+      if ((uint32_t)(gid + 16 - base0) >= wl) y0 = -INFINITY;
+      if ((uint32_t)(gid + 16 - base1) >= wl) y1 = -INFINITY;
+      if ((uint32_t)(gid + 24 - base0) >= wl) y2 = -INFINITY;
+      if ((uint32_t)(gid + 24 - base1) >= wl) y3 = -INFINITY;
+    }
+    float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
 #pragma unroll
-  for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-    st.acc[mt][0] *= al0;
-    st.acc[mt][1] *= al1;
-    st.acc[mt][2] *= al0;
-    st.acc[mt][3] *= al1;
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[nh][0], mx0), mn1 = fmaxf(st.m[nh][1], mx1);
+    // a column that has seen no visible position yet keeps weight 0 (not NaN)
+    const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(st.m[nh][0] - mb0), al1 = exp2f(st.m[nh][1] - mb1);
+    const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1), p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
+    const float q0 = exp2f(y0 - mb0), q1 = exp2f(y1 - mb1), q2 = exp2f(y2 - mb0), q3 = exp2f(y3 - mb1);
+    st.l[nh][0] = st.l[nh][0] * al0 + ((p0 + p2) + (q0 + q2));
+    st.l[nh][1] = st.l[nh][1] * al1 + ((p1 + p3) + (q1 + q3));
+    st.m[nh][0] = mn0;
+    st.m[nh][1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+      st.acc[nh][mt][0] *= al0;
+      st.acc[nh][mt][1] *= al1;
+      st.acc[nh][mt][2] *= al0;
+      st.acc[nh][mt][3] *= al1;
+    }
+    // the V scales folded into the weights
+    pa[nh][0] = movmatrix_trans(pack_f16x2(p0 * m.vs, p1 * m.vs));
+    pa[nh][1] = movmatrix_trans(pack_f16x2(p2 * m.vs, p3 * m.vs));
+    pc[nh][0] = movmatrix_trans(pack_f16x2(q0 * m.vs1, q1 * m.vs1));
+    pc[nh][1] = movmatrix_trans(pack_f16x2(q2 * m.vs1, q3 * m.vs1));
   }
-  // the V scales folded into the weights
-  fp8_pv<Cfg>(st, tv0, lane, movmatrix_trans(pack_f16x2(p0 * m.vs, p1 * m.vs)),
-              movmatrix_trans(pack_f16x2(p2 * m.vs, p3 * m.vs)));
-  if (two)
-    fp8_pv<Cfg>(st, tv1, lane, movmatrix_trans(pack_f16x2(q0 * m.vs1, q1 * m.vs1)),
-                movmatrix_trans(pack_f16x2(q2 * m.vs1, q3 * m.vs1)));
+  fp8_pv<Cfg>(st, tv0, lane, pa);
+  if (two) fp8_pv<Cfg>(st, tv1, lane, pc);
 }
 
 // Head-dim index held by accumulator row group `r` (0: gid, 1: gid + 8) of m-tile mt.
@@ -612,44 +642,48 @@ template <class Cfg>
 __device__ __forceinline__ void mma_finish(MmaState<Cfg> &st, const DecodeParams &p, const StageMeta &m,
                                            int w, int lane) {
   const int gid = lane >> 2, tig = lane & 3;
-  float l0 = st.l0, l1 = st.l1;
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(kFull, l0, off);
-    l1 += __shfl_xor_sync(kFull, l1, off);
-  }
-  // a row with no visible position (context shorter than q_len) gives 0
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const int h = m.hu / p.NC, r0 = (m.hu % p.NC) * Cfg::GC;
   const int gc = min(Cfg::GC, p.R - r0);
-  const int hA = 2 * tig, hB = 2 * tig + 1;
-  if (m.flags & kComplete) {
-    const size_t baseA = hA < gc ? query_row(p, m.b, h, r0 + hA) : 0;
-    const size_t baseB = hB < gc ? query_row(p, m.b, h, r0 + hB) : 0;
+  const bool complete = m.flags & kComplete;
+  // partials: [worker][slot][GC rows][D]
+  const size_t base = ((size_t)w * 2 + ((m.flags & kWFirst) ? 0 : 1)) * Cfg::GC;
 #pragma unroll
-    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+  for (int nh = 0; nh < MmaState<Cfg>::NH; ++nh) {
+    float l0 = st.l[nh][0], l1 = st.l[nh][1];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int d = mma_dim<Cfg>(mt, r, gid);
-        if (hA < gc) store_scalar(typename Cfg::Q{}, p.out, baseA + d, st.acc[mt][2 * r] * inv0);
-        if (hB < gc) store_scalar(typename Cfg::Q{}, p.out, baseB + d, st.acc[mt][2 * r + 1] * inv1);
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    // a row with no visible position (context shorter than q_len) gives 0
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    const int hA = 8 * nh + 2 * tig, hB = hA + 1;
+    if (complete) {
+      const size_t baseA = hA < gc ? query_row(p, m.b, h, r0 + hA) : 0;
+      const size_t baseB = hB < gc ? query_row(p, m.b, h, r0 + hB) : 0;
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int d = mma_dim<Cfg>(mt, r, gid);
+          if (hA < gc) store_scalar(typename Cfg::Q{}, p.out, baseA + d, st.acc[nh][mt][2 * r] * inv0);
+          if (hB < gc) store_scalar(typename Cfg::Q{}, p.out, baseB + d, st.acc[nh][mt][2 * r + 1] * inv1);
+        }
+    } else {
+      float *oA = p.part_o + (base + hA) * Cfg::D;
+      float *oB = p.part_o + (base + hB) * Cfg::D;
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int d = mma_dim<Cfg>(mt, r, gid);
+          if (hA < gc) oA[d] = st.acc[nh][mt][2 * r] * inv0;
+          if (hB < gc) oB[d] = st.acc[nh][mt][2 * r + 1] * inv1;
+        }
+      if (gid == 0) {
+        if (hA < gc) p.part_lse[base + hA] = st.m[nh][0] + log2f(l0);
+        if (hB < gc) p.part_lse[base + hB] = st.m[nh][1] + log2f(l1);
       }
-  } else {
-    const int slot = (m.flags & kWFirst) ? 0 : 1;
-    const size_t base = ((size_t)w * 2 + slot) * kChunkMax;
-    float *oA = p.part_o + (base + hA) * Cfg::D;
-    float *oB = p.part_o + (base + hB) * Cfg::D;
-#pragma unroll
-    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int d = mma_dim<Cfg>(mt, r, gid);
-        if (hA < gc) oA[d] = st.acc[mt][2 * r] * inv0;
-        if (hB < gc) oB[d] = st.acc[mt][2 * r + 1] * inv1;
-      }
-    if (gid == 0) {
-      if (hA < gc) p.part_lse[base + hA] = st.m0 + log2f(l0);
-      if (hB < gc) p.part_lse[base + hB] = st.m1 + log2f(l1);
     }
   }
 }
@@ -836,7 +870,7 @@ __device__ __forceinline__ void simt_finish(SimtState<Cfg> &st, const DecodePara
     }
   } else {
     const int slot = (m.flags & kWFirst) ? 0 : 1;
-    const size_t base = ((size_t)w * 2 + slot) * kChunkMax;
+    const size_t base = ((size_t)w * 2 + slot) * Cfg::GC;  // [worker][slot][GC rows][D]
 #pragma unroll
     for (int g = 0; g < Cfg::GC; ++g) {
       if (g >= gc) break;

@@ -11,6 +11,7 @@ namespace pkv {
 // bytes per instruction of the bf16 kernel); stages of two blocks (2 stages of
 // 8 KiB) share the per-stage and per-softmax-update work between 32 tokens.
 constexpr int kFp8Warps = 4;
+constexpr int kFp8WideBudget = 24 * 1024;
 
 int register_decode_fp8(DecodeKernel *out) {
   int n = 0;
@@ -18,6 +19,13 @@ int register_decode_fp8(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 8, true, kFp8Warps, kBudget, 2>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, kFp8Warps, kBudget, 2>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 8, true, kFp8Warps, kBudget, 2>>();
+  // 16-row units (kv heads with more than 8 query rows): twice the
+  // accumulators and q fragments per warp, so two CTAs of 4 warps per SM
+  // with 3 stages each
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, kFp8Warps, kFp8WideBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 16, true, kFp8Warps, kFp8WideBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 16, true, kFp8Warps, kFp8WideBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 16, true, kFp8Warps, kFp8WideBudget, 2>>();
 #ifdef PKV_SWEEP_SHAPES
   // for comparison runs and sweeps only, not in the product build: the
   // CUDA-core path on this cache type (PKV_PATH=simt), one block per stage
@@ -36,6 +44,11 @@ int register_decode_fp8(DecodeKernel *out) {
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 5, 16 * 1024, 2>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 6, 16 * 1024, 2>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 3, 24 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, 4, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, 5, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, 6, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, 8, 16 * 1024, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 16, true, 3, 24 * 1024, 2>>();
 #endif
   return n;
 }

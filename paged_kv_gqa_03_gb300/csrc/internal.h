@@ -10,7 +10,7 @@
 namespace pkv {
 
 constexpr int kBlock = 16;      // tokens per physical block (PKV_BLOCK_SIZE)
-constexpr int kChunkMax = 8;    // most query heads one work unit serves
+constexpr int kChunkMax = 16;   // most query rows one work unit serves
 
 // Workspace header written by the plan kernel each call.
 // Workspace header.  `status` is published by the merge kernel at the end of
@@ -58,8 +58,8 @@ struct DecodeParams {
   WsHeader *hdr;
   int32_t *prefix;      // [B+1] exclusive prefix of blocks per sequence
   int4 *starts;         // [P+1] {s, b, hu, j} of each worker's first item
-  float *part_o;        // [P][2][kChunkMax][D]
-  float *part_lse;      // [P][2][kChunkMax], log2 domain
+  float *part_o;        // [P][2][GC][D]
+  float *part_lse;      // [P][2][GC], log2 domain
   int32_t *cta_flags;   // [decode CTAs] PKV_FLAG_* bits of each decode CTA
   int64_t num_blocks;
   int B, Hq, Hkv, D, G, GC, NC, HU, P;
@@ -107,7 +107,7 @@ void record_cuda_error(cudaError_t e);
 struct WsLayout {
   size_t hdr, prefix, starts, part_o, part_lse, cta_flags, total;
 };
-WsLayout ws_layout(int B, int P, int D);
+WsLayout ws_layout(int B, int P, int D, int GC);  // GC = rows per unit
 
 // One compiled decode kernel variant.
 struct DecodeKernel {

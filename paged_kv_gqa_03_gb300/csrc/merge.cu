@@ -145,7 +145,7 @@ __device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 
   }
 }
 
-__global__ void __launch_bounds__(256) splitk_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(512) splitk_merge_kernel(const DecodeParams p) {
   constexpr int kSegChunk = 32;
   constexpr int kBatch = 8;  // partials whose loads are in flight together
   __shared__ float s_lse[kSegChunk][kChunkMax];
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(256) splitk_merge_kernel(const DecodeParams p)
       const int64_t sw = W * w / Pe, ew = W * (w + 1) / Pe;
       const bool valid = (a > sw ? a : sw) < (e < ew ? e : ew);
       const int slot = sw >= a ? 0 : 1;
-      const int32_t base = (int32_t)(((int64_t)w * 2 + slot) * kChunkMax);
+      const int32_t base = (int32_t)(((int64_t)w * 2 + slot) * p.GC);  // [worker][slot][GC rows]
       if (gg == 0) s_base[sgi] = base;
       s_lse[sgi][gg] = (valid && gg < gc) ? p.part_lse[base + gg] : -INFINITY;
     }
@@ -249,7 +249,8 @@ cudaError_t launch_splitk_merge(const DecodeParams &p, cudaStream_t stream, bool
   if (units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   // one float4 of a unit's rows per thread (D <= 128): as many threads as the
-  // widest unit has float4s (an MHA unit has one row, 32 float4s at D = 128)
+  // widest unit has float4s (an MHA unit has one row, 32 float4s at D = 128;
+  // a 16-row fp8 unit 512)
   const int rows = p.GC < p.R ? p.GC : p.R;
   const int threads = (rows * p.D / 4 + 31) / 32 * 32;
   cfg.gridDim = dim3(units);

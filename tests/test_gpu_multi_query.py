@@ -36,7 +36,7 @@ def _check_step(w, num_splits=0):
         assert np.array_equal(step.v_scale.cpu().numpy(), vs)
     rc, flags = _pkv().paged_decode_status(step.workspace, step.stream)
     assert rc == 0 and flags == 0
-    assert out.shape == (w.B, w.q_len, w.Hq, w.D)
+    assert out.shape == ((w.B, w.q_len, w.Hq, w.D) if w.q.dim() == 4 else (w.B, w.Hq, w.D))
     return compare(out, ref, w.dtype, f"{w.name} q_len {w.q_len}")
 
 
@@ -303,11 +303,35 @@ def test_transposed_kernel_fp8(q_dtype, Hq, Hkv, q_len, ctx, window):
         _check_step(workloads.make(spec, seed=91))
 
 
+# FP8 caches with more than 8 query rows per kv head on the decode kernel:
+# 16-row units (two 8-row column groups share each widened K / V fragment).
+# Rows per unit 9-16 and a ragged second unit, D 64 and 128, bf16 and f16
+# queries, windows, and fixed split counts (partials of 16-row units through
+# the split-KV merge).
+@pytest.mark.parametrize("q_dtype,Hq,Hkv,D,q_len,ctx,window", [
+    ("bf16", 12, 3, 128, 3, [3, 47, 300, 1029], 0),          # R = 12: one unit, 4 rows unused
+    ("f16", 8, 2, 64, 4, [4, 17, 64, 700], 0),               # R = 16, D 64
+    ("bf16", 8, 1, 128, 3, [3, 200, 33], 0),                 # MQA, R = 24: units of 16 + 8 rows
+    ("bf16", 32, 8, 128, 8, [8, 500, 2048, 77], 37),         # R = 32, window
+    ("f16", 4, 2, 128, 5, [5, 99, 1000], 1),                 # R = 10, window 1
+    ("bf16", 16, 1, 128, 1, [1, 40, 3000, 512], 0),          # q_len 1, group 16
+    ("bf16", 12, 1, 64, 1, [7, 129, 2100], 100),             # q_len 1, group 12, window
+], ids=lambda v: str(v))
+def test_fp8_sixteen_row_units(q_dtype, Hq, Hkv, D, q_len, ctx, window):
+    spec = dict(B=len(ctx), Hq=Hq, Hkv=Hkv, D=D, dtype="fp8_e4m3", q_dtype=q_dtype, q_len=q_len, ctx=ctx,
+                free_frac=0.3, min_free=16, window=window)
+    if q_len == 1:
+        del spec["q_len"]  # the single-token form: q [B, Hq, D]
+    with routes(multi_query="units"):
+        for seed, splits in ((95, 0), (96, 5), (97, 1000)):
+            _check_step(workloads.make(spec, seed=seed), num_splits=splits)
+
+
 @pytest.mark.parametrize("route", ["transposed", "auto"])
 def test_fp8_long_context_layer_multi_query(route):
     """The long-context fp8 layer (16 sequences of 32768 positions, Hq 32,
     Hkv 8) verifying 4 draft tokens per sequence (16 rows per kv head), on
-    the transposed kernel (forced) and on the default route (the 8-row
+    the transposed kernel (forced) and on the default route (the 16-row
     units); every output compared."""
     w = workloads.config(5, q_len=4)
     with routes(multi_query=route):
