@@ -41,6 +41,7 @@ class _Staging:
             n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
             self.views[name] = self.buf[off:off + n].view(dtype).view(shape)
         self.done = None   # event recorded after the last copy out of this buffer
+        self.replayed = None  # the event run() records after each graph replay
 
     def __getitem__(self, name):
         return self.views[name]
@@ -267,7 +268,12 @@ class DecodeStep:
 
         The first step runs eagerly (it configures the kernels and encodes
         their tensor maps outside any capture), and so does a step with
-        copy-on-write pairs (rare): the graphs hold no block copy."""
+        copy-on-write pairs (rare): the graphs hold no block copy.
+
+        A loop may also keep one step queued ahead of the host (two pinned
+        output tensors alternating): issue step n, wait for step n - 1 and
+        read its output, then prepare() step n + 1 — prepare() waits for the
+        step that last read the staging buffer it switches to."""
         if not h_out.is_pinned():
             raise ValueError("h_out must be pinned host memory")
         if self.stream.cuda_stream == 0:
@@ -285,6 +291,13 @@ class DecodeStep:
             self._graphs[key] = graph
         with torch.cuda.stream(self.stream):
             graph.replay()
+        # the graph's copy out of this staging buffer is done once the step
+        # is: prepare() waits for it before rewriting the buffer
+        hs = self._host[self._turn]
+        if hs.replayed is None:
+            hs.replayed = torch.cuda.Event()
+        hs.replayed.record(self.stream)
+        hs.done = hs.replayed
 
     def replay(self):
         with torch.cuda.stream(self.stream):
