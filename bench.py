@@ -154,11 +154,11 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-TRAFFIC_RECORDS = {"bf16": "decode_traffic.json", "f16": "decode_traffic_f16.json",
-                   "fp8_e4m3": "decode_traffic_fp8.json"}
+TRAFFIC_RECORDS = {"bf16": ("decode_traffic.json",), "f16": ("decode_traffic_f16.json",),
+                   "fp8_e4m3": ("decode_traffic_fp8.json", "decode_traffic_fp8_qlen4.json")}
 
 
-def kernel_traffic(w, kernel=""):
+def kernel_traffic(w, kernel="", profiles_dir=None):
     """DRAM bytes per launch of the dominant kernel, from the committed ncu
     capture of that kernel (the decode kernel for the cache's dtype, or the
     transposed multi-query kernel) on a smaller case of the same kernel:
@@ -169,23 +169,22 @@ def kernel_traffic(w, kernel=""):
     if w.window or w.prefix_blocks:
         return None
     mq = kernel.startswith("mq_decode_kernel")
-    name = "mq_traffic.json" if mq else TRAFFIC_RECORDS.get(w.dtype)
-    if name is None:
-        return None
-    try:
-        with open(os.path.join(ROOT, "profiles", name)) as f:
-            rec = json.load(f)
-    except Exception:
-        return None
-    h = hashlib.sha256()
-    for src in rec.get("sources", ("common.cuh", "decode.cuh", "internal.h")):
-        with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", src), "rb") as f:
-            h.update(f.read())
-    if rec.get("source_sha256") != h.hexdigest() or rec.get("q_len", 1) != w.q_len:
-        return None
-    if "kv_bytes" not in rec:
-        return None
-    return int(rec["dram_bytes_read"] / rec["kv_bytes"] * w.kv_bytes() + rec["dram_bytes_write"])
+    for name in ("mq_traffic.json",) if mq else TRAFFIC_RECORDS.get(w.dtype, ()):
+        try:
+            with open(os.path.join(profiles_dir or os.path.join(ROOT, "profiles"), name)) as f:
+                rec = json.load(f)
+        except Exception:
+            continue
+        if rec.get("q_len", 1) != w.q_len or "kv_bytes" not in rec:
+            continue
+        h = hashlib.sha256()
+        for src in rec.get("sources", ("common.cuh", "decode.cuh", "internal.h")):
+            with open(os.path.join(ROOT, "paged_kv_gqa_03_gb300", "csrc", src), "rb") as f:
+                h.update(f.read())
+        if rec.get("source_sha256") != h.hexdigest():
+            continue
+        return int(rec["dram_bytes_read"] / rec["kv_bytes"] * w.kv_bytes() + rec["dram_bytes_write"])
+    return None
 
 
 def oracle_sample_rate(w, seconds, threads=0):
