@@ -89,8 +89,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // the softmax may finish tile g + 1 before the MMA warp waits for tile g, but
   // it cannot finish tile g + SBUF before that.)
   __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF];
-  // per item: Q staged, O read out; row-max exchange per tile, row-sum exchange per item
-  __shared__ __align__(8) uint64_t q_full, o_free, xch[2], xl, fin;
+  // per item: Q staged, O read out; per pair of softmax warps holding the same
+  // rows (w, w + 4): row-max exchange per tile, row-sum exchange per item
+  __shared__ __align__(8) uint64_t q_full, o_free, fin;
+  __shared__ __align__(8) uint64_t xch[Cfg::SOFTMAX / 64][2], xl[Cfg::SOFTMAX / 64];
+  static_assert(Cfg::SOFTMAX / 64 == 4, "four pairs of softmax warps (w, w + 4)");
   __shared__ __align__(8) uint64_t dead;
   __shared__ float red[2][2][Cfg::M];  // partial row maxima [tile parity][half][row]
   __shared__ float red_l[2][Cfg::M];   // partial row sums [half][row]
@@ -120,9 +123,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     mbar_init(&q_full, Cfg::SOFTMAX / 32);
     mbar_init(&o_free, Cfg::SOFTMAX / 32);
-    mbar_init(&xch[0], Cfg::SOFTMAX / 32);
-    mbar_init(&xch[1], Cfg::SOFTMAX / 32);
-    mbar_init(&xl, Cfg::SOFTMAX / 32);
+#pragma unroll
+    for (int pr = 0; pr < Cfg::SOFTMAX / 64; ++pr) {
+      mbar_init(&xch[pr][0], 2);
+      mbar_init(&xch[pr][1], 2);
+      mbar_init(&xl[pr], 2);
+    }
     mbar_init(&fin, 2);  // one commit from each issuing warp
     mbar_init(&dead, 1);  // failure-path test hook: nothing ever arrives on it
     fence_barrier_init();
@@ -436,8 +442,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // the row max over both halves (double-buffered exchange, bounded wait)
         red[gj & 1][half][row] = mx;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xch[gj & 1]);
-        ok = warp_wait(&xch[gj & 1], (uint32_t)(gj >> 1) & 1u, p.timeout_ns);
+        if (lane == 0) mbar_arrive(&xch[warp & 3][gj & 1]);
+        ok = warp_wait(&xch[warp & 3][gj & 1], (uint32_t)(gj >> 1) & 1u, p.timeout_ns);
         if (!ok) break;
         mx = fmaxf(mx, red[gj & 1][half ^ 1][row]);
         const float m_new = fmaxf(m_run, mx * c);
@@ -493,8 +499,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (ok) {  // the row sum over both halves
           red_l[half][row] = l;
           __syncwarp();
-          if (lane == 0) mbar_arrive(&xl);
-          ok = warp_wait(&xl, (uint32_t)o_items & 1u, p.timeout_ns);
+          if (lane == 0) mbar_arrive(&xl[warp & 3]);
+          ok = warp_wait(&xl[warp & 3], (uint32_t)o_items & 1u, p.timeout_ns);
         }
         if (!ok) break;
         tc::fence_after();
