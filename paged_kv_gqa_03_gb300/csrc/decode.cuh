@@ -414,28 +414,36 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
   if ((uint32_t)(gid + 8 - base0) >= wl) x2 = -INFINITY;
   if ((uint32_t)(gid + 8 - base1) >= wl) x3 = -INFINITY;
   float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+  // the running maxima change only when some lane holds a larger score;
+  // otherwise the exchange and the rescale (by exactly 1) are skipped
+  if (__any_sync(kFull, (mx0 > st.m[0][0]) | (mx1 > st.m[0][1]))) {
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[0][0], mx0), mn1 = fmaxf(st.m[0][1], mx1);
+    // a column that has seen no visible position yet keeps weight 0 (not NaN)
+    const float nb0 = mn0 == -INFINITY ? 0.f : mn0, nb1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(st.m[0][0] - nb0), al1 = exp2f(st.m[0][1] - nb1);
+    st.l[0][0] *= al0;
+    st.l[0][1] *= al1;
+    st.m[0][0] = mn0;
+    st.m[0][1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
+      st.acc[0][mt][0] *= al0;
+      st.acc[0][mt][1] *= al1;
+      st.acc[0][mt][2] *= al0;
+      st.acc[0][mt][3] *= al1;
+    }
   }
-  const float mn0 = fmaxf(st.m[0][0], mx0), mn1 = fmaxf(st.m[0][1], mx1);
-  // a column that has seen no visible position yet keeps weight 0 (not NaN)
-  const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(st.m[0][0] - mb0), al1 = exp2f(st.m[0][1] - mb1);
+  const float mb0 = st.m[0][0] == -INFINITY ? 0.f : st.m[0][0];
+  const float mb1 = st.m[0][1] == -INFINITY ? 0.f : st.m[0][1];
   const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1);
   const float p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
-  st.l[0][0] = st.l[0][0] * al0 + (p0 + p2);
-  st.l[0][1] = st.l[0][1] * al1 + (p1 + p3);
-  st.m[0][0] = mn0;
-  st.m[0][1] = mn1;
-#pragma unroll
-  for (int mt = 0; mt < MmaFrags<Cfg>::MT; ++mt) {
-    st.acc[0][mt][0] *= al0;
-    st.acc[0][mt][1] *= al1;
-    st.acc[0][mt][2] *= al0;
-    st.acc[0][mt][3] *= al1;
-  }
+  st.l[0][0] += p0 + p2;
+  st.l[0][1] += p1 + p3;
 
   // ---- O^T += V^T . P^T ----
   if constexpr (Cfg::FP8) {
@@ -608,28 +616,38 @@ __device__ __forceinline__ void mma_pair(MmaState<Cfg> &st, const DecodeParams &
       if ((uint32_t)(gid + 24 - base1) >= wl) y3 = -INFINITY;
     }
     float mx0 = fmaxf(fmaxf(x0, x2), fmaxf(y0, y2)), mx1 = fmaxf(fmaxf(x1, x3), fmaxf(y1, y3));
+    // The running maxima change only when some lane holds a larger score;
+    // otherwise (16-row units) the column maxima, the rescale (a factor of
+    // exactly 1) and the max exchange are skipped (warp-uniform vote).  The
+    // 8-row units always exchange: the vote measured slower there.
+    if (NH == 1 || __any_sync(kFull, (mx0 > st.m[nh][0]) | (mx1 > st.m[nh][1]))) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+      }
+      const float mn0 = fmaxf(st.m[nh][0], mx0), mn1 = fmaxf(st.m[nh][1], mx1);
+      // a column that has seen no visible position yet keeps weight 0 (not NaN)
+      const float nb0 = mn0 == -INFINITY ? 0.f : mn0, nb1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(st.m[nh][0] - nb0), al1 = exp2f(st.m[nh][1] - nb1);
+      st.l[nh][0] *= al0;
+      st.l[nh][1] *= al1;
+      st.m[nh][0] = mn0;
+      st.m[nh][1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
+        st.acc[nh][mt][0] *= al0;
+        st.acc[nh][mt][1] *= al1;
+        st.acc[nh][mt][2] *= al0;
+        st.acc[nh][mt][3] *= al1;
+      }
     }
-    const float mn0 = fmaxf(st.m[nh][0], mx0), mn1 = fmaxf(st.m[nh][1], mx1);
-    // a column that has seen no visible position yet keeps weight 0 (not NaN)
-    const float mb0 = mn0 == -INFINITY ? 0.f : mn0, mb1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(st.m[nh][0] - mb0), al1 = exp2f(st.m[nh][1] - mb1);
+    const float mb0 = st.m[nh][0] == -INFINITY ? 0.f : st.m[nh][0];
+    const float mb1 = st.m[nh][1] == -INFINITY ? 0.f : st.m[nh][1];
     const float p0 = exp2f(x0 - mb0), p1 = exp2f(x1 - mb1), p2 = exp2f(x2 - mb0), p3 = exp2f(x3 - mb1);
     const float q0 = exp2f(y0 - mb0), q1 = exp2f(y1 - mb1), q2 = exp2f(y2 - mb0), q3 = exp2f(y3 - mb1);
-    st.l[nh][0] = st.l[nh][0] * al0 + ((p0 + p2) + (q0 + q2));
-    st.l[nh][1] = st.l[nh][1] * al1 + ((p1 + p3) + (q1 + q3));
-    st.m[nh][0] = mn0;
-    st.m[nh][1] = mn1;
-#pragma unroll
-    for (int mt = 0; mt < MmaState<Cfg>::MT; ++mt) {
-      st.acc[nh][mt][0] *= al0;
-      st.acc[nh][mt][1] *= al1;
-      st.acc[nh][mt][2] *= al0;
-      st.acc[nh][mt][3] *= al1;
-    }
+    st.l[nh][0] += (p0 + p2) + (q0 + q2);
+    st.l[nh][1] += (p1 + p3) + (q1 + q3);
     // the V scales folded into the weights
     pa[nh][0] = movmatrix_trans(pack_f16x2(p0 * m.vs, p1 * m.vs));
     pa[nh][1] = movmatrix_trans(pack_f16x2(p2 * m.vs, p3 * m.vs));
