@@ -519,7 +519,9 @@ __device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_
     a[3] = e4m3x2_to_f16x2((uint16_t)(k1 >> 16));
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh) {
-      if (ks & 1)
+      // one chain per column group when there are two groups (the groups'
+      // chains interleave); an 8-row unit alternates two chains
+      if (NH == 1 && (ks & 1))
         mma16816<false>(s1[nh], a, st.qb[nh][ks][0], st.qb[nh][ks][1]);
       else
         mma16816<false>(s0[nh], a, st.qb[nh][ks][0], st.qb[nh][ks][1]);
@@ -528,7 +530,7 @@ __device__ __forceinline__ void fp8_scores(const MmaState<Cfg> &st, const uint8_
 #pragma unroll
   for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[nh][i] = s0[nh][i] + s1[nh][i];
+    for (int i = 0; i < 4; ++i) s[nh][i] = NH == 1 ? s0[nh][i] + s1[nh][i] : s0[nh][i];
 }
 
 // O^T += V^T . P^T of one fp8 block for every 8-row group, P (with the
