@@ -250,12 +250,13 @@ int cache_map(CUtensorMap *map, const void *base, int dtype, int64_t num_blocks,
 
 struct Choice {
   int ki;   // registry index
-  int GC;   // heads per unit
+  int GC;   // query rows per unit
   int NC;   // units per kv head
 };
 
-// Picks the kernel for a shape: tensor cores (8-head chunks, unused head
-// columns padded) for every group size on 16-bit and fp8 caches — even for
+// Picks the kernel for a shape: tensor cores (8-row units, unused columns
+// padded; 16-row units on fp8 caches past 8 rows) for every group size on
+// 16-bit and fp8 caches — even for
 // MHA the mma.sync block step measured faster on GB300 than the CUDA-core one
 // (5.83 vs 5.56 TB/s, fp16 MHA layer) — and CUDA cores for fp32 caches.  The
 // first compiled match is the default pipeline shape.  A build with
@@ -528,7 +529,8 @@ int paged_decode_attention_multi(void *out, const void *q, int q_dtype, const vo
   if (q_len >= 2 && num_splits == 0) {
     // Several new tokens per sequence on a 16-bit cache: a tensor-core
     // kernel streams each (sequence, kv head)'s K/V once for all of its
-    // q_len * G rows (the 8-row units below stream it once per unit).
+    // q_len * G rows (the decode kernel's units below stream it once per
+    // unit).
     //  * up to 32 rows and head dim 128: the transposed kernel (positions on
     //    the tensor core's M side, stream-K over every item's tiles, so any
     //    batch fills the GPU);

@@ -1,7 +1,7 @@
 // decode.cuh — the paged decode-attention kernel (steps a4–a8 up to the
 // partial results), templated on cache dtype, head dim and compute path.
 //
-// Work decomposition.  A "unit" is (sequence b, kv head h, head chunk c): the
+// Work decomposition.  A "unit" is (sequence b, kv head h, row chunk c): the
 // query rows c*GC ... (at most GC of them) of the R = q_len * G rows that
 // share kv head h ("大模型推理加速——KV Cache篇" §6.2 GQA).  Row r is query head
 // h*G + r % G of new token r / G; with q_len > 1 (several new tokens per
@@ -384,7 +384,7 @@ __device__ __forceinline__ void mma_compute(MmaState<Cfg> &st, const MmaFrags<Cf
   const int base0 = m.rem - st.back[0][0] - p.wlen, base1 = m.rem - st.back[0][1] - p.wlen;
   const uint32_t wl = (uint32_t)p.wlen;
 
-  // ---- scores S^T = K . Q^T (16 tokens x 8 heads), two independent chains ----
+  // ---- scores S^T = K . Q^T (16 tokens x 8 rows), two independent chains ----
   float s[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < MmaFrags<Cfg>::KS; ++ks) {
