@@ -126,12 +126,12 @@ cudaError_t launch_plan(const DecodeParams &p, cudaStream_t stream) {
 // launched behind the decode kernel with programmatic dependent launch.  One
 // CTA per unit; a unit processed whole by one warp was already written.  Partition w covers
 // items [floor(w W / P), floor((w+1) W / P)) — the plan kernel's rule,
-// recomputed.  Segments are taken in chunks whose LSEs are staged in shared
-// memory; each thread keeps an online max / sum for its head and accumulates
-// 4 head-dim elements of every partial with one 16-byte load, eight
-// partials' loads in flight at a time (a long context cut over many warps —
-// the 32K fp8 layer has ~14 partials per unit — would otherwise pay one L2
-// latency per partial in sequence).
+// recomputed.  Segments are taken in chunks whose partial indices are staged
+// in shared memory; each thread keeps an online max / sum for its row and
+// accumulates 4 head-dim elements of every partial with one 16-byte load,
+// eight partials' LSE and output loads in flight at a time (a long context
+// cut over many warps — the 32K fp8 layer has ~14 partials per unit — would
+// otherwise pay one L2 latency per partial in sequence).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 v) {
   if (dtype == PKV_F32) {
@@ -148,8 +148,7 @@ __device__ __forceinline__ void store4_out(int dtype, void *p, size_t i, float4 
 __global__ void __launch_bounds__(512) splitk_merge_kernel(const DecodeParams p) {
   constexpr int kSegChunk = 32;
   constexpr int kBatch = 8;  // partials whose loads are in flight together
-  __shared__ float s_lse[kSegChunk][kChunkMax];
-  __shared__ int32_t s_base[kSegChunk];
+  __shared__ int32_t s_base[kSegChunk];  // partial index of each segment of a chunk (-1: none)
   grid_dep_wait();
   if (blockIdx.x == 0 && threadIdx.x < 32) {  // publish the call's status bits
     int f = p.inline_plan ? 0 : p.hdr->plan_flags;
@@ -194,49 +193,48 @@ __global__ void __launch_bounds__(512) splitk_merge_kernel(const DecodeParams p)
   float M = -INFINITY, den = 0.f;
   for (int cs = wf; cs <= wl; cs += kSegChunk) {
     const int ns = min(kSegChunk, wl - cs + 1);
-    __syncthreads();  // the previous chunk's staging has been consumed
-    for (int i = threadIdx.x; i < ns * kChunkMax; i += blockDim.x) {
-      const int sgi = i / kChunkMax, gg = i % kChunkMax;
+    __syncthreads();  // the previous chunk's segment table has been read
+    for (int sgi = threadIdx.x; sgi < ns; sgi += blockDim.x) {
       const int w = cs + sgi;
       const int64_t sw = W * w / Pe, ew = W * (w + 1) / Pe;
       const bool valid = (a > sw ? a : sw) < (e < ew ? e : ew);
       const int slot = sw >= a ? 0 : 1;
-      const int32_t base = (int32_t)(((int64_t)w * 2 + slot) * p.GC);  // [worker][slot][GC rows]
-      if (gg == 0) s_base[sgi] = base;
-      s_lse[sgi][gg] = (valid && gg < gc) ? p.part_lse[base + gg] : -INFINITY;
+      s_base[sgi] = valid ? (int32_t)(((int64_t)w * 2 + slot) * p.GC) : -1;  // [worker][slot][GC rows]
     }
     __syncthreads();
     if (v >= nvec) continue;
-    float cm = -INFINITY;
-    for (int sgi = 0; sgi < ns; ++sgi) cm = fmaxf(cm, s_lse[sgi][g]);
-    if (cm == -INFINITY) continue;
-    const float mn = fmaxf(M, cm);
-    const float rescale = exp2f(M - mn);
-    acc.x *= rescale; acc.y *= rescale; acc.z *= rescale; acc.w *= rescale;
-    den *= rescale;
-    // a batch of partials is loaded before any is used, so their L2
-    // latencies overlap (empty partials load nothing and weigh 0)
+    // a batch of partials: their lse and output loads are issued together,
+    // so the L2 latencies overlap; the batch then joins the running merge
     for (int s0 = 0; s0 < ns; s0 += kBatch) {
       float4 o[kBatch];
-      float wt[kBatch];
+      float l[kBatch];
 #pragma unroll
       for (int t = 0; t < kBatch; ++t) {
-        const int sgi = s0 + t < ns ? s0 + t : 0;
-        const float l = s0 + t < ns ? s_lse[sgi][g] : -INFINITY;
-        wt[t] = l == -INFINITY ? 0.f : exp2f(l - mn);
-        o[t] = l == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f)
-                              : *reinterpret_cast<const float4 *>(p.part_o + ((size_t)s_base[sgi] + g) * D + d);
+        const int base = s0 + t < ns ? s_base[s0 + t] : -1;
+        l[t] = base >= 0 ? p.part_lse[base + g] : -INFINITY;
+        o[t] = base >= 0 ? *reinterpret_cast<const float4 *>(p.part_o + ((size_t)base + g) * D + d)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float cm = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) cm = fmaxf(cm, l[t]);
+      if (cm == -INFINITY) continue;  // no partial of the batch saw a position of this row
+      const float mn = fmaxf(M, cm);
+      const float rescale = exp2f(M - mn);
+      acc.x *= rescale; acc.y *= rescale; acc.z *= rescale; acc.w *= rescale;
+      den *= rescale;
 #pragma unroll
       for (int t = 0; t < kBatch; ++t) {
-        acc.x = fmaf(wt[t], o[t].x, acc.x);
-        acc.y = fmaf(wt[t], o[t].y, acc.y);
-        acc.z = fmaf(wt[t], o[t].z, acc.z);
-        acc.w = fmaf(wt[t], o[t].w, acc.w);
-        den += wt[t];
+        const bool on = l[t] != -INFINITY;  // empty partials weigh 0 (and are not read)
+        const float wt = on ? exp2f(l[t] - mn) : 0.f;
+        acc.x = fmaf(wt, on ? o[t].x : 0.f, acc.x);
+        acc.y = fmaf(wt, on ? o[t].y : 0.f, acc.y);
+        acc.z = fmaf(wt, on ? o[t].z : 0.f, acc.z);
+        acc.w = fmaf(wt, on ? o[t].w : 0.f, acc.w);
+        den += wt;
       }
+      M = mn;
     }
-    M = mn;
   }
   if (v < nvec) {
     const float inv = den > 0.f ? 1.f / den : 0.f;  // no visible position: 0
