@@ -360,3 +360,47 @@ def test_transposed_kernel_fp8_flags_a_bad_block_id():
     ref = oracle.decode(w.q[:1], "bf16", w.k_cache, w.v_cache, "fp8_e4m3", table[:1], lens[:1], scale=w.scale,
                         k_scale=w.k_scale.numpy(), v_scale=w.v_scale.numpy())
     compare(out[:1], ref, "fp8_e4m3", "the good sequence")
+
+
+# Non-finite data where no attended position lies: every free pool block
+# (the blocks a step's appends open) and every stale row past a context in
+# its last block hold NaN, so a stale K row reaching a score unmasked, or a
+# stale V row reaching P . V (0 * NaN), shows in the output.  The oracle
+# reads attended positions only.
+@pytest.mark.parametrize("dtype,q_dtype,Hq,Hkv,q_len,route", [
+    ("bf16", "bf16", 64, 8, 1, "auto"),
+    ("bf16", "bf16", 64, 8, 4, "auto"),          # transposed kernel
+    ("bf16", "bf16", 16, 2, 4, "units"),         # 8-row units, q_len 4
+    ("f16", "f16", 4, 4, 3, "auto"),
+    ("fp8_e4m3", "bf16", 32, 8, 1, "auto"),      # 8-row fp8 units
+    ("fp8_e4m3", "bf16", 32, 8, 4, "auto"),      # 16-row fp8 units
+    ("fp8_e4m3", "f16", 16, 2, 5, "auto"),       # R = 40: 16 + 16 + 8 rows
+    ("f32", "f32", 8, 2, 2, "auto"),             # CUDA cores
+], ids=lambda v: str(v))
+def test_stale_rows_and_free_blocks_hold_nan(dtype, q_dtype, Hq, Hkv, q_len, route):
+    ctx = [q_len, 37, 300, 1000, 2051]
+    spec = dict(B=len(ctx), Hq=Hq, Hkv=Hkv, D=128, dtype=dtype, q_dtype=q_dtype, ctx=ctx, free_frac=0.3,
+                min_free=16)
+    if q_len > 1:
+        spec["q_len"] = q_len
+    w = workloads.make(spec, seed=99)
+    used = {blk for t in w.tables for blk in t}
+    nan_byte = 0x7F  # E4M3 NaN
+    for cache in (w.k_cache, w.v_cache):
+        raw = cache.view(torch.uint8) if dtype == "fp8_e4m3" else None
+        for blk in range(w.num_blocks):
+            if blk not in used:
+                if raw is not None:
+                    raw[blk] = nan_byte
+                else:
+                    cache[blk] = float("nan")
+        for b in range(w.B):
+            end = w.cached[b] + w.q_len  # the context after this step's appends
+            j, off = (end - 1) // 16, end % 16
+            if off and j < len(w.tables[b]):
+                if raw is not None:
+                    raw[w.tables[b][j], :, off:] = nan_byte
+                else:
+                    cache[w.tables[b][j], :, off:] = float("nan")
+    with routes(multi_query=route):
+        _check_step(w)
