@@ -5,19 +5,21 @@
 namespace pkv {
 
 // fp8 blocks carry half the bytes of bf16 ones for the same per-block work, so
-// they want more warps in flight: 4 warps x 16 KiB, 3 CTAs per SM.  With one
-// block per stage (4 stages) that shape measured 5.91 TB/s on the long-context
-// fp8 layer against 5.11 for 5 x 16 KiB, and it was issue-bound (half the
-// bytes per instruction of the bf16 kernel); stages of two blocks (2 stages of
-// 8 KiB) share the per-stage and per-softmax-update work between 32 tokens.
+// they want more warps in flight: 12 warps per SM with 16 KiB each.  With one
+// block per stage (4 stages) 4 warps x 3 CTAs measured 5.91 TB/s on the
+// long-context fp8 layer against 5.11 for 5 x 16 KiB x 2 CTAs, and it was
+// issue-bound (half the bytes per instruction of the bf16 kernel); stages of
+// two blocks (2 stages of 8 KiB) share the per-stage and per-softmax-update
+// work between 32 tokens.  With two-block stages, 6 warps x 2 CTAs measured
+// 0.5-0.6 % faster than 4 x 3 at head dim 128.
 constexpr int kFp8Warps = 4;
 constexpr int kFp8WideBudget = 24 * 1024;
 
 int register_decode_fp8(DecodeKernel *out) {
   int n = 0;
-  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, kFp8Warps, kBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 128, 8, true, 6, kBudget, 2>>();  // 6 x 16 KiB, 2 CTAs
   out[n++] = decode_entry<DecodeCfg<E4M3, BF16, 64, 8, true, kFp8Warps, kBudget, 2>>();
-  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, kFp8Warps, kBudget, 2>>();
+  out[n++] = decode_entry<DecodeCfg<E4M3, F16, 128, 8, true, 6, kBudget, 2>>();
   out[n++] = decode_entry<DecodeCfg<E4M3, F16, 64, 8, true, kFp8Warps, kBudget, 2>>();
   // 16-row units (kv heads with more than 8 query rows): twice the
   // accumulators and q fragments per warp, so two CTAs of 4 warps per SM
