@@ -9,9 +9,10 @@
 // the causal mask of "苦猿的大模型日记 Day45" PART 04.  The tile pipeline both
 // kernels run:
 //  * K / V tiles of 128 positions = 8 paged blocks, fetched by TMA through the
-//    block table (one 2 KiB box per block and 64-element panel) into a 3-deep
-//    K ring and a 2-deep V ring: a K slot frees as soon as S = Q . K^T has
-//    read it, a V slot when P . V has;
+//    block table (one 2 KiB box per block and 64-element panel) into a 2-deep
+//    K ring and a 3-deep V ring: a K slot frees as soon as S = Q . K^T has
+//    read it, a V slot when P . V has (V, read later, gets the deeper ring:
+//    0.8 % faster than 3 + 2 on chunked prefill);
 //  * S (128 x 128, f32) and O (128 x D, f32) live in tensor memory; S has three
 //    buffers, and each buffer's P (the 16-bit weights) is written back over
 //    the S columns its thread has read, so P . V takes A from tensor memory
@@ -62,7 +63,7 @@ struct PrefillCfg {
   static constexpr int PANEL_KV = N * 128;              // one K or V panel (128 positions)
   static constexpr int Q_BYTES = PANELS * PANEL_Q;
   static constexpr int KV_BYTES = PANELS * PANEL_KV;    // one K (or V) tile
-  static constexpr int KSTAGES = 3, VSTAGES = 2;
+  static constexpr int KSTAGES = 2, VSTAGES = 3;
   static constexpr int LOADS = BLOCKS * PANELS;         // TMA boxes per K (or V) tile
   static constexpr size_t SMEM = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * KV_BYTES;
   static constexpr int SBUF = 3;                        // S / P buffers in tensor memory
