@@ -173,7 +173,9 @@ int paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
  *
  * Work decomposition (GB300 design, not taken from the pages): the
  * concatenation of every (sequence, kv-head) block list is cut into
- * `num_splits` contiguous, equally long partitions, one per warp; a warp
+ * `num_splits` contiguous, equally long partitions, one per warp (a kv head
+ * with more query rows than a unit holds — 8, or 16 on FP8 caches — has one
+ * block list per unit of rows); a warp
  * streams its blocks through a TMA pipeline and keeps an fp32 online softmax
  * (running max m, running sum l, rescaled accumulator — "LLM推理优化实战", §3.2
  * flash_attention online softmax).  Partitions that cover only part of a
