@@ -326,10 +326,14 @@ int paged_prefill_attention(void *out, const void *q, int q_dtype,
  * without `workspace` / `workspace_bytes`: the scratch comes from one array of
  * PKV_STATIC_SCRATCH_BYTES bytes that the library keeps in device memory on
  * every GPU that loads it, until the process exits.
- *  - Limit: a shape whose paged_decode_workspace_bytes() exceeds
- *    PKV_STATIC_SCRATCH_BYTES is rejected with PKV_EWORKSPACE before anything
- *    runs (16 MiB holds D = 128 with ~2000 partitions, more than one per
- *    resident warp of a GB300).
+ *  - Limit: with num_splits > 0, a shape whose
+ *    paged_decode_workspace_bytes() exceeds PKV_STATIC_SCRATCH_BYTES is
+ *    rejected with PKV_EWORKSPACE before anything runs.  With num_splits = 0
+ *    the library takes its usual partition count (one per resident warp) when
+ *    that fits (16 MiB holds D = 128 with 8-row units and ~2000 partitions),
+ *    else the largest count that fits (FP8 caches with more than 8 query rows
+ *    per kv head keep 16-row partials, 16 KiB a partition at D = 128); only a
+ *    shape that does not fit with one partition is rejected.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *  - Set-up: every call looks up the array's device address in the current
  *    device's context (cudaGetSymbolAddress, a host-side lookup that

@@ -40,6 +40,29 @@ int scratch_on_current_device(void **out) {
   return PKV_OK;
 }
 
+// Largest partition count whose workspace fits the scratch, for a call that
+// left the count to the library (num_splits == 0) but whose usual count, one
+// partition per resident warp, needs more scratch than the array holds (FP8
+// caches with more than 8 query rows per kv head at D = 128 keep 16-row
+// partials, 16 KiB per partition).  The workspace size grows with the count,
+// so a bisection over [1, 2^24] finds it; PKV_EWORKSPACE if even one
+// partition does not fit.
+int partitions_that_fit(int B, int Hq, int Hkv, int D, int cache_dtype, int q_dtype, int *splits) {
+  const size_t cap = (size_t)PKV_STATIC_SCRATCH_BYTES;
+  int lo = 0, hi = 1 << 24;  // need(lo) fits (lo > 0), need(hi + 1) does not
+  while (lo < hi) {
+    const int mid = lo + (hi - lo + 1) / 2;
+    size_t need = 0;
+    const int rc = paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, mid, &need);
+    if (rc != PKV_OK) return rc;
+    if (need <= cap) lo = mid;
+    else hi = mid - 1;
+  }
+  if (lo == 0) return PKV_EWORKSPACE;
+  *splits = lo;
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" int paged_decode_attention_static(void *out, const void *q, int q_dtype, const void *k_cache,
@@ -51,7 +74,11 @@ extern "C" int paged_decode_attention_static(void *out, const void *q, int q_dty
   size_t need = 0;
   int rc = paged_decode_workspace_bytes(B, Hq, Hkv, D, cache_dtype, q_dtype, num_splits, &need);
   if (rc != PKV_OK) return rc;
-  if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_EWORKSPACE;  // beyond the fixed capacity
+  if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) {
+    if (num_splits != 0) return PKV_EWORKSPACE;  // the caller's own count, beyond the fixed capacity
+    rc = partitions_that_fit(B, Hq, Hkv, D, cache_dtype, q_dtype, &num_splits);
+    if (rc != PKV_OK) return rc;
+  }
   void *scratch = nullptr;
   rc = scratch_on_current_device(&scratch);
   if (rc != PKV_OK) return rc;

@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
         for (int q = 0; q < SC / 32; ++q)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q][e]));
+          for (int e = 0; e < 32; e += 2) mx = fmax3(mx, __uint_as_float(s[q][e]), __uint_as_float(s[q][e + 1]));
         // the row max over both halves (double-buffered exchange, bounded wait)
         red[gj & 1][half][row] = mx;
         __syncwarp();
@@ -455,23 +455,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           m_run = m_new;
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
-        float sum = 0.f;
+        const uint64_t cmu = f2_pack(c, c), nmu = f2_pack(-mu, -mu);
+        uint64_t sum2 = f2_pack(0.f, 0.f);
         uint32_t w[SC / 2], wl[Cfg::BF ? SC / 2 : 1];
 #pragma unroll
         for (int e = 0; e < SC / 2; ++e) {
           const int col = 2 * e;
-          const float a0 = ex2(fmaf(__uint_as_float(s[col >> 5][col & 31]), c, -mu));
-          const float a1 = ex2(fmaf(__uint_as_float(s[(col + 1) >> 5][(col + 1) & 31]), c, -mu));
-          sum += a0 + a1;
-          if constexpr (Cfg::BF) {  // bf16 high part and residual: ~16 significant bits
-            const __nv_bfloat162 hp = __floats2bfloat162_rn(a0, a1);
-            const float2 hf = __bfloat1622float2(hp);
-            w[e] = *reinterpret_cast<const uint32_t *>(&hp);
-            wl[e] = pack_bf16x2(a0 - hf.x, a1 - hf.y);
-          } else {
-            w[e] = pack_f16x2(a0, a1);
-          }
+          uint32_t lo_;
+          p_pair<Cfg::BF>(s[col >> 5][col & 31], s[(col + 1) >> 5][(col + 1) & 31], cmu, nmu, sum2, w[e], lo_);
+          if constexpr (Cfg::BF) wl[e] = lo_;
         }
+        const float2 sp = f2_unpack(sum2);
+        const float sum = sp.x + sp.y;
         l = l * alpha + sum;
         // P over this thread's own (already read) S columns
         tc::st32(scol, w);

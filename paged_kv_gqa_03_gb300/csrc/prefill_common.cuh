@@ -93,6 +93,66 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Two f32 values as one 64-bit register pair, for the packed f32x2
+// arithmetic of sm_100 and later (one instruction issue for both lanes).
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max(a, b, c) in one instruction (sm_100 and later); like fmaxf, a NaN
+// operand loses to a number.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// The softmax weights of two adjacent S columns, p = 2^(s * c - mu):
+// `cmu` = {c, c} and `nmu` = {-mu, -mu} as f32x2 pairs, the two weights added
+// lane-wise into `sum` (two partial row sums), and the pair packed as the
+// cache's 16-bit type into `hi` — for bf16 with the residuals p - bf16(p),
+// themselves rounded to bf16, in `lo` (~16 significant bits together).
+template <bool BF>
+__device__ __forceinline__ void p_pair(uint32_t s0, uint32_t s1, uint64_t cmu, uint64_t nmu, uint64_t &sum,
+                                       uint32_t &hi, uint32_t &lo) {
+  const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(s0), __uint_as_float(s1)), cmu, nmu));
+  const float a0 = ex2(t.x), a1 = ex2(t.y);
+  const uint64_t a = f2_pack(a0, a1);
+  sum = f2_add(sum, a);
+  if constexpr (BF) {
+    const __nv_bfloat162 hp = __floats2bfloat162_rn(a0, a1);
+    hi = *reinterpret_cast<const uint32_t *>(&hp);
+    // the two rounded values back in f32: bf16 is the upper half of an f32
+    const uint64_t h = f2_pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+    const float2 r = f2_unpack(f2_sub(a, h));
+    lo = pack_bf16x2(r.x, r.y);
+  } else {
+    hi = pack_f16x2(a0, a1);
+    lo = 0u;
+  }
+}
+
 template <bool BF>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF)

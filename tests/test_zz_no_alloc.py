@@ -7,9 +7,10 @@ on each GPU.
 The checks, through the C ABI: two calls in a row (different shapes, so the
 second reuses the scratch the first left behind) give the same outputs as the
 workspace-taking entry point within the attention tolerances, and match the
-oracle; the status of the shared scratch reads clean after each; a request
-that needs more scratch than the fixed capacity is refused before anything
-runs.  This file is named to be collected last."""
+oracle; the status of the shared scratch reads clean after each; a shape
+whose usual partition count needs more scratch than the array holds runs on
+fewer partitions; an explicit partition count beyond the fixed capacity is
+refused before anything runs.  This file is named to be collected last."""
 import pytest
 import torch
 
@@ -39,6 +40,26 @@ def test_static_scratch_entry_matches_workspace_entry_on_two_calls():
         compare(out_static, out_ws.double().cpu().numpy(), w.dtype, f"static scratch vs workspace ({w.name})")
         *_, ref = run_oracle_step(w)
         compare(out_static, ref, w.dtype, f"static scratch vs oracle ({w.name})")
+
+
+def test_static_scratch_shrinks_the_library_partition_count_to_fit():
+    """FP8 cache, 16 query rows per kv head, D 128: 16-row partials at one
+    partition per resident warp need more than the fixed scratch; with
+    num_splits = 0 the entry takes fewer partitions and still runs."""
+    import paged_kv_gqa_03_gb300 as pkv
+    w = workloads.make(dict(B=3, Hq=32, Hkv=2, D=128, dtype="fp8_e4m3", q_dtype="bf16",
+                            ctx=[900, 17, 2100], free_frac=0.3, min_free=3), 4242)
+    usual = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, torch.float8_e4m3fn, torch.bfloat16)
+    assert usual > 16 << 20                  # the usual count does not fit
+    step, out_ws = run_gpu_step(w)
+    q = w.q.to("cuda")
+    out_static = torch.full_like(out_ws, float("nan"))
+    _call_static(pkv, step, q, out_static)
+    rc, flags = pkv.paged_decode_static_status(step.stream)
+    assert (rc, flags) == (pkv.PKV_OK, 0)
+    compare(out_static, out_ws.double().cpu().numpy(), w.dtype, "static scratch, fewer partitions, vs workspace")
+    *_, ref = run_oracle_step(w)
+    compare(out_static, ref, w.dtype, "static scratch, fewer partitions, vs oracle")
 
 
 def test_static_scratch_refuses_requests_beyond_its_capacity():
