@@ -337,15 +337,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int row = tid & (Cfg::M - 1), half = tid / Cfg::M;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
-    // thread (row, half) stages half of row `row` of item i's Q tile (zeros past R)
-    auto stage_q = [&](int i, bool async) {
+    // where thread (row, half) reads row `row` of item i's Q tile (null past R: zeros)
+    auto q_src = [&](int i) -> const uint4 * {
       const PrefillItem it = prefill_item<Cfg>(p, i);
       const int r = it.r0 + row;
       const int ii = r / p.G, g = r - ii * p.G;
-      const uint4 *src = r < it.R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
-                                                                  ((size_t)(it.qs + ii) * p.Hq + it.h * p.G + g) *
-                                                                      Cfg::D)
-                                  : nullptr;
+      return r < it.R ? reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
+                                                       ((size_t)(it.qs + ii) * p.Hq + it.h * p.G + g) * Cfg::D)
+                      : nullptr;
+    };
+    // thread (row, half) stages its half of a Q row from `src`
+    auto stage_q = [&](const uint4 *src, bool async) {
 #pragma unroll
       for (int k = 0; k < Cfg::D / 16; ++k) {
         const int cc = half * (Cfg::D / 16) + k;
@@ -374,11 +376,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       return k;
     };
+    // Lookahead: `kn2` is the round of the item with tiles after the one whose
+    // Q is staged, and `src2` where this thread reads that item's Q row.  Both
+    // are looked up while an epilogue waits for its item's last P . V, so the
+    // last tile of an item (which stages the next Q) does no global loads.
+    int kn2 = n_rounds;
+    const uint4 *src2 = nullptr;
     {
       const int first = next_work(0);
       if (first < n_rounds) {
-        stage_q(round_item(first), false);
+        stage_q(q_src(round_item(first)), false);
         release_q(false);
+        kn2 = next_work(first + 1);
+        if (kn2 < n_rounds) src2 = q_src(round_item(kn2));
       }
     }
     bool ok = true;
@@ -418,9 +428,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (j + 1 == T) {
           // every S MMA of this item has completed (its last S just landed):
           // the next item's Q can replace this one's while the softmax runs
-          const int nxt = next_work(k + 1);
-          if (nxt < n_rounds) {
-            stage_q(round_item(nxt), true);
+          if (kn2 < n_rounds) {
+            stage_q(src2, true);
             staged = true;
           }
         }
@@ -486,7 +495,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       if (!ok) break;
       // the next item's Q: its copy overlapped this item's last tile
-      if (staged) release_q(true);
+      if (staged) {
+        release_q(true);
+        kn2 = next_work(kn2 + 1);  // and the item after it, while the last P . V runs
+        src2 = kn2 < n_rounds ? q_src(round_item(kn2)) : nullptr;
+      }
       // epilogue: O of this item
       if (T > 0) {
         const int gl = g + T - 1;
