@@ -71,6 +71,13 @@ __device__ __forceinline__ int round_item(int k) {
   return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
+// Shared memory the persistent kernel's epilogue stages output rows in: 2 KiB
+// per softmax warp.  A thread holds half of one output row; written straight
+// to global memory, each 16-byte store of a warp touches 32 rows' lines.
+// Staged and read back transposed, each store of a warp covers whole
+// half-rows (4 of them at D = 128, 8 at D = 64): one line per 128 bytes.
+constexpr int kOutStage = 8 * 2048;
+
 // Persistent: one CTA per SM walks its work items round by round; tensor
 // memory, barriers and the K / V pipeline live across items, so one item's
 // epilogue overlaps the next item's loads and S MMAs.
@@ -83,6 +90,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + Cfg::Q_BYTES;
   uint8_t *sV = sK + (size_t)Cfg::KSTAGES * Cfg::KV_BYTES;
+  uint8_t *sO = sV + (size_t)Cfg::VSTAGES * Cfg::KV_BYTES;  // epilogue staging, kOutStage bytes
   __shared__ __align__(8) uint64_t k_full[Cfg::KSTAGES], k_empty[Cfg::KSTAGES];
   __shared__ __align__(8) uint64_t v_full[Cfg::VSTAGES], v_empty[Cfg::VSTAGES];
   // per S buffer: S written, P written, P . V done.  (One P barrier per buffer:
@@ -522,18 +530,40 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free);
-        if (dst) {
+        {
+          // the warp's 32 half-rows of CH 16-byte chunks, RP rows per pass
+          // through its 2 KiB of staging (16-byte unit u of a pass at unit
+          // (u & ~7) | ((u ^ (u >> 3)) & 7): conflict-free writes of a chunk
+          // by 8 rows and reads of 8 chunks), then stored RPI rows per
+          // instruction; rows past R (null dst) are skipped
+          constexpr int CH = OC / 8, RP = 2048 / (CH * 16), RPI = 32 / CH;
+          uint8_t *stage = sO + (size_t)(warp * 2048);
+          auto unit = [](int u) { return (u & ~7) | ((u ^ (u >> 3)) & 7); };
 #pragma unroll
-          for (int q = 0; q < OC / 32; ++q)
+          for (int pass = 0; pass < 32 / RP; ++pass) {
+            if (lane / RP == pass) {
+              const int lr = lane - pass * RP;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t wv[4];
+              for (int ch = 0; ch < CH; ++ch) {
+                const uint32_t *src = &o[ch / 4][(ch % 4) * 8];
+                uint32_t wv[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                wv[e] = pack2<Cfg::BF>(__uint_as_float(o[q][v * 8 + 2 * e]) * inv,
-                                       __uint_as_float(o[q][v * 8 + 2 * e + 1]) * inv);
-              dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                for (int e = 0; e < 4; ++e)
+                  wv[e] = pack2<Cfg::BF>(__uint_as_float(src[2 * e]) * inv, __uint_as_float(src[2 * e + 1]) * inv);
+                sts128(smem_u32(stage + unit(lr * CH + ch) * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+              }
             }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < RP / RPI; ++i) {
+              const int lr = i * RPI + lane / CH, ch = lane % CH;
+              uint4 *d = reinterpret_cast<uint4 *>(
+                  __shfl_sync(kFull, reinterpret_cast<unsigned long long>(dst), pass * RP + lr));
+              const uint4 v = lds128(smem_u32(stage + unit(lr * CH + ch) * 16));
+              if (d) d[ch] = v;
+            }
+            __syncwarp();
+          }
         }
         ++o_items;
       } else if (dst) {  // no visible position for any row of the tile: zeros
@@ -579,7 +609,8 @@ static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, co
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    e = cudaFuncSetAttribute(prefill_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(Cfg::SMEM + kOutStage));
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -591,7 +622,8 @@ static cudaError_t launch_cfg(const PrefillParams &p, const CUtensorMap &tmK, co
   const int64_t items = (int64_t)p.max_tiles * p.Hkv * p.B;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)(items < sms[dev] ? items : sms[dev]);  // one persistent CTA per SM
-  prefill_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(p, tmK, tmV);
+  static_assert(Cfg::SMEM + kOutStage + 4096 <= 232448, "shared memory");
+  prefill_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM + kOutStage, stream>>>(p, tmK, tmV);
   return cudaGetLastError();
 }
 
