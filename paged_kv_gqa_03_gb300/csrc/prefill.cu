@@ -71,11 +71,8 @@ __device__ __forceinline__ int round_item(int k) {
   return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
-// Shared memory the persistent kernel's epilogue stages output rows in: 2 KiB
-// per softmax warp.  A thread holds half of one output row; written straight
-// to global memory, each 16-byte store of a warp touches 32 rows' lines.
-// Staged and read back transposed, each store of a warp covers whole
-// half-rows (4 of them at D = 128, 8 at D = 64): one line per 128 bytes.
+// Shared memory the persistent kernel's epilogue stages output rows in
+// (store_rows_staged): 2 KiB per softmax warp.
 constexpr int kOutStage = 8 * 2048;
 
 // Persistent: one CTA per SM walks its work items round by round; tensor
@@ -530,41 +527,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free);
-        {
-          // the warp's 32 half-rows of CH 16-byte chunks, RP rows per pass
-          // through its 2 KiB of staging (16-byte unit u of a pass at unit
-          // (u & ~7) | ((u ^ (u >> 3)) & 7): conflict-free writes of a chunk
-          // by 8 rows and reads of 8 chunks), then stored RPI rows per
-          // instruction; rows past R (null dst) are skipped
-          constexpr int CH = OC / 8, RP = 2048 / (CH * 16), RPI = 32 / CH;
-          uint8_t *stage = sO + (size_t)(warp * 2048);
-          auto unit = [](int u) { return (u & ~7) | ((u ^ (u >> 3)) & 7); };
-#pragma unroll
-          for (int pass = 0; pass < 32 / RP; ++pass) {
-            if (lane / RP == pass) {
-              const int lr = lane - pass * RP;
-#pragma unroll
-              for (int ch = 0; ch < CH; ++ch) {
-                const uint32_t *src = &o[ch / 4][(ch % 4) * 8];
-                uint32_t wv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  wv[e] = pack2<Cfg::BF>(__uint_as_float(src[2 * e]) * inv, __uint_as_float(src[2 * e + 1]) * inv);
-                sts128(smem_u32(stage + unit(lr * CH + ch) * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-              }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < RP / RPI; ++i) {
-              const int lr = i * RPI + lane / CH, ch = lane % CH;
-              uint4 *d = reinterpret_cast<uint4 *>(
-                  __shfl_sync(kFull, reinterpret_cast<unsigned long long>(dst), pass * RP + lr));
-              const uint4 v = lds128(smem_u32(stage + unit(lr * CH + ch) * 16));
-              if (d) d[ch] = v;
-            }
-            __syncwarp();
-          }
-        }
+        store_rows_staged<Cfg>(o, inv, dst, sO + (size_t)(warp * 2048), lane);
         ++o_items;
       } else if (dst) {  // no visible position for any row of the tile: zeros
 #pragma unroll

@@ -208,6 +208,47 @@ __device__ __forceinline__ void zero_v_rows(uint8_t *vt, int z0, int z1, int lan
   }
 }
 
+// Warp-wide: writes this thread's half output row — the D / 2 values `o` of
+// O times `inv`, in the cache's 16-bit type — to `dst` (null: not stored)
+// through 2 KiB of shared memory at `stage`.  Stored directly, each 16-byte
+// store of a warp would touch 32 rows' lines; staged and read back
+// transposed, each store covers whole half-rows (4 at D = 128, 8 at D = 64),
+// one line per 128 bytes.  The warp's 32 half-rows of CH 16-byte chunks go
+// through in passes of RP rows; 16-byte unit u of a pass sits at unit
+// (u & ~7) | ((u ^ (u >> 3)) & 7), so 8 rows writing one chunk and a row's
+// chunks read by 8 lanes hit distinct banks.
+template <class Cfg>
+__device__ __forceinline__ void store_rows_staged(const uint32_t (&o)[Cfg::D / 64][32], float inv, uint4 *dst,
+                                                  uint8_t *stage, int lane) {
+  constexpr int CH = Cfg::D / 16, RP = 2048 / (CH * 16), RPI = 32 / CH;
+  auto unit = [](int u) { return (u & ~7) | ((u ^ (u >> 3)) & 7); };
+#pragma unroll
+  for (int pass = 0; pass < 32 / RP; ++pass) {
+    if (lane / RP == pass) {
+      const int lr = lane - pass * RP;
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) {
+        const uint32_t *src = &o[ch / 4][(ch % 4) * 8];
+        uint32_t wv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          wv[e] = pack2<Cfg::BF>(__uint_as_float(src[2 * e]) * inv, __uint_as_float(src[2 * e + 1]) * inv);
+        sts128(smem_u32(stage + unit(lr * CH + ch) * 16), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < RP / RPI; ++i) {
+      const int lr = i * RPI + lane / CH, ch = lane % CH;
+      uint4 *d =
+          reinterpret_cast<uint4 *>(__shfl_sync(kFull, reinterpret_cast<unsigned long long>(dst), pass * RP + lr));
+      const uint4 v = lds128(smem_u32(stage + unit(lr * CH + ch) * 16));
+      if (d) d[ch] = v;
+    }
+    __syncwarp();
+  }
+}
+
 // Warp-wide: multiplies this thread's OC columns of O (tensor memory at ta)
 // by alpha.
 template <class Cfg>

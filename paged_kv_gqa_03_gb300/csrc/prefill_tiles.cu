@@ -378,27 +378,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                          : nullptr;
       if constexpr (REP == 1) {
         const float inv = lt > 0.f ? 1.f / lt : 0.f;  // a row that sees nothing gives 0
+        uint32_t o[OC / 32][32];
 #pragma unroll
         for (int q = 0; q < OC / 32; ++q) {
-          uint32_t o[32];
           if (T > 0) {
-            tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o);
+            tc::ld32(tbase + lane_base + Cfg::COL_O + (uint32_t)(half * OC + q * 32), o[q]);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
-          }
-          if (dst) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t wv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                wv[e] = pack2<Cfg::BF>(__uint_as_float(o[v * 8 + 2 * e]) * inv,
-                                       __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
-              dst[q * 4 + v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            }
+            for (int e = 0; e < 32; ++e) o[q][e] = 0u;
           }
         }
+        // staged in the K ring, idle now that every S has completed
+        store_rows_staged<Cfg>(o, inv, dst, sK + (size_t)(warp * 2048), lane);
       } else if (T == 0) {  // no tile: every replica saw nothing
         if (dst && rep == 0) {
 #pragma unroll
