@@ -38,7 +38,11 @@
 //    11 P . V issue (S waits only for K and for its buffer's last P . V,
 //    P . V only for V and P: neither stream waits behind the other's inputs).  Every wait is bounded; a timeout sets
 //    PKV_FLAG_TIMEOUT, the CTA drains its copies and MMAs and frees its tensor
-//    memory.
+//    memory;
+//  * the softmax's per-column work runs two columns per instruction on the
+//    packed f32x2 arithmetic of sm_100 and later, with a three-input max
+//    (p_pair); the epilogue stages each warp's output rows in shared memory
+//    so that its global stores cover whole half-rows (store_rows_staged).
 #pragma once
 
 #include <math.h>
