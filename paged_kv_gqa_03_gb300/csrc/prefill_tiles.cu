@@ -35,7 +35,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // per S buffer: S written, P written, P . V done.  (One P barrier per buffer:
   // the softmax may finish tile j + 1 before the MMA warp waits for tile j, but
   // it cannot finish tile j + SBUF before that.)
-  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xch[2], xl;
+  __shared__ __align__(8) uint64_t s_full[Cfg::SBUF], p_full[Cfg::SBUF], pv_done[Cfg::SBUF], fin, xl;
+  // row-max exchange per tile between the two warps holding the same rows (w, w + 4)
+  __shared__ __align__(8) uint64_t xch[Cfg::SOFTMAX / 64][2];
   __shared__ __align__(8) uint64_t mrg[2];  // replica merge: (max, sum) written, partial O staged
   __shared__ __align__(8) uint64_t dead;
   static_assert(REP == 1 || REP == 2 || REP == 4, "replicas");
@@ -83,8 +85,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(&p_full[s], Cfg::SOFTMAX / 32);
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(&xch[0], Cfg::SOFTMAX / 32);
-    mbar_init(&xch[1], Cfg::SOFTMAX / 32);
+#pragma unroll
+    for (int pr = 0; pr < Cfg::SOFTMAX / 64; ++pr) {
+      mbar_init(&xch[pr][0], 2);
+      mbar_init(&xch[pr][1], 2);
+    }
     mbar_init(&xl, Cfg::SOFTMAX / 32);
     mbar_init(&mrg[0], Cfg::SOFTMAX / 32);
     mbar_init(&mrg[1], Cfg::SOFTMAX / 32);
@@ -297,8 +302,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // the row max over both halves (double-buffered exchange, bounded wait)
       red[j & 1][half][row] = mx;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&xch[j & 1]);
-      ok = warp_wait(&xch[j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
+      if (lane == 0) mbar_arrive(&xch[warp & 3][j & 1]);
+      ok = warp_wait(&xch[warp & 3][j & 1], (uint32_t)(j >> 1) & 1u, p.timeout_ns);
       if (!ok) break;
       mx = fmaxf(mx, red[j & 1][half ^ 1][row]);
       const float m_new = fmaxf(m_run, mx * c);
