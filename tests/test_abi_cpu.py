@@ -97,6 +97,32 @@ def test_multi_query_argument_errors_without_gpu():
     assert size.value == one.value          # partials are per worker, not per query row
 
 
+def test_workspace_grows_by_the_unit_width_per_partition():
+    """Per partition the workspace holds a partial O and a log-sum-exp per
+    query row of a unit and both column groups, a plan entry and a flag.
+    FP8 caches with more than 8 query rows per kv head use 16-row units, so
+    their partitions are twice as wide; 16-bit caches keep 8-row units."""
+    pkv = _lib()
+    L = pkv.lib()
+
+    def ws(Hq, Hkv, D, cache, q, splits):
+        size = ctypes.c_size_t(0)
+        assert L.paged_decode_workspace_bytes(3, Hq, Hkv, D, cache, q, splits, ctypes.byref(size)) == pkv.PKV_OK
+        return size.value
+
+    def per_partition(rows, D):
+        return 2 * rows * D * 4 + 2 * rows * 4 + 16 + 4
+
+    BF16, FP8 = 2, 3  # PKV_BF16, PKV_FP8_E4M3 in include/pagedkv.h
+    for Hq, Hkv, D, cache, rows in [(32, 2, 128, FP8, 16), (32, 2, 64, FP8, 16), (16, 2, 128, FP8, 8),
+                                    (32, 2, 128, BF16, 8), (64, 8, 128, BF16, 8)]:
+        # 256 partitions more: every region grows by a multiple of its 256-byte alignment
+        assert ws(Hq, Hkv, D, cache, BF16, 1280) - ws(Hq, Hkv, D, cache, BF16, 1024) == 256 * per_partition(rows, D)
+    # the fixed scratch of the static entry: ~1000 16-row partitions at D = 128
+    cap = pkv.PKV_STATIC_SCRATCH_BYTES
+    assert ws(32, 2, 128, FP8, BF16, 1000) <= cap < ws(32, 2, 128, FP8, BF16, 1100)
+
+
 def test_append_copy_merge_argument_errors_without_gpu():
     pkv = _lib()
     L = pkv.lib()
